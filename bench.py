@@ -1,0 +1,528 @@
+"""Benchmark of the block-quantized decode path on GB300.
+
+Default workload (one JSON line): the Q8_0 tied-embedding logit projection
+with soft-cap and top-k over the 262,144 x 5376 vocabulary matrix (1.5 GB of
+weights, far larger than L2).  One step = one gq_logits_topk call: stage x,
+stream every weight row, soft-cap, per-CTA top-k, final merge.  The metric is
+effective weight GB/s: the algorithmic bytes of a step (weights + x + the
+k (index, value) pairs written) divided by the device time of the step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--config NAME | --suite]
+
+Other workloads (--config / --suite) print one line each with the same keys:
+q4_0_matvec_4096x4096, q4_k_matvec_21504x5376, q4_0_ffn_gelu_21504x5376,
+q4_0_gemm_q8act_512x21504x5376.  Small matrices rotate over enough
+independent copies that the working set exceeds 4x the L2 size.
+
+--impl reference times the fp64 C oracle on the host cores on a bounded
+sample of the same workload (the oracle is the reference of this project).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "q8_0_logits_topk_262144x5376"
+METRIC = "quant matvec effective weight GB/s (% of GB300 HBM peak); M=512 int8 GEMM TOPS"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ---------------------------------------------------------------- environment
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_quantized_matvec_gq_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    sources are unchanged since the capture; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel") != kernel or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        def window(a, b):
+            return [p for (t, p) in self.samples if a <= t <= b]
+        sel = window(t0, t1)
+        where = "timed"
+        if not sel:  # timed region shorter than the sampling period: use the second before it
+            sel = window(t0 - 1.5, t1 + 0.3)
+            where = "timed+preceding load"
+        if not sel:
+            return None
+        sm = [float(p[1]) for p in sel if p[1].replace(".", "").isdigit()]
+        mx = [float(p[2]) for p in sel if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in sel for n, v in zip(names, p[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sel), "window": where}
+
+
+# ---------------------------------------------------------------- workloads
+
+class Workload:
+    name = ""
+    kernel = ""           # dominant kernel (for the roofline)
+    bound = "hbm"
+
+    def setup(self, torch, gq):
+        raise NotImplementedError
+
+    def step(self, i):
+        raise NotImplementedError
+
+
+def _to_dev(torch, a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+class LogitsTopK(Workload):
+    name = "q8_0_logits_topk_262144x5376"
+    kernel = "k_q8_0_logits_topk"
+    rows, K, k, cap = 262144, 5376, 10, 30.0
+    launches_per_step = 2
+
+    def setup(self, torch, gq):
+        W, x = synth.q8_0_logits_inputs(self.rows, self.K)
+        self.x_host = x
+        Wc = _to_dev(torch, W.reshape(-1))
+        del W
+        self.Wp = gq.pack(gq.GQ_FORMAT_Q8_0, Wc, self.rows, self.K)
+        del Wc
+        self.x = _to_dev(torch, x)
+        self.wsb = gq.gq_logits_topk_workspace_bytes(self.rows, self.K, self.k)
+        self.ws = torch.empty(self.wsb, dtype=torch.uint8, device="cuda")
+        self.idx = torch.empty(self.k, dtype=torch.int32, device="cuda")
+        self.val = torch.empty(self.k, dtype=torch.float32, device="cuda")
+        self.gq = gq
+        self.bytes_per_step = gq.gq_packed_bytes(1, self.rows, self.K) + 4 * self.K + 8 * self.k
+        self.weight_bytes = gq.gq_packed_bytes(1, self.rows, self.K)
+        self.working_set = self.weight_bytes
+        self.l2_policy = "inputs larger than L2 (1.5 GB weight matrix)"
+
+    def step(self, i):
+        self.gq.gq_logits_topk(self.Wp, self.x, self.cap, self.k, self.idx, self.val, None, self.ws,
+                               self.wsb, self.rows, self.K)
+
+    def e2e_setup(self, torch):
+        self.xh = torch.from_numpy(self.x_host.copy()).pin_memory()
+        self.idx_h = torch.empty(self.k, dtype=torch.int32).pin_memory()
+        self.val_h = torch.empty(self.k, dtype=torch.float32).pin_memory()
+        self.h2d, self.d2h = self.xh.numel() * 4, self.k * 8
+
+    def e2e_step(self, torch):
+        self.x.copy_(self.xh, non_blocking=True)
+        self.step(0)
+        self.idx_h.copy_(self.idx, non_blocking=True)
+        self.val_h.copy_(self.val, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    def cpu_reference(self, oracle, rows_sample):
+        W, x = synth.q8_0_logits_inputs(self.rows, self.K)
+        n = min(rows_sample, self.rows)
+        sel = np.arange(n, dtype=np.int64)
+
+        def run():
+            y, _ = oracle.matvec(oracle.FORMAT_Q8_0, W, x, self.rows, self.K, row_idx=sel)
+            c = np.array([oracle.softcap(v, self.cap) for v in y])
+            oracle.topk(c, self.k)
+        return run, n * (self.K // 32) * 34, f"{n} of {self.rows} rows (fp64 decode, soft-cap, full-sort top-{self.k})"
+
+
+class Rotating(Workload):
+    """A matvec-like workload over R independent weight copies (working set > 4x L2)."""
+    launches_per_step = 1
+
+    def _rotate(self, torch, one_copy_bytes):
+        l2 = torch.cuda.get_device_properties(0).L2_cache_size
+        need = max(4 * l2, 256 << 20)
+        return max(1, -(-need // one_copy_bytes))
+
+
+class Q40Matvec(Rotating):
+    name = "q4_0_matvec_4096x4096"
+    kernel = "k_q4_0_matvec"
+    rows, K = 4096, 4096
+
+    def setup(self, torch, gq):
+        W, x = synth.q4_0_matvec_inputs(self.rows, self.K)
+        nbytes = gq.gq_packed_bytes(0, self.rows, self.K)
+        R = self._rotate(torch, nbytes)
+        Wp = gq.pack(0, _to_dev(torch, W.reshape(-1)), self.rows, self.K)
+        self.copies = [Wp] + [Wp.clone() for _ in range(R - 1)]
+        self.x = _to_dev(torch, x)
+        self.y = torch.empty(self.rows, dtype=torch.float32, device="cuda")
+        self.gq = gq
+        self.bytes_per_step = nbytes + 4 * self.K + 4 * self.rows
+        self.weight_bytes = nbytes
+        self.working_set = nbytes * R
+        self.l2_policy = f"{R} rotating weight copies ({nbytes * R / 2**20:.0f} MiB > 4x L2)"
+
+    def step(self, i):
+        self.gq.gq_q4_0_matvec(self.copies[i % len(self.copies)], self.x, self.y, self.rows, self.K)
+
+
+class Q4KMatvec(Rotating):
+    name = "q4_k_matvec_21504x5376"
+    kernel = "k_q4k_matvec"
+    rows, K = 21504, 5376
+
+    def setup(self, torch, gq):
+        W, x = synth.q4_k_matvec_inputs(self.rows, self.K)
+        nbytes = gq.gq_packed_bytes(2, self.rows, self.K)
+        R = self._rotate(torch, nbytes)
+        Wp = gq.pack(2, _to_dev(torch, W.reshape(-1)), self.rows, self.K)
+        self.copies = [Wp] + [Wp.clone() for _ in range(R - 1)]
+        self.x = _to_dev(torch, x)
+        self.y = torch.empty(self.rows, dtype=torch.float32, device="cuda")
+        self.gq = gq
+        self.bytes_per_step = nbytes + 4 * self.K + 4 * self.rows
+        self.weight_bytes = nbytes
+        self.working_set = nbytes * R
+        self.l2_policy = f"{R} rotating weight copies ({nbytes * R / 2**20:.0f} MiB > 4x L2)"
+
+    def step(self, i):
+        self.gq.gq_q4k_matvec(self.copies[i % len(self.copies)], self.x, self.y, self.rows, self.K)
+
+
+class FFN(Rotating):
+    name = "q4_0_ffn_gelu_21504x5376"
+    kernel = "k_ffn_gate_up"
+    rows, K = 21504, 5376
+    launches_per_step = 2
+
+    def setup(self, torch, gq):
+        Wg, Wu, Wd, x = synth.ffn_inputs(self.rows, self.K)
+        nb = gq.gq_packed_bytes(0, self.rows, self.K)
+        R = self._rotate(torch, 3 * nb)
+        g = gq.pack(0, _to_dev(torch, Wg.reshape(-1)), self.rows, self.K)
+        u = gq.pack(0, _to_dev(torch, Wu.reshape(-1)), self.rows, self.K)
+        d = gq.pack(0, _to_dev(torch, Wd.reshape(-1)), self.K, self.rows)
+        self.copies = [(g, u, d)] + [(g.clone(), u.clone(), d.clone()) for _ in range(R - 1)]
+        self.x = _to_dev(torch, x)
+        self.h = torch.empty(self.rows, dtype=torch.float32, device="cuda")
+        self.y = torch.empty(self.K, dtype=torch.float32, device="cuda")
+        self.gq = gq
+        self.bytes_per_step = 3 * nb + 4 * self.K + 2 * 4 * self.rows + 4 * self.K
+        self.weight_bytes = 3 * nb
+        self.working_set = 3 * nb * R
+        self.l2_policy = f"{R} rotating weight sets ({3 * nb * R / 2**20:.0f} MiB > 4x L2)"
+
+    def step(self, i):
+        g, u, d = self.copies[i % len(self.copies)]
+        self.gq.gq_ffn_gate_up_gelu(g, u, self.x, self.h, self.rows, self.K)
+        self.gq.gq_q4_0_matvec(d, self.h, self.y, self.K, self.rows)
+
+
+class Gemm(Workload):
+    name = "q4_0_gemm_q8act_512x21504x5376"
+    kernel = "k_gemm_q8act"
+    bound = "tensor"
+    rows, K, M = 21504, 5376, 512
+    launches_per_step = 2
+
+    def setup(self, torch, gq):
+        W, X = synth.gemm_inputs(self.rows, self.K, self.M)
+        self.Wp = gq.pack(0, _to_dev(torch, W.reshape(-1)), self.rows, self.K)
+        self.X = _to_dev(torch, X)
+        self.Xq = torch.empty((self.M, self.K), dtype=torch.int8, device="cuda")
+        self.dx = torch.empty((self.M, self.K // 32), dtype=torch.float32, device="cuda")
+        self.Y = torch.empty((self.M, self.rows), dtype=torch.float32, device="cuda")
+        self.gq = gq
+        self.ops_per_step = 2 * self.M * self.rows * self.K
+        self.bytes_per_step = gq.gq_packed_bytes(0, self.rows, self.K) + 4 * self.M * self.K + 4 * self.M * self.rows
+        self.weight_bytes = gq.gq_packed_bytes(0, self.rows, self.K)
+        self.working_set = self.bytes_per_step
+        self.l2_policy = "compute-bound contraction (inputs stay resident)"
+
+    def step(self, i):
+        self.gq.gq_quantize_q8_0(self.X, self.Xq, self.dx, self.K, self.M)
+        self.gq.gq_q4_0_gemm_q8act(self.Wp, self.Xq, self.dx, self.Y, self.rows, self.K, self.M)
+
+
+WORKLOADS = {w.name: w for w in (LogitsTopK, Q40Matvec, Q4KMatvec, FFN, Gemm)}
+
+
+# ---------------------------------------------------------------- timing
+
+def run_gpu(wl_cls, args, rank, world, torch, dist):
+    import block_quantized_matvec_gq_gb300 as gq
+    gq.lib()
+    wl = wl_cls()
+    wl.setup(torch, gq)
+    stream = torch.cuda.current_stream()
+    use_graph = not isinstance(wl, LogitsTopK)   # small steps: replay a captured graph of K steps
+
+    for i in range(args.warmup):
+        wl.step(i)
+    torch.cuda.synchronize()
+
+    graph = None
+    if use_graph:
+        # capture exactly K steps; the timed region replays them once
+        s = torch.cuda.Stream()
+        s.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graph, stream=s):
+                for i in range(args.steps):
+                    wl.step(i)
+        torch.cuda.synchronize()
+        graph.replay()  # one untimed replay (warm)
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        # load the GPU for ~1.5 s so the clock samples reflect a busy GPU
+        t_end = time.time() + 1.5
+        j = 0
+        while time.time() < t_end:
+            if graph is not None:
+                graph.replay()
+            else:
+                wl.step(j)
+                j += 1
+            torch.cuda.synchronize()
+
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    e0.record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(args.steps):
+            wl.step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    clocks = None
+    if sampler:
+        time.sleep(0.25)
+        sampler.stop()
+        clocks = sampler.summary(t0, t1)
+
+    if dist is not None:
+        tt = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    # end to end through the public API with host buffers (default workload only)
+    e2e = None
+    if hasattr(wl, "e2e_setup") and rank == 0:
+        wl.e2e_setup(torch)
+        for _ in range(3):
+            wl.e2e_step(torch)
+        n = args.steps
+        t_a = time.perf_counter()
+        for _ in range(n):
+            wl.e2e_step(torch)
+        t_b = time.perf_counter()
+        e2e_ms = (t_b - t_a) * 1e3 / n
+        e2e = {"value": round(wl.bytes_per_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": wl.h2d, "d2h_bytes_per_step": wl.d2h,
+               "ms_per_step": round(e2e_ms, 4)}
+    return wl, ms, clocks, e2e
+
+
+def cpu_baseline(wl_cls, sample_rows):
+    import oracle
+    oracle.build()
+    wl = wl_cls()
+    if not hasattr(wl, "cpu_reference"):
+        return None
+    run, nbytes, desc = wl.cpu_reference(oracle, sample_rows)
+    t = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.threads(),
+            "kind": "oracle", "sample": desc, "seconds": round(dt, 3)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--suite", action="store_true", help="every workload, one line each")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank)
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    names = sorted(WORKLOADS) if args.suite else [args.config]
+    for name in names:
+        wl, ms, clocks, e2e = run_gpu(WORKLOADS[name], args, rank, world, torch, dist)
+        if rank != 0:
+            continue
+        ms_step = ms / args.steps
+        sec = ms_step * 1e-3
+        if wl.bound == "tensor":
+            value = wl.ops_per_step / sec / 1e12 * world
+            unit = "TOPS"
+            achieved = wl.ops_per_step / sec / 1e12
+            roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16, "unit": "TFLOP/s",
+                    "frac": round(achieved / bf16, 4), "traffic": recorded_traffic(wl.kernel, wl.name),
+                    "peak_source": f"{peak_src} bf16 dense (f16 MMA on exact integers has the same rate)"}
+        else:
+            value = wl.bytes_per_step / sec / 1e9 * world
+            unit = "GB/s"
+            roof = {"bound": "hbm", "achieved": round(wl.bytes_per_step / sec / 1e9, 2), "peak": hbm,
+                    "unit": "GB/s", "frac": round(wl.bytes_per_step / sec / 1e9 / hbm, 4),
+                    "traffic": recorded_traffic(wl.kernel, wl.name),
+                    "peak_source": f"{peak_src} HBM copy bandwidth",
+                    "timing": "events bracket every launch of the step (the dominant kernel plus "
+                              "any small follow-up kernel), so achieved is a lower bound"}
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; shapes and distributions of the workload)",
+            "config": {"workload": wl.name, "bytes_per_step": wl.bytes_per_step,
+                       "weight_bytes": wl.weight_bytes, "working_set_bytes": wl.working_set,
+                       "l2": wl.l2_policy, "parallelism": f"replicas x{world}"},
+            "roofline": roof, "clocks": clocks, "e2e": e2e,
+            "gpu_launches": wl.launches_per_step * args.steps,
+        }
+        if not args.no_cpu_baseline and world == 1 and hasattr(wl, "cpu_reference"):
+            line["cpu_baseline"] = cpu_baseline(WORKLOADS[name], sample_rows=wl.rows)
+        else:
+            line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_reference(args, rank):
+    """The oracle (fp64 C, OpenMP) on the host cores: rank 0 only."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    wl_cls = WORKLOADS[args.config]
+    wl = wl_cls()
+    if not hasattr(wl, "cpu_reference"):
+        print(json.dumps({"impl": "reference", "unavailable": f"no oracle timing for {wl.name}"}))
+        return
+    sample = 32768
+    run, nbytes, desc = wl.cpu_reference(oracle, sample)
+    for _ in range(args.warmup):
+        run()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t) / args.steps
+    value = nbytes / dt / 1e9
+    cores = oracle.threads()
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.name},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+if __name__ == "__main__":
+    main()

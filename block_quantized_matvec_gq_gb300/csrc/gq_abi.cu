@@ -1,0 +1,166 @@
+// gq_abi.cu -- the exported C entry points: argument validation, then launch.
+//
+// "Metal kernel capability table (Phase B ground truth)", section 9: legal
+// dimensions are checked at dispatch, not assumed; section 8, findings F4,
+// F6, F17: a silent no-op or a silently truncated K is a defect.  Every
+// entry point here rejects what its kernels cannot compute exactly, before
+// launching anything.
+#include "gq_host.h"
+
+using namespace gq;
+
+namespace {
+
+int block_weights(int format) { return format == GQ_FORMAT_Q4_K ? 256 : 32; }
+
+int block_bytes(int format)
+{
+    switch (format) {
+    case GQ_FORMAT_Q4_0: return 18;
+    case GQ_FORMAT_Q8_0: return 34;
+    case GQ_FORMAT_Q4_K: return 144;
+    }
+    return 0;
+}
+
+bool valid_format(int format)
+{
+    return format == GQ_FORMAT_Q4_0 || format == GQ_FORMAT_Q8_0 || format == GQ_FORMAT_Q4_K;
+}
+
+int check_matvec(int format, const void *W, const float *x, const float *y, int rows, int K, int M)
+{
+    if (!W || !x || !y) return GQ_ERR_NULL;
+    if (!aligned16(W) || !aligned16(x) || !aligned16(y)) return GQ_ERR_ALIGN;
+    if (rows < 1 || M != 1 || K < block_weights(format) || K % block_weights(format) != 0 || K > GQ_MAX_K)
+        return GQ_ERR_SHAPE;
+    return GQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gq_status_string(int status)
+{
+    switch (status) {
+    case GQ_OK: return "GQ_OK";
+    case GQ_ERR_NULL: return "GQ_ERR_NULL: a required pointer is NULL";
+    case GQ_ERR_ALIGN: return "GQ_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case GQ_ERR_SHAPE: return "GQ_ERR_SHAPE: rows/K/M/k outside the legal range";
+    case GQ_ERR_WORKSPACE: return "GQ_ERR_WORKSPACE: workspace missing or too small";
+    case GQ_ERR_CUDA: return "GQ_ERR_CUDA: the CUDA runtime reported an error";
+    case GQ_ERR_TIMEOUT: return "GQ_ERR_TIMEOUT: a bounded in-kernel wait gave up";
+    case GQ_ERR_FORMAT: return "GQ_ERR_FORMAT: unknown block format";
+    }
+    return "unknown gq_status";
+}
+
+size_t gq_packed_bytes(int format, int rows, int K)
+{
+    if (!valid_format(format) || rows < 1 || K < block_weights(format) || K % block_weights(format) != 0)
+        return 0;
+    return static_cast<size_t>(rows) * static_cast<size_t>(K / block_weights(format)) *
+           static_cast<size_t>(block_bytes(format));
+}
+
+static int pack_common(int format, const void *src, void *dst, int rows, int K, bool unpack, gq_stream_t s)
+{
+    if (!valid_format(format)) return GQ_ERR_FORMAT;
+    if (!src || !dst) return GQ_ERR_NULL;
+    if (!aligned16(src) || !aligned16(dst)) return GQ_ERR_ALIGN;
+    if (gq_packed_bytes(format, rows, K) == 0) return GQ_ERR_SHAPE;
+    return launch_pack(format, src, dst, rows, K, unpack, reinterpret_cast<cudaStream_t>(s));
+}
+
+int gq_pack(int format, const void *W_canon, void *W_packed, int rows, int K, gq_stream_t stream)
+{
+    return pack_common(format, W_canon, W_packed, rows, K, false, stream);
+}
+
+int gq_unpack(int format, const void *W_packed, void *W_canon, int rows, int K, gq_stream_t stream)
+{
+    return pack_common(format, W_packed, W_canon, rows, K, true, stream);
+}
+
+int gq_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K, int M, gq_stream_t stream)
+{
+    int st = check_matvec(GQ_FORMAT_Q4_0, W, x, y, rows, K, M);
+    if (st != GQ_OK) return st;
+    return launch_q4_0_matvec(W, x, y, rows, K, choose_matvec_geo(GQ_FORMAT_Q4_0, rows, K / 32),
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gq_q8_0_matvec(const void *W, const float *x, float *y, int rows, int K, int M, gq_stream_t stream)
+{
+    int st = check_matvec(GQ_FORMAT_Q8_0, W, x, y, rows, K, M);
+    if (st != GQ_OK) return st;
+    if (!aligned32(W)) return GQ_ERR_ALIGN;  // 32-byte weight loads
+    return launch_q8_0_matvec(W, x, y, rows, K, choose_matvec_geo(GQ_FORMAT_Q8_0, rows, K / 32),
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gq_q4k_matvec(const void *W, const float *x, float *y, int rows, int K, int M, gq_stream_t stream)
+{
+    int st = check_matvec(GQ_FORMAT_Q4_K, W, x, y, rows, K, M);
+    if (st != GQ_OK) return st;
+    return launch_q4k_matvec(W, x, y, rows, K, choose_matvec_geo(GQ_FORMAT_Q4_K, rows, K / 32),
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gq_ffn_gate_up_gelu(const void *W_gate, const void *W_up, const float *x, float *h, int rows, int K,
+                        int M, gq_stream_t stream)
+{
+    if (!W_up) return GQ_ERR_NULL;
+    if (!aligned16(W_up)) return GQ_ERR_ALIGN;
+    int st = check_matvec(GQ_FORMAT_Q4_0, W_gate, x, h, rows, K, M);
+    if (st != GQ_OK) return st;
+    MatvecGeo g = choose_matvec_geo(GQ_FORMAT_Q4_0, rows, K / 32);
+    g.r = 1;  // two weight streams (gate and up) per row group
+    return launch_ffn_gate_up(W_gate, W_up, x, h, rows, K, g, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t gq_logits_topk_workspace_bytes(int rows, int K, int k)
+{
+    if (rows < 1 || k < 1 || k > GQ_MAX_TOPK) return 0;
+    return logits_topk_ws_bytes(rows, K, k);
+}
+
+int gq_logits_topk(const void *W, const float *x, float softcap, int k, int *idx, float *val,
+                   float *logits_or_null, void *workspace, size_t workspace_bytes, int rows, int K, int M,
+                   gq_stream_t stream)
+{
+    int st = check_matvec(GQ_FORMAT_Q8_0, W, x, x, rows, K, M);
+    if (st != GQ_OK) return st;
+    if (!aligned32(W)) return GQ_ERR_ALIGN;  // 32-byte weight loads
+    if (!idx || !val) return GQ_ERR_NULL;
+    if (!aligned16(idx) || !aligned16(val) || (logits_or_null && !aligned16(logits_or_null)))
+        return GQ_ERR_ALIGN;
+    if (k < 1 || k > GQ_MAX_TOPK || k > rows) return GQ_ERR_SHAPE;
+    if (!(softcap == softcap)) return GQ_ERR_SHAPE; /* NaN cap */
+    if (!workspace) return GQ_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return GQ_ERR_ALIGN;
+    if (workspace_bytes < logits_topk_ws_bytes(rows, K, k)) return GQ_ERR_WORKSPACE;
+    MatvecGeo g = choose_matvec_geo(GQ_FORMAT_Q8_0, rows, K / 32);
+    return launch_logits_topk(W, x, softcap, k, idx, val, logits_or_null, workspace, workspace_bytes, rows,
+                              K, g, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gq_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, gq_stream_t stream)
+{
+    if (!X || !Xq || !dx) return GQ_ERR_NULL;
+    if (!aligned16(X) || !aligned16(Xq) || !aligned16(dx)) return GQ_ERR_ALIGN;
+    if (M < 1 || K < 32 || K % 32 != 0) return GQ_ERR_SHAPE;
+    return launch_quantize_q8_0(X, Xq, dx, K, M, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gq_q4_0_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows, int K, int M,
+                       gq_stream_t stream)
+{
+    if (!W || !Xq || !dx || !Y) return GQ_ERR_NULL;
+    if (!aligned16(W) || !aligned16(Xq) || !aligned16(dx) || !aligned16(Y)) return GQ_ERR_ALIGN;
+    if (rows < 1 || M < 1 || K < 32 || K % 32 != 0) return GQ_ERR_SHAPE;
+    return launch_gemm_q8act(W, Xq, dx, Y, rows, K, M, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

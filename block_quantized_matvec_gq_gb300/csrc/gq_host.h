@@ -1,0 +1,106 @@
+// gq_host.h -- host-side helpers shared by the libgq launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "gq.h"
+
+namespace gq {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+inline int status_from(cudaError_t e) { return e == cudaSuccess ? GQ_OK : GQ_ERR_CUDA; }
+
+// Streaming multiprocessor count of the current device (cached per device).
+inline int sm_count()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 1;
+    }
+    return cache[dev];
+}
+
+// Resident CTAs per SM for (kernel, threads, dynamic smem), cached; also
+// raises the kernel's dynamic shared-memory limit the first time.
+inline int ctas_per_sm(const void *kern, int threads, size_t smem)
+{
+    struct Entry {
+        const void *k;
+        int dev, threads;
+        size_t smem;
+        int occ;
+    };
+    static Entry tab[256];
+    static int used = 0;
+    static std::mutex mu;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (tab[i].k == kern && tab[i].dev == dev && tab[i].threads == threads && tab[i].smem == smem)
+            return tab[i].occ;
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem) != cudaSuccess)
+        occ = 0;
+    if (used < 256) tab[used++] = Entry{kern, dev, threads, smem, occ};
+    return occ;
+}
+
+// Launch with programmatic stream serialization allowed (the kernel itself
+// calls griddepcontrol.wait before it reads anything a previous kernel wrote).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// ---------------------------------------------------------------- internal launchers
+// Matvec geometry: LG lanes per row group, R rows per group, U blocks in flight.
+struct MatvecGeo {
+    int lg, r, u, warps;
+};
+
+MatvecGeo choose_matvec_geo(int format, int rows, int nb);
+
+int launch_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K, MatvecGeo g,
+                       cudaStream_t s);
+int launch_q8_0_matvec(const void *W, const float *x, float *y, int rows, int K, MatvecGeo g,
+                       cudaStream_t s);
+int launch_q4k_matvec(const void *W, const float *x, float *y, int rows, int K, MatvecGeo g,
+                      cudaStream_t s);
+int launch_ffn_gate_up(const void *Wg, const void *Wu, const float *x, float *h, int rows, int K,
+                       MatvecGeo g, cudaStream_t s);
+size_t logits_topk_ws_bytes(int rows, int K, int k);
+int launch_logits_topk(const void *W, const float *x, float softcap, int k, int *idx, float *val,
+                       float *logits, void *ws, size_t ws_bytes, int rows, int K, MatvecGeo g,
+                       cudaStream_t s);
+
+int launch_pack(int format, const void *src, void *dst, int rows, int K, bool unpack,
+                cudaStream_t s);
+int launch_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, cudaStream_t s);
+int launch_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows, int K,
+                      int M, cudaStream_t s);
+
+}  // namespace gq

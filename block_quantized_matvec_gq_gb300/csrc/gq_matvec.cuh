@@ -1,0 +1,211 @@
+// gq_matvec.cuh -- weight-streaming cores of the decode matvecs.
+//
+// Geometry (all compile-time): a warp is split into G = 32/LG lane groups of
+// LG lanes; each lane group owns NS row streams at a time, and lane lp of a
+// group handles blocks lp, lp+LG, lp+2LG, ... of each of its rows.  One x
+// block (32 floats, from the swizzled shared copy) is loaded once per lane
+// and used for all NS rows; lanes of different groups that read the same x
+// block get a shared-memory broadcast.  Per row and lane the products are
+// summed per block in packed f32x2 registers, scaled by the block's d, and
+// accumulated across the lane's blocks; the group then reduces its LG
+// partial sums with shuffles.  U blocks per row are loaded before any is
+// used, so each lane keeps U*NS 16-byte weight loads in flight.
+#pragma once
+
+#include "gq_internal.cuh"
+
+namespace gq {
+
+// ---------------------------------------------------------------- Q4_0
+// Packed Q4_0: nibble plane (16 B per block, element order) + fp16 scale plane.
+template <int LG, int NS, int U>
+__device__ __forceinline__ void q4_0_stream(const uint4 *const (&wp)[NS],
+                                            const uint16_t *const (&sp)[NS], const float *xs,
+                                            int nb, int lp, float (&out)[NS])
+{
+    float2 acc[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
+
+    for (int b0 = lp; b0 < nb; b0 += LG * U) {
+        uint4 w[U][NS];
+        float d[U][NS];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int b = b0 + u * LG;
+            const bool ok = b < nb;
+#pragma unroll
+            for (int i = 0; i < NS; ++i) {
+                w[u][i] = ok ? ld_stream16(wp[i] + b) : make_uint4(0u, 0u, 0u, 0u);
+                d[u][i] = ok ? __half2float(__ushort_as_half(ld_stream_u16(sp[i] + b))) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int b = b0 + u * LG;
+            if (b < nb) {
+                float2 blk[NS];
+#pragma unroll
+                for (int i = 0; i < NS; ++i) blk[i] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float4 xa = ld_xchunk(xs, b, 2 * t);
+                    const float4 xb = ld_xchunk(xs, b, 2 * t + 1);
+#pragma unroll
+                    for (int i = 0; i < NS; ++i) {
+                        const uint32_t word = (t == 0) ? w[u][i].x : (t == 1) ? w[u][i].y
+                                            : (t == 2) ? w[u][i].z : w[u][i].w;
+                        blk[i] = nib8_dot<8>(word, xa, xb, blk[i]);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < NS; ++i) acc[i] = ffma2(blk[i], make_float2(d[u][i], d[u][i]), acc[i]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
+}
+
+// ---------------------------------------------------------------- Q8_0
+// Packed Q8_0: byte plane (32 B per block, offset binary) + fp16 scale plane.
+template <int LG, int NS, int U>
+__device__ __forceinline__ void q8_0_stream(const uint4 *const (&wp)[NS],
+                                            const uint16_t *const (&sp)[NS], const float *xs,
+                                            int nb, int lp, float (&out)[NS])
+{
+    float2 acc[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
+
+    for (int b0 = lp; b0 < nb; b0 += LG * U) {
+        uint4 w[U][NS][2];
+        float d[U][NS];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int b = b0 + u * LG;
+            const bool ok = b < nb;
+#pragma unroll
+            for (int i = 0; i < NS; ++i) {
+                if (ok) {
+                    ld_stream32(wp[i] + 2 * b, w[u][i][0], w[u][i][1]);
+                } else {
+                    w[u][i][0] = make_uint4(0u, 0u, 0u, 0u);
+                    w[u][i][1] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                d[u][i] = ok ? __half2float(__ushort_as_half(ld_stream_u16(sp[i] + b))) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int b = b0 + u * LG;
+            if (b < nb) {
+                float2 blk[NS];
+#pragma unroll
+                for (int i = 0; i < NS; ++i) blk[i] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const float4 x4 = ld_xchunk(xs, b, m);
+#pragma unroll
+                    for (int i = 0; i < NS; ++i) {
+                        const uint4 &h = w[u][i][m >> 2];
+                        const uint32_t word = ((m & 3) == 0) ? h.x : ((m & 3) == 1) ? h.y
+                                            : ((m & 3) == 2) ? h.z : h.w;
+                        blk[i] = byte4_dot(word, x4, blk[i]);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < NS; ++i) acc[i] = ffma2(blk[i], make_float2(d[u][i], d[u][i]), acc[i]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
+}
+
+// ---------------------------------------------------------------- Q4_K
+// Packed Q4_K: nibble plane (128 B per super-block, sub-block s at 16 s, element
+// order) + record plane (16 B per super-block: d, dmin, 12 scale bytes).
+// A lane handles one 32-weight sub-block per step: sub-block index sb (global
+// within the row), super-block sb/8, sub-block s = sb%8.  xsum holds the sum
+// of each 32-element block of x (shared memory).
+__device__ __forceinline__ void q4k_scale_min(uint4 rec, int s, float &sc, float &mn)
+{
+    const int sh = 8 * (s & 3);
+    const uint32_t A = (rec.y >> sh) & 0xFFu;  // scale byte s&3
+    const uint32_t B = (rec.z >> sh) & 0xFFu;  // scale byte (s&3)+4
+    const uint32_t C = (rec.w >> sh) & 0xFFu;  // scale byte (s&3)+8
+    uint32_t isc, imn;
+    if (s < 4) {
+        isc = A & 63u;
+        imn = B & 63u;
+    } else {
+        isc = (C & 15u) | ((A >> 6) << 4);
+        imn = (C >> 4) | ((B >> 6) << 4);
+    }
+    sc = static_cast<float>(isc);
+    mn = static_cast<float>(imn);
+}
+
+template <int LG, int NS, int U>
+__device__ __forceinline__ void q4k_stream(const uint4 *const (&wp)[NS], const uint4 *const (&rp)[NS],
+                                           const float *xs, const float *xsum, int nsb, int lp,
+                                           float (&out)[NS])
+{
+    float2 acc[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
+
+    for (int b0 = lp; b0 < nsb; b0 += LG * U) {
+        uint4 w[U][NS];
+        uint4 rec[U][NS];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int b = b0 + u * LG;
+            const bool ok = b < nsb;
+#pragma unroll
+            for (int i = 0; i < NS; ++i) {
+                w[u][i] = ok ? ld_stream16(wp[i] + b) : make_uint4(0u, 0u, 0u, 0u);
+                // the 16-byte record is shared by the 8 lanes of a super-block
+                rec[u][i] = ok ? __ldg(rp[i] + (b >> 3)) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int b = b0 + u * LG;
+            if (b < nsb) {
+                float2 blk[NS];
+#pragma unroll
+                for (int i = 0; i < NS; ++i) blk[i] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float4 xa = ld_xchunk(xs, b, 2 * t);
+                    const float4 xb = ld_xchunk(xs, b, 2 * t + 1);
+#pragma unroll
+                    for (int i = 0; i < NS; ++i) {
+                        const uint32_t word = (t == 0) ? w[u][i].x : (t == 1) ? w[u][i].y
+                                            : (t == 2) ? w[u][i].z : w[u][i].w;
+                        blk[i] = nib8_dot<0>(word, xa, xb, blk[i]);
+                    }
+                }
+                const float xsb = xsum[b];
+#pragma unroll
+                for (int i = 0; i < NS; ++i) {
+                    float sc, mn;
+                    q4k_scale_min(rec[u][i], b & 7, sc, mn);
+                    const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(rec[u][i].x & 0xFFFFu)));
+                    const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(rec[u][i].x >> 16)));
+                    // d*sc and dmin*m are exact in f32 (11-bit x 6-bit products)
+                    const float dsc = d * sc, dm = dmin * mn;
+                    acc[i].x = fmaf(dsc, blk[i].x, acc[i].x);
+                    acc[i].y = fmaf(dsc, blk[i].y, acc[i].y);
+                    acc[i].x = fmaf(-dm, xsb, acc[i].x);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
+}
+
+}  // namespace gq

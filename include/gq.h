@@ -1,0 +1,178 @@
+/*
+ * gq.h -- C ABI of libgq: block-quantized matrix-vector products for GB300
+ * (sm_103a) with the dequantization fused in, their epilogues, and the
+ * Q4_0 x Q8_0 prefill contraction.
+ *
+ * Sources (page title, section):
+ *   "Gemma 4 M4 Max kernel roadmap" (gem, docs/research/kernel-roadmap.md),
+ *       K2 "Metal decode path": the decode steps in order -- a Q4_0
+ *       matrix-vector product with fused dequantization and F32
+ *       accumulation (step 1), the gated GELU FFN projection pair (step 5),
+ *       the Q8_0 embedding/output projection with on-GPU top-k (step 6);
+ *       K3 "prefill path": batched Q4_0 matrix-matrix kernels;
+ *       K4 "scheduling and memory": arenas are allocated once and
+ *       generation performs no tensor-sized allocation.
+ *   "Metal kernel capability table (Phase B ground truth)", section 1
+ *       "Quant matvec family" (Q4_0 18 B, Q4_K 144 B, Q8_0 blocks; legal K
+ *       and tail handling), section 9 (legal dimensions are checked at
+ *       dispatch, not assumed; one explicit kernel per format), section 8
+ *       findings F4, F6 and F17 (silent no-ops and silent truncation are
+ *       defects).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are caller-owned DEVICE memory, 16-byte aligned
+ *     (packed Q8_0 weights: 32-byte aligned, for 32-byte loads).
+ *     The library allocates nothing, never synchronizes the device, and
+ *     launches only on `stream` (NULL = the legacy default stream).
+ *   - Argument errors are reported before any launch as a negative gq_status;
+ *     nothing is launched and no output is touched.  After a launch,
+ *     a CUDA launch error is returned as GQ_ERR_CUDA.
+ *   - rows, K, M are element counts.  K must be whole blocks (a multiple of
+ *     32; of 256 for Q4_K); K is never silently truncated.  Rows need not
+ *     divide any tile: the row tail is masked inside the kernels.
+ *   - Weights W are in the PACKED layout written by gq_pack (same byte count
+ *     as the canonical GGUF-order blocks; see gq_pack).
+ *   - Results are deterministic: the same inputs give bitwise the same
+ *     outputs on the same GPU and launch configuration.
+ */
+#ifndef GQ_H
+#define GQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* identical to cudaStream_t */
+typedef struct CUstream_st *gq_stream_t;
+
+typedef enum {
+    GQ_OK = 0,
+    GQ_ERR_NULL = -1,      /* a required pointer is NULL */
+    GQ_ERR_ALIGN = -2,     /* a pointer is not 16-byte aligned */
+    GQ_ERR_SHAPE = -3,     /* rows/K/M/k outside the legal range */
+    GQ_ERR_WORKSPACE = -4, /* workspace missing or too small */
+    GQ_ERR_CUDA = -5,      /* the CUDA runtime reported an error */
+    GQ_ERR_TIMEOUT = -6,   /* a bounded in-kernel wait gave up */
+    GQ_ERR_FORMAT = -7     /* unknown block format */
+} gq_status;
+
+enum {
+    GQ_FORMAT_Q4_0 = 0, /* 18 B / 32 weights: fp16 d, 16 B nibbles; w = (q - 8) d   */
+    GQ_FORMAT_Q8_0 = 1, /* 34 B / 32 weights: fp16 d, 32 int8 q;     w = q d        */
+    GQ_FORMAT_Q4_K = 2  /* 144 B / 256 weights: fp16 d, dmin, 12 B 6-bit sc/m,
+                           128 B nibbles;                       w = d sc q - dmin m */
+};
+
+/* Largest K accepted by the single-pass matvec kernels (the whole activation
+ * vector is staged in shared memory). */
+#define GQ_MAX_K 49152
+/* Largest k accepted by gq_logits_topk. */
+#define GQ_MAX_TOPK 64
+
+/* Human-readable name of a gq_status value (static storage). */
+const char *gq_status_string(int status);
+
+/* ---------------------------------------------------------------------------
+ * Packing (one-time, not on the decode path).
+ *
+ * The canonical blocks are the GGUF byte order: Q4_0 byte j holds element j
+ * (low nibble) and element j+16 (high nibble); Q4_K's 128 nibble bytes are
+ * four 32-byte chunks, chunk c holding sub-block 2c in the low nibbles and
+ * 2c+1 in the high nibbles.  The packed layout keeps every bit of every
+ * block and the same total byte count; it is a bijection, undone exactly by
+ * gq_unpack.  Packed layout of a rows x K matrix with nb blocks per row:
+ *   Q4_0: plane 0 = rows*nb 16-byte payloads, row-major, nibbles in element
+ *         order (byte i = element 2i low, 2i+1 high); plane 1 = rows*nb fp16
+ *         scales d, row-major.
+ *   Q8_0: plane 0 = rows*nb 32-byte payloads, each byte q XOR 0x80
+ *         (offset binary); plane 1 = rows*nb fp16 scales d.
+ *   Q4_K: plane 0 = rows*ns 128-byte payloads (ns super-blocks per row),
+ *         sub-block s at bytes 16s..16s+15, nibbles in element order;
+ *         plane 1 = rows*ns 16-byte records {d, dmin, 12 scale bytes}
+ *         copied unchanged.
+ * W_canon and W_packed must not overlap.  Both are device pointers.
+ * ------------------------------------------------------------------------ */
+size_t gq_packed_bytes(int format, int rows, int K); /* 0 if invalid */
+int gq_pack(int format, const void *W_canon, void *W_packed, int rows, int K,
+            gq_stream_t stream);
+int gq_unpack(int format, const void *W_packed, void *W_canon, int rows, int K,
+              gq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Decode matvecs: y[i] = sum_j w_ij x_j with w decoded from the block and all
+ * arithmetic in f32 ("Gemma 4 M4 Max kernel roadmap", K2 step 1; "Metal
+ * kernel capability table", section 1, q4_f32_matvec / q4k_matvec rows).
+ *   W  packed weights, rows x K   x  f32[K]   y  f32[rows] (overwritten)
+ *   M  batch size; must be 1 (decode).  1 <= rows, 32 <= K <= GQ_MAX_K.
+ * Accuracy: |y_i - exact_i| <= 1e-5 * sum_j |w_ij x_j| for finite inputs.
+ * ------------------------------------------------------------------------ */
+int gq_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K, int M,
+                   gq_stream_t stream);
+int gq_q8_0_matvec(const void *W, const float *x, float *y, int rows, int K, int M,
+                   gq_stream_t stream);
+int gq_q4k_matvec(const void *W, const float *x, float *y, int rows, int K, int M,
+                  gq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Gated GELU FFN gate/up pair ("Gemma 4 M4 Max kernel roadmap", K2 step 5;
+ * "Metal kernel capability table", section 4 FFN family):
+ *   g = W_gate x, u = W_up x (both Q4_0, rows x K, packed), and
+ *   h[i] = gelu_tanh(g[i]) * u[i],
+ *   gelu_tanh(a) = 0.5 a (1 + tanh(sqrt(2/pi) (a + 0.044715 a^3))), the tanh
+ *   argument clamped to +-15 (finite for every finite a).
+ * One pass over x, two weight streams.  h is f32[rows].  M must be 1.
+ * The down projection is gq_q4_0_matvec with x = h.
+ * ------------------------------------------------------------------------ */
+int gq_ffn_gate_up_gelu(const void *W_gate, const void *W_up, const float *x, float *h,
+                        int rows, int K, int M, gq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Tied-embedding Q8_0 logits with soft-cap and on-GPU top-k
+ * ("Gemma 4 M4 Max kernel roadmap", K2 step 6; K1 logit soft-capping;
+ * K5 device top-k with (value, token) pair frontiers):
+ *   l[i] = sum_j w_ij x_j (W: Q8_0, rows x K, packed),
+ *   l'[i] = softcap * tanh(l[i] / softcap)   (softcap <= 0: l' = l),
+ *   idx[0..k), val[0..k) = the k largest l' in descending order; equal
+ *   values rank by the lower row index; NaN ranks below every number;
+ *   -0 ranks equal to +0.
+ *   logits_or_null: if not NULL, receives l' for every row (f32[rows]).
+ *   workspace: device scratch of at least gq_logits_topk_workspace_bytes
+ *   bytes (caller-owned; contents need no initialisation; two calls that may
+ *   run concurrently must not share it).
+ *   1 <= k <= min(GQ_MAX_TOPK, rows); M must be 1.
+ * Two kernels are launched on `stream`.
+ * ------------------------------------------------------------------------ */
+size_t gq_logits_topk_workspace_bytes(int rows, int K, int k);
+int gq_logits_topk(const void *W, const float *x, float softcap, int k, int *idx, float *val,
+                   float *logits_or_null, void *workspace, size_t workspace_bytes, int rows,
+                   int K, int M, gq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Q8_0 activation quantization ("Metal kernel capability table", section 2,
+ * quantize_q8: f32 -> int8 plus per-32 scales; finding F6):
+ *   for every token t < M and 32-block b of X[t, 0..K):
+ *     amax = max |x|, d = amax / 127 (IEEE f32 division),
+ *     q = clamp(round_half_away(x / d), -127, 127), and q = 0 when d = 0.
+ *   X f32[M][K] row-major, Xq int8[M][K], dx f32[M][K/32].  Bit-exact.
+ * ------------------------------------------------------------------------ */
+int gq_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, gq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Prefill contraction ("Gemma 4 M4 Max kernel roadmap", K3 batched Q4_0
+ * matrix-matrix) of packed Q4_0 weights W (rows x K) with Q8_0 activations
+ * (Xq int8[M][K], dx f32[M][K/32], as written by gq_quantize_q8_0):
+ *   D[t][r][b] = sum_{j<32} Xq[t][32b+j] * (q_w[r][32b+j] - 8)   (exact integers)
+ *   Y[t][r]    = sum_b d_w[r][b] * dx[t][b] * D[t][r][b]          (f32)
+ * Y is f32[M][rows] row-major (one row of Y per token).
+ * ------------------------------------------------------------------------ */
+int gq_q4_0_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows,
+                       int K, int M, gq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQ_H */

@@ -1,0 +1,85 @@
+"""GPU parity of the Q8_0 activation quantizer (bit-exact) and the Q4_0 x Q8_0
+prefill contraction (|Y - Y_ref| <= 1e-5 * sum_b |d_w d_x D|)."""
+
+import numpy as np
+import pytest
+
+import block_quantized_matvec_gq_gb300 as gq
+import oracle
+import synth
+from gpu_util import dev, guarded, packed, torch
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_quantize(X, M, K):
+    t = torch()
+    Xq = t.empty((M, K), dtype=t.int8, device="cuda")
+    dx = t.empty((M, K // 32), dtype=t.float32, device="cuda")
+    gq.gq_quantize_q8_0(dev(X), Xq, dx, K, M)
+    t.cuda.synchronize()
+    return Xq, dx
+
+
+@pytest.mark.parametrize("M,K", [(1, 32), (3, 96), (512, 5376), (7, 21504)])
+def test_quantize_bit_exact(M, K):
+    X = synth.normal((M, K), synth.stream(400 + M, K))
+    X[0, :32] = 0.0                                  # a zero block
+    if K >= 64:
+        X[0, 32:64] = np.arange(32, dtype=np.float32) - 15.5   # half-way quotients
+    Xq, dx = gpu_quantize(X, M, K)
+    q_ref, d_ref = oracle.quantize_q8_0(X, M, K)
+    assert np.array_equal(dx.cpu().numpy().view(np.uint32), d_ref.view(np.uint32))
+    assert np.array_equal(Xq.cpu().numpy(), q_ref)
+
+
+def run_gemm(W, Xq_np, dx_np, rows, K, M):
+    t = torch()
+    Wp = packed(oracle.FORMAT_Q4_0, W, rows, K)
+    full, Y, check = guarded(M * rows, t.float32)
+    gq.gq_q4_0_gemm_q8act(Wp, dev(Xq_np), dev(dx_np), Y, rows, K, M)
+    t.cuda.synchronize()
+    check()
+    return Y.view(M, rows).cpu().numpy()
+
+
+@pytest.mark.parametrize("M,rows,K", [(1, 1, 32), (37, 100, 256), (64, 64, 64), (130, 257, 544),
+                                      (5, 3000, 5376)])
+def test_gemm_matches_oracle(M, rows, K):
+    W = synth.q4_0_weights(rows, K, synth.stream(500 + M, 0))
+    X = synth.normal((M, K), synth.stream(500 + M, 1))
+    Xq, dx = oracle.quantize_q8_0(X, M, K)
+    Y = run_gemm(W, Xq, dx, rows, K, M)
+    Y_ref, A = oracle.gemm_q8act(W, Xq, dx, rows, K, M)
+    err = np.abs(Y.astype(np.float64) - Y_ref)
+    assert np.all(err <= 1e-5 * A), float(np.max(err / np.maximum(A, 1e-300)))
+
+
+def test_gemm_full_512x21504x5376_sampled():
+    rows, K, M = 21504, 5376, 512
+    W, X = synth.gemm_inputs()
+    Xq_g, dx_g = gpu_quantize(X, M, K)
+    q_ref, d_ref = oracle.quantize_q8_0(X, M, K)
+    assert np.array_equal(Xq_g.cpu().numpy(), q_ref)
+    t = torch()
+    Wp = packed(oracle.FORMAT_Q4_0, W, rows, K)
+    Y = t.empty((M, rows), dtype=t.float32, device="cuda")
+    gq.gq_q4_0_gemm_q8act(Wp, Xq_g, dx_g, Y, rows, K, M)
+    t.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    toks = np.concatenate([[0, 1, 127, 128, 511], rng.choice(M, 27, replace=False)])
+    rws = np.concatenate([[0, 1, 255, 256, 21503], rng.choice(rows, 123, replace=False)])
+    Y_ref, A = oracle.gemm_q8act(W, q_ref, d_ref, rows, K, M, tok_idx=toks, row_idx=rws)
+    Yg = Y.cpu().numpy()[np.ix_(toks, rws)].astype(np.float64)
+    assert np.all(np.abs(Yg - Y_ref) <= 1e-5 * A)
+
+
+def test_gemm_all_eight_weights_exact_zero():
+    import blockenc as be
+    rows, K, M = 70, 128, 9
+    blk = be.enc_q4_0(np.full(32, 8), 0.5)
+    W = be.rows_from_blocks([[blk] * (K // 32)] * rows)
+    X = synth.normal((M, K), synth.stream(501, 1))
+    Xq, dx = oracle.quantize_q8_0(X, M, K)
+    Y = run_gemm(W, Xq, dx, rows, K, M)
+    assert np.all(Y == 0.0)

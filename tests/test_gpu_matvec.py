@@ -1,0 +1,155 @@
+"""GPU parity of the decode matvecs (Q4_0, Q8_0, Q4_K) against the fp64 oracle.
+
+Bound (per row): |y - y_ref| <= 1e-5 * sum_j |w_ij x_j|.  Cases span several
+tiles and a ragged row tail, K at the block minimum, the lane-group widths
+(blocks per row divisible by 32, by 8 only, by none), the full 4096 x 4096
+Q4_0 and 21504 x 5376 Q4_K workloads, and the degenerate inputs of each
+format (all-8 nibbles, one-hot x, zero scales).
+"""
+
+import numpy as np
+import pytest
+
+import block_quantized_matvec_gq_gb300 as gq
+import oracle
+import synth
+from gpu_util import assert_within, dev, guarded, packed, torch
+
+pytestmark = pytest.mark.gpu
+
+FMT_FN = {
+    oracle.FORMAT_Q4_0: gq.gq_q4_0_matvec,
+    oracle.FORMAT_Q8_0: gq.gq_q8_0_matvec,
+    oracle.FORMAT_Q4_K: gq.gq_q4k_matvec,
+}
+
+
+def run_matvec(fmt, W_canon, x, rows, K):
+    t = torch()
+    Wp = packed(fmt, W_canon, rows, K)
+    full, y, check = guarded(rows, t.float32)
+    FMT_FN[fmt](Wp, dev(x), y, rows, K)
+    t.cuda.synchronize()
+    check()
+    return y.cpu().numpy()
+
+
+SHAPES = [(1, 32), (3, 64), (37, 96), (257, 256), (1000, 512), (129, 4096), (515, 5376), (77, 21504),
+          (33, 2304), (250, 800), (8, 49152)]
+
+
+@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K])
+@pytest.mark.parametrize("rows,K", SHAPES)
+def test_matvec_matches_oracle(fmt, rows, K):
+    if fmt == oracle.FORMAT_Q4_K and K % 256:
+        pytest.skip("Q4_K needs K % 256 == 0")
+    seed = 1000 + rows + K
+    W = synth.weights(fmt, rows, K, synth.stream(seed, 0))
+    x = synth.normal(K, synth.stream(seed, 1))
+    y = run_matvec(fmt, W, x, rows, K)
+    y_ref, a_ref = oracle.matvec(fmt, W, x, rows, K)
+    assert_within(y, y_ref, a_ref, what=f"fmt{fmt} {rows}x{K}")
+
+
+def test_q4_0_full_4096x4096_workload():
+    W, x = synth.q4_0_matvec_inputs()
+    y = run_matvec(oracle.FORMAT_Q4_0, W, x, 4096, 4096)
+    y_ref, a_ref = oracle.matvec(oracle.FORMAT_Q4_0, W, x, 4096, 4096)
+    assert_within(y, y_ref, a_ref, what="q4_0 4096x4096")
+
+
+def test_q4_k_full_21504x5376_workload():
+    W, x = synth.q4_k_matvec_inputs()
+    y = run_matvec(oracle.FORMAT_Q4_K, W, x, 21504, 5376)
+    y_ref, a_ref = oracle.matvec(oracle.FORMAT_Q4_K, W, x, 21504, 5376)
+    assert_within(y, y_ref, a_ref, what="q4_k 21504x5376")
+
+
+@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K])
+def test_one_hot_x_is_bit_exact(fmt):
+    rows, K = 70, 512
+    W = synth.weights(fmt, rows, K, synth.stream(5, fmt))
+    Wp = packed(fmt, W, rows, K)
+    dense = oracle.dequant(fmt, W, K)
+    t = torch()
+    y = t.empty(rows, dtype=t.float32, device="cuda")
+    for j in (0, 1, 16, 17, 31, 32, 255, 256, 511):
+        x = np.zeros(K, np.float32)
+        x[j] = 1.0
+        FMT_FN[fmt](Wp, dev(x), y, rows, K)
+        got = y.cpu().numpy().astype(np.float64)
+        assert np.array_equal(got, dense[:, j]), (fmt, j)
+
+
+def test_q4_0_all_eight_rows_are_exactly_zero():
+    import blockenc as be
+    rows, K = 40, 256
+    W = synth.q4_0_weights(rows, K, synth.stream(6, 0))
+    zero_blk = np.frombuffer(be.enc_q4_0(np.full(32, 8), 1.75), np.uint8)
+    Wb = W.reshape(rows, K // 32, 18)
+    for r in (0, 7, 39):
+        Wb[r, :, :] = zero_blk
+    x = synth.normal(K, synth.stream(6, 1)) * 50
+    y = run_matvec(oracle.FORMAT_Q4_0, W, x, rows, K)
+    for r in (0, 7, 39):
+        assert y[r] == 0.0
+    y_ref, a_ref = oracle.matvec(oracle.FORMAT_Q4_0, W, x, rows, K)
+    assert_within(y, y_ref, a_ref, what="q4_0 with zero rows")
+
+
+def test_q4_k_zero_scales_and_mins():
+    import blockenc as be
+    rows, K = 16, 512
+    rng = np.random.default_rng(0)
+    blocks = []
+    for r in range(rows):
+        row = []
+        for s in range(2):
+            q = rng.integers(0, 16, 256)
+            sc = [0] * 8 if r % 2 == 0 else list(rng.integers(0, 64, 8))
+            m = [0] * 8 if r % 3 == 0 else list(rng.integers(0, 64, 8))
+            row.append(be.enc_q4_k(q, sc, m, 0.01, 0.02))
+        blocks.append(row)
+    W = be.rows_from_blocks(blocks)
+    x = synth.normal(K, synth.stream(7, 1))
+    y = run_matvec(oracle.FORMAT_Q4_K, W, x, rows, K)
+    y_ref, a_ref = oracle.matvec(oracle.FORMAT_Q4_K, W, x, rows, K)
+    assert_within(y, y_ref, a_ref, what="q4_k special scales")
+    assert y[0] == 0.0 and y[6] == 0.0     # sc = 0 and m = 0
+
+
+@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K])
+def test_repeat_runs_are_bitwise_identical(fmt):
+    rows, K = 3001, 5376 if fmt != oracle.FORMAT_Q4_0 else 4096
+    W = synth.weights(fmt, rows, K, synth.stream(8, 0))
+    t = torch()
+    Wp = packed(fmt, W, rows, K)
+    x = dev(synth.normal(K, synth.stream(8, 1)))
+    ys = []
+    for _ in range(5):
+        y = t.empty(rows, dtype=t.float32, device="cuda")
+        FMT_FN[fmt](Wp, x, y, rows, K)
+        ys.append(y)
+    for y in ys[1:]:
+        assert t.equal(y, ys[0])
+
+
+def test_argument_errors_launch_nothing():
+    t = torch()
+    W = t.zeros(1024, dtype=t.uint8, device="cuda")
+    x = t.zeros(64, dtype=t.float32, device="cuda")
+    y = t.full((4,), 3.0, dtype=t.float32, device="cuda")
+    with pytest.raises(gq.GQError) as e:
+        gq.gq_q4_0_matvec(W, x, y, 4, 48)          # partial block
+    assert e.value.status == gq.GQ_ERR_SHAPE
+    with pytest.raises(gq.GQError) as e:
+        gq.gq_q4_0_matvec(W, x, y, 4, 64, M=2)      # batched decode not offered
+    assert e.value.status == gq.GQ_ERR_SHAPE
+    with pytest.raises(gq.GQError) as e:
+        gq.gq_q4k_matvec(W, x, y, 1, 64)            # Q4_K needs K % 256
+    assert e.value.status == gq.GQ_ERR_SHAPE
+    with pytest.raises(gq.GQError) as e:
+        gq.gq_q8_0_matvec(W, x.data_ptr() + 4, y, 4, 32)
+    assert e.value.status == gq.GQ_ERR_ALIGN
+    t.cuda.synchronize()
+    assert t.equal(y, t.full((4,), 3.0, dtype=t.float32, device="cuda"))
