@@ -329,7 +329,7 @@ def run_gpu(wl_cls, args, rank, world, torch, dist):
     wl = wl_cls()
     wl.setup(torch, gq)
     stream = torch.cuda.current_stream()
-    use_graph = not isinstance(wl, LogitsTopK)   # small steps: replay a captured graph of K steps
+    use_graph = True   # replay a captured graph of exactly K steps (no host launch cost in the timing)
 
     for i in range(args.warmup):
         wl.step(i)
@@ -433,6 +433,8 @@ def main():
     ap.add_argument("--config", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--suite", action="store_true", help="every workload, one line each")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="logits workload only: vocabulary rows (default 262144; smaller for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -450,6 +452,9 @@ def main():
         dist.init_process_group("nccl")
     hbm, bf16, bf16_sus, peak_src = peaks()
     names = sorted(WORKLOADS) if args.suite else [args.config]
+    if args.rows:
+        LogitsTopK.rows = args.rows
+        LogitsTopK.name = f"q8_0_logits_topk_{args.rows}x5376"
     for name in names:
         wl, ms, clocks, e2e = run_gpu(WORKLOADS[name], args, rank, world, torch, dist)
         if rank != 0:

@@ -58,6 +58,8 @@ def _declare(L):
         "gq_logits_topk": ([P, P, ctypes.c_float, I, P, P, P, P, S, I, I, I, P], I),
         "gq_quantize_q8_0": ([P, P, P, I, I, P], I),
         "gq_q4_0_gemm_q8act": ([P, P, P, P, I, I, I, P], I),
+        "gq_q4_0_gemm_block_dots": ([P, P, P, I, I, I, P], I),
+        "gq_device_status": ([I], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -160,6 +162,16 @@ def gq_quantize_q8_0(X, Xq, dx, K, M, stream=None):
 def gq_q4_0_gemm_q8act(W, Xq, dx, Y, rows, K, M, stream=None):
     _check(lib().gq_q4_0_gemm_q8act(_ptr(W), _ptr(Xq), _ptr(dx), _ptr(Y), rows, K, M, _stream(stream)),
            "gq_q4_0_gemm_q8act")
+
+
+def gq_q4_0_gemm_block_dots(W, Xq, D, rows, K, M, stream=None):
+    _check(lib().gq_q4_0_gemm_block_dots(_ptr(W), _ptr(Xq), _ptr(D), rows, K, M, _stream(stream)),
+           "gq_q4_0_gemm_block_dots")
+
+
+def gq_device_status(reset: bool = True) -> int:
+    """Synchronizes; GQ_ERR_TIMEOUT if a bounded in-kernel wait gave up."""
+    return int(lib().gq_device_status(1 if reset else 0))
 
 
 # ---------------------------------------------------------------- conveniences (allocation only)

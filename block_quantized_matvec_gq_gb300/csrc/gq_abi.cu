@@ -115,9 +115,8 @@ int gq_ffn_gate_up_gelu(const void *W_gate, const void *W_up, const float *x, fl
     if (!aligned16(W_up)) return GQ_ERR_ALIGN;
     int st = check_matvec(GQ_FORMAT_Q4_0, W_gate, x, h, rows, K, M);
     if (st != GQ_OK) return st;
-    MatvecGeo g = choose_matvec_geo(GQ_FORMAT_Q4_0, rows, K / 32);
-    g.r = 1;  // two weight streams (gate and up) per row group
-    return launch_ffn_gate_up(W_gate, W_up, x, h, rows, K, g, reinterpret_cast<cudaStream_t>(stream));
+    return launch_ffn_gate_up(W_gate, W_up, x, h, rows, K, choose_ffn_geo(rows, K / 32),
+                              reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t gq_logits_topk_workspace_bytes(int rows, int K, int k)
@@ -141,9 +140,8 @@ int gq_logits_topk(const void *W, const float *x, float softcap, int k, int *idx
     if (!workspace) return GQ_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GQ_ERR_ALIGN;
     if (workspace_bytes < logits_topk_ws_bytes(rows, K, k)) return GQ_ERR_WORKSPACE;
-    MatvecGeo g = choose_matvec_geo(GQ_FORMAT_Q8_0, rows, K / 32);
     return launch_logits_topk(W, x, softcap, k, idx, val, logits_or_null, workspace, workspace_bytes, rows,
-                              K, g, reinterpret_cast<cudaStream_t>(stream));
+                              K, choose_logits_geo(rows, K / 32), reinterpret_cast<cudaStream_t>(stream));
 }
 
 int gq_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, gq_stream_t stream)
@@ -160,7 +158,18 @@ int gq_q4_0_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *
     if (!W || !Xq || !dx || !Y) return GQ_ERR_NULL;
     if (!aligned16(W) || !aligned16(Xq) || !aligned16(dx) || !aligned16(Y)) return GQ_ERR_ALIGN;
     if (rows < 1 || M < 1 || K < 32 || K % 32 != 0) return GQ_ERR_SHAPE;
-    return launch_gemm_q8act(W, Xq, dx, Y, rows, K, M, reinterpret_cast<cudaStream_t>(stream));
+    return launch_gemm_q8act_tc(W, Xq, dx, Y, rows, K, M, reinterpret_cast<cudaStream_t>(stream));
 }
+
+int gq_q4_0_gemm_block_dots(const void *W, const int8_t *Xq, int32_t *D, int rows, int K, int M,
+                            gq_stream_t stream)
+{
+    if (!W || !Xq || !D) return GQ_ERR_NULL;
+    if (!aligned16(W) || !aligned16(Xq) || !aligned16(D)) return GQ_ERR_ALIGN;
+    if (rows < 1 || M < 1 || K < 32 || K % 32 != 0) return GQ_ERR_SHAPE;
+    return launch_block_dots_tc(W, Xq, D, rows, K, M, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gq_device_status(int reset) { return read_device_status(reset != 0); }
 
 }  // extern "C"

@@ -1,0 +1,534 @@
+// gq_gemm_tc.cu -- Q4_0 weights x Q8_0 activations on the 5th-generation
+// tensor cores (tcgen05), with exact integer block dot products.
+//
+// "Gemma 4 M4 Max kernel roadmap", K3 "prefill path": batched Q4_0
+// matrix-matrix kernels sized for the 5376 embedding and 21504 FFN (there a
+// 64-output x 32-prompt SIMD-matrix tile with threadgroup staging).
+//   D[t][r][b] = sum_{j<32} Xq[t][32b+j] * (q_w[r][32b+j] - 8)
+//   Y[t][r]    = sum_b d_w[r][b] * dx[t][b] * D[t][r][b]
+//
+// On sm_103a the int8 form of tcgen05.mma is not available, so both
+// operands are fed as f16: q_w - 8 in [-8, 7] and Xq in [-127, 127] are
+// exact in f16, every partial sum of a 32-term block dot is an integer of
+// magnitude <= 32 * 8 * 127 = 32512 < 2^24, so the f32 accumulator in
+// tensor memory holds D exactly.  Because the scales change every 32
+// elements, each block's D is read out of tensor memory and folded into the
+// f32 result by the epilogue warps (Y += dx * d_w * D) while the tensor core
+// already computes the next block into the other D buffer.
+//
+// CTA (512 threads, one per SM, persistent over 128-token x 192-row tiles):
+//   warps 0-2   producers: cp.async the packed codes and scales of each
+//               32-block into a raw ring, convert them to f16 in the UMMA
+//               K-major no-swizzle layout, signal `full`;
+//   warps 3-14  epilogue: warp w owns TMEM lanes 32*(w%4).. and 64 columns;
+//   warp 15     MMA: one elected lane issues 2 x (M128 N192 K16) per block.
+// Every mbarrier wait is bounded: on timeout the kernel records
+// GQ_ERR_TIMEOUT in a device flag, the other roles leave their loops, TMEM
+// is released and the kernel returns.
+#include "gq_host.h"
+#include "gq_internal.cuh"
+
+namespace gq {
+
+__device__ int g_device_status = 0;
+
+namespace tc {
+
+constexpr int TM = 128;  // tokens per tile (MMA M, TMEM lanes)
+constexpr int TN = 192;  // weight rows per tile (MMA N, TMEM columns)
+constexpr int KB = 32;   // K per quantization block
+constexpr int S = 4;     // converted operand stages
+constexpr int RAW = 8;   // raw packed-data stages (cp.async ring)
+constexpr int PROD_WARPS = 3;
+constexpr int EPI_WARPS = 12;
+constexpr int MMA_WARP = PROD_WARPS + EPI_WARPS;
+constexpr int NWARPS = MMA_WARP + 1;
+constexpr int NTHREADS = NWARPS * 32;
+constexpr int NPROD = PROD_WARPS * 32;
+constexpr int EPI_COLS = TN / (EPI_WARPS / 4);  // 64
+constexpr int TMEM_COLS = 512;
+constexpr int DBUF = 256;  // TMEM column offset of the second D buffer
+
+constexpr int A_BYTES = TM * KB * 2;  // 8192
+constexpr int B_BYTES = TN * KB * 2;  // 12288
+constexpr int RA_BYTES = TM * KB;     // 4096: int8 codes
+constexpr int RB_BYTES = TN * 16;     // 3072: nibbles
+constexpr int RX_BYTES = TM * 4;      // 512: f32 dx
+constexpr int RW_BYTES = TN * 4;      // 768: aligned fp16 pairs holding d_w
+constexpr int RAW_BYTES = RA_BYTES + RB_BYTES + RX_BYTES + RW_BYTES;
+constexpr int SCL_BYTES = (TM + TN) * 4;
+
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + S * A_BYTES;
+constexpr int OFF_RAW = OFF_B + S * B_BYTES;
+constexpr int OFF_SCL = OFF_RAW + RAW * RAW_BYTES;
+constexpr int OFF_BAR = OFF_SCL + S * SCL_BYTES;
+constexpr int N_BARS = 2 * S + 4 + 1;  // full[S], empty[S], dfull[2], dempty[2], drain
+constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 16;
+
+static_assert(OFF_B % 1024 == 0 && OFF_RAW % 16 == 0 && OFF_SCL % 16 == 0 && OFF_BAR % 8 == 0, "align");
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+
+// Bounded wait for the phase of `bar` with the given parity.  Returns false
+// (and raises the CTA abort flag and the device status) on timeout, or when
+// another role has already aborted.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0u) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                atomicExch(&g_device_status, GQ_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4_zfill(uint32_t dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// tcgen05 shared-memory matrix descriptor, K-major, no swizzle: start
+// address, LBO = byte stride between core matrices along K, SBO = byte
+// stride between 8-row groups along M/N, descriptor version 1 (bit 46).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo >> 4) << 16) |
+           (static_cast<uint64_t>(sbo >> 4) << 32) | (1ull << 46);
+}
+// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B f16
+// (bits 7-9, 10-12 = 0), both K-major, N >> 3 at bits 17-22, M >> 4 at 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (static_cast<uint32_t>(TN >> 3) << 17) | (static_cast<uint32_t>(TM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// 32 consecutive f32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------- operand conversion
+// Both operands of a 32-block are written as four 8-element K groups; inside
+// a group the elements are stored in the order 0,4,1,5,2,6,3,7 (the order in
+// which the nibble unpacking below produces them).  A and B use the same
+// order, so the dot products are unchanged.
+__device__ __forceinline__ uint4 nib8_to_f16(uint32_t w)
+{
+    const uint32_t w2 = w >> 8;
+    __half2 h0 = __halves2half2(__ushort_as_half(0), __ushort_as_half(0));
+    uint32_t a0 = (w & 0x000F000Fu) | 0x64006400u;   // 1024 + (e0, e4)
+    uint32_t a1 = (w & 0x00F000F0u) | 0x64006400u;   // 1024 + 16 (e1, e5)
+    uint32_t a2 = (w2 & 0x000F000Fu) | 0x64006400u;  // 1024 + (e2, e6)
+    uint32_t a3 = (w2 & 0x00F000F0u) | 0x64006400u;  // 1024 + 16 (e3, e7)
+    const __half2 c1032 = __float2half2_rn(1032.0f);
+    const __half2 c16 = __float2half2_rn(0.0625f);
+    const __half2 c72 = __float2half2_rn(-72.0f);
+    __half2 r0 = __hsub2(*reinterpret_cast<__half2 *>(&a0), c1032);
+    __half2 r1 = __hfma2(*reinterpret_cast<__half2 *>(&a1), c16, c72);
+    __half2 r2 = __hsub2(*reinterpret_cast<__half2 *>(&a2), c1032);
+    __half2 r3 = __hfma2(*reinterpret_cast<__half2 *>(&a3), c16, c72);
+    (void)h0;
+    uint4 o;
+    o.x = *reinterpret_cast<uint32_t *>(&r0);
+    o.y = *reinterpret_cast<uint32_t *>(&r1);
+    o.z = *reinterpret_cast<uint32_t *>(&r2);
+    o.w = *reinterpret_cast<uint32_t *>(&r3);
+    return o;
+}
+// Eight int8 codes (two words, elements 0..3 and 4..7) -> f16 in group order.
+__device__ __forceinline__ uint4 s8x8_to_f16(uint32_t lo, uint32_t hi)
+{
+    lo ^= 0x80808080u;  // offset binary: u = q + 128
+    hi ^= 0x80808080u;
+    const uint32_t t01 = __byte_perm(lo, hi, 0x5140);  // u0 u4 u1 u5
+    const uint32_t t23 = __byte_perm(lo, hi, 0x7362);  // u2 u6 u3 u7
+    uint32_t a0 = __byte_perm(t01, 0x64646464u, 0x4140);  // 1024 + (u0, u4)
+    uint32_t a1 = __byte_perm(t01, 0x64646464u, 0x4342);  // 1024 + (u1, u5)
+    uint32_t a2 = __byte_perm(t23, 0x64646464u, 0x4140);
+    uint32_t a3 = __byte_perm(t23, 0x64646464u, 0x4342);
+    const __half2 c = __float2half2_rn(1152.0f);
+    __half2 r0 = __hsub2(*reinterpret_cast<__half2 *>(&a0), c);
+    __half2 r1 = __hsub2(*reinterpret_cast<__half2 *>(&a1), c);
+    __half2 r2 = __hsub2(*reinterpret_cast<__half2 *>(&a2), c);
+    __half2 r3 = __hsub2(*reinterpret_cast<__half2 *>(&a3), c);
+    uint4 o;
+    o.x = *reinterpret_cast<uint32_t *>(&r0);
+    o.y = *reinterpret_cast<uint32_t *>(&r1);
+    o.z = *reinterpret_cast<uint32_t *>(&r2);
+    o.w = *reinterpret_cast<uint32_t *>(&r3);
+    return o;
+}
+// Byte offset of (row, K group kg) in an operand stage: core matrix
+// (row/8, kg) at ((row/8)*4 + kg)*128, row%8 at 16-byte steps inside it.
+__device__ __forceinline__ uint32_t op_off(int row, int kg) { return (((row >> 3) * 4 + kg) << 7) + ((row & 7) << 4); }
+
+struct Work {
+    int ntm, ntiles, nb;
+};
+
+// Block gb (running index over this CTA's tiles and their K blocks) -> tile, b.
+__device__ __forceinline__ bool block_coords(const Work &w, long long gb, int &tile, int &b)
+{
+    const long long it = gb / w.nb;
+    b = static_cast<int>(gb - it * w.nb);
+    const long long t = blockIdx.x + it * static_cast<long long>(gridDim.x);
+    tile = static_cast<int>(t);
+    return t < w.ntiles;
+}
+
+// ---------------------------------------------------------------- the kernel
+template <bool kDumpD>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_gemm_q8act_tc(const uint8_t *__restrict__ nib, const uint16_t *__restrict__ dsc,
+                    const int8_t *__restrict__ Xq, const float *__restrict__ dx, float *__restrict__ Y,
+                    int32_t *__restrict__ Dout, int rows, int K, int M)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase + OFF_BAR, bar_empty = bar_full + 8 * S;
+    const uint32_t bar_dfull = bar_empty + 8 * S, bar_dempty = bar_dfull + 16, bar_drain = bar_dempty + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+
+    Work w;
+    w.nb = K / KB;
+    w.ntm = (M + TM - 1) / TM;
+    w.ntiles = w.ntm * ((rows + TN - 1) / TN);
+    const int my_tiles = (w.ntiles > static_cast<int>(blockIdx.x))
+                             ? (w.ntiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                             : 0;
+    const long long nblocks = static_cast<long long>(my_tiles) * w.nb;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_full + 8 * s, NPROD);
+            mbar_init(bar_empty + 8 * s, 1 + EPI_WARPS);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_dfull + 8 * b, 1);
+            mbar_init(bar_dempty + 8 * b, EPI_WARPS);
+        }
+        mbar_init(bar_drain, 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == MMA_WARP) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();
+
+    if (warp < PROD_WARPS) {
+        // ------------------------------------------------ producers
+        const int p = threadIdx.x;  // 0..NPROD-1
+        auto issue = [&](long long gb) {
+            int tile, b;
+            const uint32_t raw = sbase + OFF_RAW + static_cast<uint32_t>(gb % RAW) * RAW_BYTES;
+            if (gb < nblocks && block_coords(w, gb, tile, b)) {
+                const int t0 = (tile % w.ntm) * TM, r0 = (tile / w.ntm) * TN;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int tt = p + h * NPROD;
+                    if (tt < TM) {
+                        const int t = t0 + tt;
+                        const bool tv = t < M;
+                        const int8_t *xs = Xq + static_cast<size_t>(tv ? t : 0) * K + b * KB;
+                        cp_async16_zfill(raw + tt * 32, xs, tv);
+                        cp_async16_zfill(raw + tt * 32 + 16, xs + 16, tv);
+                        const bool xv = tv && dx != nullptr;  // the block-dot dump reads no scales
+                        cp_async4_zfill(raw + RA_BYTES + RB_BYTES + tt * 4,
+                                        xv ? static_cast<const void *>(dx + static_cast<size_t>(t) * w.nb + b)
+                                           : static_cast<const void *>(Xq),
+                                        xv);
+                    }
+                    const int rr = p + h * NPROD;
+                    if (rr < TN) {
+                        const int r = r0 + rr;
+                        const bool rv = r < rows;
+                        const size_t e = static_cast<size_t>(rv ? r : 0) * w.nb + b;
+                        cp_async16_zfill(raw + RA_BYTES + rr * 16, nib + e * 16, rv);
+                        cp_async4_zfill(raw + RA_BYTES + RB_BYTES + RX_BYTES + rr * 4, dsc + (e & ~static_cast<size_t>(1)), rv);
+                    }
+                }
+            }
+            cp_async_commit();
+        };
+        for (int j = 0; j < RAW; ++j) issue(j);
+        for (long long gb = 0; gb < nblocks; ++gb) {
+            const int s = static_cast<int>(gb % S);
+            cp_async_wait<RAW - 1>();
+            if (!wait_bounded(bar_empty + 8 * s, static_cast<uint32_t>(((gb / S) & 1) ^ 1), abort)) break;
+            int tile, b;
+            block_coords(w, gb, tile, b);
+            const int r0 = (tile / w.ntm) * TN;
+            const uint8_t *raw = smem + OFF_RAW + (gb % RAW) * RAW_BYTES;
+            uint8_t *opA = smem + OFF_A + s * A_BYTES;
+            uint8_t *opB = smem + OFF_B + s * B_BYTES;
+            float *scl = reinterpret_cast<float *>(smem + OFF_SCL + s * SCL_BYTES);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int tt = p + h * NPROD;
+                if (tt < TM) {
+                    const uint4 q0 = *reinterpret_cast<const uint4 *>(raw + tt * 32);
+                    const uint4 q1 = *reinterpret_cast<const uint4 *>(raw + tt * 32 + 16);
+                    *reinterpret_cast<uint4 *>(opA + op_off(tt, 0)) = s8x8_to_f16(q0.x, q0.y);
+                    *reinterpret_cast<uint4 *>(opA + op_off(tt, 1)) = s8x8_to_f16(q0.z, q0.w);
+                    *reinterpret_cast<uint4 *>(opA + op_off(tt, 2)) = s8x8_to_f16(q1.x, q1.y);
+                    *reinterpret_cast<uint4 *>(opA + op_off(tt, 3)) = s8x8_to_f16(q1.z, q1.w);
+                    scl[tt] = *reinterpret_cast<const float *>(raw + RA_BYTES + RB_BYTES + tt * 4);
+                }
+                const int rr = p + h * NPROD;
+                if (rr < TN) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(raw + RA_BYTES + rr * 16);
+                    *reinterpret_cast<uint4 *>(opB + op_off(rr, 0)) = nib8_to_f16(v.x);
+                    *reinterpret_cast<uint4 *>(opB + op_off(rr, 1)) = nib8_to_f16(v.y);
+                    *reinterpret_cast<uint4 *>(opB + op_off(rr, 2)) = nib8_to_f16(v.z);
+                    *reinterpret_cast<uint4 *>(opB + op_off(rr, 3)) = nib8_to_f16(v.w);
+                    const uint32_t pair = *reinterpret_cast<const uint32_t *>(raw + RA_BYTES + RB_BYTES + RX_BYTES + rr * 4);
+                    const size_t e = static_cast<size_t>(r0 + rr) * w.nb + b;
+                    const uint16_t hbits = static_cast<uint16_t>((e & 1) ? (pair >> 16) : (pair & 0xFFFFu));
+                    scl[TM + rr] = __half2float(__ushort_as_half(hbits));
+                }
+            }
+            fence_async_smem();
+            mbar_arrive(bar_full + 8 * s);
+            issue(gb + RAW);
+        }
+        cp_async_wait<0>();
+    } else if (warp == MMA_WARP) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            long long gb = 0;
+            for (; gb < nblocks; ++gb) {
+                const int s = static_cast<int>(gb % S);
+                const int buf = static_cast<int>(gb & 1);
+                if (!wait_bounded(bar_full + 8 * s, static_cast<uint32_t>((gb / S) & 1), abort)) break;
+                if (!wait_bounded(bar_dempty + 8 * buf, static_cast<uint32_t>(((gb >> 1) & 1) ^ 1), abort)) break;
+                tc_fence_after();
+                const uint32_t a0 = sbase + OFF_A + s * A_BYTES, b0 = sbase + OFF_B + s * B_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks)
+                    mma_f16(tmem + buf * DBUF, smem_desc(a0 + ks * 256, 128, 512), smem_desc(b0 + ks * 256, 128, 512),
+                            ks);
+                mma_commit(bar_empty + 8 * s);
+                mma_commit(bar_dfull + 8 * buf);
+            }
+            // every issued MMA has completed before tensor memory is released
+            mma_commit(bar_drain);
+            wait_bounded(bar_drain, 0u, abort);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue
+        const int e = warp - PROD_WARPS;  // 0..EPI_WARPS-1
+        const int q = warp & 3;           // TMEM lane quarter
+        const int c0 = (e >> 2) * EPI_COLS;
+        float acc[EPI_COLS];
+#pragma unroll
+        for (int c = 0; c < EPI_COLS; ++c) acc[c] = 0.f;
+        for (long long gb = 0; gb < nblocks; ++gb) {
+            const int s = static_cast<int>(gb % S);
+            const int buf = static_cast<int>(gb & 1);
+            if (!wait_bounded(bar_dfull + 8 * buf, static_cast<uint32_t>((gb >> 1) & 1), abort)) break;
+            // the staged scales of this block: their phase of `full` is complete (the
+            // stage cannot be refilled before this warp releases it through `empty`)
+            if (!wait_bounded(bar_full + 8 * s, static_cast<uint32_t>((gb / S) & 1), abort)) break;
+            tc_fence_after();
+            int tile, b;
+            block_coords(w, gb, tile, b);
+            const float *scl = reinterpret_cast<const float *>(smem + OFF_SCL + s * SCL_BYTES);
+            const float dxt = scl[q * 32 + lane];
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * DBUF + c0;
+            const int t0 = (tile % w.ntm) * TM, r0 = (tile / w.ntm) * TN;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float d[32];
+                tmem_ld32(taddr + half * 32, d);
+                if (half == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_dempty + 8 * buf);
+                }
+                if (kDumpD) {
+                    const int t = t0 + q * 32 + lane;
+                    if (t < M) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const int r = r0 + c0 + half * 32 + c;
+                            if (r < rows) Dout[(static_cast<size_t>(t) * rows + r) * w.nb + b] = __float2int_rz(d[c]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 wv = *reinterpret_cast<const float4 *>(scl + TM + c0 + half * 32 + c);
+                        const float2 s01 = __fmul2_rn(make_float2(dxt, dxt), make_float2(wv.x, wv.y));
+                        const float2 s23 = __fmul2_rn(make_float2(dxt, dxt), make_float2(wv.z, wv.w));
+                        float2 a01 = __ffma2_rn(s01, make_float2(d[c], d[c + 1]),
+                                                make_float2(acc[half * 32 + c], acc[half * 32 + c + 1]));
+                        float2 a23 = __ffma2_rn(s23, make_float2(d[c + 2], d[c + 3]),
+                                                make_float2(acc[half * 32 + c + 2], acc[half * 32 + c + 3]));
+                        acc[half * 32 + c] = a01.x;
+                        acc[half * 32 + c + 1] = a01.y;
+                        acc[half * 32 + c + 2] = a23.x;
+                        acc[half * 32 + c + 3] = a23.y;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+            if (!kDumpD && b == w.nb - 1) {
+                const int t = t0 + q * 32 + lane;
+                if (t < M) {
+                    float *yrow = Y + static_cast<size_t>(t) * rows + r0 + c0;
+                    const int nvalid = rows - (r0 + c0);
+                    if (nvalid >= EPI_COLS && (rows & 3) == 0) {
+#pragma unroll
+                        for (int c = 0; c < EPI_COLS; c += 4)
+                            *reinterpret_cast<float4 *>(yrow + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < EPI_COLS; ++c)
+                            if (c < nvalid) yrow[c] = acc[c];
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < EPI_COLS; ++c) acc[c] = 0.f;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    pdl_launch_dependents();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+}  // namespace tc
+
+static int launch_tc(bool dump, const void *W, const int8_t *Xq, const float *dx, float *Y, int32_t *D, int rows,
+                     int K, int M, cudaStream_t s)
+{
+    const int nb = K / 32;
+    const uint8_t *nib = static_cast<const uint8_t *>(W);
+    const uint16_t *dsc = reinterpret_cast<const uint16_t *>(nib + static_cast<size_t>(rows) * nb * 16);
+    const int ntiles = ((M + tc::TM - 1) / tc::TM) * ((rows + tc::TN - 1) / tc::TN);
+    auto kern = dump ? tc::k_gemm_q8act_tc<true> : tc::k_gemm_q8act_tc<false>;
+    const int occ = ctas_per_sm(reinterpret_cast<const void *>(kern), tc::NTHREADS, tc::SMEM_BYTES);
+    if (occ <= 0) return GQ_ERR_CUDA;
+    int grid = sm_count();
+    if (grid > ntiles) grid = ntiles;
+    return status_from(launch_pdl(kern, dim3(grid), dim3(tc::NTHREADS), static_cast<size_t>(tc::SMEM_BYTES), s,
+                                  nib, dsc, Xq, dx, Y, D, rows, K, M));
+}
+
+int launch_gemm_q8act_tc(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows, int K, int M,
+                         cudaStream_t s)
+{
+    return launch_tc(false, W, Xq, dx, Y, nullptr, rows, K, M, s);
+}
+
+int launch_block_dots_tc(const void *W, const int8_t *Xq, int32_t *D, int rows, int K, int M, cudaStream_t s)
+{
+    return launch_tc(true, W, Xq, nullptr, nullptr, D, rows, K, M, s);
+}
+
+int read_device_status(bool reset)
+{
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return GQ_ERR_CUDA;
+    if (reset && v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return GQ_ERR_CUDA;
+    }
+    return v;
+}
+
+}  // namespace gq

@@ -57,6 +57,17 @@ inline int ctas_per_sm(const void *kern, int threads, size_t smem)
     return occ;
 }
 
+// Persistent grid: enough CTAs for ntasks warp tasks, at most SMs x resident CTAs.
+inline int persistent_grid(const void *kern, int threads, size_t smem, long long ntasks)
+{
+    const int occ = ctas_per_sm(kern, threads, smem);
+    if (occ <= 0) return -1;
+    const int warps = threads / 32;
+    const long long want = (ntasks + warps - 1) / warps;
+    const long long cap = static_cast<long long>(sm_count()) * occ;
+    return static_cast<int>(want < cap ? want : cap);
+}
+
 // Launch with programmatic stream serialization allowed (the kernel itself
 // calls griddepcontrol.wait before it reads anything a previous kernel wrote).
 template <typename... KArgs, typename... Args>
@@ -83,6 +94,8 @@ struct MatvecGeo {
 };
 
 MatvecGeo choose_matvec_geo(int format, int rows, int nb);
+MatvecGeo choose_logits_geo(int rows, int nb);
+MatvecGeo choose_ffn_geo(int rows, int nb);
 
 int launch_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K, MatvecGeo g,
                        cudaStream_t s);
@@ -102,5 +115,10 @@ int launch_pack(int format, const void *src, void *dst, int rows, int K, bool un
 int launch_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, cudaStream_t s);
 int launch_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows, int K,
                       int M, cudaStream_t s);
+int launch_gemm_q8act_tc(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows, int K,
+                         int M, cudaStream_t s);
+int launch_block_dots_tc(const void *W, const int8_t *Xq, int32_t *D, int rows, int K, int M,
+                         cudaStream_t s);
+int read_device_status(bool reset);
 
 }  // namespace gq

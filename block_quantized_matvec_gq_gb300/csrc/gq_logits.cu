@@ -1,0 +1,205 @@
+// gq_logits.cu -- Q8_0 tied-embedding logits with soft-cap and on-GPU top-k.
+//
+// "Gemma 4 M4 Max kernel roadmap": K1 (logit soft-capping), K2 step 6 (final
+// Q8_0 embedding/output projection and on-GPU top-k reduction), K5 (a
+// pair-valued (value, token) frontier instead of gathering full logits;
+// exact truncation of every merge to k pairs).
+//
+// Phase 1 (k_q8_0_logits_topk): the Q8_0 matvec core; each warp soft-caps
+// its rows' logits, optionally stores them, and keeps the k best (value, row)
+// keys it has seen in a warp-resident sorted list; each CTA then merges its
+// warps' lists and writes k keys to the workspace.
+// Phase 2 (k_topk_merge, one CTA): every key that can still be in the final
+// top k is at least the largest k-th key of any CTA list (that list alone
+// holds k keys above it), so keys below that threshold are skipped before
+// the remaining candidates are merged.
+#include "gq_host.h"
+#include "gq_matvec.cuh"
+
+namespace gq {
+
+// Insert every key of `key` (one per lane; 0 = none) that beats the list's
+// admission threshold; thr never drops below floor_thr.
+__device__ __forceinline__ void offer(WarpTopK &top, unsigned long long &thr, unsigned long long floor_thr,
+                                      unsigned long long key, int k)
+{
+    unsigned int want = __ballot_sync(0xffffffffu, key > thr);
+    while (want) {
+        const int src = __ffs(want) - 1;
+        want &= want - 1;
+        const unsigned long long kk = __shfl_sync(0xffffffffu, key, src);
+        if (kk > thr) {
+            top.insert(kk, k);
+            const unsigned long long t = top.kth(k);
+            thr = t > floor_thr ? t : floor_thr;
+        }
+    }
+}
+
+template <int LG, int R, int U>
+__global__ void __launch_bounds__(kThreadsPerCta, 2)
+    k_q8_0_logits_topk(const uint4 *__restrict__ qb, const uint16_t *__restrict__ dsc,
+                       const float *__restrict__ x, float softcap, int k,
+                       float *__restrict__ logits, unsigned long long *__restrict__ ws, int rows,
+                       int nb)
+{
+    extern __shared__ __align__(16) float xs[];
+    __shared__ unsigned long long cta_keys[kWarpsPerCta * GQ_MAX_TOPK];
+    constexpr int G = 32 / LG, TR = G * R;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane / LG, lp = lane % LG;
+    const int ntasks = (rows + TR - 1) / TR;
+    const bool cap = softcap > 0.f;
+    const int first = blockIdx.x * kWarpsPerCta + warp;
+
+    if (first < ntasks) {
+        const void *rp[TR];
+#pragma unroll
+        for (int i = 0; i < TR; ++i) rp[i] = qb + static_cast<size_t>(min(first * TR + i, rows - 1)) * nb * 2;
+        prefetch_rows_l2<TR>(rp, static_cast<uint32_t>(nb) * 32u, lane);
+    }
+    pdl_wait();
+    stage_x(xs, x, nb * 32);
+    pdl_launch_dependents();
+
+    WarpTopK top;
+    top.init();
+    unsigned long long thr = 0ull;
+
+    for (int task = first; task < ntasks; task += gridDim.x * kWarpsPerCta) {
+        const int r0 = task * TR + g * R;
+        const uint4 *wp[R];
+        const uint16_t *sp[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int r = min(r0 + i, rows - 1);
+            wp[i] = qb + static_cast<size_t>(r) * nb * 2;
+            sp[i] = dsc + static_cast<size_t>(r) * nb;
+        }
+        float out[R];
+        q8_0_stream<LG, R, U>(wp, sp, xs, nb, lp, out);
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            float l = group_sum<LG>(out[i]);
+            const int r = r0 + i;
+            if (cap) l = softcap * tanhf(__fdiv_rn(l, softcap));
+            if (lp == 0 && r < rows && logits != nullptr) logits[r] = l;
+            const unsigned long long key = (lp == 0 && r < rows) ? topk_key(l, static_cast<uint32_t>(r)) : 0ull;
+            offer(top, thr, 0ull, key, k);
+        }
+    }
+
+    // merge the warps' lists (lane j holds entry j in e0 and entry j+32 in e1)
+    for (int j = lane; j < k; j += 32) cta_keys[warp * k + j] = (j < 32) ? top.e0 : top.e1;
+    __syncthreads();
+    if (warp == 0) {
+        top.init();
+        thr = 0ull;
+        for (int base = 0; base < kWarpsPerCta * k; base += 32) {
+            const int j = base + lane;
+            offer(top, thr, 0ull, (j < kWarpsPerCta * k) ? cta_keys[j] : 0ull, k);
+        }
+        if (lane < k) ws[static_cast<size_t>(blockIdx.x) * k + lane] = top.e0;
+        if (lane + 32 < k) ws[static_cast<size_t>(blockIdx.x) * k + lane + 32] = top.e1;
+    }
+}
+
+constexpr int kMergeThreads = 256;
+constexpr int kMergeWarps = kMergeThreads / 32;
+
+__global__ void __launch_bounds__(kMergeThreads)
+    k_topk_merge(const unsigned long long *__restrict__ ws, int nlists, int k, int *__restrict__ idx,
+                 float *__restrict__ val)
+{
+    __shared__ unsigned long long wkeys[kMergeWarps * GQ_MAX_TOPK];
+    __shared__ unsigned long long wmax[kMergeWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    pdl_wait();
+
+    // threshold: the largest k-th key over all lists
+    unsigned long long t = 0ull;
+    for (int c = threadIdx.x; c < nlists; c += kMergeThreads) {
+        const unsigned long long v = ws[static_cast<size_t>(c) * k + (k - 1)];
+        t = v > t ? v : t;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long v = __shfl_xor_sync(0xffffffffu, t, o);
+        t = v > t ? v : t;
+    }
+    if (lane == 0) wmax[warp] = t;
+    __syncthreads();
+    unsigned long long T = 0ull;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) T = wmax[w] > T ? wmax[w] : T;
+    const unsigned long long floor_thr = T > 0ull ? T - 1ull : 0ull;  // admit keys >= T
+
+    WarpTopK top;
+    top.init();
+    unsigned long long thr = floor_thr;
+    const int nkeys = nlists * k;
+    for (int base = warp * 32; base < nkeys; base += kMergeThreads) {
+        const int j = base + lane;
+        offer(top, thr, floor_thr, (j < nkeys) ? ws[j] : 0ull, k);
+    }
+    for (int j = lane; j < k; j += 32) wkeys[warp * k + j] = (j < 32) ? top.e0 : top.e1;
+    __syncthreads();
+    if (warp == 0) {
+        top.init();
+        thr = floor_thr;
+        for (int base = 0; base < kMergeWarps * k; base += 32) {
+            const int j = base + lane;
+            offer(top, thr, floor_thr, (j < kMergeWarps * k) ? wkeys[j] : 0ull, k);
+        }
+        if (lane < k) {
+            idx[lane] = static_cast<int>(key_row(top.e0));
+            val[lane] = key_value(top.e0);
+        }
+        if (lane + 32 < k) {
+            idx[lane + 32] = static_cast<int>(key_row(top.e1));
+            val[lane + 32] = key_value(top.e1);
+        }
+    }
+}
+
+// Upper bound on the CTAs of the logits kernel, fixed so the workspace size
+// depends only on the arguments, not on the GPU.
+constexpr int kLogitsMaxCtas = 2048;
+
+size_t logits_topk_ws_bytes(int rows, int K, int k)
+{
+    (void)K;
+    const long long tasks_ctas = (static_cast<long long>(rows) + 7) / 8;
+    const long long ctas = tasks_ctas < kLogitsMaxCtas ? tasks_ctas : kLogitsMaxCtas;
+    return static_cast<size_t>(ctas) * static_cast<size_t>(k) * sizeof(unsigned long long);
+}
+
+int launch_logits_topk(const void *W, const float *x, float softcap, int k, int *idx, float *val,
+                       float *logits, void *ws, size_t ws_bytes, int rows, int K, MatvecGeo geo,
+                       cudaStream_t s)
+{
+    const int nb = K / 32;
+    const uint4 *qb = static_cast<const uint4 *>(W);
+    const uint16_t *dsc = reinterpret_cast<const uint16_t *>(qb + static_cast<size_t>(rows) * nb * 2);
+    const size_t smem = static_cast<size_t>(K) * sizeof(float);
+    const long long ntasks = (rows + (32 / geo.lg) * geo.r - 1) / ((32 / geo.lg) * geo.r);
+    unsigned long long *keys = static_cast<unsigned long long *>(ws);
+#define CASE(LG, R, U)                                                                                 \
+    {                                                                                                  \
+        auto kern = k_q8_0_logits_topk<LG, R, U>;                                                      \
+        int grid = persistent_grid(reinterpret_cast<const void *>(kern), kThreadsPerCta, smem, ntasks); \
+        if (grid <= 0) return GQ_ERR_SHAPE;                                                            \
+        if (grid > kLogitsMaxCtas) grid = kLogitsMaxCtas;                                              \
+        if (static_cast<size_t>(grid) * k * sizeof(unsigned long long) > ws_bytes) return GQ_ERR_WORKSPACE; \
+        cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, qb, dsc, x, softcap, k, \
+                                   logits, keys, rows, nb);                                            \
+        if (e != cudaSuccess) return GQ_ERR_CUDA;                                                      \
+        e = launch_pdl(k_topk_merge, dim3(1), dim3(kMergeThreads), 0, s,                               \
+                       static_cast<const unsigned long long *>(keys), grid, k, idx, val);              \
+        return status_from(e);                                                                         \
+    }
+    GQ_GEO_SWITCH(geo, CASE);
+#undef CASE
+}
+
+}  // namespace gq

@@ -208,4 +208,59 @@ __device__ __forceinline__ void q4k_stream(const uint4 *const (&wp)[NS], const u
     for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
 }
 
+// ---------------------------------------------------------------- kernel-side common
+constexpr int kThreadsPerCta = 256;
+constexpr int kWarpsPerCta = kThreadsPerCta / 32;
+
+// Before waiting on the previous kernel, ask L2 to fetch the weight rows of
+// this warp's first task (weights never depend on the previous kernel).
+// One lane per row issues a bulk prefetch of the whole row.
+template <int NS>
+__device__ __forceinline__ void prefetch_rows_l2(const void *const (&rowp)[NS], uint32_t row_bytes, int lane)
+{
+#pragma unroll
+    for (int i = 0; i < NS; ++i)
+        if (lane == i) prefetch_l2_bulk(rowp[i], row_bytes);
+}
+
+// GELU, tanh form, with the tanh argument clamped to +-15 (tanh(15) rounds
+// to 1 in f32, so the clamp changes no finite result and keeps it finite).
+__device__ __forceinline__ float gelu_tanh(float a)
+{
+    const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+    float t = k0 * (a + 0.044715f * a * a * a);
+    t = fminf(fmaxf(t, -15.f), 15.f);
+    return 0.5f * a * (1.f + tanhf(t));
+}
+
 }  // namespace gq
+
+// ---------------------------------------------------------------- host-side dispatch
+// Every matvec-family kernel is instantiated for these geometries; the
+// entry points pick one by shape (choose_matvec_geo).
+#define GQ_GEO_CASE1(geo, CASE, LG, R)                                  \
+    if ((geo).lg == LG && (geo).r == R && (geo).u == 2) { CASE(LG, R, 2); } \
+    if ((geo).lg == LG && (geo).r == R && (geo).u == 4) { CASE(LG, R, 4); }
+#define GQ_GEO_SWITCH(geo, CASE)              \
+    do {                                      \
+        GQ_GEO_CASE1(geo, CASE, 32, 1)        \
+        GQ_GEO_CASE1(geo, CASE, 32, 2)        \
+        GQ_GEO_CASE1(geo, CASE, 32, 4)        \
+        GQ_GEO_CASE1(geo, CASE, 16, 1)        \
+        GQ_GEO_CASE1(geo, CASE, 16, 2)        \
+        GQ_GEO_CASE1(geo, CASE, 16, 4)        \
+        GQ_GEO_CASE1(geo, CASE, 8, 1)         \
+        GQ_GEO_CASE1(geo, CASE, 8, 2)         \
+        GQ_GEO_CASE1(geo, CASE, 8, 4)         \
+        return GQ_ERR_SHAPE;                  \
+    } while (0)
+#define GQ_GEO_SWITCH_R12(geo, CASE)          \
+    do {                                      \
+        GQ_GEO_CASE1(geo, CASE, 32, 1)        \
+        GQ_GEO_CASE1(geo, CASE, 32, 2)        \
+        GQ_GEO_CASE1(geo, CASE, 16, 1)        \
+        GQ_GEO_CASE1(geo, CASE, 16, 2)        \
+        GQ_GEO_CASE1(geo, CASE, 8, 1)         \
+        GQ_GEO_CASE1(geo, CASE, 8, 2)         \
+        return GQ_ERR_SHAPE;                  \
+    } while (0)

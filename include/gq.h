@@ -171,6 +171,20 @@ int gq_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, gq_str
 int gq_q4_0_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows,
                        int K, int M, gq_stream_t stream);
 
+/* The integer block dot products of the same contraction, as the tensor-core
+ * path computes them: D int32[M][rows][K/32] (D[t][r][b] above), exact.
+ * Meant for checking small problems (the output is M*rows*K/32 words). */
+int gq_q4_0_gemm_block_dots(const void *W, const int8_t *Xq, int32_t *D, int rows, int K, int M,
+                            gq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Device status: GQ_ERR_TIMEOUT if a kernel launched since the last reset
+ * gave up one of its bounded in-kernel waits (its outputs are then invalid),
+ * else GQ_OK; GQ_ERR_CUDA if the status cannot be read.  This call
+ * SYNCHRONIZES with the device.  reset != 0 clears the status.
+ * ------------------------------------------------------------------------ */
+int gq_device_status(int reset);
+
 #ifdef __cplusplus
 }
 #endif

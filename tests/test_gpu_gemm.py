@@ -83,3 +83,38 @@ def test_gemm_all_eight_weights_exact_zero():
     Xq, dx = oracle.quantize_q8_0(X, M, K)
     Y = run_gemm(W, Xq, dx, rows, K, M)
     assert np.all(Y == 0.0)
+
+
+@pytest.mark.parametrize("M,rows,K", [(1, 1, 32), (128, 192, 64), (130, 200, 96), (37, 385, 256)])
+def test_tensor_core_block_dots_are_bit_exact(M, rows, K):
+    """The integer block dot products computed on the tensor cores (f16
+    operands holding exact small integers, f32 accumulation) equal the int32
+    brute force exactly."""
+    t = torch()
+    W = synth.q4_0_weights(rows, K, synth.stream(700 + M, rows))
+    Xq = np.random.default_rng(M + rows).integers(-127, 128, size=(M, K)).astype(np.int8)
+    Xq[0, :32] = 127
+    Xq[-1, -32:] = -127
+    Wp = packed(oracle.FORMAT_Q4_0, W, rows, K)
+    D = t.full((M, rows, K // 32), -999999, dtype=t.int32, device="cuda")
+    gq.gq_q4_0_gemm_block_dots(Wp, dev(Xq), D, rows, K, M)
+    t.cuda.synchronize()
+    assert gq.gq_device_status() == gq.GQ_OK
+    ref = oracle.block_dots(W, Xq, rows, K, M, 0, M, 0, rows)
+    assert np.array_equal(D.cpu().numpy(), ref)
+
+
+def test_gemm_extreme_block_dots_exact():
+    """All-15 nibbles against all-127 codes: the largest block dot (32 * 7 * 127)."""
+    import blockenc as be
+    rows, K, M = 5, 64, 3
+    W = be.rows_from_blocks([[be.enc_q4_0(np.full(32, 15), 1.0), be.enc_q4_0(np.zeros(32, int), 1.0)]] * rows)
+    Xq = np.full((M, K), 127, np.int8)
+    Xq[1] = -127
+    t = torch()
+    D = t.empty((M, rows, 2), dtype=t.int32, device="cuda")
+    gq.gq_q4_0_gemm_block_dots(packed(oracle.FORMAT_Q4_0, W, rows, K), dev(Xq), D, rows, K, M)
+    t.cuda.synchronize()
+    got = D.cpu().numpy()
+    assert np.all(got[0, :, 0] == 32 * 7 * 127) and np.all(got[0, :, 1] == -32 * 8 * 127)
+    assert np.all(got[1, :, 0] == -32 * 7 * 127) and np.all(got[1, :, 1] == 32 * 8 * 127)
