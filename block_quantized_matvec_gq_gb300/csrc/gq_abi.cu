@@ -87,7 +87,7 @@ int gq_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K, int
 {
     int st = check_matvec(GQ_FORMAT_Q4_0, W, x, y, rows, K, M);
     if (st != GQ_OK) return st;
-    return launch_q4_0_matvec(W, x, y, rows, K, choose_matvec_geo(GQ_FORMAT_Q4_0, rows, K / 32),
+    return launch_q4_0_matvec(W, x, y, rows, K, choose_matvec_geo(GQ_FORMAT_Q4_0, rows, K / 32, aligned32(W)),
                               reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -96,7 +96,7 @@ int gq_q8_0_matvec(const void *W, const float *x, float *y, int rows, int K, int
     int st = check_matvec(GQ_FORMAT_Q8_0, W, x, y, rows, K, M);
     if (st != GQ_OK) return st;
     if (!aligned32(W)) return GQ_ERR_ALIGN;  // 32-byte weight loads
-    return launch_q8_0_matvec(W, x, y, rows, K, choose_matvec_geo(GQ_FORMAT_Q8_0, rows, K / 32),
+    return launch_q8_0_matvec(W, x, y, rows, K, choose_matvec_geo(GQ_FORMAT_Q8_0, rows, K / 32, false),
                               reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -104,7 +104,7 @@ int gq_q4k_matvec(const void *W, const float *x, float *y, int rows, int K, int 
 {
     int st = check_matvec(GQ_FORMAT_Q4_K, W, x, y, rows, K, M);
     if (st != GQ_OK) return st;
-    return launch_q4k_matvec(W, x, y, rows, K, choose_matvec_geo(GQ_FORMAT_Q4_K, rows, K / 32),
+    return launch_q4k_matvec(W, x, y, rows, K, choose_matvec_geo(GQ_FORMAT_Q4_K, rows, K / 32, aligned32(W)),
                              reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -115,7 +115,7 @@ int gq_ffn_gate_up_gelu(const void *W_gate, const void *W_up, const float *x, fl
     if (!aligned16(W_up)) return GQ_ERR_ALIGN;
     int st = check_matvec(GQ_FORMAT_Q4_0, W_gate, x, h, rows, K, M);
     if (st != GQ_OK) return st;
-    return launch_ffn_gate_up(W_gate, W_up, x, h, rows, K, choose_ffn_geo(rows, K / 32),
+    return launch_ffn_gate_up(W_gate, W_up, x, h, rows, K, choose_ffn_geo(rows, K / 32, aligned32(W_gate) && aligned32(W_up)),
                               reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -11,7 +11,7 @@
 
 namespace gq {
 
-template <int LG, int R, int U>
+template <int LG, int R, int U, int P>
 __global__ void __launch_bounds__(kThreadsPerCta, 2)
     k_ffn_gate_up(const uint4 *__restrict__ gnib, const uint16_t *__restrict__ gsc,
                   const uint4 *__restrict__ unib, const uint16_t *__restrict__ usc,
@@ -51,7 +51,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
             sp[R + i] = usc + static_cast<size_t>(r) * nb;
         }
         float out[2 * R];
-        q4_0_stream<LG, 2 * R, U>(wp, sp, xs, nb, lp, out);
+        if (P == 2)
+            q4_0_stream2<LG, 2 * R, U>(wp, sp, xs, nb, lp, out);
+        else
+            q4_0_stream<LG, 2 * R, U>(wp, sp, xs, nb, lp, out);
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             const float gv = group_sum<LG>(out[i]);
@@ -73,12 +76,18 @@ int launch_ffn_gate_up(const void *Wg, const void *Wu, const float *x, float *h,
     const long long ntasks = (rows + (32 / geo.lg) * geo.r - 1) / ((32 / geo.lg) * geo.r);
 #define CASE(LG, R, U)                                                                                 \
     {                                                                                                  \
-        auto kern = k_ffn_gate_up<LG, R, U>;                                                           \
+        auto kern = k_ffn_gate_up<LG, R, U, PP>;                                                       \
         const int grid = persistent_grid(reinterpret_cast<const void *>(kern), kThreadsPerCta, smem, ntasks); \
         if (grid <= 0) return GQ_ERR_SHAPE;                                                            \
         return status_from(launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, gn, gs, un, us, x, h, rows, nb)); \
     }
-    GQ_GEO_SWITCH_R12(geo, CASE);
+    if (geo.p == 2) {
+        constexpr int PP = 2;
+        GQ_PAIR_SWITCH(geo, CASE);
+    } else {
+        constexpr int PP = 1;
+        GQ_GEO_SWITCH_R12(geo, CASE);
+    }
 #undef CASE
 }
 

@@ -9,65 +9,69 @@
 //
 // On sm_103a the int8 form of tcgen05.mma is not available, so both
 // operands are fed as f16: q_w - 8 in [-8, 7] and Xq in [-127, 127] are
-// exact in f16, every partial sum of a 32-term block dot is an integer of
-// magnitude <= 32 * 8 * 127 = 32512 < 2^24, so the f32 accumulator in
+// exact in f16, and every partial sum of a 32-term block dot is an integer
+// of magnitude <= 32 * 8 * 127 = 32512 < 2^24, so the f32 accumulator in
 // tensor memory holds D exactly.  Because the scales change every 32
 // elements, each block's D is read out of tensor memory and folded into the
-// f32 result by the epilogue warps (Y += dx * d_w * D) while the tensor core
-// already computes the next block into the other D buffer.
+// f32 result (Y += dx * d_w * D) while the tensor core already computes the
+// next block into the other D buffer.
 //
-// CTA (512 threads, one per SM, persistent over 128-token x 192-row tiles):
-//   warps 0-2   producers: cp.async the packed codes and scales of each
-//               32-block into a raw ring, convert them to f16 in the UMMA
-//               K-major no-swizzle layout, signal `full`;
-//   warps 3-14  epilogue: warp w owns TMEM lanes 32*(w%4).. and 64 columns;
-//   warp 15     MMA: one elected lane issues 2 x (M128 N192 K16) per block.
+// CTA: 512 threads, one per SM, persistent over 128-token x 192-row tiles.
+//   warps 0-11  workers.  For block g: wait for its D, tcgen05.ld it (warp w
+//               owns TMEM lanes 32*(w%4).. and 64 of the 192 columns), fold it
+//               into the f32 accumulators, release the D buffer; then convert
+//               block g+S from the raw TMA tiles into the f16 UMMA operand
+//               layout (the stage the MMA of block g has just finished with)
+//               and stage its scales.
+//   warp 12     one lane issues the TMA tile loads (int8 codes 128 x 32 B,
+//               nibbles 192 x 16 B per block) into an RAW-deep ring.
+//   warp 13     one lane issues 2 x (M128 N192 K16) MMAs per block; the warp
+//               owns the TMEM allocation.
 // Every mbarrier wait is bounded: on timeout the kernel records
-// GQ_ERR_TIMEOUT in a device flag, the other roles leave their loops, TMEM
+// GQ_ERR_TIMEOUT in the device status word, every role leaves its loop, TMEM
 // is released and the kernel returns.
+#include <cuda.h>
+
 #include "gq_host.h"
 #include "gq_internal.cuh"
 
 namespace gq {
-
-__device__ int g_device_status = 0;
-
 namespace tc {
 
 constexpr int TM = 128;  // tokens per tile (MMA M, TMEM lanes)
 constexpr int TN = 192;  // weight rows per tile (MMA N, TMEM columns)
 constexpr int KB = 32;   // K per quantization block
-constexpr int S = 4;     // converted operand stages
-constexpr int RAW = 8;   // raw packed-data stages (cp.async ring)
-constexpr int PROD_WARPS = 3;
-constexpr int EPI_WARPS = 12;
-constexpr int MMA_WARP = PROD_WARPS + EPI_WARPS;
-constexpr int NWARPS = MMA_WARP + 1;
-constexpr int NTHREADS = NWARPS * 32;
-constexpr int NPROD = PROD_WARPS * 32;
-constexpr int EPI_COLS = TN / (EPI_WARPS / 4);  // 64
+constexpr int S = 4;     // f16 operand stages
+constexpr int SR = 2 * S;  // scale stages
+constexpr int RAW = 8;   // raw TMA stages
+constexpr int WORK_WARPS = 12;
+constexpr int NWORK = WORK_WARPS * 32;
+constexpr int TMA_WARP = 12;
+constexpr int MMA_WARP = 13;
+constexpr int NTHREADS = 512;
+constexpr int EPI_COLS = TN / (WORK_WARPS / 4);  // 64
 constexpr int TMEM_COLS = 512;
 constexpr int DBUF = 256;  // TMEM column offset of the second D buffer
 
-constexpr int A_BYTES = TM * KB * 2;  // 8192
-constexpr int B_BYTES = TN * KB * 2;  // 12288
-constexpr int RA_BYTES = TM * KB;     // 4096: int8 codes
-constexpr int RB_BYTES = TN * 16;     // 3072: nibbles
-constexpr int RX_BYTES = TM * 4;      // 512: f32 dx
-constexpr int RW_BYTES = TN * 4;      // 768: aligned fp16 pairs holding d_w
-constexpr int RAW_BYTES = RA_BYTES + RB_BYTES + RX_BYTES + RW_BYTES;
+constexpr int A_BYTES = TM * KB * 2;  // 8192: f16 operand A
+constexpr int B_BYTES = TN * KB * 2;  // 12288: f16 operand B
+constexpr int RA_BYTES = TM * KB;     // 4096: int8 codes (TMA box 32 x 128)
+constexpr int RB_BYTES = TN * 16;     // 3072: nibbles (TMA box 16 x 192)
+constexpr int RAW_BYTES = RA_BYTES + RB_BYTES;
 constexpr int SCL_BYTES = (TM + TN) * 4;
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + S * A_BYTES;
 constexpr int OFF_RAW = OFF_B + S * B_BYTES;
 constexpr int OFF_SCL = OFF_RAW + RAW * RAW_BYTES;
-constexpr int OFF_BAR = OFF_SCL + S * SCL_BYTES;
-constexpr int N_BARS = 2 * S + 4 + 1;  // full[S], empty[S], dfull[2], dempty[2], drain
+constexpr int OFF_BAR = OFF_SCL + SR * SCL_BYTES;
+constexpr int N_BARS = 2 * RAW + S + 4 + 1;  // raw_full, raw_empty, full, dfull[2], dempty[2], drain
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16;
 
-static_assert(OFF_B % 1024 == 0 && OFF_RAW % 16 == 0 && OFF_SCL % 16 == 0 && OFF_BAR % 8 == 0, "align");
+static_assert(OFF_B % 1024 == 0 && OFF_RAW % 1024 == 0 && RAW_BYTES % 1024 == 0 && OFF_SCL % 16 == 0 &&
+                  OFF_BAR % 8 == 0,
+              "alignment");
 
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -81,6 +85,11 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
@@ -102,40 +111,37 @@ __device__ __forceinline__ uint64_t globaltimer()
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 
 // Bounded wait for the phase of `bar` with the given parity.  Returns false
-// (and raises the CTA abort flag and the device status) on timeout, or when
+// (raising the CTA abort flag and the device status) on timeout, or when
 // another role has already aborted.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort)
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort, int *status)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0u) {
+        if ((i & 63u) == 0u) {
             if (*abort) return false;
             if (globaltimer() - t0 > kWaitLimitNs) {
                 *abort = 1;
-                atomicExch(&g_device_status, GQ_ERR_TIMEOUT);
+                atomicExch(status, GQ_ERR_TIMEOUT);
                 return false;
             }
         }
     }
 }
+// Warp-uniform form (all lanes agree).
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort, int *status)
+{
+    return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort, status));
+}
 
-__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, bool valid)
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar)
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async4_zfill(uint32_t dst, const void *src, bool valid)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait()
-{
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -167,21 +173,18 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
-// 32 consecutive f32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+// 16 consecutive f32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
 {
-    uint32_t r[32];
+    uint32_t r[16];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // ---------------------------------------------------------------- operand conversion
@@ -192,7 +195,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
 __device__ __forceinline__ uint4 nib8_to_f16(uint32_t w)
 {
     const uint32_t w2 = w >> 8;
-    __half2 h0 = __halves2half2(__ushort_as_half(0), __ushort_as_half(0));
     uint32_t a0 = (w & 0x000F000Fu) | 0x64006400u;   // 1024 + (e0, e4)
     uint32_t a1 = (w & 0x00F000F0u) | 0x64006400u;   // 1024 + 16 (e1, e5)
     uint32_t a2 = (w2 & 0x000F000Fu) | 0x64006400u;  // 1024 + (e2, e6)
@@ -204,7 +206,6 @@ __device__ __forceinline__ uint4 nib8_to_f16(uint32_t w)
     __half2 r1 = __hfma2(*reinterpret_cast<__half2 *>(&a1), c16, c72);
     __half2 r2 = __hsub2(*reinterpret_cast<__half2 *>(&a2), c1032);
     __half2 r3 = __hfma2(*reinterpret_cast<__half2 *>(&a3), c16, c72);
-    (void)h0;
     uint4 o;
     o.x = *reinterpret_cast<uint32_t *>(&r0);
     o.y = *reinterpret_cast<uint32_t *>(&r1);
@@ -244,27 +245,64 @@ struct Work {
 };
 
 // Block gb (running index over this CTA's tiles and their K blocks) -> tile, b.
-__device__ __forceinline__ bool block_coords(const Work &w, long long gb, int &tile, int &b)
+__device__ __forceinline__ void block_coords(const Work &w, long long gb, int &tile, int &b)
 {
     const long long it = gb / w.nb;
     b = static_cast<int>(gb - it * w.nb);
-    const long long t = blockIdx.x + it * static_cast<long long>(gridDim.x);
-    tile = static_cast<int>(t);
-    return t < w.ntiles;
+    tile = static_cast<int>(blockIdx.x + it * static_cast<long long>(gridDim.x));
+}
+
+// Scales of block gb for this worker thread: thread i < TM loads dx of token i,
+// TM <= i < TM + TN loads d_w of row i - TM (0 for rows/tokens past the end).
+__device__ __forceinline__ float load_scale(const Work &w, long long gb, int i, const uint16_t *dsc, const float *dx,
+                                            int rows, int M)
+{
+    int tile, b;
+    block_coords(w, gb, tile, b);
+    const int t0 = (tile % w.ntm) * TM, r0 = (tile / w.ntm) * TN;
+    if (i < TM) {
+        const int t = t0 + i;
+        return (t < M && dx != nullptr) ? __ldg(dx + static_cast<size_t>(t) * w.nb + b) : 0.f;
+    }
+    if (i < TM + TN) {
+        const int r = r0 + i - TM;
+        return (r < rows) ? __half2float(__ushort_as_half(__ldg(dsc + static_cast<size_t>(r) * w.nb + b))) : 0.f;
+    }
+    return 0.f;
+}
+
+// Convert raw block (codes, nibbles) into the f16 operand stage.
+__device__ __forceinline__ void convert_block(const uint8_t *raw, uint8_t *opA, uint8_t *opB, int tid)
+{
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = tid + k * NWORK;
+        if (i < TM * 4) {
+            const int row = i % TM, kg = i / TM;
+            const uint2 v = *reinterpret_cast<const uint2 *>(raw + row * 32 + kg * 8);
+            *reinterpret_cast<uint4 *>(opA + op_off(row, kg)) = s8x8_to_f16(v.x, v.y);
+        } else if (i < TM * 4 + TN * 4) {
+            const int j = i - TM * 4;
+            const int row = j % TN, kg = j / TN;
+            const uint32_t v = *reinterpret_cast<const uint32_t *>(raw + RA_BYTES + row * 16 + kg * 4);
+            *reinterpret_cast<uint4 *>(opB + op_off(row, kg)) = nib8_to_f16(v);
+        }
+    }
 }
 
 // ---------------------------------------------------------------- the kernel
 template <bool kDumpD>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    k_gemm_q8act_tc(const uint8_t *__restrict__ nib, const uint16_t *__restrict__ dsc,
-                    const int8_t *__restrict__ Xq, const float *__restrict__ dx, float *__restrict__ Y,
-                    int32_t *__restrict__ Dout, int rows, int K, int M)
+    k_gemm_q8act_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                    const uint16_t *__restrict__ dsc, const float *__restrict__ dx, float *__restrict__ Y,
+                    int32_t *__restrict__ Dout, int rows, int K, int M, int *__restrict__ status)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_full = sbase + OFF_BAR, bar_empty = bar_full + 8 * S;
-    const uint32_t bar_dfull = bar_empty + 8 * S, bar_dempty = bar_dfull + 16, bar_drain = bar_dempty + 16;
+    const uint32_t bar_rfull = sbase + OFF_BAR, bar_rempty = bar_rfull + 8 * RAW;
+    const uint32_t bar_full = bar_rempty + 8 * RAW, bar_dfull = bar_full + 8 * S;
+    const uint32_t bar_dempty = bar_dfull + 16, bar_drain = bar_dempty + 16;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
@@ -278,13 +316,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const long long nblocks = static_cast<long long>(my_tiles) * w.nb;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(bar_full + 8 * s, NPROD);
-            mbar_init(bar_empty + 8 * s, 1 + EPI_WARPS);
+        for (int i = 0; i < RAW; ++i) {
+            mbar_init(bar_rfull + 8 * i, 1);
+            mbar_init(bar_rempty + 8 * i, WORK_WARPS);
         }
+        for (int s = 0; s < S; ++s) mbar_init(bar_full + 8 * s, WORK_WARPS);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_dfull + 8 * b, 1);
-            mbar_init(bar_dempty + 8 * b, EPI_WARPS);
+            mbar_init(bar_dempty + 8 * b, WORK_WARPS);
         }
         mbar_init(bar_drain, 1);
         *abort = 0;
@@ -302,133 +341,94 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t tmem = *tmem_slot;
     pdl_wait();
 
-    if (warp < PROD_WARPS) {
-        // ------------------------------------------------ producers
-        const int p = threadIdx.x;  // 0..NPROD-1
-        auto issue = [&](long long gb) {
-            int tile, b;
-            const uint32_t raw = sbase + OFF_RAW + static_cast<uint32_t>(gb % RAW) * RAW_BYTES;
-            if (gb < nblocks && block_coords(w, gb, tile, b)) {
+    if (warp == TMA_WARP) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            for (long long gb = 0; gb < nblocks; ++gb) {
+                const int rs = static_cast<int>(gb % RAW);
+                if (!wait_bounded(bar_rempty + 8 * rs, static_cast<uint32_t>(((gb / RAW) & 1) ^ 1), abort, status))
+                    break;
+                int tile, b;
+                block_coords(w, gb, tile, b);
                 const int t0 = (tile % w.ntm) * TM, r0 = (tile / w.ntm) * TN;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int tt = p + h * NPROD;
-                    if (tt < TM) {
-                        const int t = t0 + tt;
-                        const bool tv = t < M;
-                        const int8_t *xs = Xq + static_cast<size_t>(tv ? t : 0) * K + b * KB;
-                        cp_async16_zfill(raw + tt * 32, xs, tv);
-                        cp_async16_zfill(raw + tt * 32 + 16, xs + 16, tv);
-                        const bool xv = tv && dx != nullptr;  // the block-dot dump reads no scales
-                        cp_async4_zfill(raw + RA_BYTES + RB_BYTES + tt * 4,
-                                        xv ? static_cast<const void *>(dx + static_cast<size_t>(t) * w.nb + b)
-                                           : static_cast<const void *>(Xq),
-                                        xv);
-                    }
-                    const int rr = p + h * NPROD;
-                    if (rr < TN) {
-                        const int r = r0 + rr;
-                        const bool rv = r < rows;
-                        const size_t e = static_cast<size_t>(rv ? r : 0) * w.nb + b;
-                        cp_async16_zfill(raw + RA_BYTES + rr * 16, nib + e * 16, rv);
-                        cp_async4_zfill(raw + RA_BYTES + RB_BYTES + RX_BYTES + rr * 4, dsc + (e & ~static_cast<size_t>(1)), rv);
-                    }
-                }
+                const uint32_t raw = sbase + OFF_RAW + rs * RAW_BYTES;
+                mbar_expect_tx(bar_rfull + 8 * rs, RAW_BYTES);
+                tma_load_2d(raw, &mapA, b * KB, t0, bar_rfull + 8 * rs);
+                tma_load_2d(raw + RA_BYTES, &mapB, b * 16, r0, bar_rfull + 8 * rs);
             }
-            cp_async_commit();
-        };
-        for (int j = 0; j < RAW; ++j) issue(j);
-        for (long long gb = 0; gb < nblocks; ++gb) {
-            const int s = static_cast<int>(gb % S);
-            cp_async_wait<RAW - 1>();
-            if (!wait_bounded(bar_empty + 8 * s, static_cast<uint32_t>(((gb / S) & 1) ^ 1), abort)) break;
-            int tile, b;
-            block_coords(w, gb, tile, b);
-            const int r0 = (tile / w.ntm) * TN;
-            const uint8_t *raw = smem + OFF_RAW + (gb % RAW) * RAW_BYTES;
-            uint8_t *opA = smem + OFF_A + s * A_BYTES;
-            uint8_t *opB = smem + OFF_B + s * B_BYTES;
-            float *scl = reinterpret_cast<float *>(smem + OFF_SCL + s * SCL_BYTES);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int tt = p + h * NPROD;
-                if (tt < TM) {
-                    const uint4 q0 = *reinterpret_cast<const uint4 *>(raw + tt * 32);
-                    const uint4 q1 = *reinterpret_cast<const uint4 *>(raw + tt * 32 + 16);
-                    *reinterpret_cast<uint4 *>(opA + op_off(tt, 0)) = s8x8_to_f16(q0.x, q0.y);
-                    *reinterpret_cast<uint4 *>(opA + op_off(tt, 1)) = s8x8_to_f16(q0.z, q0.w);
-                    *reinterpret_cast<uint4 *>(opA + op_off(tt, 2)) = s8x8_to_f16(q1.x, q1.y);
-                    *reinterpret_cast<uint4 *>(opA + op_off(tt, 3)) = s8x8_to_f16(q1.z, q1.w);
-                    scl[tt] = *reinterpret_cast<const float *>(raw + RA_BYTES + RB_BYTES + tt * 4);
-                }
-                const int rr = p + h * NPROD;
-                if (rr < TN) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(raw + RA_BYTES + rr * 16);
-                    *reinterpret_cast<uint4 *>(opB + op_off(rr, 0)) = nib8_to_f16(v.x);
-                    *reinterpret_cast<uint4 *>(opB + op_off(rr, 1)) = nib8_to_f16(v.y);
-                    *reinterpret_cast<uint4 *>(opB + op_off(rr, 2)) = nib8_to_f16(v.z);
-                    *reinterpret_cast<uint4 *>(opB + op_off(rr, 3)) = nib8_to_f16(v.w);
-                    const uint32_t pair = *reinterpret_cast<const uint32_t *>(raw + RA_BYTES + RB_BYTES + RX_BYTES + rr * 4);
-                    const size_t e = static_cast<size_t>(r0 + rr) * w.nb + b;
-                    const uint16_t hbits = static_cast<uint16_t>((e & 1) ? (pair >> 16) : (pair & 0xFFFFu));
-                    scl[TM + rr] = __half2float(__ushort_as_half(hbits));
-                }
-            }
-            fence_async_smem();
-            mbar_arrive(bar_full + 8 * s);
-            issue(gb + RAW);
+            // No tile load may still be landing in shared memory when the CTA exits
+            // (relevant only after an abort: normally every load has been consumed).
+            volatile int no_abort = 0;
+            for (long long gb = (nblocks > RAW ? nblocks - RAW : 0); gb < nblocks; ++gb)
+                wait_bounded(bar_rfull + 8 * static_cast<int>(gb % RAW), static_cast<uint32_t>((gb / RAW) & 1),
+                             &no_abort, status);
         }
-        cp_async_wait<0>();
+        __syncwarp();
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            long long gb = 0;
-            for (; gb < nblocks; ++gb) {
+            for (long long gb = 0; gb < nblocks; ++gb) {
                 const int s = static_cast<int>(gb % S);
                 const int buf = static_cast<int>(gb & 1);
-                if (!wait_bounded(bar_full + 8 * s, static_cast<uint32_t>((gb / S) & 1), abort)) break;
-                if (!wait_bounded(bar_dempty + 8 * buf, static_cast<uint32_t>(((gb >> 1) & 1) ^ 1), abort)) break;
+                if (!wait_bounded(bar_full + 8 * s, static_cast<uint32_t>((gb / S) & 1), abort, status)) break;
+                if (!wait_bounded(bar_dempty + 8 * buf, static_cast<uint32_t>(((gb >> 1) & 1) ^ 1), abort, status))
+                    break;
                 tc_fence_after();
                 const uint32_t a0 = sbase + OFF_A + s * A_BYTES, b0 = sbase + OFF_B + s * B_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks)
                     mma_f16(tmem + buf * DBUF, smem_desc(a0 + ks * 256, 128, 512), smem_desc(b0 + ks * 256, 128, 512),
                             ks);
-                mma_commit(bar_empty + 8 * s);
                 mma_commit(bar_dfull + 8 * buf);
             }
             // every issued MMA has completed before tensor memory is released
             mma_commit(bar_drain);
-            wait_bounded(bar_drain, 0u, abort);
+            wait_bounded(bar_drain, 0u, abort, status);
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------ epilogue
-        const int e = warp - PROD_WARPS;  // 0..EPI_WARPS-1
-        const int q = warp & 3;           // TMEM lane quarter
-        const int c0 = (e >> 2) * EPI_COLS;
+    } else if (warp < WORK_WARPS) {
+        // ------------------------------------------------ workers
+        const int tid = threadIdx.x;  // 0..NWORK-1
+        const int q = warp & 3;       // TMEM lane quarter
+        const int c0 = (warp >> 2) * EPI_COLS;
+        bool ok = true;
+        // stage blocks 0..S-1
+        for (long long gb = 0; gb < S && gb < nblocks && ok; ++gb) {
+            const int rs = static_cast<int>(gb % RAW);
+            const float sv = load_scale(w, gb, tid, dsc, dx, rows, M);
+            ok = wait_warp(bar_rfull + 8 * rs, static_cast<uint32_t>((gb / RAW) & 1), abort, status);
+            if (!ok) break;
+            convert_block(smem + OFF_RAW + rs * RAW_BYTES, smem + OFF_A + (gb % S) * A_BYTES,
+                          smem + OFF_B + (gb % S) * B_BYTES, tid);
+            if (tid < TM + TN) reinterpret_cast<float *>(smem + OFF_SCL + (gb % SR) * SCL_BYTES)[tid] = sv;
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar_full + 8 * (gb % S));
+                mbar_arrive(bar_rempty + 8 * rs);
+            }
+        }
         float acc[EPI_COLS];
 #pragma unroll
         for (int c = 0; c < EPI_COLS; ++c) acc[c] = 0.f;
-        for (long long gb = 0; gb < nblocks; ++gb) {
-            const int s = static_cast<int>(gb % S);
+        for (long long gb = 0; gb < nblocks && ok; ++gb) {
             const int buf = static_cast<int>(gb & 1);
-            if (!wait_bounded(bar_dfull + 8 * buf, static_cast<uint32_t>((gb >> 1) & 1), abort)) break;
-            // the staged scales of this block: their phase of `full` is complete (the
-            // stage cannot be refilled before this warp releases it through `empty`)
-            if (!wait_bounded(bar_full + 8 * s, static_cast<uint32_t>((gb / S) & 1), abort)) break;
+            const long long gn = gb + S;  // block converted in this iteration
+            const float sv = (gn < nblocks) ? load_scale(w, gn, tid, dsc, dx, rows, M) : 0.f;
+            ok = wait_warp(bar_dfull + 8 * buf, static_cast<uint32_t>((gb >> 1) & 1), abort, status);
+            if (!ok) break;
             tc_fence_after();
             int tile, b;
             block_coords(w, gb, tile, b);
-            const float *scl = reinterpret_cast<const float *>(smem + OFF_SCL + s * SCL_BYTES);
+            const int t0 = (tile % w.ntm) * TM, r0 = (tile / w.ntm) * TN;
+            const float *scl = reinterpret_cast<const float *>(smem + OFF_SCL + (gb % SR) * SCL_BYTES);
             const float dxt = scl[q * 32 + lane];
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * DBUF + c0;
-            const int t0 = (tile % w.ntm) * TM, r0 = (tile / w.ntm) * TN;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float d[32];
-                tmem_ld32(taddr + half * 32, d);
-                if (half == 1) {
+            for (int part = 0; part < EPI_COLS / 16; ++part) {
+                float d[16];
+                tmem_ld16(taddr + part * 16, d);
+                if (part == EPI_COLS / 16 - 1) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_dempty + 8 * buf);
@@ -437,30 +437,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int t = t0 + q * 32 + lane;
                     if (t < M) {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            const int r = r0 + c0 + half * 32 + c;
+                        for (int c = 0; c < 16; ++c) {
+                            const int r = r0 + c0 + part * 16 + c;
                             if (r < rows) Dout[(static_cast<size_t>(t) * rows + r) * w.nb + b] = __float2int_rz(d[c]);
                         }
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 32; c += 4) {
-                        const float4 wv = *reinterpret_cast<const float4 *>(scl + TM + c0 + half * 32 + c);
+                    for (int c = 0; c < 16; c += 4) {
+                        const int cc = part * 16 + c;
+                        const float4 wv = *reinterpret_cast<const float4 *>(scl + TM + c0 + cc);
                         const float2 s01 = __fmul2_rn(make_float2(dxt, dxt), make_float2(wv.x, wv.y));
                         const float2 s23 = __fmul2_rn(make_float2(dxt, dxt), make_float2(wv.z, wv.w));
-                        float2 a01 = __ffma2_rn(s01, make_float2(d[c], d[c + 1]),
-                                                make_float2(acc[half * 32 + c], acc[half * 32 + c + 1]));
-                        float2 a23 = __ffma2_rn(s23, make_float2(d[c + 2], d[c + 3]),
-                                                make_float2(acc[half * 32 + c + 2], acc[half * 32 + c + 3]));
-                        acc[half * 32 + c] = a01.x;
-                        acc[half * 32 + c + 1] = a01.y;
-                        acc[half * 32 + c + 2] = a23.x;
-                        acc[half * 32 + c + 3] = a23.y;
+                        float2 a01 = __ffma2_rn(s01, make_float2(d[c], d[c + 1]), make_float2(acc[cc], acc[cc + 1]));
+                        float2 a23 = __ffma2_rn(s23, make_float2(d[c + 2], d[c + 3]), make_float2(acc[cc + 2], acc[cc + 3]));
+                        acc[cc] = a01.x;
+                        acc[cc + 1] = a01.y;
+                        acc[cc + 2] = a23.x;
+                        acc[cc + 3] = a23.y;
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
             if (!kDumpD && b == w.nb - 1) {
                 const int t = t0 + q * 32 + lane;
                 if (t < M) {
@@ -479,6 +476,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int c = 0; c < EPI_COLS; ++c) acc[c] = 0.f;
             }
+            // convert block gb + S into the stage the MMA of block gb has finished with
+            if (gn < nblocks) {
+                const int rs = static_cast<int>(gn % RAW);
+                ok = wait_warp(bar_rfull + 8 * rs, static_cast<uint32_t>((gn / RAW) & 1), abort, status);
+                if (!ok) break;
+                convert_block(smem + OFF_RAW + rs * RAW_BYTES, smem + OFF_A + (gn % S) * A_BYTES,
+                              smem + OFF_B + (gn % S) * B_BYTES, tid);
+                if (tid < TM + TN) reinterpret_cast<float *>(smem + OFF_SCL + (gn % SR) * SCL_BYTES)[tid] = sv;
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar_full + 8 * (gn % S));
+                    mbar_arrive(bar_rempty + 8 * rs);
+                }
+            }
         }
     }
 
@@ -493,20 +505,63 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 }  // namespace tc
 
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D byte tensor [outer][inner] with row stride `stride` bytes; box inner x outer.
+static bool make_map_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t stride,
+                        uint32_t box_inner, uint32_t box_outer)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {stride};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static int launch_tc(bool dump, const void *W, const int8_t *Xq, const float *dx, float *Y, int32_t *D, int rows,
                      int K, int M, cudaStream_t s)
 {
     const int nb = K / 32;
     const uint8_t *nib = static_cast<const uint8_t *>(W);
     const uint16_t *dsc = reinterpret_cast<const uint16_t *>(nib + static_cast<size_t>(rows) * nb * 16);
+    CUtensorMap mapA, mapB;
+    if (!make_map_u8(&mapA, Xq, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(K), tc::KB,
+                     tc::TM))
+        return GQ_ERR_CUDA;
+    if (!make_map_u8(&mapB, nib, static_cast<uint64_t>(nb) * 16, static_cast<uint64_t>(rows),
+                     static_cast<uint64_t>(nb) * 16, 16, tc::TN))
+        return GQ_ERR_CUDA;
     const int ntiles = ((M + tc::TM - 1) / tc::TM) * ((rows + tc::TN - 1) / tc::TN);
     auto kern = dump ? tc::k_gemm_q8act_tc<true> : tc::k_gemm_q8act_tc<false>;
     const int occ = ctas_per_sm(reinterpret_cast<const void *>(kern), tc::NTHREADS, tc::SMEM_BYTES);
     if (occ <= 0) return GQ_ERR_CUDA;
     int grid = sm_count();
     if (grid > ntiles) grid = ntiles;
-    return status_from(launch_pdl(kern, dim3(grid), dim3(tc::NTHREADS), static_cast<size_t>(tc::SMEM_BYTES), s,
-                                  nib, dsc, Xq, dx, Y, D, rows, K, M));
+    return status_from(launch_pdl(kern, dim3(grid), dim3(tc::NTHREADS), static_cast<size_t>(tc::SMEM_BYTES), s, mapA,
+                                  mapB, dsc, dx, Y, D, rows, K, M, status_word()));
 }
 
 int launch_gemm_q8act_tc(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows, int K, int M,
@@ -518,17 +573,6 @@ int launch_gemm_q8act_tc(const void *W, const int8_t *Xq, const float *dx, float
 int launch_block_dots_tc(const void *W, const int8_t *Xq, int32_t *D, int rows, int K, int M, cudaStream_t s)
 {
     return launch_tc(true, W, Xq, nullptr, nullptr, D, rows, K, M, s);
-}
-
-int read_device_status(bool reset)
-{
-    int v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return GQ_ERR_CUDA;
-    if (reset && v != 0) {
-        const int zero = 0;
-        if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return GQ_ERR_CUDA;
-    }
-    return v;
 }
 
 }  // namespace gq

@@ -1,36 +1,34 @@
 // gq_geo.cu -- geometry choice for the matvec-family kernels.
 //
-// Chosen by measurement on GB300 (a sweep over lane-group width LG, rows per
-// group R and blocks in flight U at the workload shapes): U = 4 wins for
-// every format; 16- or 32-lane groups beat 8-lane groups for the 4-bit
-// formats; the tied-logit kernel prefers 8-lane groups of 2 rows.
+// Chosen by measurement on GB300 (sweeps over lane-group width LG, rows per
+// group R, loads in flight U, and blocks per lane load P at the workload
+// shapes).  The 4-bit formats use P = 2 (32-byte loads of two consecutive
+// blocks) whenever a row holds an even number of blocks and the weights are
+// 32-byte aligned (measured: on par with or slightly ahead of 16-byte loads).
 #include "gq_host.h"
 
 namespace gq {
 
-MatvecGeo choose_matvec_geo(int format, int rows, int nb)
+MatvecGeo choose_matvec_geo(int format, int rows, int nb, bool pair_ok)
 {
     (void)rows;
-    const int lg_wide = (nb % 32 == 0) ? 32 : 16;
-    switch (format) {
-    case GQ_FORMAT_Q8_0: return MatvecGeo{16, 2, 4, 8};
-    case GQ_FORMAT_Q4_0:
-    case GQ_FORMAT_Q4_K:
-    default: return MatvecGeo{lg_wide, nb >= 512 ? 1 : 2, 4, 8};
-    }
+    if (format == GQ_FORMAT_Q8_0) return MatvecGeo{16, 2, 4, 8, 1};
+    if (pair_ok && nb % 2 == 0) return MatvecGeo{32, 2, nb >= 512 ? 4 : 2, 8, 2};
+    return MatvecGeo{(nb % 32 == 0) ? 32 : 16, nb >= 512 ? 1 : 2, 4, 8, 1};
 }
 
 MatvecGeo choose_logits_geo(int rows, int nb)
 {
     (void)rows;
     (void)nb;
-    return MatvecGeo{8, 2, 4, 8};
+    return MatvecGeo{8, 2, 4, 8, 1};
 }
 
-MatvecGeo choose_ffn_geo(int rows, int nb)
+MatvecGeo choose_ffn_geo(int rows, int nb, bool pair_ok)
 {
     (void)rows;
-    return MatvecGeo{(nb % 32 == 0) ? 32 : 16, 1, 4, 8};
+    if (pair_ok && nb % 2 == 0) return MatvecGeo{32, 2, 2, 8, 2};
+    return MatvecGeo{(nb % 32 == 0) ? 32 : 16, 1, 4, 8, 1};
 }
 
 }  // namespace gq

@@ -29,8 +29,10 @@ inline int sm_count()
     return cache[dev];
 }
 
-// Resident CTAs per SM for (kernel, threads, dynamic smem), cached; also
-// raises the kernel's dynamic shared-memory limit the first time.
+// Resident CTAs per SM for (kernel, threads, dynamic smem), cached.  The
+// first time a kernel is seen on a device its dynamic shared-memory limit is
+// raised to the device's opt-in maximum (once: lowering it again for a
+// smaller launch would break a later larger one).
 inline int ctas_per_sm(const void *kern, int threads, size_t smem)
 {
     struct Entry {
@@ -39,8 +41,13 @@ inline int ctas_per_sm(const void *kern, int threads, size_t smem)
         size_t smem;
         int occ;
     };
-    static Entry tab[256];
-    static int used = 0;
+    struct Raised {
+        const void *k;
+        int dev;
+    };
+    static Entry tab[512];
+    static Raised raised[256];
+    static int used = 0, nraised = 0;
     static std::mutex mu;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -48,12 +55,25 @@ inline int ctas_per_sm(const void *kern, int threads, size_t smem)
     for (int i = 0; i < used; ++i)
         if (tab[i].k == kern && tab[i].dev == dev && tab[i].threads == threads && tab[i].smem == smem)
             return tab[i].occ;
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    bool done = false;
+    for (int i = 0; i < nraised; ++i)
+        if (raised[i].k == kern && raised[i].dev == dev) done = true;
+    if (!done) {
+        int optin = 0;
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaFuncAttributes fa;
+        const size_t static_smem = (cudaFuncGetAttributes(&fa, kern) == cudaSuccess) ? fa.sharedSizeBytes : 0;
+        const int maxdyn = optin - static_cast<int>(static_smem);
+        if (maxdyn > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, maxdyn);
+        cudaGetLastError();  // never leave an error behind for a later launch check
+        if (nraised < 256) raised[nraised++] = Raised{kern, dev};
+    }
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem) != cudaSuccess) {
+        cudaGetLastError();  // clear: an unfit configuration is reported as occ = 0
         occ = 0;
-    if (used < 256) tab[used++] = Entry{kern, dev, threads, smem, occ};
+    }
+    if (used < 512) tab[used++] = Entry{kern, dev, threads, smem, occ};
     return occ;
 }
 
@@ -91,11 +111,12 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 // Matvec geometry: LG lanes per row group, R rows per group, U blocks in flight.
 struct MatvecGeo {
     int lg, r, u, warps;
+    int p;  // blocks per lane load: 1 (16/32-byte loads) or 2 (32-byte block pairs, Q4 formats)
 };
 
-MatvecGeo choose_matvec_geo(int format, int rows, int nb);
+MatvecGeo choose_matvec_geo(int format, int rows, int nb, bool pair_ok);
 MatvecGeo choose_logits_geo(int rows, int nb);
-MatvecGeo choose_ffn_geo(int rows, int nb);
+MatvecGeo choose_ffn_geo(int rows, int nb, bool pair_ok);
 
 int launch_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K, MatvecGeo g,
                        cudaStream_t s);
@@ -120,5 +141,6 @@ int launch_gemm_q8act_tc(const void *W, const int8_t *Xq, const float *dx, float
 int launch_block_dots_tc(const void *W, const int8_t *Xq, int32_t *D, int rows, int K, int M,
                          cudaStream_t s);
 int read_device_status(bool reset);
+int *status_word();  // device address of the status word (current device)
 
 }  // namespace gq

@@ -162,9 +162,15 @@ __global__ void __launch_bounds__(kMergeThreads)
     }
 }
 
-// Upper bound on the CTAs of the logits kernel, fixed so the workspace size
+// Upper bound on the CTAs of the logits kernels, fixed so the workspace size
 // depends only on the arguments, not on the GPU.
 constexpr int kLogitsMaxCtas = 2048;
+int logits_max_ctas() { return kLogitsMaxCtas; }
+
+int launch_topk_merge(const unsigned long long *keys, int nlists, int k, int *idx, float *val, cudaStream_t s)
+{
+    return status_from(launch_pdl(k_topk_merge, dim3(1), dim3(kMergeThreads), 0, s, keys, nlists, k, idx, val));
+}
 
 size_t logits_topk_ws_bytes(int rows, int K, int k)
 {

@@ -208,6 +208,151 @@ __device__ __forceinline__ void q4k_stream(const uint4 *const (&wp)[NS], const u
     for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
 }
 
+
+// ---------------------------------------------------------------- 32-byte loads (block pairs)
+// Same arithmetic with two consecutive blocks per lane and row per load (one
+// 256-bit load of 32 nibble bytes, one 32-bit load of the two scales): twice
+// the bytes per memory request of the one-block form.  Lane lp of a group
+// takes pairs lp, lp+LG, ...; pair p is blocks 2p and 2p+1 (nb even).
+__device__ __forceinline__ uint32_t ld_stream_u32(const void *p)
+{
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+template <int LG, int NS, int U>
+__device__ __forceinline__ void q4_0_stream2(const uint4 *const (&wp)[NS], const uint16_t *const (&sp)[NS],
+                                             const float *xs, int nb, int lp, float (&out)[NS])
+{
+    const int np = nb >> 1;
+    float2 acc[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
+
+    for (int p0 = lp; p0 < np; p0 += LG * U) {
+        uint4 w[U][NS][2];
+        uint32_t dd[U][NS];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int p = p0 + u * LG;
+            const bool ok = p < np;
+#pragma unroll
+            for (int i = 0; i < NS; ++i) {
+                if (ok) {
+                    ld_stream32(wp[i] + 2 * p, w[u][i][0], w[u][i][1]);
+                    dd[u][i] = ld_stream_u32(sp[i] + 2 * p);
+                } else {
+                    w[u][i][0] = make_uint4(0u, 0u, 0u, 0u);
+                    w[u][i][1] = make_uint4(0u, 0u, 0u, 0u);
+                    dd[u][i] = 0u;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int p = p0 + u * LG;
+            if (p < np) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int b = 2 * p + h;
+                    float2 blk[NS];
+#pragma unroll
+                    for (int i = 0; i < NS; ++i) blk[i] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float4 xa = ld_xchunk(xs, b, 2 * t);
+                        const float4 xb = ld_xchunk(xs, b, 2 * t + 1);
+#pragma unroll
+                        for (int i = 0; i < NS; ++i) {
+                            const uint4 &q = w[u][i][h];
+                            const uint32_t word = (t == 0) ? q.x : (t == 1) ? q.y : (t == 2) ? q.z : q.w;
+                            blk[i] = nib8_dot<8>(word, xa, xb, blk[i]);
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < NS; ++i) {
+                        const uint16_t hb = static_cast<uint16_t>(h ? (dd[u][i] >> 16) : (dd[u][i] & 0xFFFFu));
+                        const float d = __half2float(__ushort_as_half(hb));
+                        acc[i] = ffma2(blk[i], make_float2(d, d), acc[i]);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
+}
+
+template <int LG, int NS, int U>
+__device__ __forceinline__ void q4k_stream2(const uint4 *const (&wp)[NS], const uint4 *const (&rp)[NS],
+                                            const float *xs, const float *xsum, int nsb, int lp, float (&out)[NS])
+{
+    const int np = nsb >> 1;
+    float2 acc[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
+
+    for (int p0 = lp; p0 < np; p0 += LG * U) {
+        uint4 w[U][NS][2];
+        uint4 rec[U][NS];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int p = p0 + u * LG;
+            const bool ok = p < np;
+#pragma unroll
+            for (int i = 0; i < NS; ++i) {
+                if (ok) {
+                    ld_stream32(wp[i] + 2 * p, w[u][i][0], w[u][i][1]);
+                    rec[u][i] = __ldg(rp[i] + (p >> 2));  // both sub-blocks lie in super-block p/4
+                } else {
+                    w[u][i][0] = make_uint4(0u, 0u, 0u, 0u);
+                    w[u][i][1] = make_uint4(0u, 0u, 0u, 0u);
+                    rec[u][i] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int p = p0 + u * LG;
+            if (p < np) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int b = 2 * p + h;
+                    float2 blk[NS];
+#pragma unroll
+                    for (int i = 0; i < NS; ++i) blk[i] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float4 xa = ld_xchunk(xs, b, 2 * t);
+                        const float4 xb = ld_xchunk(xs, b, 2 * t + 1);
+#pragma unroll
+                        for (int i = 0; i < NS; ++i) {
+                            const uint4 &q = w[u][i][h];
+                            const uint32_t word = (t == 0) ? q.x : (t == 1) ? q.y : (t == 2) ? q.z : q.w;
+                            blk[i] = nib8_dot<0>(word, xa, xb, blk[i]);
+                        }
+                    }
+                    const float xsb = xsum[b];
+#pragma unroll
+                    for (int i = 0; i < NS; ++i) {
+                        float sc, mn;
+                        q4k_scale_min(rec[u][i], b & 7, sc, mn);
+                        const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(rec[u][i].x & 0xFFFFu)));
+                        const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(rec[u][i].x >> 16)));
+                        const float dsc = d * sc, dm = dmin * mn;
+                        acc[i].x = fmaf(dsc, blk[i].x, acc[i].x);
+                        acc[i].y = fmaf(dsc, blk[i].y, acc[i].y);
+                        acc[i].x = fmaf(-dm, xsb, acc[i].x);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
+}
+
 // ---------------------------------------------------------------- kernel-side common
 constexpr int kThreadsPerCta = 256;
 constexpr int kWarpsPerCta = kThreadsPerCta / 32;
@@ -221,6 +366,24 @@ __device__ __forceinline__ void prefetch_rows_l2(const void *const (&rowp)[NS], 
 #pragma unroll
     for (int i = 0; i < NS; ++i)
         if (lane == i) prefetch_l2_bulk(rowp[i], row_bytes);
+}
+
+// Per-block sums of x (for the min term), after stage_x.
+__device__ __forceinline__ void stage_xsum(float *xsum, const float *xs, int nb)
+{
+    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+        float s = 0.f;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const float4 v = ld_xchunk(xs, b, m);
+            s += v.x;
+            s += v.y;
+            s += v.z;
+            s += v.w;
+        }
+        xsum[b] = s;
+    }
+    __syncthreads();
 }
 
 // GELU, tanh form, with the tanh argument clamped to +-15 (tanh(15) rounds
@@ -252,6 +415,19 @@ __device__ __forceinline__ float gelu_tanh(float a)
         GQ_GEO_CASE1(geo, CASE, 8, 1)         \
         GQ_GEO_CASE1(geo, CASE, 8, 2)         \
         GQ_GEO_CASE1(geo, CASE, 8, 4)         \
+        return GQ_ERR_SHAPE;                  \
+    } while (0)
+// Block-pair (32-byte load) kernels: LG in {4, 8, 16, 32}, R in {1, 2}, U in {2, 4}.
+#define GQ_PAIR_SWITCH(geo, CASE)             \
+    do {                                      \
+        GQ_GEO_CASE1(geo, CASE, 32, 1)        \
+        GQ_GEO_CASE1(geo, CASE, 32, 2)        \
+        GQ_GEO_CASE1(geo, CASE, 16, 1)        \
+        GQ_GEO_CASE1(geo, CASE, 16, 2)        \
+        GQ_GEO_CASE1(geo, CASE, 8, 1)         \
+        GQ_GEO_CASE1(geo, CASE, 8, 2)         \
+        GQ_GEO_CASE1(geo, CASE, 4, 1)         \
+        GQ_GEO_CASE1(geo, CASE, 4, 2)         \
         return GQ_ERR_SHAPE;                  \
     } while (0)
 #define GQ_GEO_SWITCH_R12(geo, CASE)          \

@@ -13,7 +13,7 @@
 
 namespace gq {
 
-template <int LG, int R, int U>
+template <int LG, int R, int U, int P>
 __global__ void __launch_bounds__(kThreadsPerCta, 2)
     k_q4_0_matvec(const uint4 *__restrict__ nib, const uint16_t *__restrict__ dsc,
                   const float *__restrict__ x, float *__restrict__ y, int rows, int nb)
@@ -46,7 +46,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
             sp[i] = dsc + static_cast<size_t>(r) * nb;
         }
         float out[R];
-        q4_0_stream<LG, R, U>(wp, sp, xs, nb, lp, out);
+        if (P == 2)
+            q4_0_stream2<LG, R, U>(wp, sp, xs, nb, lp, out);
+        else
+            q4_0_stream<LG, R, U>(wp, sp, xs, nb, lp, out);
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             const float s = group_sum<LG>(out[i]);
@@ -65,12 +68,18 @@ int launch_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K,
     const long long ntasks = (rows + (32 / geo.lg) * geo.r - 1) / ((32 / geo.lg) * geo.r);
 #define CASE(LG, R, U)                                                                                 \
     {                                                                                                  \
-        auto kern = k_q4_0_matvec<LG, R, U>;                                                           \
+        auto kern = k_q4_0_matvec<LG, R, U, PP>;                                                       \
         const int grid = persistent_grid(reinterpret_cast<const void *>(kern), kThreadsPerCta, smem, ntasks); \
         if (grid <= 0) return GQ_ERR_SHAPE;                                                            \
         return status_from(launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, nib, dsc, x, y, rows, nb)); \
     }
-    GQ_GEO_SWITCH(geo, CASE);
+    if (geo.p == 2) {
+        constexpr int PP = 2;
+        GQ_PAIR_SWITCH(geo, CASE);
+    } else {
+        constexpr int PP = 1;
+        GQ_GEO_SWITCH(geo, CASE);
+    }
 #undef CASE
 }
 

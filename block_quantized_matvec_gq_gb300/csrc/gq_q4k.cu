@@ -11,25 +11,7 @@
 
 namespace gq {
 
-// Per-block sums of x (for the min term), after stage_x.
-__device__ __forceinline__ void stage_xsum(float *xsum, const float *xs, int nb)
-{
-    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-        float s = 0.f;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const float4 v = ld_xchunk(xs, b, m);
-            s += v.x;
-            s += v.y;
-            s += v.z;
-            s += v.w;
-        }
-        xsum[b] = s;
-    }
-    __syncthreads();
-}
-
-template <int LG, int R, int U>
+template <int LG, int R, int U, int P>
 __global__ void __launch_bounds__(kThreadsPerCta, 2)
     k_q4k_matvec(const uint4 *__restrict__ nib, const uint4 *__restrict__ rec,
                  const float *__restrict__ x, float *__restrict__ y, int rows, int nsb)
@@ -65,7 +47,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
             rp[i] = rec + static_cast<size_t>(r) * ns;
         }
         float out[R];
-        q4k_stream<LG, R, U>(wp, rp, xs, xsum, nsb, lp, out);
+        if (P == 2)
+            q4k_stream2<LG, R, U>(wp, rp, xs, xsum, nsb, lp, out);
+        else
+            q4k_stream<LG, R, U>(wp, rp, xs, xsum, nsb, lp, out);
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             const float s = group_sum<LG>(out[i]);
@@ -84,12 +69,18 @@ int launch_q4k_matvec(const void *W, const float *x, float *y, int rows, int K, 
     const long long ntasks = (rows + (32 / geo.lg) * geo.r - 1) / ((32 / geo.lg) * geo.r);
 #define CASE(LG, R, U)                                                                                 \
     {                                                                                                  \
-        auto kern = k_q4k_matvec<LG, R, U>;                                                            \
+        auto kern = k_q4k_matvec<LG, R, U, PP>;                                                        \
         const int grid = persistent_grid(reinterpret_cast<const void *>(kern), kThreadsPerCta, smem, ntasks); \
         if (grid <= 0) return GQ_ERR_SHAPE;                                                            \
         return status_from(launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, nib, rec, x, y, rows, nsb)); \
     }
-    GQ_GEO_SWITCH(geo, CASE);
+    if (geo.p == 2) {
+        constexpr int PP = 2;
+        GQ_PAIR_SWITCH(geo, CASE);
+    } else {
+        constexpr int PP = 1;
+        GQ_GEO_SWITCH(geo, CASE);
+    }
 #undef CASE
 }
 
