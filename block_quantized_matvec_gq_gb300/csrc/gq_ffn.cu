@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
         prefetch_rows_l2<2 * TR>(rp, static_cast<uint32_t>(nb) * 16u, lane);
     }
     pdl_wait();
-    stage_x(xs, x, nb * 32);
+    stage_x_perm8(xs, x, nb * 32);
     pdl_launch_dependents();
 
     for (int task = first; task < ntasks; task += gridDim.x * kWarpsPerCta) {

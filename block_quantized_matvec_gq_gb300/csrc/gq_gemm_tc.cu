@@ -16,16 +16,18 @@
 // f32 result (Y += dx * d_w * D) while the tensor core already computes the
 // next block into the other D buffer.
 //
-// CTA: 512 threads, one per SM, persistent over 128-token x 192-row tiles.
-//   warps 0-11  workers.  For block g: wait for its D, tcgen05.ld it (warp w
-//               owns TMEM lanes 32*(w%4).. and 64 of the 192 columns), fold it
+// CTA: 576 threads, one per SM, persistent over 128-token x 128-row tiles,
+// four 128-column accumulator buffers in TMEM (the MMA runs up to three
+// blocks ahead of the epilogue).
+//   warps 0-15  workers.  For block g: wait for its D, tcgen05.ld it (warp w
+//               owns TMEM lanes 32*(w%4).. and 32 of the 128 columns), fold it
 //               into the f32 accumulators, release the D buffer; then convert
 //               block g+S from the raw TMA tiles into the f16 UMMA operand
 //               layout (the stage the MMA of block g has just finished with)
 //               and stage its scales.
-//   warp 12     one lane issues the TMA tile loads (int8 codes 128 x 32 B,
-//               nibbles 192 x 16 B per block) into an RAW-deep ring.
-//   warp 13     one lane issues 2 x (M128 N192 K16) MMAs per block; the warp
+//   warp 16     one lane issues the TMA tile loads (int8 codes 128 x 32 B,
+//               nibbles 128 x 16 B per block) into an RAW-deep ring.
+//   warp 17     one lane issues 2 x (M128 N128 K16) MMAs per block; the warp
 //               owns the TMEM allocation.
 // Every mbarrier wait is bounded: on timeout the kernel records
 // GQ_ERR_TIMEOUT in the device status word, every role leaves its loop, TMEM
@@ -39,24 +41,25 @@ namespace gq {
 namespace tc {
 
 constexpr int TM = 128;  // tokens per tile (MMA M, TMEM lanes)
-constexpr int TN = 192;  // weight rows per tile (MMA N, TMEM columns)
+constexpr int TN = 128;  // weight rows per tile (MMA N, TMEM columns)
 constexpr int KB = 32;   // K per quantization block
 constexpr int S = 4;     // f16 operand stages
 constexpr int SR = 2 * S;  // scale stages
-constexpr int RAW = 8;   // raw TMA stages
-constexpr int WORK_WARPS = 12;
+constexpr int RAW = 16;  // raw TMA stages (12 blocks of lead over the conversion)
+constexpr int WORK_WARPS = 16;
 constexpr int NWORK = WORK_WARPS * 32;
-constexpr int TMA_WARP = 12;
-constexpr int MMA_WARP = 13;
-constexpr int NTHREADS = 512;
-constexpr int EPI_COLS = TN / (WORK_WARPS / 4);  // 64
+constexpr int TMA_WARP = 16;
+constexpr int MMA_WARP = 17;
+constexpr int NTHREADS = 18 * 32;
+constexpr int EPI_COLS = TN / (WORK_WARPS / 4);  // 32
+constexpr int NDBUF = 4;     // TMEM accumulator buffers (4 x 128 columns)
 constexpr int TMEM_COLS = 512;
-constexpr int DBUF = 256;  // TMEM column offset of the second D buffer
+constexpr int DBUF = 128;  // TMEM column offset between D buffers
 
 constexpr int A_BYTES = TM * KB * 2;  // 8192: f16 operand A
 constexpr int B_BYTES = TN * KB * 2;  // 12288: f16 operand B
 constexpr int RA_BYTES = TM * KB;     // 4096: int8 codes (TMA box 32 x 128)
-constexpr int RB_BYTES = TN * 16;     // 3072: nibbles (TMA box 16 x 192)
+constexpr int RB_BYTES = TN * 16;     // 2048: nibbles (TMA box 16 x 128)
 constexpr int RAW_BYTES = RA_BYTES + RB_BYTES;
 constexpr int SCL_BYTES = (TM + TN) * 4;
 
@@ -65,7 +68,7 @@ constexpr int OFF_B = OFF_A + S * A_BYTES;
 constexpr int OFF_RAW = OFF_B + S * B_BYTES;
 constexpr int OFF_SCL = OFF_RAW + RAW * RAW_BYTES;
 constexpr int OFF_BAR = OFF_SCL + SR * SCL_BYTES;
-constexpr int N_BARS = 2 * RAW + S + 4 + 1;  // raw_full, raw_empty, full, dfull[2], dempty[2], drain
+constexpr int N_BARS = 2 * RAW + S + 2 * NDBUF + 1;  // raw_full, raw_empty, full, dfull, dempty, drain
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16;
 
@@ -91,14 +94,18 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
+// A waiting thread may be suspended up to this long inside one try_wait
+// (it resumes as soon as the phase completes), so waiting warps do not
+// compete with working warps for issue slots.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -275,7 +282,7 @@ __device__ __forceinline__ float load_scale(const Work &w, long long gb, int i, 
 __device__ __forceinline__ void convert_block(const uint8_t *raw, uint8_t *opA, uint8_t *opB, int tid)
 {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < (TM * 4 + TN * 4 + NWORK - 1) / NWORK; ++k) {
         const int i = tid + k * NWORK;
         if (i < TM * 4) {
             const int row = i % TM, kg = i / TM;
@@ -302,7 +309,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_rfull = sbase + OFF_BAR, bar_rempty = bar_rfull + 8 * RAW;
     const uint32_t bar_full = bar_rempty + 8 * RAW, bar_dfull = bar_full + 8 * S;
-    const uint32_t bar_dempty = bar_dfull + 16, bar_drain = bar_dempty + 16;
+    const uint32_t bar_dempty = bar_dfull + 8 * NDBUF, bar_drain = bar_dempty + 8 * NDBUF;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
@@ -321,7 +328,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(bar_rempty + 8 * i, WORK_WARPS);
         }
         for (int s = 0; s < S; ++s) mbar_init(bar_full + 8 * s, WORK_WARPS);
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NDBUF; ++b) {
             mbar_init(bar_dfull + 8 * b, 1);
             mbar_init(bar_dempty + 8 * b, WORK_WARPS);
         }
@@ -369,9 +376,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) {
             for (long long gb = 0; gb < nblocks; ++gb) {
                 const int s = static_cast<int>(gb % S);
-                const int buf = static_cast<int>(gb & 1);
+                const int buf = static_cast<int>(gb % NDBUF);
                 if (!wait_bounded(bar_full + 8 * s, static_cast<uint32_t>((gb / S) & 1), abort, status)) break;
-                if (!wait_bounded(bar_dempty + 8 * buf, static_cast<uint32_t>(((gb >> 1) & 1) ^ 1), abort, status))
+                if (!wait_bounded(bar_dempty + 8 * buf, static_cast<uint32_t>(((gb / NDBUF) & 1) ^ 1), abort, status))
                     break;
                 tc_fence_after();
                 const uint32_t a0 = sbase + OFF_A + s * A_BYTES, b0 = sbase + OFF_B + s * B_BYTES;
@@ -411,11 +418,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float acc[EPI_COLS];
 #pragma unroll
         for (int c = 0; c < EPI_COLS; ++c) acc[c] = 0.f;
+        // scales are loaded one iteration before they are staged
+        float sv_next = (S < nblocks) ? load_scale(w, S, tid, dsc, dx, rows, M) : 0.f;
         for (long long gb = 0; gb < nblocks && ok; ++gb) {
-            const int buf = static_cast<int>(gb & 1);
+            const int buf = static_cast<int>(gb % NDBUF);
             const long long gn = gb + S;  // block converted in this iteration
-            const float sv = (gn < nblocks) ? load_scale(w, gn, tid, dsc, dx, rows, M) : 0.f;
-            ok = wait_warp(bar_dfull + 8 * buf, static_cast<uint32_t>((gb >> 1) & 1), abort, status);
+            const float sv = sv_next;
+            sv_next = (gn + 1 < nblocks) ? load_scale(w, gn + 1, tid, dsc, dx, rows, M) : 0.f;
+            ok = wait_warp(bar_dfull + 8 * buf, static_cast<uint32_t>((gb / NDBUF) & 1), abort, status);
             if (!ok) break;
             tc_fence_after();
             int tile, b;

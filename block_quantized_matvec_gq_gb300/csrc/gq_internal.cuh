@@ -143,11 +143,111 @@ __device__ __forceinline__ float2 nib8_dot(uint32_t w, float4 xa, float4 xb, flo
     return acc;
 }
 
+
+// ---------------------------------------------------------------- 4-bit codes via f16 magic
+// A second exact route from nibbles to f32 that spends one logic operation
+// per TWO codes: OR-ing two nibbles (at bits p and p+16, p < 10) into the
+// pattern 0x6400 of each half gives the halves 1024 + q * 2^p exactly; a
+// mixed-precision add / fma (f16 source, f32 result and constant) then
+// removes 1024 (and the offset) without rounding.  Inside each 8-element
+// group the codes come out in the order 0,4,1,5,2,6,3,7, so x is staged in
+// that order (stage_x_perm8) and the packed f32x2 FMAs pair them directly.
+__device__ __forceinline__ float2 h2_to_f2_add(uint32_t h, float c)
+{
+    float a, b;
+    asm("{\n .reg .f16 lo, hi;\n mov.b32 {lo, hi}, %2;\n add.rn.f32.f16 %0, lo, %3;\n add.rn.f32.f16 %1, hi, %3;\n}"
+        : "=f"(a), "=f"(b)
+        : "r"(h), "f"(c));
+    return make_float2(a, b);
+}
+__device__ __forceinline__ float2 h2_to_f2_fma(uint32_t h, uint16_t s, float c)
+{
+    float a, b;
+    asm("{\n .reg .f16 lo, hi;\n mov.b32 {lo, hi}, %2;\n fma.rn.f32.f16 %0, lo, %3, %4;\n fma.rn.f32.f16 %1, hi, %3, %4;\n}"
+        : "=f"(a), "=f"(b)
+        : "r"(h), "h"(s), "f"(c));
+    return make_float2(a, b);
+}
+// acc += (q - OFF) . x over the 8 nibbles of w (element order), with x given
+// in group order: xa = (x0, x4, x1, x5), xb = (x2, x6, x3, x7).
+template <int OFF>
+__device__ __forceinline__ float2 nib8_dot_h(uint32_t w, float4 xa, float4 xb, float2 acc)
+{
+    constexpr float c0 = -(1024.0f + OFF);
+    constexpr float c1 = -(64.0f + OFF);
+    constexpr uint16_t k16 = 0x2C00;  // f16 1/16
+    const uint32_t w2 = w >> 8;
+    const float2 q04 = h2_to_f2_add((w & 0x000F000Fu) | 0x64006400u, c0);          // e0, e4
+    const float2 q15 = h2_to_f2_fma((w & 0x00F000F0u) | 0x64006400u, k16, c1);     // e1, e5
+    const float2 q26 = h2_to_f2_add((w2 & 0x000F000Fu) | 0x64006400u, c0);         // e2, e6
+    const float2 q37 = h2_to_f2_fma((w2 & 0x00F000F0u) | 0x64006400u, k16, c1);    // e3, e7
+    acc = ffma2(q04, mk2(xa.x, xa.y), acc);
+    acc = ffma2(q15, mk2(xa.z, xa.w), acc);
+    acc = ffma2(q26, mk2(xb.x, xb.y), acc);
+    acc = ffma2(q37, mk2(xb.z, xb.w), acc);
+    return acc;
+}
+
+// Partial sum of one 32-bit word, started fresh (no incoming accumulator),
+// so the words of a block form independent dependency chains that the
+// caller adds as a tree.
+template <int OFF>
+__device__ __forceinline__ float2 nib8_part_h(uint32_t w, float4 xa, float4 xb)
+{
+    constexpr float c0 = -(1024.0f + OFF);
+    constexpr float c1 = -(64.0f + OFF);
+    constexpr uint16_t k16 = 0x2C00;  // f16 1/16
+    const uint32_t w2 = w >> 8;
+    const float2 q04 = h2_to_f2_add((w & 0x000F000Fu) | 0x64006400u, c0);
+    const float2 q15 = h2_to_f2_fma((w & 0x00F000F0u) | 0x64006400u, k16, c1);
+    const float2 q26 = h2_to_f2_add((w2 & 0x000F000Fu) | 0x64006400u, c0);
+    const float2 q37 = h2_to_f2_fma((w2 & 0x00F000F0u) | 0x64006400u, k16, c1);
+    float2 acc = __fmul2_rn(q04, mk2(xa.x, xa.y));
+    acc = ffma2(q15, mk2(xa.z, xa.w), acc);
+    acc = ffma2(q26, mk2(xb.x, xb.y), acc);
+    acc = ffma2(q37, mk2(xb.z, xb.w), acc);
+    return acc;
+}
+// Sum over a 16-byte chunk (4 words = 32 nibbles) of one block: four
+// independent word chains, added pairwise.
+template <int OFF>
+__device__ __forceinline__ float2 nib32_dot_h(uint4 w, const float4 (&x)[8])
+{
+    const float2 a0 = nib8_part_h<OFF>(w.x, x[0], x[1]);
+    const float2 a1 = nib8_part_h<OFF>(w.y, x[2], x[3]);
+    const float2 a2 = nib8_part_h<OFF>(w.z, x[4], x[5]);
+    const float2 a3 = nib8_part_h<OFF>(w.w, x[6], x[7]);
+    return __fadd2_rn(__fadd2_rn(a0, a1), __fadd2_rn(a2, a3));
+}
+
+// Stage x like stage_x, with every 8-element group stored in the order
+// 0,4,1,5,2,6,3,7.  Ends with a CTA barrier.
+__device__ __forceinline__ void stage_x_perm8(float *xs, const float *__restrict__ x, int K)
+{
+    const int ngroups = K >> 3;
+    for (int g = threadIdx.x; g < ngroups; g += blockDim.x) {
+        const float4 a = *reinterpret_cast<const float4 *>(x + 8 * g);
+        const float4 b = *reinterpret_cast<const float4 *>(x + 8 * g + 4);
+        const int blk = g >> 2, t = g & 3;
+        reinterpret_cast<float4 *>(xs)[xswz(blk, 2 * t)] = make_float4(a.x, b.x, a.y, b.y);
+        reinterpret_cast<float4 *>(xs)[xswz(blk, 2 * t + 1)] = make_float4(a.z, b.z, a.w, b.w);
+    }
+    __syncthreads();
+}
+
 // Offset-binary bytes (u = q + 128) to exact f32 q: PRMT places byte k in
 // the low byte of 0x4B0000uu (= 2^23 + u); subtracting 2^23 + 128 is exact.
 __device__ __forceinline__ float byte_f(uint32_t w, uint32_t sel)
 {
     return __uint_as_float(__byte_perm(w, kMagic, sel));
+}
+// q * x for the four bytes of w against x4, started fresh.
+__device__ __forceinline__ float2 byte4_part(uint32_t w, float4 x4)
+{
+    const float2 off = mk2(-(0x1p23f + 128.0f), -(0x1p23f + 128.0f));
+    float2 q01 = __fadd2_rn(mk2(byte_f(w, 0x7540u), byte_f(w, 0x7541u)), off);
+    float2 q23 = __fadd2_rn(mk2(byte_f(w, 0x7542u), byte_f(w, 0x7543u)), off);
+    return ffma2(q23, mk2(x4.z, x4.w), __fmul2_rn(q01, mk2(x4.x, x4.y)));
 }
 // acc += q * x for the four bytes of w against x4.
 __device__ __forceinline__ float2 byte4_dot(uint32_t w, float4 x4, float2 acc)

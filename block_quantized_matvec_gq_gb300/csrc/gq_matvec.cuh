@@ -44,20 +44,12 @@ __device__ __forceinline__ void q4_0_stream(const uint4 *const (&wp)[NS],
         for (int u = 0; u < U; ++u) {
             const int b = b0 + u * LG;
             if (b < nb) {
+                float4 xv[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) xv[m] = ld_xchunk(xs, b, m);
                 float2 blk[NS];
 #pragma unroll
-                for (int i = 0; i < NS; ++i) blk[i] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const float4 xa = ld_xchunk(xs, b, 2 * t);
-                    const float4 xb = ld_xchunk(xs, b, 2 * t + 1);
-#pragma unroll
-                    for (int i = 0; i < NS; ++i) {
-                        const uint32_t word = (t == 0) ? w[u][i].x : (t == 1) ? w[u][i].y
-                                            : (t == 2) ? w[u][i].z : w[u][i].w;
-                        blk[i] = nib8_dot<8>(word, xa, xb, blk[i]);
-                    }
-                }
+                for (int i = 0; i < NS; ++i) blk[i] = nib32_dot_h<8>(w[u][i], xv);
 #pragma unroll
                 for (int i = 0; i < NS; ++i) acc[i] = ffma2(blk[i], make_float2(d[u][i], d[u][i]), acc[i]);
             }
@@ -100,19 +92,19 @@ __device__ __forceinline__ void q8_0_stream(const uint4 *const (&wp)[NS],
         for (int u = 0; u < U; ++u) {
             const int b = b0 + u * LG;
             if (b < nb) {
+                float4 xv[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) xv[m] = ld_xchunk(xs, b, m);
                 float2 blk[NS];
 #pragma unroll
-                for (int i = 0; i < NS; ++i) blk[i] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const float4 x4 = ld_xchunk(xs, b, m);
-#pragma unroll
-                    for (int i = 0; i < NS; ++i) {
-                        const uint4 &h = w[u][i][m >> 2];
-                        const uint32_t word = ((m & 3) == 0) ? h.x : ((m & 3) == 1) ? h.y
-                                            : ((m & 3) == 2) ? h.z : h.w;
-                        blk[i] = byte4_dot(word, x4, blk[i]);
-                    }
+                for (int i = 0; i < NS; ++i) {
+                    const uint4 &h0 = w[u][i][0];
+                    const uint4 &h1 = w[u][i][1];
+                    const float2 p0 = byte4_dot(h0.y, xv[1], byte4_part(h0.x, xv[0]));
+                    const float2 p1 = byte4_dot(h0.w, xv[3], byte4_part(h0.z, xv[2]));
+                    const float2 p2 = byte4_dot(h1.y, xv[5], byte4_part(h1.x, xv[4]));
+                    const float2 p3 = byte4_dot(h1.w, xv[7], byte4_part(h1.z, xv[6]));
+                    blk[i] = __fadd2_rn(__fadd2_rn(p0, p1), __fadd2_rn(p2, p3));
                 }
 #pragma unroll
                 for (int i = 0; i < NS; ++i) acc[i] = ffma2(blk[i], make_float2(d[u][i], d[u][i]), acc[i]);
@@ -174,20 +166,12 @@ __device__ __forceinline__ void q4k_stream(const uint4 *const (&wp)[NS], const u
         for (int u = 0; u < U; ++u) {
             const int b = b0 + u * LG;
             if (b < nsb) {
+                float4 xv[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) xv[m] = ld_xchunk(xs, b, m);
                 float2 blk[NS];
 #pragma unroll
-                for (int i = 0; i < NS; ++i) blk[i] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const float4 xa = ld_xchunk(xs, b, 2 * t);
-                    const float4 xb = ld_xchunk(xs, b, 2 * t + 1);
-#pragma unroll
-                    for (int i = 0; i < NS; ++i) {
-                        const uint32_t word = (t == 0) ? w[u][i].x : (t == 1) ? w[u][i].y
-                                            : (t == 2) ? w[u][i].z : w[u][i].w;
-                        blk[i] = nib8_dot<0>(word, xa, xb, blk[i]);
-                    }
-                }
+                for (int i = 0; i < NS; ++i) blk[i] = nib32_dot_h<0>(w[u][i], xv);
                 const float xsb = xsum[b];
 #pragma unroll
                 for (int i = 0; i < NS; ++i) {
@@ -256,20 +240,12 @@ __device__ __forceinline__ void q4_0_stream2(const uint4 *const (&wp)[NS], const
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int b = 2 * p + h;
+                    float4 xv[8];
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) xv[m] = ld_xchunk(xs, b, m);
                     float2 blk[NS];
 #pragma unroll
-                    for (int i = 0; i < NS; ++i) blk[i] = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const float4 xa = ld_xchunk(xs, b, 2 * t);
-                        const float4 xb = ld_xchunk(xs, b, 2 * t + 1);
-#pragma unroll
-                        for (int i = 0; i < NS; ++i) {
-                            const uint4 &q = w[u][i][h];
-                            const uint32_t word = (t == 0) ? q.x : (t == 1) ? q.y : (t == 2) ? q.z : q.w;
-                            blk[i] = nib8_dot<8>(word, xa, xb, blk[i]);
-                        }
-                    }
+                    for (int i = 0; i < NS; ++i) blk[i] = nib32_dot_h<8>(w[u][i][h], xv);
 #pragma unroll
                     for (int i = 0; i < NS; ++i) {
                         const uint16_t hb = static_cast<uint16_t>(h ? (dd[u][i] >> 16) : (dd[u][i] & 0xFFFFu));
@@ -319,20 +295,12 @@ __device__ __forceinline__ void q4k_stream2(const uint4 *const (&wp)[NS], const 
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int b = 2 * p + h;
+                    float4 xv[8];
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) xv[m] = ld_xchunk(xs, b, m);
                     float2 blk[NS];
 #pragma unroll
-                    for (int i = 0; i < NS; ++i) blk[i] = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const float4 xa = ld_xchunk(xs, b, 2 * t);
-                        const float4 xb = ld_xchunk(xs, b, 2 * t + 1);
-#pragma unroll
-                        for (int i = 0; i < NS; ++i) {
-                            const uint4 &q = w[u][i][h];
-                            const uint32_t word = (t == 0) ? q.x : (t == 1) ? q.y : (t == 2) ? q.z : q.w;
-                            blk[i] = nib8_dot<0>(word, xa, xb, blk[i]);
-                        }
-                    }
+                    for (int i = 0; i < NS; ++i) blk[i] = nib32_dot_h<0>(w[u][i][h], xv);
                     const float xsb = xsum[b];
 #pragma unroll
                     for (int i = 0; i < NS; ++i) {

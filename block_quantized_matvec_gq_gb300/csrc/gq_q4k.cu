@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
         prefetch_rows_l2<TR>(rp, static_cast<uint32_t>(nsb) * 16u, lane);
     }
     pdl_wait();
-    stage_x(xs, x, nsb * 32);
+    stage_x_perm8(xs, x, nsb * 32);
     stage_xsum(xsum, xs, nsb);
     pdl_launch_dependents();
 
