@@ -56,6 +56,7 @@ def _declare(L):
         "gq_ffn_gate_up_gelu": ([P, P, P, P, I, I, I, P], I),
         "gq_logits_topk_workspace_bytes": ([I, I, I], S),
         "gq_logits_topk": ([P, P, ctypes.c_float, I, P, P, P, P, S, I, I, I, P], I),
+        "gq_logits_topk_noalloc": ([P, P, ctypes.c_float, I, P, P, P, I, I, I, P], I),
         "gq_quantize_q8_0": ([P, P, P, I, I, P], I),
         "gq_q4_0_gemm_q8act": ([P, P, P, P, I, I, I, P], I),
         "gq_q4_0_gemm_block_dots": ([P, P, P, I, I, I, P], I),
@@ -153,6 +154,13 @@ def gq_logits_topk(W, x, softcap, k, idx, val, logits_or_null, workspace, worksp
     _check(lib().gq_logits_topk(_ptr(W), _ptr(x), float(softcap), k, _ptr(idx), _ptr(val),
                                 _ptr(logits_or_null), _ptr(workspace), int(workspace_bytes), rows, K, M,
                                 _stream(stream)), "gq_logits_topk")
+
+
+def gq_logits_topk_noalloc(W, x, softcap, k, idx, val, logits_or_null, rows, K, M=1, stream=None):
+    """gq_logits_topk with the key lists in the library's own fixed device array
+    (for callers that cannot allocate; calls that may overlap on the GPU race)."""
+    _check(lib().gq_logits_topk_noalloc(_ptr(W), _ptr(x), float(softcap), k, _ptr(idx), _ptr(val),
+                                        _ptr(logits_or_null), rows, K, M, _stream(stream)), "gq_logits_topk_noalloc")
 
 
 def gq_quantize_q8_0(X, Xq, dx, K, M, stream=None):

@@ -150,6 +150,20 @@ int gq_logits_topk(const void *W, const float *x, float softcap, int k, int *idx
                    float *logits_or_null, void *workspace, size_t workspace_bytes, int rows,
                    int K, int M, gq_stream_t stream);
 
+/* The same computation without the workspace argument, for callers that
+ * cannot allocate device memory (a serving loop that must not call cudaMalloc
+ * while it runs, a runtime that hands the library only its inputs and
+ * outputs).  The source pages have no counterpart of this entry point.  The
+ * per-CTA key lists live in a fixed 1 MiB array inside libgq (held on every
+ * GPU that loads the library until the process exits); every call
+ * gq_logits_topk accepts fits, and a call that would not fit is rejected with
+ * GQ_ERR_SHAPE.  The first call on a device looks the array's address up
+ * (cudaGetSymbolAddress) -- make that first call before any stream capture.
+ * Calls share the array: calls that may overlap on the GPU race on it.
+ * Nothing is allocated. */
+int gq_logits_topk_noalloc(const void *W, const float *x, float softcap, int k, int *idx, float *val,
+                           float *logits_or_null, int rows, int K, int M, gq_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Q8_0 activation quantization ("Metal kernel capability table", section 2,
  * quantize_q8: f32 -> int8 plus per-32 scales; finding F6):
