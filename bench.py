@@ -297,10 +297,12 @@ class Gemm(Workload):
     kernel = "k_gemm_q8act"
     bound = "tensor"
     rows, K, M = 21504, 5376, 512
-    launches_per_step = 2
+    launches_per_step = 3
 
     def setup(self, torch, gq):
         W, X = synth.gemm_inputs(self.rows, self.K, self.M)
+        self.ws_bytes = gq.gq_q4_0_gemm_workspace_bytes(self.K, self.M)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
         self.Wp = gq.pack(0, _to_dev(torch, W.reshape(-1)), self.rows, self.K)
         self.X = _to_dev(torch, X)
         self.Xq = torch.empty((self.M, self.K), dtype=torch.int8, device="cuda")
@@ -315,7 +317,8 @@ class Gemm(Workload):
 
     def step(self, i):
         self.gq.gq_quantize_q8_0(self.X, self.Xq, self.dx, self.K, self.M)
-        self.gq.gq_q4_0_gemm_q8act(self.Wp, self.Xq, self.dx, self.Y, self.rows, self.K, self.M)
+        self.gq.gq_q4_0_gemm_q8act(self.Wp, self.Xq, self.dx, self.Y, self.ws, self.ws_bytes, self.rows, self.K,
+                                   self.M)
 
 
 WORKLOADS = {w.name: w for w in (LogitsTopK, Q40Matvec, Q4KMatvec, FFN, Gemm)}

@@ -58,8 +58,9 @@ def _declare(L):
         "gq_logits_topk": ([P, P, ctypes.c_float, I, P, P, P, P, S, I, I, I, P], I),
         "gq_logits_topk_noalloc": ([P, P, ctypes.c_float, I, P, P, P, I, I, I, P], I),
         "gq_quantize_q8_0": ([P, P, P, I, I, P], I),
-        "gq_q4_0_gemm_q8act": ([P, P, P, P, I, I, I, P], I),
-        "gq_q4_0_gemm_block_dots": ([P, P, P, I, I, I, P], I),
+        "gq_q4_0_gemm_workspace_bytes": ([I, I], S),
+        "gq_q4_0_gemm_q8act": ([P, P, P, P, P, S, I, I, I, P], I),
+        "gq_q4_0_gemm_block_dots": ([P, P, P, P, S, I, I, I, P], I),
         "gq_device_status": ([I], I),
     }
     for name, (args, res) in sig.items():
@@ -167,14 +168,18 @@ def gq_quantize_q8_0(X, Xq, dx, K, M, stream=None):
     _check(lib().gq_quantize_q8_0(_ptr(X), _ptr(Xq), _ptr(dx), K, M, _stream(stream)), "gq_quantize_q8_0")
 
 
-def gq_q4_0_gemm_q8act(W, Xq, dx, Y, rows, K, M, stream=None):
-    _check(lib().gq_q4_0_gemm_q8act(_ptr(W), _ptr(Xq), _ptr(dx), _ptr(Y), rows, K, M, _stream(stream)),
-           "gq_q4_0_gemm_q8act")
+def gq_q4_0_gemm_workspace_bytes(K, M) -> int:
+    return int(lib().gq_q4_0_gemm_workspace_bytes(K, M))
 
 
-def gq_q4_0_gemm_block_dots(W, Xq, D, rows, K, M, stream=None):
-    _check(lib().gq_q4_0_gemm_block_dots(_ptr(W), _ptr(Xq), _ptr(D), rows, K, M, _stream(stream)),
-           "gq_q4_0_gemm_block_dots")
+def gq_q4_0_gemm_q8act(W, Xq, dx, Y, workspace, workspace_bytes, rows, K, M, stream=None):
+    _check(lib().gq_q4_0_gemm_q8act(_ptr(W), _ptr(Xq), _ptr(dx), _ptr(Y), _ptr(workspace), int(workspace_bytes),
+                                    rows, K, M, _stream(stream)), "gq_q4_0_gemm_q8act")
+
+
+def gq_q4_0_gemm_block_dots(W, Xq, D, workspace, workspace_bytes, rows, K, M, stream=None):
+    _check(lib().gq_q4_0_gemm_block_dots(_ptr(W), _ptr(Xq), _ptr(D), _ptr(workspace), int(workspace_bytes),
+                                         rows, K, M, _stream(stream)), "gq_q4_0_gemm_block_dots")
 
 
 def gq_device_status(reset: bool = True) -> int:

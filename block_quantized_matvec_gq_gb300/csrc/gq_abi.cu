@@ -152,22 +152,27 @@ int gq_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, gq_str
     return launch_quantize_q8_0(X, Xq, dx, K, M, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int gq_q4_0_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows, int K, int M,
-                       gq_stream_t stream)
+size_t gq_q4_0_gemm_workspace_bytes(int K, int M) { return gemm_workspace_bytes(K, M); }
+
+int gq_q4_0_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *Y, void *workspace,
+                       size_t workspace_bytes, int rows, int K, int M, gq_stream_t stream)
 {
-    if (!W || !Xq || !dx || !Y) return GQ_ERR_NULL;
-    if (!aligned16(W) || !aligned16(Xq) || !aligned16(dx) || !aligned16(Y)) return GQ_ERR_ALIGN;
+    if (!W || !Xq || !dx || !Y || !workspace) return GQ_ERR_NULL;
+    if (!aligned16(W) || !aligned16(Xq) || !aligned16(dx) || !aligned16(Y) || !aligned16(workspace))
+        return GQ_ERR_ALIGN;
     if (rows < 1 || M < 1 || K < 32 || K % 32 != 0) return GQ_ERR_SHAPE;
-    return launch_gemm_q8act_tc(W, Xq, dx, Y, rows, K, M, reinterpret_cast<cudaStream_t>(stream));
+    return launch_gemm_q8act_tc(W, Xq, dx, Y, workspace, workspace_bytes, rows, K, M,
+                                reinterpret_cast<cudaStream_t>(stream));
 }
 
-int gq_q4_0_gemm_block_dots(const void *W, const int8_t *Xq, int32_t *D, int rows, int K, int M,
-                            gq_stream_t stream)
+int gq_q4_0_gemm_block_dots(const void *W, const int8_t *Xq, int32_t *D, void *workspace, size_t workspace_bytes,
+                            int rows, int K, int M, gq_stream_t stream)
 {
-    if (!W || !Xq || !D) return GQ_ERR_NULL;
-    if (!aligned16(W) || !aligned16(Xq) || !aligned16(D)) return GQ_ERR_ALIGN;
+    if (!W || !Xq || !D || !workspace) return GQ_ERR_NULL;
+    if (!aligned16(W) || !aligned16(Xq) || !aligned16(D) || !aligned16(workspace)) return GQ_ERR_ALIGN;
     if (rows < 1 || M < 1 || K < 32 || K % 32 != 0) return GQ_ERR_SHAPE;
-    return launch_block_dots_tc(W, Xq, D, rows, K, M, reinterpret_cast<cudaStream_t>(stream));
+    return launch_block_dots_tc(W, Xq, D, workspace, workspace_bytes, rows, K, M,
+                                reinterpret_cast<cudaStream_t>(stream));
 }
 
 int gq_device_status(int reset) { return read_device_status(reset != 0); }

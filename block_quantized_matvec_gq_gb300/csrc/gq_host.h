@@ -136,10 +136,11 @@ int launch_pack(int format, const void *src, void *dst, int rows, int K, bool un
 int launch_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, cudaStream_t s);
 int launch_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows, int K,
                       int M, cudaStream_t s);
-int launch_gemm_q8act_tc(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows, int K,
+size_t gemm_workspace_bytes(int K, int M);
+int launch_gemm_q8act_tc(const void *W, const int8_t *Xq, const float *dx, float *Y, void *ws, size_t ws_bytes,
+                         int rows, int K, int M, cudaStream_t s);
+int launch_block_dots_tc(const void *W, const int8_t *Xq, int32_t *D, void *ws, size_t ws_bytes, int rows, int K,
                          int M, cudaStream_t s);
-int launch_block_dots_tc(const void *W, const int8_t *Xq, int32_t *D, int rows, int K, int M,
-                         cudaStream_t s);
 int read_device_status(bool reset);
 int *status_word();  // device address of the status word (current device)
 

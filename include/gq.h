@@ -181,15 +181,23 @@ int gq_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, gq_str
  *   D[t][r][b] = sum_{j<32} Xq[t][32b+j] * (q_w[r][32b+j] - 8)   (exact integers)
  *   Y[t][r]    = sum_b d_w[r][b] * dx[t][b] * D[t][r][b]          (f32)
  * Y is f32[M][rows] row-major (one row of Y per token).
+ *
+ * The workspace (device memory, 16-byte aligned, at least
+ * gq_q4_0_gemm_workspace_bytes(K, M) bytes, owned by the caller) receives
+ * the activation codes converted once to f16 tensor-core operand tiles; its
+ * contents are scratch before and after the call.  Two calls in flight at
+ * the same time need two workspaces.  GQ_ERR_WORKSPACE if it is too small.
  * ------------------------------------------------------------------------ */
-int gq_q4_0_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows,
-                       int K, int M, gq_stream_t stream);
+size_t gq_q4_0_gemm_workspace_bytes(int K, int M); /* 0 if K or M is invalid */
+int gq_q4_0_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *Y, void *workspace,
+                       size_t workspace_bytes, int rows, int K, int M, gq_stream_t stream);
 
 /* The integer block dot products of the same contraction, as the tensor-core
  * path computes them: D int32[M][rows][K/32] (D[t][r][b] above), exact.
- * Meant for checking small problems (the output is M*rows*K/32 words). */
-int gq_q4_0_gemm_block_dots(const void *W, const int8_t *Xq, int32_t *D, int rows, int K, int M,
-                            gq_stream_t stream);
+ * Meant for checking small problems (the output is M*rows*K/32 words).
+ * Same workspace rule as gq_q4_0_gemm_q8act. */
+int gq_q4_0_gemm_block_dots(const void *W, const int8_t *Xq, int32_t *D, void *workspace,
+                            size_t workspace_bytes, int rows, int K, int M, gq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Device status: GQ_ERR_TIMEOUT if a kernel launched since the last reset

@@ -106,10 +106,18 @@ def test_ffn_logits_quant_gemm_pack_validation(lib):
     assert call("gq_quantize_q8_0", A, U, A, 64, 2, None) == gq.GQ_ERR_ALIGN
     assert call("gq_quantize_q8_0", A, A, A, 65, 2, None) == gq.GQ_ERR_SHAPE
     assert call("gq_quantize_q8_0", A, A, A, 64, 0, None) == gq.GQ_ERR_SHAPE
-    assert call("gq_q4_0_gemm_q8act", A, A, A, None, 8, 64, 4, None) == gq.GQ_ERR_NULL
-    assert call("gq_q4_0_gemm_q8act", A, A, U, A, 8, 64, 4, None) == gq.GQ_ERR_ALIGN
-    assert call("gq_q4_0_gemm_q8act", A, A, A, A, 8, 48, 4, None) == gq.GQ_ERR_SHAPE
-    assert call("gq_q4_0_gemm_q8act", A, A, A, A, 8, 64, 0, None) == gq.GQ_ERR_SHAPE
+    gws = gq.gq_q4_0_gemm_workspace_bytes(64, 4)
+    assert gws == 8192 * 2  # one 128-token tile x two 32-blocks of f16 operand
+    assert gq.gq_q4_0_gemm_workspace_bytes(48, 4) == 0 and gq.gq_q4_0_gemm_workspace_bytes(64, 0) == 0
+    assert call("gq_q4_0_gemm_q8act", A, A, A, None, A, gws, 8, 64, 4, None) == gq.GQ_ERR_NULL
+    assert call("gq_q4_0_gemm_q8act", A, A, A, A, None, gws, 8, 64, 4, None) == gq.GQ_ERR_NULL
+    assert call("gq_q4_0_gemm_q8act", A, A, U, A, A, gws, 8, 64, 4, None) == gq.GQ_ERR_ALIGN
+    assert call("gq_q4_0_gemm_q8act", A, A, A, A, U, gws, 8, 64, 4, None) == gq.GQ_ERR_ALIGN
+    assert call("gq_q4_0_gemm_q8act", A, A, A, A, A, gws, 8, 48, 4, None) == gq.GQ_ERR_SHAPE
+    assert call("gq_q4_0_gemm_q8act", A, A, A, A, A, gws, 8, 64, 0, None) == gq.GQ_ERR_SHAPE
+    assert call("gq_q4_0_gemm_q8act", A, A, A, A, A, gws - 16, 8, 64, 4, None) == gq.GQ_ERR_WORKSPACE
+    assert call("gq_q4_0_gemm_block_dots", A, A, A, A, gws - 16, 8, 64, 4, None) == gq.GQ_ERR_WORKSPACE
+    assert call("gq_q4_0_gemm_block_dots", A, A, None, A, gws, 8, 64, 4, None) == gq.GQ_ERR_NULL
     assert call("gq_pack", 9, A, A, 1, 32, None) == gq.GQ_ERR_FORMAT
     assert call("gq_pack", 0, A, None, 1, 32, None) == gq.GQ_ERR_NULL
     assert call("gq_pack", 0, A, U, 1, 32, None) == gq.GQ_ERR_ALIGN

@@ -33,18 +33,28 @@ def test_quantize_bit_exact(M, K):
     assert np.array_equal(Xq.cpu().numpy(), q_ref)
 
 
+def workspace(K, M):
+    t = torch()
+    n = gq.gq_q4_0_gemm_workspace_bytes(K, M)
+    # stale contents must not matter: the pre-pass overwrites every byte the GEMM reads
+    return t.full((n,), 0x7B, dtype=t.uint8, device="cuda"), n
+
+
 def run_gemm(W, Xq_np, dx_np, rows, K, M):
     t = torch()
     Wp = packed(oracle.FORMAT_Q4_0, W, rows, K)
     full, Y, check = guarded(M * rows, t.float32)
-    gq.gq_q4_0_gemm_q8act(Wp, dev(Xq_np), dev(dx_np), Y, rows, K, M)
+    ws, n = workspace(K, M)
+    gq.gq_q4_0_gemm_q8act(Wp, dev(Xq_np), dev(dx_np), Y, ws, n, rows, K, M)
     t.cuda.synchronize()
     check()
     return Y.view(M, rows).cpu().numpy()
 
 
 @pytest.mark.parametrize("M,rows,K", [(1, 1, 32), (37, 100, 256), (64, 64, 64), (130, 257, 544),
-                                      (5, 3000, 5376)])
+                                      (5, 3000, 5376),
+                                      # several tiles per CTA, each of fewer blocks than operand stages
+                                      (260, 40000, 64)])
 def test_gemm_matches_oracle(M, rows, K):
     W = synth.q4_0_weights(rows, K, synth.stream(500 + M, 0))
     X = synth.normal((M, K), synth.stream(500 + M, 1))
@@ -64,7 +74,8 @@ def test_gemm_full_512x21504x5376_sampled():
     t = torch()
     Wp = packed(oracle.FORMAT_Q4_0, W, rows, K)
     Y = t.empty((M, rows), dtype=t.float32, device="cuda")
-    gq.gq_q4_0_gemm_q8act(Wp, Xq_g, dx_g, Y, rows, K, M)
+    ws, n = workspace(K, M)
+    gq.gq_q4_0_gemm_q8act(Wp, Xq_g, dx_g, Y, ws, n, rows, K, M)
     t.cuda.synchronize()
     rng = np.random.default_rng(0)
     toks = np.concatenate([[0, 1, 127, 128, 511], rng.choice(M, 27, replace=False)])
@@ -85,7 +96,8 @@ def test_gemm_all_eight_weights_exact_zero():
     assert np.all(Y == 0.0)
 
 
-@pytest.mark.parametrize("M,rows,K", [(1, 1, 32), (128, 192, 64), (130, 200, 96), (37, 385, 256)])
+@pytest.mark.parametrize("M,rows,K", [(1, 1, 32), (128, 192, 64), (130, 200, 96), (37, 385, 256),
+                                      (260, 40000, 64)])
 def test_tensor_core_block_dots_are_bit_exact(M, rows, K):
     """The integer block dot products computed on the tensor cores (f16
     operands holding exact small integers, f32 accumulation) equal the int32
@@ -97,7 +109,8 @@ def test_tensor_core_block_dots_are_bit_exact(M, rows, K):
     Xq[-1, -32:] = -127
     Wp = packed(oracle.FORMAT_Q4_0, W, rows, K)
     D = t.full((M, rows, K // 32), -999999, dtype=t.int32, device="cuda")
-    gq.gq_q4_0_gemm_block_dots(Wp, dev(Xq), D, rows, K, M)
+    ws, n = workspace(K, M)
+    gq.gq_q4_0_gemm_block_dots(Wp, dev(Xq), D, ws, n, rows, K, M)
     t.cuda.synchronize()
     assert gq.gq_device_status() == gq.GQ_OK
     ref = oracle.block_dots(W, Xq, rows, K, M, 0, M, 0, rows)
@@ -113,7 +126,8 @@ def test_gemm_extreme_block_dots_exact():
     Xq[1] = -127
     t = torch()
     D = t.empty((M, rows, 2), dtype=t.int32, device="cuda")
-    gq.gq_q4_0_gemm_block_dots(packed(oracle.FORMAT_Q4_0, W, rows, K), dev(Xq), D, rows, K, M)
+    ws, n = workspace(K, M)
+    gq.gq_q4_0_gemm_block_dots(packed(oracle.FORMAT_Q4_0, W, rows, K), dev(Xq), D, ws, n, rows, K, M)
     t.cuda.synchronize()
     got = D.cpu().numpy()
     assert np.all(got[0, :, 0] == 32 * 7 * 127) and np.all(got[0, :, 1] == -32 * 8 * 127)
