@@ -11,11 +11,11 @@
 
 namespace gq {
 
-template <int LG, int R, int U, int P>
+template <int LG, int R, int U>
 __global__ void __launch_bounds__(kThreadsPerCta, 2)
     k_ffn_gate_up(const uint4 *__restrict__ gnib, const uint16_t *__restrict__ gsc,
                   const uint4 *__restrict__ unib, const uint16_t *__restrict__ usc,
-                  const float *__restrict__ x, float *__restrict__ h, int rows, int nb)
+                  const float *__restrict__ x, float *__restrict__ h, int rows, int nb, int early)
 {
     extern __shared__ __align__(16) float xs[];
     constexpr int G = 32 / LG, TR = G * R;
@@ -23,7 +23,26 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     const int g = lane / LG, lp = lane % LG;
     const int ntasks = (rows + TR - 1) / TR;
     const int first = blockIdx.x * kWarpsPerCta + warp;
+    const int stride = gridDim.x * kWarpsPerCta;
 
+    // rows 0..R-1 of the stream are gate rows, R..2R-1 the matching up rows
+    Q40Stream<LG, 2 * R, U> st;
+    auto setup = [&](int task) {
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int r = min(task * TR + g * R + i, rows - 1);
+            st.wp[i] = gnib + static_cast<size_t>(r) * nb;
+            st.sp[i] = gsc + static_cast<size_t>(r) * nb;
+            st.wp[R + i] = unib + static_cast<size_t>(r) * nb;
+            st.sp[R + i] = usc + static_cast<size_t>(r) * nb;
+        }
+        st.prime(nb, lp);
+    };
+    // Weights never depend on the previous kernel: prefetch this warp's first
+    // rows into L2 before waiting for it and, when warps have about one task
+    // each (`early`, decided by the host), issue that task's first loads too.
+    // (Measured: with several tasks per warp the early loads cost more than
+    // they save.)
     if (first < ntasks) {
         const void *rp[2 * TR];
 #pragma unroll
@@ -33,28 +52,17 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
             rp[TR + i] = unib + r * nb;
         }
         prefetch_rows_l2<2 * TR>(rp, static_cast<uint32_t>(nb) * 16u, lane);
+        if (early) setup(first);
     }
     pdl_wait();
-    stage_x_perm8(xs, x, nb * 32);
+    stage_x_q4<false>(xs, x, nb * 32);
     pdl_launch_dependents();
 
-    for (int task = first; task < ntasks; task += gridDim.x * kWarpsPerCta) {
-        const int r0 = task * TR + g * R;
-        const uint4 *wp[2 * R];
-        const uint16_t *sp[2 * R];
-#pragma unroll
-        for (int i = 0; i < R; ++i) {
-            const int r = min(r0 + i, rows - 1);
-            wp[i] = gnib + static_cast<size_t>(r) * nb;
-            sp[i] = gsc + static_cast<size_t>(r) * nb;
-            wp[R + i] = unib + static_cast<size_t>(r) * nb;
-            sp[R + i] = usc + static_cast<size_t>(r) * nb;
-        }
+    for (int task = first; task < ntasks; task += stride) {
+        if (task != first || !early) setup(task);
         float out[2 * R];
-        if (P == 2)
-            q4_0_stream2<LG, 2 * R, U>(wp, sp, xs, nb, lp, out);
-        else
-            q4_0_stream<LG, 2 * R, U>(wp, sp, xs, nb, lp, out);
+        st.run(xs, nb, lp, out);
+        const int r0 = task * TR + g * R;
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             const float gv = group_sum<LG>(out[i]);
@@ -72,22 +80,18 @@ int launch_ffn_gate_up(const void *Wg, const void *Wu, const float *x, float *h,
     const uint16_t *gs = reinterpret_cast<const uint16_t *>(gn + static_cast<size_t>(rows) * nb);
     const uint4 *un = static_cast<const uint4 *>(Wu);
     const uint16_t *us = reinterpret_cast<const uint16_t *>(un + static_cast<size_t>(rows) * nb);
-    const size_t smem = static_cast<size_t>(K) * sizeof(float);
+    const size_t smem = static_cast<size_t>(nb) * kXBlk * sizeof(float);
     const long long ntasks = (rows + (32 / geo.lg) * geo.r - 1) / ((32 / geo.lg) * geo.r);
+    if (geo.p != 1) return GQ_ERR_SHAPE;
 #define CASE(LG, R, U)                                                                                 \
     {                                                                                                  \
-        auto kern = k_ffn_gate_up<LG, R, U, PP>;                                                       \
+        auto kern = k_ffn_gate_up<LG, R, U>;                                                           \
         const int grid = persistent_grid(reinterpret_cast<const void *>(kern), kThreadsPerCta, smem, ntasks); \
         if (grid <= 0) return GQ_ERR_SHAPE;                                                            \
-        return status_from(launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, gn, gs, un, us, x, h, rows, nb)); \
+        const int early = ntasks * 4 <= static_cast<long long>(grid) * kWarpsPerCta * 5;              \
+        return status_from(launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, gn, gs, un, us, x, h, rows, nb, early)); \
     }
-    if (geo.p == 2) {
-        constexpr int PP = 2;
-        GQ_PAIR_SWITCH(geo, CASE);
-    } else {
-        constexpr int PP = 1;
-        GQ_GEO_SWITCH_R12(geo, CASE);
-    }
+    GQ_GEO_SWITCH_R12(geo, CASE);
 #undef CASE
 }
 

@@ -275,6 +275,7 @@ __device__ __forceinline__ uint32_t op_off(int row, int kg) { return (((row >> 3
 __global__ void __launch_bounds__(256) k_xq_to_ops(const int8_t *__restrict__ Xq, uint4 *__restrict__ Xh, int K,
                                                    int M, long long npieces)
 {
+    pdl_launch_dependents();  // the GEMM's prologue may overlap; it waits for this grid before reading Xh
     pdl_wait();
     const int nb = K / KB;
     for (long long p = blockIdx.x * 256ll + threadIdx.x; p < npieces; p += static_cast<long long>(gridDim.x) * 256) {
@@ -291,7 +292,6 @@ __global__ void __launch_bounds__(256) k_xq_to_ops(const int8_t *__restrict__ Xq
         }
         Xh[p] = o;
     }
-    pdl_launch_dependents();
 }
 
 struct Work {

@@ -2,9 +2,10 @@
 //
 // Chosen by measurement on GB300 (sweeps over lane-group width LG, rows per
 // group R, loads in flight U, and blocks per lane load P at the workload
-// shapes).  The 4-bit formats use P = 2 (32-byte loads of two consecutive
-// blocks) whenever a row holds an even number of blocks and the weights are
-// 32-byte aligned (measured: on par with or slightly ahead of 16-byte loads).
+// shapes).  With the register-lean 4-bit core, 16-byte loads (P = 1) beat
+// the 32-byte block-pair loads at every measured shape; LG = 32 when a row's
+// block count is a multiple of 32, else 16 (less idle lanes in the last
+// step); U = 4 for long rows (K >= 16384).
 #include "gq_host.h"
 
 namespace gq {
@@ -12,9 +13,9 @@ namespace gq {
 MatvecGeo choose_matvec_geo(int format, int rows, int nb, bool pair_ok)
 {
     (void)rows;
+    (void)pair_ok;
     if (format == GQ_FORMAT_Q8_0) return MatvecGeo{16, 2, 4, 8, 1};
-    if (pair_ok && nb % 2 == 0) return MatvecGeo{32, 2, nb >= 512 ? 4 : 2, 8, 2};
-    return MatvecGeo{(nb % 32 == 0) ? 32 : 16, nb >= 512 ? 1 : 2, 4, 8, 1};
+    return MatvecGeo{(nb % 32 == 0) ? 32 : 16, 2, nb >= 512 ? 4 : 2, 8, 1};
 }
 
 MatvecGeo choose_logits_geo(int rows, int nb)
@@ -27,8 +28,9 @@ MatvecGeo choose_logits_geo(int rows, int nb)
 MatvecGeo choose_ffn_geo(int rows, int nb, bool pair_ok)
 {
     (void)rows;
-    if (pair_ok && nb % 2 == 0) return MatvecGeo{32, 2, 2, 8, 2};
-    return MatvecGeo{(nb % 32 == 0) ? 32 : 16, 1, 4, 8, 1};
+    (void)nb;
+    (void)pair_ok;
+    return MatvecGeo{8, 1, 4, 8, 1};
 }
 
 }  // namespace gq

@@ -99,138 +99,120 @@ __device__ __forceinline__ float group_sum(float v)
 }
 
 // ---------------------------------------------------------------- exact code -> f32
-// Four-bit codes are turned into exact f32 values without an int-to-float
-// conversion: OR-ing the code (at bit position p < 20) into the bit pattern
-// of 2^23 gives the float 2^23 + q * 2^p exactly; one FMA with 2^-p and a
-// constant then removes 2^(23-p) (and the Q4_0 offset 8) without rounding,
-// since the exact result is a small integer.
+// Codes are turned into exact f32 values without an int-to-float
+// conversion: OR-ing a code (at bit position p < 20) into the bit pattern of
+// 2^23 gives the float 2^23 + q * 2^p exactly; one FMA with 2^-p and a
+// constant then removes 2^(23-p) (and an offset) without rounding, since the
+// exact result is a small integer.
 constexpr uint32_t kMagic = 0x4B000000u;  // bit pattern of 2^23
 
 __device__ __forceinline__ float2 mk2(float a, float b) { return make_float2(a, b); }
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
-__device__ __forceinline__ float2 nib2(uint32_t va, uint32_t ma, uint32_t vb, uint32_t mb)
-{
-    return make_float2(__uint_as_float((va & ma) | kMagic), __uint_as_float((vb & mb) | kMagic));
-}
+// ---------------------------------------------------------------- 4-bit codes
+// One 32-bit word w holds the 8 nibbles of one 8-element group in element
+// order (nibble k = bits 4k..4k+3).  For i = 0..3 the pair (nibble i, nibble
+// i+4) is isolated in place by one LOP3 each: (w & 0xF<<4i) | 0x4B000000 is
+// the f32 2^23 + q*16^i, and the same on w>>16 gives element i+4.  One packed
+// f32x2 FMA by 16^-i minus (2^(23-4i) + OFF) turns the pair into
+// (q_i - OFF, q_{i+4} - OFF) exactly, and one packed FMA adds its products
+// with (x_i, x_{i+4}).  x is staged per 8-group in the order
+// x0,x4,x1,x5,x2,x6,x3,x7, so each pair of x values is one aligned 64-bit
+// register pair.  The whole word is one asm block so that the LOP3 results
+// land directly in the 64-bit pairs the packed instructions read.
+#define GQ_NIB8_BODY(FIRST)                                                                                      \
+    "{\n"                                                                                                        \
+    " .reg .b32 h, l0, h0, l1, h1, l2, h2, l3, h3;\n"                                                           \
+    " .reg .b64 p0, p1, p2, p3, x0, x1, x2, x3, a, c0, c1, c2, c3, s1, s2, s3;\n"                               \
+    " shr.u32 h, %2, 16;\n"                                                                                      \
+    " lop3.b32 l0, %2, 0x0000000F, 0x4B000000, 0xEA;\n lop3.b32 h0, h, 0x0000000F, 0x4B000000, 0xEA;\n"         \
+    " lop3.b32 l1, %2, 0x000000F0, 0x4B000000, 0xEA;\n lop3.b32 h1, h, 0x000000F0, 0x4B000000, 0xEA;\n"         \
+    " lop3.b32 l2, %2, 0x00000F00, 0x4B000000, 0xEA;\n lop3.b32 h2, h, 0x00000F00, 0x4B000000, 0xEA;\n"         \
+    " lop3.b32 l3, %2, 0x0000F000, 0x4B000000, 0xEA;\n lop3.b32 h3, h, 0x0000F000, 0x4B000000, 0xEA;\n"         \
+    " mov.b64 p0, {l0, h0};\n mov.b64 p1, {l1, h1};\n mov.b64 p2, {l2, h2};\n mov.b64 p3, {l3, h3};\n"         \
+    " mov.b64 c0, {%13, %13};\n mov.b64 c1, {%14, %14};\n mov.b64 c2, {%15, %15};\n mov.b64 c3, {%16, %16};\n" \
+    " mov.b64 s1, {%17, %17};\n mov.b64 s2, {%18, %18};\n mov.b64 s3, {%19, %19};\n"                           \
+    " add.rn.f32x2 p0, p0, c0;\n"                                                                                \
+    " fma.rn.f32x2 p1, p1, s1, c1;\n fma.rn.f32x2 p2, p2, s2, c2;\n fma.rn.f32x2 p3, p3, s3, c3;\n"             \
+    " mov.b64 x0, {%3, %4};\n mov.b64 x1, {%5, %6};\n mov.b64 x2, {%7, %8};\n mov.b64 x3, {%9, %10};\n"         \
+    " mov.b64 a, {%11, %12};\n" FIRST                                                                            \
+    " fma.rn.f32x2 a, p1, x1, a;\n fma.rn.f32x2 a, p2, x2, a;\n fma.rn.f32x2 a, p3, x3, a;\n"                   \
+    " mov.b64 {%0, %1}, a;\n"                                                                                    \
+    "}"
 
-// q - OFF for the eight nibbles of word w (element order: nibble e of the
-// word at bits 4e..4e+3), accumulated against x[0..8) into acc:
-//   acc += (q_e - OFF) * x_e, as four packed f32x2 FMAs.
-// OFF = 8 for Q4_0 (centred codes), 0 for Q4_K (plain codes).
 template <int OFF>
-__device__ __forceinline__ float2 nib8_dot(uint32_t w, float4 xa, float4 xb, float2 acc)
+struct NibConsts {
+    static constexpr float c0 = -(8388608.0f + OFF);  // -(2^23 + OFF)
+    static constexpr float c1 = -(524288.0f + OFF);   // -(2^19 + OFF)
+    static constexpr float c2 = -(32768.0f + OFF);    // -(2^15 + OFF)
+    static constexpr float c3 = -(2048.0f + OFF);     // -(2^11 + OFF)
+};
+
+// Returns acc + sum over the word of (q - OFF) * x as a packed pair of
+// partial sums; kStart ignores acc (starts a new chain).
+template <int OFF, bool kStart>
+__device__ __forceinline__ float2 nib8_fma(uint32_t w, float4 xa, float4 xb, float2 acc)
 {
-    constexpr float o = static_cast<float>(OFF);
-    const uint32_t v = w, u = w >> 12;  // u holds nibbles 5,6,7 at bits 8,12,16
-    // nibbles 0,1 at bits 0,4
-    float2 q01 = ffma2(nib2(v, 0xFu, v, 0xF0u), mk2(1.0f, 0x1p-4f),
-                       mk2(-(0x1p23f + o), -(0x1p19f + o)));
-    // nibbles 2,3 at bits 8,12
-    float2 q23 = ffma2(nib2(v, 0xF00u, v, 0xF000u), mk2(0x1p-8f, 0x1p-12f),
-                       mk2(-(0x1p15f + o), -(0x1p11f + o)));
-    // nibble 4 at bit 16 of v, nibble 5 at bit 8 of u
-    float2 q45 = ffma2(nib2(v, 0xF0000u, u, 0xF00u), mk2(0x1p-16f, 0x1p-8f),
-                       mk2(-(0x1p7f + o), -(0x1p15f + o)));
-    // nibbles 6,7 at bits 12,16 of u
-    float2 q67 = ffma2(nib2(u, 0xF000u, u, 0xF0000u), mk2(0x1p-12f, 0x1p-16f),
-                       mk2(-(0x1p11f + o), -(0x1p7f + o)));
-    acc = ffma2(q01, mk2(xa.x, xa.y), acc);
-    acc = ffma2(q23, mk2(xa.z, xa.w), acc);
-    acc = ffma2(q45, mk2(xb.x, xb.y), acc);
-    acc = ffma2(q67, mk2(xb.z, xb.w), acc);
-    return acc;
+    float2 r;
+    if (kStart) {
+        asm(GQ_NIB8_BODY(" mul.rn.f32x2 a, p0, x0;\n")
+            : "=f"(r.x), "=f"(r.y)
+            : "r"(w), "f"(xa.x), "f"(xa.y), "f"(xa.z), "f"(xa.w), "f"(xb.x), "f"(xb.y), "f"(xb.z), "f"(xb.w),
+              "f"(acc.x), "f"(acc.y), "f"(NibConsts<OFF>::c0), "f"(NibConsts<OFF>::c1), "f"(NibConsts<OFF>::c2),
+              "f"(NibConsts<OFF>::c3), "f"(0.0625f), "f"(0.00390625f), "f"(0.000244140625f));
+    } else {
+        asm(GQ_NIB8_BODY(" fma.rn.f32x2 a, p0, x0, a;\n")
+            : "=f"(r.x), "=f"(r.y)
+            : "r"(w), "f"(xa.x), "f"(xa.y), "f"(xa.z), "f"(xa.w), "f"(xb.x), "f"(xb.y), "f"(xb.z), "f"(xb.w),
+              "f"(acc.x), "f"(acc.y), "f"(NibConsts<OFF>::c0), "f"(NibConsts<OFF>::c1), "f"(NibConsts<OFF>::c2),
+              "f"(NibConsts<OFF>::c3), "f"(0.0625f), "f"(0.00390625f), "f"(0.000244140625f));
+    }
+    return r;
 }
 
+// ---------------------------------------------------------------- activation staging for 4-bit formats
+// x is kept in shared memory as K/32 blocks of kXBlk = 36 floats (144 bytes):
+// the block's 32 values, every 8-element group in the order
+// 0,4,1,5,2,6,3,7 (the pair order of nib8_fma), then the block's sum of x
+// (the Q4_K min term) and 3 unused floats.  Lanes reading the same 16-byte
+// chunk of consecutive blocks are 144 bytes apart, i.e. on distinct bank
+// groups, so 128-bit loads are conflict-free with a fixed immediate offset
+// per chunk.
+constexpr int kXBlk = 36;
 
-// ---------------------------------------------------------------- 4-bit codes via f16 magic
-// A second exact route from nibbles to f32 that spends one logic operation
-// per TWO codes: OR-ing two nibbles (at bits p and p+16, p < 10) into the
-// pattern 0x6400 of each half gives the halves 1024 + q * 2^p exactly; a
-// mixed-precision add / fma (f16 source, f32 result and constant) then
-// removes 1024 (and the offset) without rounding.  Inside each 8-element
-// group the codes come out in the order 0,4,1,5,2,6,3,7, so x is staged in
-// that order (stage_x_perm8) and the packed f32x2 FMAs pair them directly.
-__device__ __forceinline__ float2 h2_to_f2_add(uint32_t h, float c)
+__device__ __forceinline__ float4 ld_xq4(const float *xb, int m)
 {
-    float a, b;
-    asm("{\n .reg .f16 lo, hi;\n mov.b32 {lo, hi}, %2;\n add.rn.f32.f16 %0, lo, %3;\n add.rn.f32.f16 %1, hi, %3;\n}"
-        : "=f"(a), "=f"(b)
-        : "r"(h), "f"(c));
-    return make_float2(a, b);
-}
-__device__ __forceinline__ float2 h2_to_f2_fma(uint32_t h, uint16_t s, float c)
-{
-    float a, b;
-    asm("{\n .reg .f16 lo, hi;\n mov.b32 {lo, hi}, %2;\n fma.rn.f32.f16 %0, lo, %3, %4;\n fma.rn.f32.f16 %1, hi, %3, %4;\n}"
-        : "=f"(a), "=f"(b)
-        : "r"(h), "h"(s), "f"(c));
-    return make_float2(a, b);
-}
-// acc += (q - OFF) . x over the 8 nibbles of w (element order), with x given
-// in group order: xa = (x0, x4, x1, x5), xb = (x2, x6, x3, x7).
-template <int OFF>
-__device__ __forceinline__ float2 nib8_dot_h(uint32_t w, float4 xa, float4 xb, float2 acc)
-{
-    constexpr float c0 = -(1024.0f + OFF);
-    constexpr float c1 = -(64.0f + OFF);
-    constexpr uint16_t k16 = 0x2C00;  // f16 1/16
-    const uint32_t w2 = w >> 8;
-    const float2 q04 = h2_to_f2_add((w & 0x000F000Fu) | 0x64006400u, c0);          // e0, e4
-    const float2 q15 = h2_to_f2_fma((w & 0x00F000F0u) | 0x64006400u, k16, c1);     // e1, e5
-    const float2 q26 = h2_to_f2_add((w2 & 0x000F000Fu) | 0x64006400u, c0);         // e2, e6
-    const float2 q37 = h2_to_f2_fma((w2 & 0x00F000F0u) | 0x64006400u, k16, c1);    // e3, e7
-    acc = ffma2(q04, mk2(xa.x, xa.y), acc);
-    acc = ffma2(q15, mk2(xa.z, xa.w), acc);
-    acc = ffma2(q26, mk2(xb.x, xb.y), acc);
-    acc = ffma2(q37, mk2(xb.z, xb.w), acc);
-    return acc;
+    return *reinterpret_cast<const float4 *>(xb + 4 * m);
 }
 
-// Partial sum of one 32-bit word, started fresh (no incoming accumulator),
-// so the words of a block form independent dependency chains that the
-// caller adds as a tree.
-template <int OFF>
-__device__ __forceinline__ float2 nib8_part_h(uint32_t w, float4 xa, float4 xb)
-{
-    constexpr float c0 = -(1024.0f + OFF);
-    constexpr float c1 = -(64.0f + OFF);
-    constexpr uint16_t k16 = 0x2C00;  // f16 1/16
-    const uint32_t w2 = w >> 8;
-    const float2 q04 = h2_to_f2_add((w & 0x000F000Fu) | 0x64006400u, c0);
-    const float2 q15 = h2_to_f2_fma((w & 0x00F000F0u) | 0x64006400u, k16, c1);
-    const float2 q26 = h2_to_f2_add((w2 & 0x000F000Fu) | 0x64006400u, c0);
-    const float2 q37 = h2_to_f2_fma((w2 & 0x00F000F0u) | 0x64006400u, k16, c1);
-    float2 acc = __fmul2_rn(q04, mk2(xa.x, xa.y));
-    acc = ffma2(q15, mk2(xa.z, xa.w), acc);
-    acc = ffma2(q26, mk2(xb.x, xb.y), acc);
-    acc = ffma2(q37, mk2(xb.z, xb.w), acc);
-    return acc;
-}
-// Sum over a 16-byte chunk (4 words = 32 nibbles) of one block: four
-// independent word chains, added pairwise.
-template <int OFF>
-__device__ __forceinline__ float2 nib32_dot_h(uint4 w, const float4 (&x)[8])
-{
-    const float2 a0 = nib8_part_h<OFF>(w.x, x[0], x[1]);
-    const float2 a1 = nib8_part_h<OFF>(w.y, x[2], x[3]);
-    const float2 a2 = nib8_part_h<OFF>(w.z, x[4], x[5]);
-    const float2 a3 = nib8_part_h<OFF>(w.w, x[6], x[7]);
-    return __fadd2_rn(__fadd2_rn(a0, a1), __fadd2_rn(a2, a3));
-}
-
-// Stage x like stage_x, with every 8-element group stored in the order
-// 0,4,1,5,2,6,3,7.  Ends with a CTA barrier.
-__device__ __forceinline__ void stage_x_perm8(float *xs, const float *__restrict__ x, int K)
+// All threads of the CTA take part; ends with a CTA barrier.
+template <bool kWithSum>
+__device__ __forceinline__ void stage_x_q4(float *xs, const float *__restrict__ x, int K)
 {
     const int ngroups = K >> 3;
     for (int g = threadIdx.x; g < ngroups; g += blockDim.x) {
         const float4 a = *reinterpret_cast<const float4 *>(x + 8 * g);
         const float4 b = *reinterpret_cast<const float4 *>(x + 8 * g + 4);
-        const int blk = g >> 2, t = g & 3;
-        reinterpret_cast<float4 *>(xs)[xswz(blk, 2 * t)] = make_float4(a.x, b.x, a.y, b.y);
-        reinterpret_cast<float4 *>(xs)[xswz(blk, 2 * t + 1)] = make_float4(a.z, b.z, a.w, b.w);
+        float *dst = xs + (g >> 2) * kXBlk + 8 * (g & 3);
+        *reinterpret_cast<float4 *>(dst) = make_float4(a.x, b.x, a.y, b.y);
+        *reinterpret_cast<float4 *>(dst + 4) = make_float4(a.z, b.z, a.w, b.w);
+    }
+    if (kWithSum) {
+        __syncthreads();
+        for (int b = threadIdx.x; b < (K >> 5); b += blockDim.x) {
+            const float *src = xs + b * kXBlk;
+            float s = 0.f;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const float4 v = ld_xq4(src, m);
+                s += v.x;
+                s += v.y;
+                s += v.z;
+                s += v.w;
+            }
+            xs[b * kXBlk + 32] = s;
+        }
     }
     __syncthreads();
 }

@@ -114,6 +114,9 @@ __global__ void __launch_bounds__(kMergeThreads)
     __shared__ unsigned long long wkeys[kMergeWarps * GQ_MAX_TOPK];
     __shared__ unsigned long long wmax[kMergeWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // Let the next kernel start its prologue (weight prefetch) now: it still
+    // waits for this grid to complete before it reads anything written here.
+    pdl_launch_dependents();
     pdl_wait();
 
     // threshold: the largest k-th key over all lists

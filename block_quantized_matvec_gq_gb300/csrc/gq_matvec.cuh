@@ -16,20 +16,59 @@
 
 namespace gq {
 
+// ---------------------------------------------------------------- Q4_0 / Q4_K block core
+// Dot products of one 32-weight block (four 32-bit nibble words in element
+// order) of NS rows against the block's staged x: two FMA chains per row
+// (words 0-1 and 2-3), added at the end.
+template <int OFF, int NS>
+__device__ __forceinline__ void q4_block(const uint4 (&w)[NS], const float *xb, float2 (&blk)[NS])
+{
+    float2 a[NS], c[NS];
+    {
+        const float4 x0 = ld_xq4(xb, 0), x1 = ld_xq4(xb, 1);
+#pragma unroll
+        for (int i = 0; i < NS; ++i) a[i] = nib8_fma<OFF, true>(w[i].x, x0, x1, mk2(0.f, 0.f));
+    }
+    {
+        const float4 x2 = ld_xq4(xb, 2), x3 = ld_xq4(xb, 3);
+#pragma unroll
+        for (int i = 0; i < NS; ++i) a[i] = nib8_fma<OFF, false>(w[i].y, x2, x3, a[i]);
+    }
+    {
+        const float4 x4 = ld_xq4(xb, 4), x5 = ld_xq4(xb, 5);
+#pragma unroll
+        for (int i = 0; i < NS; ++i) c[i] = nib8_fma<OFF, true>(w[i].z, x4, x5, mk2(0.f, 0.f));
+    }
+    {
+        const float4 x6 = ld_xq4(xb, 6), x7 = ld_xq4(xb, 7);
+#pragma unroll
+        for (int i = 0; i < NS; ++i) c[i] = nib8_fma<OFF, false>(w[i].w, x6, x7, c[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < NS; ++i) blk[i] = __fadd2_rn(a[i], c[i]);
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t h)
+{
+    return __half2float(__ushort_as_half(static_cast<uint16_t>(h)));
+}
+
 // ---------------------------------------------------------------- Q4_0
 // Packed Q4_0: nibble plane (16 B per block, element order) + fp16 scale plane.
+// One row task of NS rows: set the row pointers, prime() loads the first U
+// blocks of every row (a kernel may call it before waiting for the previous
+// kernel, since weights never depend on it), run() streams the rest.  Loads
+// of the next U blocks alternate between two register sets (the loop body
+// is written twice), so no copies are needed between iterations.
 template <int LG, int NS, int U>
-__device__ __forceinline__ void q4_0_stream(const uint4 *const (&wp)[NS],
-                                            const uint16_t *const (&sp)[NS], const float *xs,
-                                            int nb, int lp, float (&out)[NS])
-{
-    float2 acc[NS];
-#pragma unroll
-    for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
+struct Q40Stream {
+    const uint4 *wp[NS];
+    const uint16_t *sp[NS];
+    uint4 wA[U][NS], wB[U][NS];
+    uint32_t dA[U][NS], dB[U][NS];
 
-    for (int b0 = lp; b0 < nb; b0 += LG * U) {
-        uint4 w[U][NS];
-        float d[U][NS];
+    __device__ __forceinline__ void load(uint4 (&w)[U][NS], uint32_t (&d)[U][NS], int b0, int nb) const
+    {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int b = b0 + u * LG;
@@ -37,27 +76,45 @@ __device__ __forceinline__ void q4_0_stream(const uint4 *const (&wp)[NS],
 #pragma unroll
             for (int i = 0; i < NS; ++i) {
                 w[u][i] = ok ? ld_stream16(wp[i] + b) : make_uint4(0u, 0u, 0u, 0u);
-                d[u][i] = ok ? __half2float(__ushort_as_half(ld_stream_u16(sp[i] + b))) : 0.f;
+                d[u][i] = ok ? ld_stream_u16(sp[i] + b) : 0u;
             }
         }
+    }
+    __device__ __forceinline__ void compute(const uint4 (&w)[U][NS], const uint32_t (&d)[U][NS], int b0, int nb,
+                                            const float *xs, float2 (&acc)[NS]) const
+    {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int b = b0 + u * LG;
             if (b < nb) {
-                float4 xv[8];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) xv[m] = ld_xchunk(xs, b, m);
                 float2 blk[NS];
+                q4_block<8, NS>(w[u], xs + b * kXBlk, blk);
 #pragma unroll
-                for (int i = 0; i < NS; ++i) blk[i] = nib32_dot_h<8>(w[u][i], xv);
-#pragma unroll
-                for (int i = 0; i < NS; ++i) acc[i] = ffma2(blk[i], make_float2(d[u][i], d[u][i]), acc[i]);
+                for (int i = 0; i < NS; ++i) {
+                    const float dd = half_bits_to_float(d[u][i]);
+                    acc[i] = ffma2(blk[i], make_float2(dd, dd), acc[i]);
+                }
             }
         }
     }
+    __device__ __forceinline__ void prime(int nb, int lp) { load(wA, dA, lp, nb); }
+    __device__ __forceinline__ void run(const float *xs, int nb, int lp, float (&out)[NS])
+    {
+        constexpr int STEP = LG * U;
+        float2 acc[NS];
 #pragma unroll
-    for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
-}
+        for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
+        for (int b0 = lp; b0 < nb; b0 += 2 * STEP) {
+            load(wB, dB, b0 + STEP, nb);
+            compute(wA, dA, b0, nb, xs, acc);
+            if (b0 + STEP >= nb) break;
+            load(wA, dA, b0 + 2 * STEP, nb);
+            compute(wB, dB, b0 + STEP, nb, xs, acc);
+        }
+#pragma unroll
+        for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
+    }
+};
 
 // ---------------------------------------------------------------- Q8_0
 // Packed Q8_0: byte plane (32 B per block, offset binary) + fp16 scale plane.
@@ -119,38 +176,49 @@ __device__ __forceinline__ void q8_0_stream(const uint4 *const (&wp)[NS],
 // Packed Q4_K: nibble plane (128 B per super-block, sub-block s at 16 s, element
 // order) + record plane (16 B per super-block: d, dmin, 12 scale bytes).
 // A lane handles one 32-weight sub-block per step: sub-block index sb (global
-// within the row), super-block sb/8, sub-block s = sb%8.  xsum holds the sum
-// of each 32-element block of x (shared memory).
-__device__ __forceinline__ void q4k_scale_min(uint4 rec, int s, float &sc, float &mn)
+// within the row), super-block sb/8, sub-block s = sb%8.  The staged x block
+// carries the block's sum of x (for the min term).
+//
+// The 6-bit scale and min of sub-block s come from the record's scale bytes
+// A = byte (s&3), B = byte (s&3)+4, C = byte (s&3)+8: sc = A&63, m = B&63
+// for s < 4; sc = (C&15) | (A>>6)<<4, m = (C>>4) | (B>>6)<<4 for s >= 4.  A
+// lane always sees the same s, so the shifts and masks are per-lane
+// constants and the decode has no branch:
+//   sc = ((y >> shA) & m1) | ((w >> shC) & m2)
+//   m  = ((z >> shA) & m1) | ((w >> (shC+4)) & m2)
+// with shA = 8(s&3) (+2 for s >= 4), shC = 8(s&3), m1 = 63 / 48, m2 = 0 / 15.
+struct Q4KSub {
+    int shA, shC;
+    uint32_t m1, m2;
+};
+__device__ __forceinline__ Q4KSub q4k_sub(int s)
 {
-    const int sh = 8 * (s & 3);
-    const uint32_t A = (rec.y >> sh) & 0xFFu;  // scale byte s&3
-    const uint32_t B = (rec.z >> sh) & 0xFFu;  // scale byte (s&3)+4
-    const uint32_t C = (rec.w >> sh) & 0xFFu;  // scale byte (s&3)+8
-    uint32_t isc, imn;
-    if (s < 4) {
-        isc = A & 63u;
-        imn = B & 63u;
-    } else {
-        isc = (C & 15u) | ((A >> 6) << 4);
-        imn = (C >> 4) | ((B >> 6) << 4);
-    }
-    sc = static_cast<float>(isc);
-    mn = static_cast<float>(imn);
+    Q4KSub c;
+    c.shC = 8 * (s & 3);
+    c.shA = c.shC + (s >= 4 ? 2 : 0);
+    c.m1 = s >= 4 ? 48u : 63u;
+    c.m2 = s >= 4 ? 15u : 0u;
+    return c;
+}
+// d * sc and dmin * m of one sub-block (both exact in f32: 11-bit x 6-bit).
+__device__ __forceinline__ void q4k_dm(uint4 rec, const Q4KSub &c, float &dsc, float &dm)
+{
+    const uint32_t isc = ((rec.y >> c.shA) & c.m1) | ((rec.w >> c.shC) & c.m2);
+    const uint32_t imn = ((rec.z >> c.shA) & c.m1) | ((rec.w >> (c.shC + 4)) & c.m2);
+    dsc = half_bits_to_float(rec.x & 0xFFFFu) * __uint2float_rn(isc);
+    dm = half_bits_to_float(rec.x >> 16) * __uint2float_rn(imn);
 }
 
+// One row task of NS Q4_K rows, in the same prime() / run() form as Q40Stream.
 template <int LG, int NS, int U>
-__device__ __forceinline__ void q4k_stream(const uint4 *const (&wp)[NS], const uint4 *const (&rp)[NS],
-                                           const float *xs, const float *xsum, int nsb, int lp,
-                                           float (&out)[NS])
-{
-    float2 acc[NS];
-#pragma unroll
-    for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
+struct Q4KStream {
+    static_assert(LG % 8 == 0, "a lane's sub-block position must be fixed");
+    const uint4 *wp[NS];
+    const uint4 *rp[NS];
+    uint4 wA[U][NS], wB[U][NS], rA[U][NS], rB[U][NS];
 
-    for (int b0 = lp; b0 < nsb; b0 += LG * U) {
-        uint4 w[U][NS];
-        uint4 rec[U][NS];
+    __device__ __forceinline__ void load(uint4 (&w)[U][NS], uint4 (&r)[U][NS], int b0, int nsb) const
+    {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int b = b0 + u * LG;
@@ -159,167 +227,50 @@ __device__ __forceinline__ void q4k_stream(const uint4 *const (&wp)[NS], const u
             for (int i = 0; i < NS; ++i) {
                 w[u][i] = ok ? ld_stream16(wp[i] + b) : make_uint4(0u, 0u, 0u, 0u);
                 // the 16-byte record is shared by the 8 lanes of a super-block
-                rec[u][i] = ok ? __ldg(rp[i] + (b >> 3)) : make_uint4(0u, 0u, 0u, 0u);
+                r[u][i] = ok ? __ldg(rp[i] + (b >> 3)) : make_uint4(0u, 0u, 0u, 0u);
             }
         }
+    }
+    __device__ __forceinline__ void compute(const uint4 (&w)[U][NS], const uint4 (&r)[U][NS], int b0, int nsb,
+                                            const float *xs, const Q4KSub &sub, float2 (&acc)[NS]) const
+    {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int b = b0 + u * LG;
             if (b < nsb) {
-                float4 xv[8];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) xv[m] = ld_xchunk(xs, b, m);
+                const float *xb = xs + b * kXBlk;
                 float2 blk[NS];
-#pragma unroll
-                for (int i = 0; i < NS; ++i) blk[i] = nib32_dot_h<0>(w[u][i], xv);
-                const float xsb = xsum[b];
+                q4_block<0, NS>(w[u], xb, blk);
+                const float xsb = xb[32];
 #pragma unroll
                 for (int i = 0; i < NS; ++i) {
-                    float sc, mn;
-                    q4k_scale_min(rec[u][i], b & 7, sc, mn);
-                    const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(rec[u][i].x & 0xFFFFu)));
-                    const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(rec[u][i].x >> 16)));
-                    // d*sc and dmin*m are exact in f32 (11-bit x 6-bit products)
-                    const float dsc = d * sc, dm = dmin * mn;
-                    acc[i].x = fmaf(dsc, blk[i].x, acc[i].x);
-                    acc[i].y = fmaf(dsc, blk[i].y, acc[i].y);
+                    float dsc, dm;
+                    q4k_dm(r[u][i], sub, dsc, dm);
+                    acc[i] = ffma2(blk[i], make_float2(dsc, dsc), acc[i]);
                     acc[i].x = fmaf(-dm, xsb, acc[i].x);
                 }
             }
         }
     }
+    __device__ __forceinline__ void prime(int nsb, int lp) { load(wA, rA, lp, nsb); }
+    __device__ __forceinline__ void run(const float *xs, int nsb, int lp, float (&out)[NS])
+    {
+        constexpr int STEP = LG * U;
+        const Q4KSub sub = q4k_sub(lp & 7);
+        float2 acc[NS];
 #pragma unroll
-    for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
-}
-
-
-// ---------------------------------------------------------------- 32-byte loads (block pairs)
-// Same arithmetic with two consecutive blocks per lane and row per load (one
-// 256-bit load of 32 nibble bytes, one 32-bit load of the two scales): twice
-// the bytes per memory request of the one-block form.  Lane lp of a group
-// takes pairs lp, lp+LG, ...; pair p is blocks 2p and 2p+1 (nb even).
-__device__ __forceinline__ uint32_t ld_stream_u32(const void *p)
-{
-    uint32_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-
-template <int LG, int NS, int U>
-__device__ __forceinline__ void q4_0_stream2(const uint4 *const (&wp)[NS], const uint16_t *const (&sp)[NS],
-                                             const float *xs, int nb, int lp, float (&out)[NS])
-{
-    const int np = nb >> 1;
-    float2 acc[NS];
-#pragma unroll
-    for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
-
-    for (int p0 = lp; p0 < np; p0 += LG * U) {
-        uint4 w[U][NS][2];
-        uint32_t dd[U][NS];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int p = p0 + u * LG;
-            const bool ok = p < np;
-#pragma unroll
-            for (int i = 0; i < NS; ++i) {
-                if (ok) {
-                    ld_stream32(wp[i] + 2 * p, w[u][i][0], w[u][i][1]);
-                    dd[u][i] = ld_stream_u32(sp[i] + 2 * p);
-                } else {
-                    w[u][i][0] = make_uint4(0u, 0u, 0u, 0u);
-                    w[u][i][1] = make_uint4(0u, 0u, 0u, 0u);
-                    dd[u][i] = 0u;
-                }
-            }
+        for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
+        for (int b0 = lp; b0 < nsb; b0 += 2 * STEP) {
+            load(wB, rB, b0 + STEP, nsb);
+            compute(wA, rA, b0, nsb, xs, sub, acc);
+            if (b0 + STEP >= nsb) break;
+            load(wA, rA, b0 + 2 * STEP, nsb);
+            compute(wB, rB, b0 + STEP, nsb, xs, sub, acc);
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int p = p0 + u * LG;
-            if (p < np) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int b = 2 * p + h;
-                    float4 xv[8];
-#pragma unroll
-                    for (int m = 0; m < 8; ++m) xv[m] = ld_xchunk(xs, b, m);
-                    float2 blk[NS];
-#pragma unroll
-                    for (int i = 0; i < NS; ++i) blk[i] = nib32_dot_h<8>(w[u][i][h], xv);
-#pragma unroll
-                    for (int i = 0; i < NS; ++i) {
-                        const uint16_t hb = static_cast<uint16_t>(h ? (dd[u][i] >> 16) : (dd[u][i] & 0xFFFFu));
-                        const float d = __half2float(__ushort_as_half(hb));
-                        acc[i] = ffma2(blk[i], make_float2(d, d), acc[i]);
-                    }
-                }
-            }
-        }
+        for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
     }
-#pragma unroll
-    for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
-}
-
-template <int LG, int NS, int U>
-__device__ __forceinline__ void q4k_stream2(const uint4 *const (&wp)[NS], const uint4 *const (&rp)[NS],
-                                            const float *xs, const float *xsum, int nsb, int lp, float (&out)[NS])
-{
-    const int np = nsb >> 1;
-    float2 acc[NS];
-#pragma unroll
-    for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
-
-    for (int p0 = lp; p0 < np; p0 += LG * U) {
-        uint4 w[U][NS][2];
-        uint4 rec[U][NS];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int p = p0 + u * LG;
-            const bool ok = p < np;
-#pragma unroll
-            for (int i = 0; i < NS; ++i) {
-                if (ok) {
-                    ld_stream32(wp[i] + 2 * p, w[u][i][0], w[u][i][1]);
-                    rec[u][i] = __ldg(rp[i] + (p >> 2));  // both sub-blocks lie in super-block p/4
-                } else {
-                    w[u][i][0] = make_uint4(0u, 0u, 0u, 0u);
-                    w[u][i][1] = make_uint4(0u, 0u, 0u, 0u);
-                    rec[u][i] = make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int p = p0 + u * LG;
-            if (p < np) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int b = 2 * p + h;
-                    float4 xv[8];
-#pragma unroll
-                    for (int m = 0; m < 8; ++m) xv[m] = ld_xchunk(xs, b, m);
-                    float2 blk[NS];
-#pragma unroll
-                    for (int i = 0; i < NS; ++i) blk[i] = nib32_dot_h<0>(w[u][i][h], xv);
-                    const float xsb = xsum[b];
-#pragma unroll
-                    for (int i = 0; i < NS; ++i) {
-                        float sc, mn;
-                        q4k_scale_min(rec[u][i], b & 7, sc, mn);
-                        const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(rec[u][i].x & 0xFFFFu)));
-                        const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(rec[u][i].x >> 16)));
-                        const float dsc = d * sc, dm = dmin * mn;
-                        acc[i].x = fmaf(dsc, blk[i].x, acc[i].x);
-                        acc[i].y = fmaf(dsc, blk[i].y, acc[i].y);
-                        acc[i].x = fmaf(-dm, xsb, acc[i].x);
-                    }
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
-}
+};
 
 // ---------------------------------------------------------------- kernel-side common
 constexpr int kThreadsPerCta = 256;
@@ -334,24 +285,6 @@ __device__ __forceinline__ void prefetch_rows_l2(const void *const (&rowp)[NS], 
 #pragma unroll
     for (int i = 0; i < NS; ++i)
         if (lane == i) prefetch_l2_bulk(rowp[i], row_bytes);
-}
-
-// Per-block sums of x (for the min term), after stage_x.
-__device__ __forceinline__ void stage_xsum(float *xsum, const float *xs, int nb)
-{
-    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-        float s = 0.f;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const float4 v = ld_xchunk(xs, b, m);
-            s += v.x;
-            s += v.y;
-            s += v.z;
-            s += v.w;
-        }
-        xsum[b] = s;
-    }
-    __syncthreads();
 }
 
 // GELU, tanh form, with the tanh argument clamped to +-15 (tanh(15) rounds
@@ -383,19 +316,6 @@ __device__ __forceinline__ float gelu_tanh(float a)
         GQ_GEO_CASE1(geo, CASE, 8, 1)         \
         GQ_GEO_CASE1(geo, CASE, 8, 2)         \
         GQ_GEO_CASE1(geo, CASE, 8, 4)         \
-        return GQ_ERR_SHAPE;                  \
-    } while (0)
-// Block-pair (32-byte load) kernels: LG in {4, 8, 16, 32}, R in {1, 2}, U in {2, 4}.
-#define GQ_PAIR_SWITCH(geo, CASE)             \
-    do {                                      \
-        GQ_GEO_CASE1(geo, CASE, 32, 1)        \
-        GQ_GEO_CASE1(geo, CASE, 32, 2)        \
-        GQ_GEO_CASE1(geo, CASE, 16, 1)        \
-        GQ_GEO_CASE1(geo, CASE, 16, 2)        \
-        GQ_GEO_CASE1(geo, CASE, 8, 1)         \
-        GQ_GEO_CASE1(geo, CASE, 8, 2)         \
-        GQ_GEO_CASE1(geo, CASE, 4, 1)         \
-        GQ_GEO_CASE1(geo, CASE, 4, 2)         \
         return GQ_ERR_SHAPE;                  \
     } while (0)
 #define GQ_GEO_SWITCH_R12(geo, CASE)          \

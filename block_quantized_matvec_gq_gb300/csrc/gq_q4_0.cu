@@ -5,7 +5,7 @@
 // accumulation.  "Metal kernel capability table (Phase B ground truth)",
 // section 1, q4_f32_matvec (rows masked; here K is never truncated).
 //
-// Persistent kernel: each CTA stages x once (swizzled, cp.async), then its
+// Persistent kernel: each CTA stages x once (padded 144-byte blocks), then its
 // warps stream packed Q4_0 rows (16-byte nibble loads + fp16 scales); see
 // gq_matvec.cuh for the lane geometry and the exact nibble-to-f32 step.
 #include "gq_host.h"
@@ -13,10 +13,10 @@
 
 namespace gq {
 
-template <int LG, int R, int U, int P>
+template <int LG, int R, int U>
 __global__ void __launch_bounds__(kThreadsPerCta, 2)
     k_q4_0_matvec(const uint4 *__restrict__ nib, const uint16_t *__restrict__ dsc,
-                  const float *__restrict__ x, float *__restrict__ y, int rows, int nb)
+                  const float *__restrict__ x, float *__restrict__ y, int rows, int nb, int early)
 {
     extern __shared__ __align__(16) float xs[];
     constexpr int G = 32 / LG, TR = G * R;
@@ -24,32 +24,39 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     const int g = lane / LG, lp = lane % LG;
     const int ntasks = (rows + TR - 1) / TR;
     const int first = blockIdx.x * kWarpsPerCta + warp;
+    const int stride = gridDim.x * kWarpsPerCta;
 
+    Q40Stream<LG, R, U> st;
+    auto setup = [&](int task) {
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int r = min(task * TR + g * R + i, rows - 1);
+            st.wp[i] = nib + static_cast<size_t>(r) * nb;
+            st.sp[i] = dsc + static_cast<size_t>(r) * nb;
+        }
+        st.prime(nb, lp);
+    };
+    // Weights never depend on the previous kernel: prefetch this warp's first
+    // rows into L2 before waiting for it and, when warps have about one task
+    // each (`early`, decided by the host), issue that task's first loads too.
+    // (Measured: with several tasks per warp the early loads cost more than
+    // they save.)
     if (first < ntasks) {
         const void *rp[TR];
 #pragma unroll
         for (int i = 0; i < TR; ++i) rp[i] = nib + static_cast<size_t>(min(first * TR + i, rows - 1)) * nb;
         prefetch_rows_l2<TR>(rp, static_cast<uint32_t>(nb) * 16u, lane);
+        if (early) setup(first);
     }
     pdl_wait();
-    stage_x_perm8(xs, x, nb * 32);
+    stage_x_q4<false>(xs, x, nb * 32);
     pdl_launch_dependents();
 
-    for (int task = first; task < ntasks; task += gridDim.x * kWarpsPerCta) {
-        const int r0 = task * TR + g * R;
-        const uint4 *wp[R];
-        const uint16_t *sp[R];
-#pragma unroll
-        for (int i = 0; i < R; ++i) {
-            const int r = min(r0 + i, rows - 1);
-            wp[i] = nib + static_cast<size_t>(r) * nb;
-            sp[i] = dsc + static_cast<size_t>(r) * nb;
-        }
+    for (int task = first; task < ntasks; task += stride) {
+        if (task != first || !early) setup(task);
         float out[R];
-        if (P == 2)
-            q4_0_stream2<LG, R, U>(wp, sp, xs, nb, lp, out);
-        else
-            q4_0_stream<LG, R, U>(wp, sp, xs, nb, lp, out);
+        st.run(xs, nb, lp, out);
+        const int r0 = task * TR + g * R;
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             const float s = group_sum<LG>(out[i]);
@@ -64,22 +71,18 @@ int launch_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K,
     const int nb = K / 32;
     const uint4 *nib = static_cast<const uint4 *>(W);
     const uint16_t *dsc = reinterpret_cast<const uint16_t *>(nib + static_cast<size_t>(rows) * nb);
-    const size_t smem = static_cast<size_t>(K) * sizeof(float);
+    const size_t smem = static_cast<size_t>(nb) * kXBlk * sizeof(float);
     const long long ntasks = (rows + (32 / geo.lg) * geo.r - 1) / ((32 / geo.lg) * geo.r);
+    if (geo.p != 1) return GQ_ERR_SHAPE;
 #define CASE(LG, R, U)                                                                                 \
     {                                                                                                  \
-        auto kern = k_q4_0_matvec<LG, R, U, PP>;                                                       \
+        auto kern = k_q4_0_matvec<LG, R, U>;                                                           \
         const int grid = persistent_grid(reinterpret_cast<const void *>(kern), kThreadsPerCta, smem, ntasks); \
         if (grid <= 0) return GQ_ERR_SHAPE;                                                            \
-        return status_from(launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, nib, dsc, x, y, rows, nb)); \
+        const int early = ntasks * 4 <= static_cast<long long>(grid) * kWarpsPerCta * 5;              \
+        return status_from(launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, nib, dsc, x, y, rows, nb, early)); \
     }
-    if (geo.p == 2) {
-        constexpr int PP = 2;
-        GQ_PAIR_SWITCH(geo, CASE);
-    } else {
-        constexpr int PP = 1;
-        GQ_GEO_SWITCH(geo, CASE);
-    }
+    GQ_GEO_SWITCH(geo, CASE);
 #undef CASE
 }
 

@@ -16,6 +16,9 @@ __global__ void __launch_bounds__(256)
                     long long nblocks)
 {
     const int lane = threadIdx.x & 31;
+    // dependents launch once every CTA of this grid has started; they still
+    // wait for its completion before reading Xq and dx
+    pdl_launch_dependents();
     pdl_wait();
     for (long long blk = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; blk < nblocks;
          blk += ((long long)gridDim.x * blockDim.x) >> 5) {
@@ -33,7 +36,6 @@ __global__ void __launch_bounds__(256)
         Xq[blk * 32 + lane] = static_cast<int8_t>(q);
         if (lane == 0) dx[blk] = d;
     }
-    pdl_launch_dependents();
 }
 
 int launch_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, cudaStream_t s)
