@@ -152,7 +152,12 @@ int gq_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, gq_str
     return launch_quantize_q8_0(X, Xq, dx, K, M, reinterpret_cast<cudaStream_t>(stream));
 }
 
-size_t gq_q4_0_gemm_workspace_bytes(int K, int M) { return gemm_workspace_bytes(K, M); }
+size_t gq_q4_0_gemm_workspace_bytes(int K, int M)
+{
+    // enough for either contraction path (the split path needs the most)
+    const size_t a = gemm_workspace_bytes(K, M), b = gemm_split_workspace_bytes(K, M);
+    return a > b ? a : b;
+}
 
 int gq_q4_0_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *Y, void *workspace,
                        size_t workspace_bytes, int rows, int K, int M, gq_stream_t stream)
@@ -161,8 +166,10 @@ int gq_q4_0_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *
     if (!aligned16(W) || !aligned16(Xq) || !aligned16(dx) || !aligned16(Y) || !aligned16(workspace))
         return GQ_ERR_ALIGN;
     if (rows < 1 || M < 1 || K < 32 || K % 32 != 0) return GQ_ERR_SHAPE;
-    return launch_gemm_q8act_tc(W, Xq, dx, Y, workspace, workspace_bytes, rows, K, M,
-                                reinterpret_cast<cudaStream_t>(stream));
+    if (workspace_bytes < gq_q4_0_gemm_workspace_bytes(K, M)) return GQ_ERR_WORKSPACE;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (gemm_split_supported(K)) return launch_gemm_split(W, Xq, dx, Y, workspace, workspace_bytes, rows, K, M, st);
+    return launch_gemm_q8act_tc(W, Xq, dx, Y, workspace, workspace_bytes, rows, K, M, st);
 }
 
 int gq_q4_0_gemm_block_dots(const void *W, const int8_t *Xq, int32_t *D, void *workspace, size_t workspace_bytes,
@@ -171,6 +178,7 @@ int gq_q4_0_gemm_block_dots(const void *W, const int8_t *Xq, int32_t *D, void *w
     if (!W || !Xq || !D || !workspace) return GQ_ERR_NULL;
     if (!aligned16(W) || !aligned16(Xq) || !aligned16(D) || !aligned16(workspace)) return GQ_ERR_ALIGN;
     if (rows < 1 || M < 1 || K < 32 || K % 32 != 0) return GQ_ERR_SHAPE;
+    if (workspace_bytes < gq_q4_0_gemm_workspace_bytes(K, M)) return GQ_ERR_WORKSPACE;
     return launch_block_dots_tc(W, Xq, D, workspace, workspace_bytes, rows, K, M,
                                 reinterpret_cast<cudaStream_t>(stream));
 }

@@ -1,0 +1,520 @@
+// gq_gemm_split.cu -- the prefill contraction with both block scales folded
+// into the tensor-core operands, so Y accumulates in tensor memory across
+// the whole of K (no per-block read-out).
+//
+// "Gemma 4 M4 Max kernel roadmap", K3 "prefill path" (batched Q4_0
+// matrix-matrix):  Y[t][r] = sum_b d_w[r][b] * dx[t][b] * D[t][r][b]
+// with D the integer dot of block b.  Written as one sum over k,
+//   Y[t][r] = sum_k A'[t][k] * B'[r][k],
+//   A'[t][k] = dx[t][k/32] * Xq[t][k]          (f32: one rounding, 2^-24)
+//   B'[r][k] = d_w[r][k/32] * (q_w[r][k] - 8)  (exact in f32: 11 x 4 bits)
+// and fed to kind::f16 MMAs with bf16 operands, each operand split into
+// bf16 pieces: B' = B1 + B2 exactly (at most 15 significant bits), A' =
+// A1 + A2 + A3 to 24 bits.  Five products per K step (A1B1, A1B2, A2B1,
+// A2B2, A3B1) leave out only A3*B2, of relative size 2^-24; every piece
+// product is exact.  The tensor core's f32 accumulation truncates (each add
+// errs toward zero, so the error grows with the number of adds), hence the
+// accumulator is read out every 8 blocks (80 MMAs) and the chunks are summed
+// in f32 registers with round-to-nearest.  The result equals the
+// block-scaled sum up to f32 rounding, like the per-block fold, at five
+// times the tensor work and one eighth of the read-outs, with no scale
+// arithmetic on the CUDA cores.
+//
+// Requires K % 256 == 0 (8-block scale tiles); other K use the per-block
+// fold in gq_gemm_tc.cu.
+//
+// Kernels:
+//   k_xq_split   writes A1, A2, A3 into the caller's workspace, one 24 KB
+//                chunk per (128-token tile, 32-block) in the UMMA K-major
+//                layout (bf16, 8-element groups in the order 0,4,1,5,2,6,3,7).
+//   k_gemm_split one 480-thread CTA per SM, persistent over 128-token x
+//                192-row tiles, two 8-block chunk accumulators in TMEM:
+//   warps 0-11  workers: for each block, build B1, B2 from the nibbles and
+//               the d_w scale tile into the operand stage the MMA of block
+//               g-S has released; after each 8-block chunk, add its
+//               accumulator into f32 registers (warp w: TMEM lanes
+//               32*(w%4).., 64 of the 192 columns) and store Y after a
+//               tile's last chunk.
+//   warp 12     one lane: TMA loads of the 192 x 16 B nibbles per block
+//               and, every 8 blocks, of the 8 x 192 d_w scale tile.
+//   warp 13     one lane: 10 MMAs (M128 N192 K16) per block into the
+//               chunk's accumulator; owns TMEM.
+//   warp 14     one lane: bulk copy of each block's 24 KB A chunk.
+// Every mbarrier wait is bounded (see gq_tc.cuh): on timeout the kernel
+// records GQ_ERR_TIMEOUT, every role leaves its loop, TMEM is released.
+#include <cuda_bf16.h>
+
+#include "gq_tc.cuh"
+
+namespace gq {
+namespace tcs {
+
+using namespace tcu;
+
+constexpr int TM = 128;   // tokens per tile (MMA M, TMEM lanes)
+constexpr int TN = 192;   // weight rows per tile (MMA N, TMEM columns)
+constexpr int KB = 32;    // K per quantization block
+constexpr int S = 4;      // operand stages
+constexpr int RAW = 8;    // raw nibble stages
+constexpr int SG = 8;     // blocks per scale tile
+constexpr int STG = 2;    // scale tile stages
+constexpr int WORK_WARPS = 12;
+constexpr int NWORK = WORK_WARPS * 32;
+constexpr int TMA_WARP = 12;
+constexpr int MMA_WARP = 13;
+constexpr int ACOPY_WARP = 14;
+constexpr int NTHREADS = 15 * 32;  // 480: up to 128 registers per thread
+constexpr int EPI_COLS = TN / (WORK_WARPS / 4);  // 64
+constexpr int NACC = 2;          // chunk accumulators (a chunk = SG blocks)
+constexpr int ACC_STRIDE = 256;  // TMEM column offset between them
+constexpr int TMEM_COLS = 512;
+
+constexpr int APIECE = TM * KB * 2;   // 8192: one bf16 piece of A
+constexpr int A_BYTES = 3 * APIECE;   // 24576: one workspace chunk
+constexpr int BPIECE = TN * KB * 2;   // 12288: one bf16 piece of B
+constexpr int B_BYTES = 2 * BPIECE;   // 24576
+constexpr int RB_BYTES = TN * 16;     // 3072: nibbles (TMA box 16 x 192)
+constexpr int STW_BYTES = TN * SG * 2;  // 3072: d_w fp16 [192 rows][8 blocks]
+
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + S * A_BYTES;
+constexpr int OFF_RAW = OFF_B + S * B_BYTES;
+constexpr int OFF_STILE = OFF_RAW + RAW * RB_BYTES;
+constexpr int OFF_BAR = OFF_STILE + STG * STW_BYTES;
+// afull, opempty, full per operand stage; rfull, rempty per raw stage;
+// cfull, cempty per chunk accumulator; sfull, sempty per scale tile stage; drain
+constexpr int N_BARS = 3 * S + 2 * RAW + 2 * NACC + 2 * STG + 1;
+constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 16;
+
+static_assert((S & (S - 1)) == 0 && (RAW & (RAW - 1)) == 0 && (SG & (SG - 1)) == 0 && (STG & (STG - 1)) == 0 &&
+                  (NACC & (NACC - 1)) == 0,
+              "ring sizes are powers of two");
+static_assert(OFF_B % 1024 == 0 && OFF_RAW % 1024 == 0 && OFF_STILE % 128 == 0 && OFF_BAR % 8 == 0 &&
+                  SMEM_BYTES <= 232448,
+              "shared memory layout");
+static_assert(NWORK * 2 == TN * 4, "two 8-element nibble groups per worker thread");
+
+constexpr uint32_t kIdesc = idesc_f16(TM, TN, true);  // bf16 A and B
+
+// ---------------------------------------------------------------- operand pieces
+__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+// (a, b) -> bf16x2 hi = RN(a, b) and the exact remainders (a - hi.x, b - hi.y).
+__device__ __forceinline__ uint32_t split_bf2(float a, float b, float &ra, float &rb)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    ra = a - __low2float(h);
+    rb = b - __high2float(h);
+    return bf2_bits(h);
+}
+
+// Activation pieces: thread p writes 16 bytes of each piece of chunk p/512
+// = (token tile T, block b), T-major, at 8-element group position p % 512
+// (= op_off(row, kg) / 16).  Tokens past M are zeros.
+__global__ void __launch_bounds__(256) k_xq_split(const int8_t *__restrict__ Xq, const float *__restrict__ dx,
+                                                  uint4 *__restrict__ Xh, int K, int M, long long npieces)
+{
+    pdl_launch_dependents();  // the GEMM's prologue may overlap; it waits for this grid before reading Xh
+    pdl_wait();
+    const int nb = K / KB;
+    for (long long p = blockIdx.x * 256ll + threadIdx.x; p < npieces; p += static_cast<long long>(gridDim.x) * 256) {
+        const long long chunk = p >> 9;
+        const int within = static_cast<int>(p & 511);
+        const int row = ((within >> 5) << 3) | (within & 7), kg = (within >> 3) & 3;
+        const long long T = chunk / nb;
+        const int b = static_cast<int>(chunk - T * nb);
+        const long long t = T * TM + row;
+        uint4 o1 = make_uint4(0u, 0u, 0u, 0u), o2 = o1, o3 = o1;
+        if (t < M) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(Xq + t * K + b * KB + kg * 8));
+            const float d = __ldg(dx + t * nb + b);
+            float e[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                e[j] = d * static_cast<float>(static_cast<int8_t>(v.x >> (8 * j)));
+                e[j + 4] = d * static_cast<float>(static_cast<int8_t>(v.y >> (8 * j)));
+            }
+            uint32_t w1[4], w2[4], w3[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {  // word i holds elements (i, i+4)
+                float r1a, r1b, r2a, r2b, r3a, r3b;
+                w1[i] = split_bf2(e[i], e[i + 4], r1a, r1b);
+                w2[i] = split_bf2(r1a, r1b, r2a, r2b);
+                w3[i] = split_bf2(r2a, r2b, r3a, r3b);
+            }
+            o1 = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+            o2 = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+            o3 = make_uint4(w3[0], w3[1], w3[2], w3[3]);
+        }
+        uint4 *dst = Xh + chunk * (A_BYTES / 16) + within;
+        dst[0] = o1;
+        dst[APIECE / 16] = o2;
+        dst[2 * APIECE / 16] = o3;
+    }
+}
+
+// Weight pieces of one 8-element group: nibbles of w (element order) and
+// the block's d_w -> B1 and B2 chunks (16 bytes each, order 0,4,1,5,...).
+__device__ __forceinline__ void nib8_split(uint32_t w, float dw, uint4 &b1, uint4 &b2)
+{
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        // exact q - 8 through the 2^23 bit pattern
+        const float qa = __uint_as_float(((w >> (4 * i)) & 15u) | kMagic) - (8388608.0f + 8.0f);
+        const float qb = __uint_as_float(((w >> (4 * i + 16)) & 15u) | kMagic) - (8388608.0f + 8.0f);
+        float ra, rb, unused_a, unused_b;
+        h[i] = split_bf2(qa * dw, qb * dw, ra, rb);
+        l[i] = split_bf2(ra, rb, unused_a, unused_b);  // exact: at most 7 bits remain
+    }
+    b1 = make_uint4(h[0], h[1], h[2], h[3]);
+    b2 = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+struct Work {
+    int ntm, ntiles, nb;
+};
+__device__ __forceinline__ void tile_origin(const Work &w, int tile, int &t0, int &r0)
+{
+    const int tr = tile / w.ntm;
+    t0 = (tile - tr * w.ntm) * TM;
+    r0 = tr * TN;
+}
+
+// ---------------------------------------------------------------- the kernel
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_gemm_split(const uint8_t *__restrict__ Xh, const __grid_constant__ CUtensorMap mapB,
+                 const __grid_constant__ CUtensorMap mapW, float *__restrict__ Y, int rows, int K, int M,
+                 int *__restrict__ status)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_afull = sbase + OFF_BAR, bar_opempty = bar_afull + 8 * S, bar_full = bar_opempty + 8 * S;
+    const uint32_t bar_rfull = bar_full + 8 * S, bar_rempty = bar_rfull + 8 * RAW;
+    const uint32_t bar_cfull = bar_rempty + 8 * RAW, bar_cempty = bar_cfull + 8 * NACC;
+    const uint32_t bar_sfull = bar_cempty + 8 * NACC, bar_sempty = bar_sfull + 8 * STG;
+    const uint32_t bar_drain = bar_sempty + 8 * STG;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+
+    Work w;
+    w.nb = K / KB;
+    w.ntm = (M + TM - 1) / TM;
+    w.ntiles = w.ntm * ((rows + TN - 1) / TN);
+    const int my_tiles = (w.ntiles > static_cast<int>(blockIdx.x))
+                             ? (w.ntiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                             : 0;
+    const int nblocks = my_tiles * w.nb;  // the host checks that this fits an int
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(bar_afull + 8 * i, 1);
+            mbar_init(bar_opempty + 8 * i, 1);
+            mbar_init(bar_full + 8 * i, WORK_WARPS);
+        }
+        for (int i = 0; i < RAW; ++i) {
+            mbar_init(bar_rfull + 8 * i, 1);
+            mbar_init(bar_rempty + 8 * i, WORK_WARPS);
+        }
+        for (int i = 0; i < NACC; ++i) {
+            mbar_init(bar_cfull + 8 * i, 1);
+            mbar_init(bar_cempty + 8 * i, WORK_WARPS);
+        }
+        for (int i = 0; i < STG; ++i) {
+            mbar_init(bar_sfull + 8 * i, 1);
+            mbar_init(bar_sempty + 8 * i, WORK_WARPS);
+        }
+        mbar_init(bar_drain, 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == MMA_WARP) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();
+
+    if (warp == TMA_WARP) {
+        // ------------------------------------------------ nibble and scale tile loads
+        if (lane == 0) {
+            int tile = static_cast<int>(blockIdx.x), b = 0, t0, r0;
+            tile_origin(w, tile, t0, r0);
+            int rs = 0, nr = 0, gi = 0;
+            uint32_t rph = 0;
+            for (int gb = 0; gb < nblocks; ++gb) {
+                if ((b & (SG - 1)) == 0) {
+                    const int sg = gi & (STG - 1);
+                    if (!wait_bounded(bar_sempty + 8 * sg, (static_cast<uint32_t>(gi / STG) & 1u) ^ 1u, abort, status))
+                        break;
+                    mbar_expect_tx(bar_sfull + 8 * sg, STW_BYTES);
+                    tma_load_2d(sbase + OFF_STILE + sg * STW_BYTES, &mapW, b, r0, bar_sfull + 8 * sg);
+                    ++gi;
+                }
+                if (!wait_bounded(bar_rempty + 8 * rs, rph ^ 1u, abort, status)) break;
+                mbar_expect_tx(bar_rfull + 8 * rs, RB_BYTES);
+                tma_load_2d(sbase + OFF_RAW + rs * RB_BYTES, &mapB, b * 16, r0, bar_rfull + 8 * rs);
+                ++nr;
+                if (++rs == RAW) {
+                    rs = 0;
+                    rph ^= 1u;
+                }
+                if (++b == w.nb) {
+                    b = 0;
+                    tile += static_cast<int>(gridDim.x);
+                    tile_origin(w, tile, t0, r0);
+                }
+            }
+            // No load may still be landing in shared memory when the CTA exits
+            // (relevant only after an abort: normally every load has been consumed).
+            volatile int no_abort = 0;
+            for (int g = (nr > RAW ? nr - RAW : 0); g < nr; ++g)
+                wait_bounded(bar_rfull + 8 * (g % RAW), static_cast<uint32_t>((g / RAW) & 1), &no_abort, status);
+            for (int g = (gi > STG ? gi - STG : 0); g < gi; ++g)
+                wait_bounded(bar_sfull + 8 * (g % STG), static_cast<uint32_t>((g / STG) & 1), &no_abort, status);
+        }
+        __syncwarp();
+    } else if (warp == ACOPY_WARP) {
+        // ------------------------------------------------ A operand copies
+        if (lane == 0) {
+            int tile = static_cast<int>(blockIdx.x), b = 0, t0, r0;
+            tile_origin(w, tile, t0, r0);
+            int s = 0, na = 0;
+            uint32_t sph = 0;
+            for (int gb = 0; gb < nblocks; ++gb) {
+                if (!wait_bounded(bar_opempty + 8 * s, sph ^ 1u, abort, status)) break;
+                mbar_expect_tx(bar_afull + 8 * s, A_BYTES);
+                bulk_load(sbase + OFF_A + s * A_BYTES,
+                          Xh + (static_cast<size_t>(t0 / TM) * w.nb + b) * static_cast<size_t>(A_BYTES), A_BYTES,
+                          bar_afull + 8 * s);
+                ++na;
+                if (++s == S) {
+                    s = 0;
+                    sph ^= 1u;
+                }
+                if (++b == w.nb) {
+                    b = 0;
+                    tile += static_cast<int>(gridDim.x);
+                    tile_origin(w, tile, t0, r0);
+                }
+            }
+            volatile int no_abort = 0;
+            for (int g = (na > S ? na - S : 0); g < na; ++g)
+                wait_bounded(bar_afull + 8 * (g % S), static_cast<uint32_t>((g / S) & 1), &no_abort, status);
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t sph = 0;
+            for (int gb = 0; gb < nblocks; ++gb) {
+                const int ci = gb / SG, acc = ci & (NACC - 1);  // chunk, its accumulator
+                const bool cfirst = (gb & (SG - 1)) == 0;
+                if (!wait_bounded(bar_afull + 8 * s, sph, abort, status)) break;
+                if (!wait_bounded(bar_full + 8 * s, sph, abort, status)) break;
+                if (cfirst &&
+                    !wait_bounded(bar_cempty + 8 * acc, (static_cast<uint32_t>(ci / NACC) & 1u) ^ 1u, abort, status))
+                    break;
+                tc_fence_after();
+                const uint32_t a0 = sbase + OFF_A + s * A_BYTES, b0 = sbase + OFF_B + s * B_BYTES;
+                const uint32_t d = tmem + acc * ACC_STRIDE;
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const uint32_t ka = a0 + ks * 256, kb = b0 + ks * 256;
+                    const uint64_t A1 = smem_desc(ka, 128, 512), A2 = smem_desc(ka + APIECE, 128, 512),
+                                   A3 = smem_desc(ka + 2 * APIECE, 128, 512);
+                    const uint64_t B1 = smem_desc(kb, 128, 512), B2 = smem_desc(kb + BPIECE, 128, 512);
+                    mma_f16(d, A1, B1, kIdesc, (cfirst && ks == 0) ? 0u : 1u);
+                    mma_f16(d, A1, B2, kIdesc, 1u);
+                    mma_f16(d, A2, B1, kIdesc, 1u);
+                    mma_f16(d, A2, B2, kIdesc, 1u);
+                    mma_f16(d, A3, B1, kIdesc, 1u);
+                }
+                mma_commit(bar_opempty + 8 * s);
+                if ((gb & (SG - 1)) == SG - 1) mma_commit(bar_cfull + 8 * acc);
+                if (++s == S) {
+                    s = 0;
+                    sph ^= 1u;
+                }
+            }
+            // every issued MMA has completed before tensor memory is released
+            mma_commit(bar_drain);
+            wait_bounded(bar_drain, 0u, abort, status);
+        }
+        __syncwarp();
+    } else if (warp < WORK_WARPS) {
+        // ------------------------------------------------ workers
+        const int tid = threadIdx.x;  // 0..NWORK-1
+        const int q = warp & 3;       // TMEM lane quarter
+        const int c0 = (warp >> 2) * EPI_COLS;
+        // this thread's two nibble groups: row tid/2, K groups 2*(tid%2) and +1
+        const int crow = tid >> 1, chalf = tid & 1;
+        const uint32_t csrc = crow * 16 + chalf * 8;
+        const uint32_t cdst = op_off(crow, 2 * chalf);
+        bool ok = true;
+
+        // Chunks hold SG consecutive blocks of one tile (nb % SG == 0).
+        const int cpt = w.nb / SG;  // chunks per tile
+        float acc[EPI_COLS];        // written first by each tile's first chunk
+        // Add chunk c's accumulator into acc; after a tile's last chunk store Y.
+        auto readout = [&](int c) {
+            const int ab = c & (NACC - 1);
+            ok = wait_warp(bar_cfull + 8 * ab, static_cast<uint32_t>(c / NACC) & 1u, abort, status);
+            if (!ok) return;
+            tc_fence_after();
+            const int ct = c % cpt;  // chunk within its tile
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + ab * ACC_STRIDE + c0;
+#pragma unroll
+            for (int part = 0; part < EPI_COLS / 16; ++part) {
+                float d[16];
+                tmem_ld16(taddr + part * 16, d);
+                if (part == EPI_COLS / 16 - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_cempty + 8 * ab);
+                }
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    float2 v = make_float2(d[e], d[e + 1]);
+                    if (ct != 0) v = __fadd2_rn(v, make_float2(acc[part * 16 + e], acc[part * 16 + e + 1]));
+                    acc[part * 16 + e] = v.x;
+                    acc[part * 16 + e + 1] = v.y;
+                }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) asm volatile("" : "+f"(acc[part * 16 + e]));
+            }
+            if (ct == cpt - 1) {
+                int t0, r0;
+                tile_origin(w, static_cast<int>(blockIdx.x) + (c / cpt) * static_cast<int>(gridDim.x), t0, r0);
+                const int t = t0 + q * 32 + lane;
+                if (t < M) {
+                    float *yrow = Y + static_cast<size_t>(t) * rows + r0 + c0;
+                    const int nvalid = rows - (r0 + c0);
+                    const bool vec = (rows & 3) == 0;
+#pragma unroll
+                    for (int cc = 0; cc < EPI_COLS; cc += 4) {
+                        if (vec && cc + 4 <= nvalid) {
+                            *reinterpret_cast<float4 *>(yrow + cc) =
+                                make_float4(acc[cc], acc[cc + 1], acc[cc + 2], acc[cc + 3]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (cc + e < nvalid) yrow[cc + e] = acc[cc + e];
+                        }
+                    }
+                }
+            }
+        };
+
+        int rc = 0;  // next chunk to read out
+        const int nchunks = nblocks / SG;
+        for (int g = 0; g < nblocks && ok; ++g) {
+            const int s = g & (S - 1), rs = g & (RAW - 1), sg = (g / SG) & (STG - 1);
+            // the stage's previous block (g - S) must be done in the tensor core
+            if (g >= S) ok = wait_warp(bar_opempty + 8 * s, static_cast<uint32_t>(g / S - 1) & 1u, abort, status);
+            if (ok && (g & (SG - 1)) == 0)
+                ok = wait_warp(bar_sfull + 8 * sg, static_cast<uint32_t>(g / (SG * STG)) & 1u, abort, status);
+            if (ok) ok = wait_warp(bar_rfull + 8 * rs, static_cast<uint32_t>(g / RAW) & 1u, abort, status);
+            if (!ok) break;
+            {
+                const uint16_t dwb =
+                    reinterpret_cast<const uint16_t *>(smem + OFF_STILE + sg * STW_BYTES)[crow * SG + (g & (SG - 1))];
+                const float dw = __half2float(__ushort_as_half(dwb));
+                const uint2 v = *reinterpret_cast<const uint2 *>(smem + OFF_RAW + rs * RB_BYTES + csrc);
+                uint8_t *dst = smem + OFF_B + s * B_BYTES + cdst;
+                uint4 h, l;
+                nib8_split(v.x, dw, h, l);
+                *reinterpret_cast<uint4 *>(dst) = h;
+                *reinterpret_cast<uint4 *>(dst + BPIECE) = l;
+                nib8_split(v.y, dw, h, l);
+                *reinterpret_cast<uint4 *>(dst + 128) = h;
+                *reinterpret_cast<uint4 *>(dst + BPIECE + 128) = l;
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar_full + 8 * s);
+                mbar_arrive(bar_rempty + 8 * rs);
+                if ((g & (SG - 1)) == SG - 1) mbar_arrive(bar_sempty + 8 * sg);
+            }
+            // chunk rc ends at block SG*(rc+1) - 1; once S more blocks have been
+            // converted the tensor core has started on that block
+            if (rc < nchunks && g >= SG * (rc + 1) + S) {
+                readout(rc);
+                ++rc;
+            }
+        }
+        while (ok && rc < nchunks) {
+            readout(rc);
+            ++rc;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    pdl_launch_dependents();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+}  // namespace tcs
+
+// ---------------------------------------------------------------- host side
+size_t gemm_split_workspace_bytes(int K, int M)
+{
+    if (K < tcs::KB || K % tcs::KB != 0 || M < 1) return 0;
+    return static_cast<size_t>((M + tcs::TM - 1) / tcs::TM) * static_cast<size_t>(K / tcs::KB) * tcs::A_BYTES;
+}
+
+bool gemm_split_supported(int K) { return K >= 256 && K % 256 == 0; }
+
+int launch_gemm_split(const void *W, const int8_t *Xq, const float *dx, float *Y, void *ws, size_t ws_bytes,
+                      int rows, int K, int M, cudaStream_t s)
+{
+    if (!gemm_split_supported(K)) return GQ_ERR_SHAPE;
+    const int nb = K / 32;
+    const size_t need = gemm_split_workspace_bytes(K, M);
+    if (need == 0) return GQ_ERR_SHAPE;
+    if (ws_bytes < need) return GQ_ERR_WORKSPACE;
+    const long long ntiles_ll =
+        static_cast<long long>((M + tcs::TM - 1) / tcs::TM) * ((rows + tcs::TN - 1) / tcs::TN);
+    if (ntiles_ll * nb > 0x7FFFFFFFll) return GQ_ERR_SHAPE;  // per-CTA block counts are ints
+    const int ntiles = static_cast<int>(ntiles_ll);
+    const uint8_t *nib = static_cast<const uint8_t *>(W);
+    const uint16_t *dsc = reinterpret_cast<const uint16_t *>(nib + static_cast<size_t>(rows) * nb * 16);
+    CUtensorMap mapB, mapW;
+    if (!make_map(&mapB, CU_TENSOR_MAP_DATA_TYPE_UINT8, nib, static_cast<uint64_t>(nb) * 16,
+                  static_cast<uint64_t>(rows), static_cast<uint64_t>(nb) * 16, 16, tcs::TN) ||
+        !make_map(&mapW, CU_TENSOR_MAP_DATA_TYPE_UINT16, dsc, static_cast<uint64_t>(nb), static_cast<uint64_t>(rows),
+                  static_cast<uint64_t>(nb) * 2, tcs::SG, tcs::TN))
+        return GQ_ERR_CUDA;
+
+    // activation codes x scales -> bf16 operand pieces
+    const long long npieces = static_cast<long long>(need / tcs::A_BYTES) * 512;
+    long long pgrid = (npieces + 255) / 256;
+    const long long pmax = static_cast<long long>(sm_count()) * 8;
+    if (pgrid > pmax) pgrid = pmax;
+    int rc = status_from(launch_pdl(tcs::k_xq_split, dim3(static_cast<unsigned>(pgrid)), dim3(256), 0, s, Xq, dx,
+                                    static_cast<uint4 *>(ws), K, M, npieces));
+    if (rc != GQ_OK) return rc;
+
+    const int occ = ctas_per_sm(reinterpret_cast<const void *>(tcs::k_gemm_split), tcs::NTHREADS, tcs::SMEM_BYTES);
+    if (occ <= 0) return GQ_ERR_CUDA;
+    int grid = sm_count();
+    if (grid > ntiles) grid = ntiles;
+    return status_from(launch_pdl(tcs::k_gemm_split, dim3(grid), dim3(tcs::NTHREADS),
+                                  static_cast<size_t>(tcs::SMEM_BYTES), s, static_cast<const uint8_t *>(ws), mapB,
+                                  mapW, Y, rows, K, M, status_word()));
+}
+
+}  // namespace gq

@@ -31,7 +31,11 @@
 //               the MMA of block g has finished with (two fixed 8-element
 //               groups per thread) and stage its scales.
 //   warp 12     one lane issues the TMA loads of the 192 x 16 B weight
-//               nibbles of each block into an RAW-deep ring.
+//               nibbles of each block into an RAW-deep ring and, when K is a
+//               multiple of 256, every 8 blocks the scale tiles of the next 8
+//               blocks (d_w fp16 8 x 192, dx f32 8 x 128) into a 2-deep ring,
+//               so the workers read scales from shared memory, never from
+//               global memory inside the loop.
 //   warp 13     one lane issues 2 x (M128 N192 K16) MMAs per block; the warp
 //               owns the TMEM allocation.
 //   warp 14     one lane issues the bulk copy of each block's A chunk into
@@ -42,13 +46,12 @@
 // Every mbarrier wait is bounded: on timeout the kernel records
 // GQ_ERR_TIMEOUT in the device status word, every role leaves its loop, TMEM
 // is released and the kernel returns.
-#include <cuda.h>
-
-#include "gq_host.h"
-#include "gq_internal.cuh"
+#include "gq_tc.cuh"
 
 namespace gq {
 namespace tc {
+
+using namespace tcu;
 
 constexpr int TM = 128;  // tokens per tile (MMA M, TMEM lanes)
 constexpr int TN = 192;  // weight rows per tile (MMA N, TMEM columns)
@@ -66,207 +69,38 @@ constexpr int EPI_COLS = TN / (WORK_WARPS / 4);  // 64
 constexpr int NDBUF = 2;     // TMEM accumulator buffers (192 of 256 columns each)
 constexpr int TMEM_COLS = 512;
 constexpr int DBUF = 256;  // TMEM column offset between D buffers
+constexpr uint32_t kIdesc = idesc_f16(TM, TN, false);  // f16 operands (exact small integers)
 
 constexpr int A_BYTES = TM * KB * 2;  // 8192: f16 operand A (one workspace chunk)
 constexpr int B_BYTES = TN * KB * 2;  // 12288: f16 operand B
 constexpr int RB_BYTES = TN * 16;     // 3072: nibbles (TMA box 16 x 192)
 constexpr int SCL_BYTES = (TM + TN) * 4;
+constexpr int SG = 8;                 // blocks per scale tile
+constexpr int STG = 2;                // scale tile stages
+constexpr int STW_BYTES = TN * SG * 2;  // 3072: d_w fp16 [TN rows][8 blocks] (TMA box 8 x 192)
+constexpr int STX_BYTES = TM * SG * 4;  // 4096: dx f32 [TM tokens][8 blocks] (TMA box 8 x 128)
+constexpr int ST_BYTES = STW_BYTES + STX_BYTES;
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + S * A_BYTES;
 constexpr int OFF_RAW = OFF_B + S * B_BYTES;
 constexpr int OFF_SCL = OFF_RAW + RAW * RB_BYTES;
-constexpr int OFF_BAR = OFF_SCL + SR * SCL_BYTES;
+constexpr int OFF_STILE = OFF_SCL + SR * SCL_BYTES;
+constexpr int OFF_BAR = OFF_STILE + STG * ST_BYTES;
 // afull, opempty, full per operand stage; rfull, rempty per raw stage;
-// dfull, dempty per D buffer; drain
-constexpr int N_BARS = 3 * S + 2 * RAW + 2 * NDBUF + 1;
+// dfull, dempty per D buffer; drain; sfull, sempty per scale tile stage
+constexpr int N_BARS = 3 * S + 2 * RAW + 2 * NDBUF + 1 + 2 * STG;
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16;
 
 static_assert((RAW & (RAW - 1)) == 0 && (S & (S - 1)) == 0 && (SR & (SR - 1)) == 0 && (NDBUF & (NDBUF - 1)) == 0,
               "ring sizes are powers of two");
+static_assert(S == SG, "the prologue converts exactly the first scale tile's blocks");
+static_assert(OFF_STILE % 128 == 0 && ST_BYTES % 128 == 0 && STW_BYTES % 128 == 0, "scale tile alignment");
 static_assert(OFF_B % 1024 == 0 && OFF_RAW % 1024 == 0 && RB_BYTES % 1024 == 0 && OFF_SCL % 16 == 0 &&
                   OFF_BAR % 8 == 0 && SMEM_BYTES <= 232448,
               "shared memory layout");
 static_assert(NWORK * 2 == TN * 4, "two 8-element nibble groups per worker thread");
-
-// ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-// A waiting thread may be suspended up to this long inside one try_wait
-// (it resumes as soon as the phase completes), so waiting warps do not
-// compete with working warps for issue slots.
-constexpr uint32_t kSuspendNs = 20000;
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(kSuspendNs)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ uint64_t globaltimer()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
-
-// Bounded wait for the phase of `bar` with the given parity.  Returns false
-// (raising the CTA abort flag and the device status) on timeout, or when
-// another role has already aborted.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort, int *status)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0u) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
-                *abort = 1;
-                atomicExch(status, GQ_ERR_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-// Warp-uniform form (all lanes agree).
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort, int *status)
-{
-    return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort, status));
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-            "r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// tcgen05 shared-memory matrix descriptor, K-major, no swizzle: start
-// address, LBO = byte stride between core matrices along K, SBO = byte
-// stride between 8-row groups along M/N, descriptor version 1 (bit 46).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
-{
-    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo >> 4) << 16) |
-           (static_cast<uint64_t>(sbo >> 4) << 32) | (1ull << 46);
-}
-// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B f16
-// (bits 7-9, 10-12 = 0), both K-major, N >> 3 at bits 17-22, M >> 4 at 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (static_cast<uint32_t>(TN >> 3) << 17) | (static_cast<uint32_t>(TM >> 4) << 24);
-
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-
-// 16 consecutive f32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
-{
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
-// ---------------------------------------------------------------- operand conversion
-// Both operands of a 32-block are written as four 8-element K groups; inside
-// a group the elements are stored in the order 0,4,1,5,2,6,3,7 (the order in
-// which the nibble unpacking below produces them).  A and B use the same
-// order, so the dot products are unchanged.
-__device__ __forceinline__ uint4 nib8_to_f16(uint32_t w)
-{
-    const uint32_t w2 = w >> 8;
-    uint32_t a0 = (w & 0x000F000Fu) | 0x64006400u;   // 1024 + (e0, e4)
-    uint32_t a1 = (w & 0x00F000F0u) | 0x64006400u;   // 1024 + 16 (e1, e5)
-    uint32_t a2 = (w2 & 0x000F000Fu) | 0x64006400u;  // 1024 + (e2, e6)
-    uint32_t a3 = (w2 & 0x00F000F0u) | 0x64006400u;  // 1024 + 16 (e3, e7)
-    const __half2 c1032 = __float2half2_rn(1032.0f);
-    const __half2 c16 = __float2half2_rn(0.0625f);
-    const __half2 c72 = __float2half2_rn(-72.0f);
-    __half2 r0 = __hsub2(*reinterpret_cast<__half2 *>(&a0), c1032);
-    __half2 r1 = __hfma2(*reinterpret_cast<__half2 *>(&a1), c16, c72);
-    __half2 r2 = __hsub2(*reinterpret_cast<__half2 *>(&a2), c1032);
-    __half2 r3 = __hfma2(*reinterpret_cast<__half2 *>(&a3), c16, c72);
-    uint4 o;
-    o.x = *reinterpret_cast<uint32_t *>(&r0);
-    o.y = *reinterpret_cast<uint32_t *>(&r1);
-    o.z = *reinterpret_cast<uint32_t *>(&r2);
-    o.w = *reinterpret_cast<uint32_t *>(&r3);
-    return o;
-}
-// Eight int8 codes (two words, elements 0..3 and 4..7) -> f16 in group order.
-__device__ __forceinline__ uint4 s8x8_to_f16(uint32_t lo, uint32_t hi)
-{
-    lo ^= 0x80808080u;  // offset binary: u = q + 128
-    hi ^= 0x80808080u;
-    const uint32_t t01 = __byte_perm(lo, hi, 0x5140);  // u0 u4 u1 u5
-    const uint32_t t23 = __byte_perm(lo, hi, 0x7362);  // u2 u6 u3 u7
-    uint32_t a0 = __byte_perm(t01, 0x64646464u, 0x4140);  // 1024 + (u0, u4)
-    uint32_t a1 = __byte_perm(t01, 0x64646464u, 0x4342);  // 1024 + (u1, u5)
-    uint32_t a2 = __byte_perm(t23, 0x64646464u, 0x4140);
-    uint32_t a3 = __byte_perm(t23, 0x64646464u, 0x4342);
-    const __half2 c = __float2half2_rn(1152.0f);
-    __half2 r0 = __hsub2(*reinterpret_cast<__half2 *>(&a0), c);
-    __half2 r1 = __hsub2(*reinterpret_cast<__half2 *>(&a1), c);
-    __half2 r2 = __hsub2(*reinterpret_cast<__half2 *>(&a2), c);
-    __half2 r3 = __hsub2(*reinterpret_cast<__half2 *>(&a3), c);
-    uint4 o;
-    o.x = *reinterpret_cast<uint32_t *>(&r0);
-    o.y = *reinterpret_cast<uint32_t *>(&r1);
-    o.z = *reinterpret_cast<uint32_t *>(&r2);
-    o.w = *reinterpret_cast<uint32_t *>(&r3);
-    return o;
-}
-// Byte offset of (row, K group kg) in an operand stage: core matrix
-// (row/8, kg) at ((row/8)*4 + kg)*128, row%8 at 16-byte steps inside it.
-__device__ __forceinline__ uint32_t op_off(int row, int kg) { return (((row >> 3) * 4 + kg) << 7) + ((row & 7) << 4); }
 
 // ---------------------------------------------------------------- activation operand chunks
 // Thread p writes 16 bytes at offset 16*p of the workspace: chunk p/512 =
@@ -366,6 +200,7 @@ __device__ __forceinline__ void fold16(float (&acc)[EPI_COLS], const float (&d)[
 template <bool kDumpD>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_gemm_q8act_tc(const uint8_t *__restrict__ Xh, const __grid_constant__ CUtensorMap mapB,
+                    const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX, int tiles,
                     const uint16_t *__restrict__ dsc, const float *__restrict__ dx, float *__restrict__ Y,
                     int32_t *__restrict__ Dout, int rows, int K, int M, int *__restrict__ status)
 {
@@ -376,6 +211,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t bar_rfull = bar_full + 8 * S, bar_rempty = bar_rfull + 8 * RAW;
     const uint32_t bar_dfull = bar_rempty + 8 * RAW, bar_dempty = bar_dfull + 8 * NDBUF;
     const uint32_t bar_drain = bar_dempty + 8 * NDBUF;
+    const uint32_t bar_sfull = bar_drain + 8, bar_sempty = bar_sfull + 8 * STG;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
@@ -403,6 +239,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(bar_dempty + 8 * b, WORK_WARPS);
         }
         mbar_init(bar_drain, 1);
+        for (int i = 0; i < STG; ++i) {
+            mbar_init(bar_sfull + 8 * i, 1);
+            mbar_init(bar_sempty + 8 * i, WORK_WARPS);
+        }
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -426,7 +266,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             int rs = 0;
             uint32_t rph = 0;
             int nr = 0;  // loads issued
+            int gi = 0;  // scale tiles issued
             for (int gb = 0; gb < nblocks; ++gb) {
+                if (tiles && (c.b & (SG - 1)) == 0) {
+                    const int sg = gi & (STG - 1);
+                    if (!wait_bounded(bar_sempty + 8 * sg, (static_cast<uint32_t>(gi / STG) & 1u) ^ 1u, abort, status))
+                        break;
+                    const uint32_t dst = sbase + OFF_STILE + sg * ST_BYTES;
+                    mbar_expect_tx(bar_sfull + 8 * sg, ST_BYTES);
+                    tma_load_2d(dst, &mapW, c.b, c.r0, bar_sfull + 8 * sg);
+                    tma_load_2d(dst + STW_BYTES, &mapX, c.b, c.t0, bar_sfull + 8 * sg);
+                    ++gi;
+                }
                 if (!wait_bounded(bar_rempty + 8 * rs, rph ^ 1u, abort, status)) break;
                 mbar_expect_tx(bar_rfull + 8 * rs, RB_BYTES);
                 tma_load_2d(sbase + OFF_RAW + rs * RB_BYTES, &mapB, c.b * 16, c.r0, bar_rfull + 8 * rs);
@@ -442,6 +293,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             volatile int no_abort = 0;
             for (int gb = (nr > RAW ? nr - RAW : 0); gb < nr; ++gb)
                 wait_bounded(bar_rfull + 8 * (gb % RAW), static_cast<uint32_t>((gb / RAW) & 1), &no_abort, status);
+            for (int g = (gi > STG ? gi - STG : 0); g < gi; ++g)
+                wait_bounded(bar_sfull + 8 * (g % STG), static_cast<uint32_t>((g / STG) & 1), &no_abort, status);
         }
         __syncwarp();
     } else if (warp == ACOPY_WARP) {
@@ -484,7 +337,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks)
                     mma_f16(tmem + buf * DBUF, smem_desc(a0 + ks * 256, 128, 512), smem_desc(b0 + ks * 256, 128, 512),
-                            ks);
+                            kIdesc, ks);
                 mma_commit(bar_dfull + 8 * buf);
                 mma_commit(bar_opempty + 8 * s);
                 if (++s == S) {
@@ -517,9 +370,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         Cursor ce, cc;
         cursor_set(w, ce, static_cast<int>(blockIdx.x));
         cc = ce;
+        // Scale of block g for this thread from the staged scale tile (the
+        // block's position in the CTA's sequence gives its tile: every tile
+        // holds whole 8-block groups); the first block of a group waits for
+        // the tile to land.
+        auto tile_scale = [&](int g) -> float {
+            const int sg = (g / SG) & (STG - 1);
+            if ((g & (SG - 1)) == 0)
+                ok = ok && wait_warp(bar_sfull + 8 * sg, static_cast<uint32_t>(g / (SG * STG)) & 1u, abort, status);
+            const uint8_t *t = smem + OFF_STILE + sg * ST_BYTES;
+            if (tid < TM) return reinterpret_cast<const float *>(t + STW_BYTES)[tid * SG + (g & (SG - 1))];
+            if (tid < TM + TN)
+                return __half2float(__ushort_as_half(reinterpret_cast<const uint16_t *>(t)[(tid - TM) * SG + (g & (SG - 1))]));
+            return 0.f;
+        };
         // stage blocks 0..S-1 (S <= RAW: their raw stages are 0..S-1, first phase)
         for (int gb = 0; gb < S && gb < nblocks && ok; ++gb) {
-            const float sv = load_scale(w, cc, tid, dsc, dx, rows, M);
+            const float sv = tiles ? tile_scale(gb) : load_scale(w, cc, tid, dsc, dx, rows, M);
+            if (!ok) break;
             ok = wait_warp(bar_rfull + 8 * gb, 0u, abort, status);
             if (!ok) break;
             {
@@ -534,12 +402,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (lane == 0) {
                 mbar_arrive(bar_full + 8 * gb);
                 mbar_arrive(bar_rempty + 8 * gb);
+                if (tiles && (gb & (SG - 1)) == SG - 1) mbar_arrive(bar_sempty + 8 * ((gb / SG) & (STG - 1)));
             }
             cursor_next(w, cc);
         }
         float acc[EPI_COLS];  // written first by each tile's block 0
-        // the scale of the next block to convert, loaded one iteration ahead
-        float sv = (S < nblocks) ? load_scale(w, cc, tid, dsc, dx, rows, M) : 0.f;
+        // without scale tiles, the scale of the next block to convert is
+        // loaded one iteration ahead
+        float sv = (!tiles && S < nblocks) ? load_scale(w, cc, tid, dsc, dx, rows, M) : 0.f;
         for (int gb = 0; gb < nblocks && ok; ++gb) {
             const int gn = gb + S;  // block converted in this iteration
             const int buf = gb & (NDBUF - 1);
@@ -597,6 +467,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // convert the nibbles of block gb + S into the stage the MMA of block gb has finished with
             if (gn < nblocks) {
                 const int rs = gn & (RAW - 1), st = gn & (S - 1);
+                if (tiles) {
+                    sv = tile_scale(gn);
+                    if (!ok) break;
+                }
                 ok = wait_warp(bar_rfull + 8 * rs, static_cast<uint32_t>(gn / RAW) & 1u, abort, status);
                 if (!ok) break;
                 {
@@ -611,9 +485,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (lane == 0) {
                     mbar_arrive(bar_full + 8 * st);
                     mbar_arrive(bar_rempty + 8 * rs);
+                    if (tiles && (gn & (SG - 1)) == SG - 1) mbar_arrive(bar_sempty + 8 * ((gn / SG) & (STG - 1)));
                 }
                 cursor_next(w, cc);
-                if (gn + 1 < nblocks) sv = load_scale(w, cc, tid, dsc, dx, rows, M);
+                if (!tiles && gn + 1 < nblocks) sv = load_scale(w, cc, tid, dsc, dx, rows, M);
             }
         }
     }
@@ -630,41 +505,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }  // namespace tc
 
 // ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_tiled()
-{
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
-// 2-D byte tensor [outer][inner] with row stride `stride` bytes; box inner x outer.
-static bool make_map_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t stride,
-                        uint32_t box_inner, uint32_t box_outer)
-{
-    EncodeTiledFn fn = encode_tiled();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {stride};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 size_t gemm_workspace_bytes(int K, int M)
 {
     if (K < tc::KB || K % tc::KB != 0 || M < 1) return 0;
@@ -685,9 +525,21 @@ static int launch_tc(bool dump, const void *W, const int8_t *Xq, const float *dx
     const uint8_t *nib = static_cast<const uint8_t *>(W);
     const uint16_t *dsc = reinterpret_cast<const uint16_t *>(nib + static_cast<size_t>(rows) * nb * 16);
     CUtensorMap mapB;
-    if (!make_map_u8(&mapB, nib, static_cast<uint64_t>(nb) * 16, static_cast<uint64_t>(rows),
-                     static_cast<uint64_t>(nb) * 16, 16, tc::TN))
+    if (!make_map(&mapB, CU_TENSOR_MAP_DATA_TYPE_UINT8, nib, static_cast<uint64_t>(nb) * 16,
+                  static_cast<uint64_t>(rows), static_cast<uint64_t>(nb) * 16, 16, tc::TN))
         return GQ_ERR_CUDA;
+    // Scale tiles need 16-byte row strides in both scale arrays: nb % 8 == 0.
+    CUtensorMap mapW, mapX;
+    std::memset(&mapW, 0, sizeof(mapW));
+    std::memset(&mapX, 0, sizeof(mapX));
+    const int tiles = (!dump && nb % tc::SG == 0) ? 1 : 0;
+    if (tiles) {
+        if (!make_map(&mapW, CU_TENSOR_MAP_DATA_TYPE_UINT16, dsc, static_cast<uint64_t>(nb),
+                      static_cast<uint64_t>(rows), static_cast<uint64_t>(nb) * 2, tc::SG, tc::TN) ||
+            !make_map(&mapX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, static_cast<uint64_t>(nb), static_cast<uint64_t>(M),
+                      static_cast<uint64_t>(nb) * 4, tc::SG, tc::TM))
+            return GQ_ERR_CUDA;
+    }
 
     // activation codes -> f16 operand chunks
     const long long npieces = static_cast<long long>(need / 16);
@@ -704,7 +556,8 @@ static int launch_tc(bool dump, const void *W, const int8_t *Xq, const float *dx
     int grid = sm_count();
     if (grid > ntiles) grid = ntiles;
     return status_from(launch_pdl(kern, dim3(grid), dim3(tc::NTHREADS), static_cast<size_t>(tc::SMEM_BYTES), s,
-                                  static_cast<const uint8_t *>(ws), mapB, dsc, dx, Y, D, rows, K, M, status_word()));
+                                  static_cast<const uint8_t *>(ws), mapB, mapW, mapX, tiles, dsc, dx, Y, D, rows, K, M,
+                                  status_word()));
 }
 
 int launch_gemm_q8act_tc(const void *W, const int8_t *Xq, const float *dx, float *Y, void *ws, size_t ws_bytes,

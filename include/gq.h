@@ -182,9 +182,15 @@ int gq_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, gq_str
  *   Y[t][r]    = sum_b d_w[r][b] * dx[t][b] * D[t][r][b]          (f32)
  * Y is f32[M][rows] row-major (one row of Y per token).
  *
+ * Y is computed on the tensor cores in one of two ways, both equal to the
+ * sum above up to f32 rounding: for K % 256 == 0 both block scales are
+ * folded into bf16 operand pieces (dx*Xq as three, d_w*(q_w-8) as two exact
+ * pieces) and Y accumulates across all of K in tensor memory; otherwise
+ * each block's exact integer D is read out and folded in f32.
+ *
  * The workspace (device memory, 16-byte aligned, at least
  * gq_q4_0_gemm_workspace_bytes(K, M) bytes, owned by the caller) receives
- * the activation codes converted once to f16 tensor-core operand tiles; its
+ * the activation operands converted once for the tensor cores; its
  * contents are scratch before and after the call.  Two calls in flight at
  * the same time need two workspaces.  GQ_ERR_WORKSPACE if it is too small.
  * ------------------------------------------------------------------------ */

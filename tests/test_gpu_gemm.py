@@ -54,7 +54,9 @@ def run_gemm(W, Xq_np, dx_np, rows, K, M):
 @pytest.mark.parametrize("M,rows,K", [(1, 1, 32), (37, 100, 256), (64, 64, 64), (130, 257, 544),
                                       (5, 3000, 5376),
                                       # several tiles per CTA, each of fewer blocks than operand stages
-                                      (260, 40000, 64)])
+                                      (260, 40000, 64),
+                                      # scale tiles (K % 256 == 0), several tiles per CTA, one group each
+                                      (300, 30000, 256)])
 def test_gemm_matches_oracle(M, rows, K):
     W = synth.q4_0_weights(rows, K, synth.stream(500 + M, 0))
     X = synth.normal((M, K), synth.stream(500 + M, 1))
@@ -85,9 +87,10 @@ def test_gemm_full_512x21504x5376_sampled():
     assert np.all(np.abs(Yg - Y_ref) <= 1e-5 * A)
 
 
-def test_gemm_all_eight_weights_exact_zero():
+@pytest.mark.parametrize("K", [128, 256])  # per-block fold; scale-folded bf16 pieces
+def test_gemm_all_eight_weights_exact_zero(K):
     import blockenc as be
-    rows, K, M = 70, 128, 9
+    rows, M = 70, 9
     blk = be.enc_q4_0(np.full(32, 8), 0.5)
     W = be.rows_from_blocks([[blk] * (K // 32)] * rows)
     X = synth.normal((M, K), synth.stream(501, 1))
