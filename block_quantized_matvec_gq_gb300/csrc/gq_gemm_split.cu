@@ -156,20 +156,38 @@ __global__ void __launch_bounds__(256) k_xq_split(const int8_t *__restrict__ Xq,
 
 // Weight pieces of one 8-element group: nibbles of w (element order) and
 // the block's d_w -> B1 and B2 chunks (16 bytes each, order 0,4,1,5,...).
+// Pair i = (nibble i, nibble i+4): OR-ed into the 2^23 pattern (exact
+// 2^23 + q*16^i), one packed FMA by 16^-i gives q - 8 exactly, one packed
+// multiply by d_w gives B' exactly (4 x 11 bits); cvt.rn.bf16x2 gives B1,
+// the exact remainder B' - B1 (at most 7 bits) converts exactly to B2.  One
+// asm block per pair keeps the temporaries in 64-bit register pairs.
+#define GQ_SPLIT_PAIR(MASK, SCALE, BIAS)                                                                      \
+    "{\n"                                                                                                     \
+    " .reg .b32 a, b, hx, hy, rx, ry, vx, vy;\n"                                                              \
+    " .reg .b64 p, v, hp, r, s2, c2, d2;\n"                                                                   \
+    " shr.u32 b, %2, 16;\n"                                                                                   \
+    " lop3.b32 a, %2, " MASK ", 0x4B000000, 0xEA;\n"                                                          \
+    " lop3.b32 b, b, " MASK ", 0x4B000000, 0xEA;\n"                                                           \
+    " mov.b64 p, {a, b};\n"                                                                                   \
+    " mov.b64 s2, {%4, %4};\n mov.b64 c2, {%5, %5};\n mov.b64 d2, {%3, %3};\n"                               \
+    " fma.rn.f32x2 p, p, s2, c2;\n"                                                                           \
+    " mul.rn.f32x2 v, p, d2;\n"                                                                               \
+    " mov.b64 {vx, vy}, v;\n"                                                                                 \
+    " cvt.rn.bf16x2.f32 %0, vy, vx;\n"                                                                        \
+    " shl.b32 hx, %0, 16;\n"                                                                                  \
+    " and.b32 hy, %0, 0xFFFF0000;\n"                                                                          \
+    " mov.b64 hp, {hx, hy};\n"                                                                                \
+    " sub.rn.f32x2 r, v, hp;\n"                                                                               \
+    " mov.b64 {rx, ry}, r;\n"                                                                                 \
+    " cvt.rn.bf16x2.f32 %1, ry, rx;\n"                                                                        \
+    "}"
+
 __device__ __forceinline__ void nib8_split(uint32_t w, float dw, uint4 &b1, uint4 &b2)
 {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        // exact q - 8 through the 2^23 bit pattern
-        const float qa = __uint_as_float(((w >> (4 * i)) & 15u) | kMagic) - (8388608.0f + 8.0f);
-        const float qb = __uint_as_float(((w >> (4 * i + 16)) & 15u) | kMagic) - (8388608.0f + 8.0f);
-        float ra, rb, unused_a, unused_b;
-        h[i] = split_bf2(qa * dw, qb * dw, ra, rb);
-        l[i] = split_bf2(ra, rb, unused_a, unused_b);  // exact: at most 7 bits remain
-    }
-    b1 = make_uint4(h[0], h[1], h[2], h[3]);
-    b2 = make_uint4(l[0], l[1], l[2], l[3]);
+    asm(GQ_SPLIT_PAIR("0x0000000F", "", "") : "=r"(b1.x), "=r"(b2.x) : "r"(w), "f"(dw), "f"(1.0f), "f"(-8388616.0f));
+    asm(GQ_SPLIT_PAIR("0x000000F0", "", "") : "=r"(b1.y), "=r"(b2.y) : "r"(w), "f"(dw), "f"(0.0625f), "f"(-524296.0f));
+    asm(GQ_SPLIT_PAIR("0x00000F00", "", "") : "=r"(b1.z), "=r"(b2.z) : "r"(w), "f"(dw), "f"(0.00390625f), "f"(-32776.0f));
+    asm(GQ_SPLIT_PAIR("0x0000F000", "", "") : "=r"(b1.w), "=r"(b2.w) : "r"(w), "f"(dw), "f"(0.000244140625f), "f"(-2056.0f));
 }
 
 struct Work {
@@ -355,8 +373,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int tid = threadIdx.x;  // 0..NWORK-1
         const int q = warp & 3;       // TMEM lane quarter
         const int c0 = (warp >> 2) * EPI_COLS;
-        // this thread's two nibble groups: row tid/2, K groups 2*(tid%2) and +1
-        const int crow = tid >> 1, chalf = tid & 1;
+        // this thread's two nibble groups: warp w covers rows 32*(w/2).. and K
+        // groups 2*(w%2), 2*(w%2)+1, so the 16-byte stores of 8 consecutive
+        // lanes fall on distinct bank groups
+        const int crow = 32 * (warp >> 1) + lane, chalf = warp & 1;
         const uint32_t csrc = crow * 16 + chalf * 8;
         const uint32_t cdst = op_off(crow, 2 * chalf);
         bool ok = true;
