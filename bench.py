@@ -294,7 +294,7 @@ class FFN(Rotating):
 
 class Gemm(Workload):
     name = "q4_0_gemm_q8act_512x21504x5376"
-    kernel = "k_gemm_q8act"
+    kernel = "k_gemm_split"  # K % 256 == 0: the scale-folded bf16 path
     bound = "tensor"
     rows, K, M = 21504, 5376, 512
     launches_per_step = 3
