@@ -11,11 +11,11 @@
 
 namespace gq {
 
-template <int LG, int R, int U>
+template <int LG, int R, int U, bool kEarly>
 __global__ void __launch_bounds__(kThreadsPerCta, 2)
     k_ffn_gate_up(const uint4 *__restrict__ gnib, const uint16_t *__restrict__ gsc,
                   const uint4 *__restrict__ unib, const uint16_t *__restrict__ usc,
-                  const float *__restrict__ x, float *__restrict__ h, int rows, int nb, int early)
+                  const float *__restrict__ x, float *__restrict__ h, int rows, int nb)
 {
     extern __shared__ __align__(16) float xs[];
     constexpr int G = 32 / LG, TR = G * R;
@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     };
     // Weights never depend on the previous kernel: prefetch this warp's first
     // rows into L2 before waiting for it and, when warps have about one task
-    // each (`early`, decided by the host), issue that task's first loads too.
+    // each (kEarly, chosen by the host), issue that task's first loads too.
     // (Measured: with several tasks per warp the early loads cost more than
     // they save.)
     if (first < ntasks) {
@@ -52,14 +52,14 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
             rp[TR + i] = unib + r * nb;
         }
         prefetch_rows_l2<2 * TR>(rp, static_cast<uint32_t>(nb) * 16u, lane);
-        if (early) setup(first);
+        if (kEarly) setup(first);
     }
     pdl_wait();
     stage_x_q4<false>(xs, x, nb * 32);
     pdl_launch_dependents();
 
     for (int task = first; task < ntasks; task += stride) {
-        if (task != first || !early) setup(task);
+        if (task != first || !kEarly) setup(task);
         float out[2 * R];
         st.run(xs, nb, lp, out);
         const int r0 = task * TR + g * R;
@@ -83,13 +83,20 @@ int launch_ffn_gate_up(const void *Wg, const void *Wu, const float *x, float *h,
     const size_t smem = static_cast<size_t>(nb) * kXBlk * sizeof(float);
     const long long ntasks = (rows + (32 / geo.lg) * geo.r - 1) / ((32 / geo.lg) * geo.r);
     if (geo.p != 1) return GQ_ERR_SHAPE;
-#define CASE(LG, R, U)                                                                                 \
-    {                                                                                                  \
-        auto kern = k_ffn_gate_up<LG, R, U>;                                                           \
-        const int grid = persistent_grid(reinterpret_cast<const void *>(kern), kThreadsPerCta, smem, ntasks); \
-        if (grid <= 0) return GQ_ERR_SHAPE;                                                            \
-        const int early = ntasks * 4 <= static_cast<long long>(grid) * kWarpsPerCta * 5;              \
-        return status_from(launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, gn, gs, un, us, x, h, rows, nb, early)); \
+#define CASE(LG, R, U)                                                                                  \
+    {                                                                                                   \
+        auto late = k_ffn_gate_up<LG, R, U, false>;                                                              \
+        int grid = persistent_grid(reinterpret_cast<const void *>(late), kThreadsPerCta, smem, ntasks); \
+        if (grid <= 0) return GQ_ERR_SHAPE;                                                             \
+        /* first loads before the dependency wait only when warps have about one task */               \
+        const bool early = ntasks * 4 <= static_cast<long long>(grid) * kWarpsPerCta * 5;               \
+        auto kern = early ? k_ffn_gate_up<LG, R, U, true> : late;                                                 \
+        if (early) { /* size through the launched instantiation too (raises its shared-memory limit) */ \
+            const int g2 = persistent_grid(reinterpret_cast<const void *>(kern), kThreadsPerCta, smem, ntasks); \
+            if (g2 <= 0) return GQ_ERR_SHAPE;                                                           \
+            if (g2 < grid) grid = g2;                                                                   \
+        }                                                                                               \
+        return status_from(launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, gn, gs, un, us, x, h, rows, nb));        \
     }
     GQ_GEO_SWITCH_R12(geo, CASE);
 #undef CASE

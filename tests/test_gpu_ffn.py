@@ -42,7 +42,7 @@ def h_bound(ref):
         np.abs(ref["g"] * ref["u"]) + np.abs(ref["h"]))
 
 
-@pytest.mark.parametrize("rows,K", [(32, 32), (96, 256), (320, 512), (1024, 5376), (544, 2048)])
+@pytest.mark.parametrize("rows,K", [(32, 32), (96, 256), (320, 512), (1024, 5376), (544, 2048), (160, 21504)])
 def test_ffn_small_end_to_end(rows, K):
     seed = 300 + rows + K
     Wg = synth.q4_0_weights(rows, K, synth.stream(seed, 0))
