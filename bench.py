@@ -158,7 +158,7 @@ class LogitsTopK(Workload):
     name = "q8_0_logits_topk_262144x5376"
     kernel = "k_q8_0_logits_topk"
     rows, K, k, cap = 262144, 5376, 10, 30.0
-    launches_per_step = 2
+    launches_per_step = 1  # the top-k merge runs inside the logits kernel
 
     def setup(self, torch, gq):
         W, x = synth.q8_0_logits_inputs(self.rows, self.K)
@@ -169,7 +169,7 @@ class LogitsTopK(Workload):
         del Wc
         self.x = _to_dev(torch, x)
         self.wsb = gq.gq_logits_topk_workspace_bytes(self.rows, self.K, self.k)
-        self.ws = torch.empty(self.wsb, dtype=torch.uint8, device="cuda")
+        self.ws = torch.zeros(self.wsb, dtype=torch.uint8, device="cuda")  # zero-filled once before first use
         self.idx = torch.empty(self.k, dtype=torch.int32, device="cuda")
         self.val = torch.empty(self.k, dtype=torch.float32, device="cuda")
         self.gq = gq

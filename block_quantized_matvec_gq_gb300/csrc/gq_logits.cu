@@ -5,18 +5,25 @@
 // pair-valued (value, token) frontier instead of gathering full logits;
 // exact truncation of every merge to k pairs).
 //
-// Phase 1 (k_q8_0_logits_topk): the Q8_0 matvec core; each warp soft-caps
+// One kernel (k_q8_0_logits_topk): the Q8_0 matvec core; each warp soft-caps
 // its rows' logits, optionally stores them, and keeps the k best (value, row)
 // keys it has seen in a warp-resident sorted list; each CTA then merges its
-// warps' lists and writes k keys to the workspace.
-// Phase 2 (k_topk_merge, one CTA): every key that can still be in the final
-// top k is at least the largest k-th key of any CTA list (that list alone
-// holds k keys above it), so keys below that threshold are skipped before
-// the remaining candidates are merged.
+// warps' lists and writes k keys to the workspace.  The last CTA to finish
+// (a counter at the start of the workspace, incremented with wrap-around so
+// it is back at zero after every call) merges all CTA lists: every key that
+// can still be in the final top k is at least the largest k-th key of any
+// CTA list (that list alone holds k keys above it), so keys below that
+// threshold are skipped before the remaining candidates are merged.  (A
+// separate one-CTA merge kernel cost 14.7 us per call at 262144 x 5376,
+// against 234 us for the whole stream.)
 #include "gq_host.h"
 #include "gq_matvec.cuh"
 
 namespace gq {
+
+// The workspace starts with a 16-byte header (the finished-CTA counter),
+// then one list of k keys per CTA.
+constexpr size_t kLogitsWsHeaderWords = 2;
 
 // Insert every key of `key` (one per lane; 0 = none) that beats the list's
 // admission threshold; thr never drops below floor_thr.
@@ -40,11 +47,15 @@ template <int LG, int R, int U>
 __global__ void __launch_bounds__(kThreadsPerCta, 2)
     k_q8_0_logits_topk(const uint4 *__restrict__ qb, const uint16_t *__restrict__ dsc,
                        const float *__restrict__ x, float softcap, int k,
-                       float *__restrict__ logits, unsigned long long *__restrict__ ws, int rows,
-                       int nb)
+                       float *__restrict__ logits, unsigned long long *__restrict__ ws, int *__restrict__ idx,
+                       float *__restrict__ val, int rows, int nb)
 {
     extern __shared__ __align__(16) float xs[];
     __shared__ unsigned long long cta_keys[kWarpsPerCta * GQ_MAX_TOPK];
+    __shared__ unsigned long long wmax[kWarpsPerCta];
+    __shared__ int s_last;
+    unsigned int *counter = reinterpret_cast<unsigned int *>(ws);
+    unsigned long long *keys = ws + kLogitsWsHeaderWords;
     constexpr int G = 32 / LG, TR = G * R;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane / LG, lp = lane % LG;
@@ -99,30 +110,22 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
             const int j = base + lane;
             offer(top, thr, 0ull, (j < kWarpsPerCta * k) ? cta_keys[j] : 0ull, k);
         }
-        if (lane < k) ws[static_cast<size_t>(blockIdx.x) * k + lane] = top.e0;
-        if (lane + 32 < k) ws[static_cast<size_t>(blockIdx.x) * k + lane + 32] = top.e1;
+        if (lane < k) keys[static_cast<size_t>(blockIdx.x) * k + lane] = top.e0;
+        if (lane + 32 < k) keys[static_cast<size_t>(blockIdx.x) * k + lane + 32] = top.e1;
+        // this CTA's keys are visible device-wide before it counts itself
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) s_last = atomicInc(counter, gridDim.x - 1) == gridDim.x - 1;
     }
-}
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();  // and the other CTAs' keys are visible here
 
-constexpr int kMergeThreads = 256;
-constexpr int kMergeWarps = kMergeThreads / 32;
-
-__global__ void __launch_bounds__(kMergeThreads)
-    k_topk_merge(const unsigned long long *__restrict__ ws, int nlists, int k, int *__restrict__ idx,
-                 float *__restrict__ val)
-{
-    __shared__ unsigned long long wkeys[kMergeWarps * GQ_MAX_TOPK];
-    __shared__ unsigned long long wmax[kMergeWarps];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // Let the next kernel start its prologue (weight prefetch) now: it still
-    // waits for this grid to complete before it reads anything written here.
-    pdl_launch_dependents();
-    pdl_wait();
-
-    // threshold: the largest k-th key over all lists
+    // ---- the last CTA: merge all CTA lists (keys read through L2)
+    const int nlists = gridDim.x;
     unsigned long long t = 0ull;
-    for (int c = threadIdx.x; c < nlists; c += kMergeThreads) {
-        const unsigned long long v = ws[static_cast<size_t>(c) * k + (k - 1)];
+    for (int c = threadIdx.x; c < nlists; c += kThreadsPerCta) {
+        const unsigned long long v = __ldcg(keys + static_cast<size_t>(c) * k + (k - 1));
         t = v > t ? v : t;
     }
 #pragma unroll
@@ -134,25 +137,24 @@ __global__ void __launch_bounds__(kMergeThreads)
     __syncthreads();
     unsigned long long T = 0ull;
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) T = wmax[w] > T ? wmax[w] : T;
+    for (int w = 0; w < kWarpsPerCta; ++w) T = wmax[w] > T ? wmax[w] : T;
     const unsigned long long floor_thr = T > 0ull ? T - 1ull : 0ull;  // admit keys >= T
 
-    WarpTopK top;
     top.init();
-    unsigned long long thr = floor_thr;
+    thr = floor_thr;
     const int nkeys = nlists * k;
-    for (int base = warp * 32; base < nkeys; base += kMergeThreads) {
+    for (int base = warp * 32; base < nkeys; base += kThreadsPerCta) {
         const int j = base + lane;
-        offer(top, thr, floor_thr, (j < nkeys) ? ws[j] : 0ull, k);
+        offer(top, thr, floor_thr, (j < nkeys) ? __ldcg(keys + j) : 0ull, k);
     }
-    for (int j = lane; j < k; j += 32) wkeys[warp * k + j] = (j < 32) ? top.e0 : top.e1;
+    for (int j = lane; j < k; j += 32) cta_keys[warp * k + j] = (j < 32) ? top.e0 : top.e1;
     __syncthreads();
     if (warp == 0) {
         top.init();
         thr = floor_thr;
-        for (int base = 0; base < kMergeWarps * k; base += 32) {
+        for (int base = 0; base < kWarpsPerCta * k; base += 32) {
             const int j = base + lane;
-            offer(top, thr, floor_thr, (j < kMergeWarps * k) ? wkeys[j] : 0ull, k);
+            offer(top, thr, floor_thr, (j < kWarpsPerCta * k) ? cta_keys[j] : 0ull, k);
         }
         if (lane < k) {
             idx[lane] = static_cast<int>(key_row(top.e0));
@@ -170,17 +172,12 @@ __global__ void __launch_bounds__(kMergeThreads)
 constexpr int kLogitsMaxCtas = 2048;
 int logits_max_ctas() { return kLogitsMaxCtas; }
 
-int launch_topk_merge(const unsigned long long *keys, int nlists, int k, int *idx, float *val, cudaStream_t s)
-{
-    return status_from(launch_pdl(k_topk_merge, dim3(1), dim3(kMergeThreads), 0, s, keys, nlists, k, idx, val));
-}
-
 size_t logits_topk_ws_bytes(int rows, int K, int k)
 {
     (void)K;
     const long long tasks_ctas = (static_cast<long long>(rows) + 7) / 8;
     const long long ctas = tasks_ctas < kLogitsMaxCtas ? tasks_ctas : kLogitsMaxCtas;
-    return static_cast<size_t>(ctas) * static_cast<size_t>(k) * sizeof(unsigned long long);
+    return (kLogitsWsHeaderWords + static_cast<size_t>(ctas) * static_cast<size_t>(k)) * sizeof(unsigned long long);
 }
 
 int launch_logits_topk(const void *W, const float *x, float softcap, int k, int *idx, float *val,
@@ -192,20 +189,17 @@ int launch_logits_topk(const void *W, const float *x, float softcap, int k, int 
     const uint16_t *dsc = reinterpret_cast<const uint16_t *>(qb + static_cast<size_t>(rows) * nb * 2);
     const size_t smem = static_cast<size_t>(K) * sizeof(float);
     const long long ntasks = (rows + (32 / geo.lg) * geo.r - 1) / ((32 / geo.lg) * geo.r);
-    unsigned long long *keys = static_cast<unsigned long long *>(ws);
+    unsigned long long *wsw = static_cast<unsigned long long *>(ws);
 #define CASE(LG, R, U)                                                                                 \
     {                                                                                                  \
         auto kern = k_q8_0_logits_topk<LG, R, U>;                                                      \
         int grid = persistent_grid(reinterpret_cast<const void *>(kern), kThreadsPerCta, smem, ntasks); \
         if (grid <= 0) return GQ_ERR_SHAPE;                                                            \
         if (grid > kLogitsMaxCtas) grid = kLogitsMaxCtas;                                              \
-        if (static_cast<size_t>(grid) * k * sizeof(unsigned long long) > ws_bytes) return GQ_ERR_WORKSPACE; \
-        cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, qb, dsc, x, softcap, k, \
-                                   logits, keys, rows, nb);                                            \
-        if (e != cudaSuccess) return GQ_ERR_CUDA;                                                      \
-        e = launch_pdl(k_topk_merge, dim3(1), dim3(kMergeThreads), 0, s,                               \
-                       static_cast<const unsigned long long *>(keys), grid, k, idx, val);              \
-        return status_from(e);                                                                         \
+        if ((kLogitsWsHeaderWords + static_cast<size_t>(grid) * k) * sizeof(unsigned long long) > ws_bytes) \
+            return GQ_ERR_WORKSPACE;                                                                   \
+        return status_from(launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, qb, dsc, x, softcap, k, \
+                                      logits, wsw, idx, val, rows, nb));                               \
     }
     GQ_GEO_SWITCH(geo, CASE);
 #undef CASE

@@ -13,15 +13,17 @@
 // address is looked up once per device with cudaGetSymbolAddress (on the
 // first call made with that device current) and passed to the kernels.
 // All calls share the array: two calls whose kernels may overlap on the GPU
-// (different streams without ordering) race on it.  Nothing in it needs to
-// start at zero -- every key a call reads was written earlier in that call.
+// (different streams without ordering) race on it.  Its counter starts at
+// zero (static device memory is zero-initialised) and every completed call
+// leaves it at zero; every key a call reads was written earlier in that call.
 #include "gq_host.h"
 
 namespace gq {
 
-// One list of up to GQ_MAX_TOPK keys for each of up to 2048 CTAs: every
-// call that gq_logits_topk accepts fits.
-constexpr size_t kNoallocScratchWords = 2048ull * GQ_MAX_TOPK;
+// A 16-byte header (the finished-CTA counter, zero at load and back at zero
+// after every call) and one list of up to GQ_MAX_TOPK keys for each of up
+// to 2048 CTAs: every call that gq_logits_topk accepts fits.
+constexpr size_t kNoallocScratchWords = 2 + 2048ull * GQ_MAX_TOPK;
 constexpr size_t kNoallocScratchBytes = kNoallocScratchWords * sizeof(unsigned long long);
 
 static __device__ __align__(256) unsigned long long g_topk_scratch[kNoallocScratchWords];

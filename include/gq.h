@@ -140,10 +140,14 @@ int gq_ffn_gate_up_gelu(const void *W_gate, const void *W_up, const float *x, fl
  *   -0 ranks equal to +0.
  *   logits_or_null: if not NULL, receives l' for every row (f32[rows]).
  *   workspace: device scratch of at least gq_logits_topk_workspace_bytes
- *   bytes (caller-owned; contents need no initialisation; two calls that may
- *   run concurrently must not share it).
+ *   bytes (caller-owned).  ZERO-FILL IT ONCE before its first use: its first
+ *   16 bytes count the CTAs that have finished (the last one merges every
+ *   CTA's candidates), and every completed call leaves that count at zero
+ *   again, so the workspace can be reused without clearing.  The rest needs
+ *   no initialisation.  Two calls that may run concurrently must not share
+ *   it.
  *   1 <= k <= min(GQ_MAX_TOPK, rows); M must be 1.
- * Two kernels are launched on `stream`.
+ * One kernel is launched on `stream`.
  * ------------------------------------------------------------------------ */
 size_t gq_logits_topk_workspace_bytes(int rows, int K, int k);
 int gq_logits_topk(const void *W, const float *x, float softcap, int k, int *idx, float *val,
@@ -154,7 +158,8 @@ int gq_logits_topk(const void *W, const float *x, float softcap, int k, int *idx
  * cannot allocate device memory (a serving loop that must not call cudaMalloc
  * while it runs, a runtime that hands the library only its inputs and
  * outputs).  The source pages have no counterpart of this entry point.  The
- * per-CTA key lists live in a fixed 1 MiB array inside libgq (held on every
+ * per-CTA key lists live in a fixed 1 MiB array inside libgq (zero at load,
+ * so it needs no clearing; held on every
  * GPU that loads the library until the process exits); every call
  * gq_logits_topk accepts fits, and a call that would not fit is rejected with
  * GQ_ERR_SHAPE.  The first call on a device looks the array's address up

@@ -27,7 +27,7 @@ pytestmark = pytest.mark.gpu
 def gpu_logits_topk(Wp, x, rows, K, k, softcap, with_logits=True):
     t = torch()
     wsb = gq.gq_logits_topk_workspace_bytes(rows, K, k)
-    ws = t.empty(wsb, dtype=t.uint8, device="cuda")
+    ws = t.zeros(wsb, dtype=t.uint8, device="cuda")  # zero-filled once before first use
     idx = t.full((k,), -1, dtype=t.int32, device="cuda")
     val = t.full((k,), float("nan"), dtype=t.float32, device="cuda")
     full, logits, check = guarded(rows, t.float32) if with_logits else (None, None, lambda: None)
@@ -170,7 +170,7 @@ def test_repeat_runs_identical_and_workspace_errors():
     b = gpu_logits_topk(Wp, x, rows, K, k, 30.0)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
     wsb = gq.gq_logits_topk_workspace_bytes(rows, K, k)
-    ws = t.empty(wsb, dtype=t.uint8, device="cuda")
+    ws = t.zeros(wsb, dtype=t.uint8, device="cuda")  # zero-filled once before first use
     idx = t.empty(k, dtype=t.int32, device="cuda")
     val = t.empty(k, dtype=t.float32, device="cuda")
     with pytest.raises(gq.GQError) as e:
@@ -182,3 +182,28 @@ def test_repeat_runs_identical_and_workspace_errors():
     with pytest.raises(gq.GQError) as e:
         gq.gq_logits_topk(Wp, dev(x), 30.0, k, idx, val, None, None, wsb, rows, K)
     assert e.value.status == gq.GQ_ERR_WORKSPACE
+
+
+def test_workspace_reused_across_calls_and_grid_sizes():
+    """The finished-CTA counter at the start of the workspace is back at zero
+    after every call: one workspace serves calls of different row counts
+    (different grids) in any order with the same results as fresh ones."""
+    t = torch()
+    K, k = 2048, 12
+    shapes = [(60000, 1), (3000, 2), (60000, 3), (700, 4), (3000, 5)]
+    big = max(gq.gq_logits_topk_workspace_bytes(r, K, k) for r, _ in shapes)
+    shared = t.zeros(big, dtype=t.uint8, device="cuda")
+    for rows, seed in shapes:
+        W = synth.q8_0_weights(rows, K, synth.stream(900 + seed, 0))
+        Wp = packed(oracle.FORMAT_Q8_0, W, rows, K)
+        x = dev(synth.normal(K, synth.stream(900 + seed, 1)))
+        fresh = gpu_logits_topk(Wp, x, rows, K, k, 30.0, with_logits=False)
+        idx = t.empty(k, dtype=t.int32, device="cuda")
+        val = t.empty(k, dtype=t.float32, device="cuda")
+        gq.gq_logits_topk(Wp, x, 30.0, k, idx, val, None, shared, big, rows, K)
+        t.cuda.synchronize()
+        assert np.array_equal(idx.cpu().numpy(), fresh[0])
+        assert np.array_equal(val.cpu().numpy(), fresh[1])
+        # the counter (first 4 bytes) is zero again
+        assert int(shared[:4].view(t.int32).item()) == 0
+    assert gq.gq_device_status() == gq.GQ_OK

@@ -26,7 +26,7 @@ pytestmark = pytest.mark.gpu
 def _with_workspace(Wp, x, rows, K, k, cap):
     t = torch()
     wsb = gq.gq_logits_topk_workspace_bytes(rows, K, k)
-    ws = t.empty(wsb, dtype=t.uint8, device="cuda")
+    ws = t.zeros(wsb, dtype=t.uint8, device="cuda")
     idx = t.empty(k, dtype=t.int32, device="cuda")
     val = t.empty(k, dtype=t.float32, device="cuda")
     logits = t.empty(rows, dtype=t.float32, device="cuda")
