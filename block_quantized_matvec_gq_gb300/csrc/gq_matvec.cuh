@@ -276,6 +276,55 @@ struct Q4KStream {
 constexpr int kThreadsPerCta = 256;
 constexpr int kWarpsPerCta = kThreadsPerCta / 32;
 
+// The row tasks (TR rows each) of one warp: rows start + j*step .. for
+// j < count, then (balanced schedule only) ntail rows from tail_begin that
+// all warps of the CTA share along K.
+//   round-robin: task t of the grid goes to warp t % (warps in the grid); the
+//     last round may be partly filled (rows past the end are not stored).
+//   balanced: each CTA takes a near-equal contiguous share of the rows; its
+//     warps process whole tasks while every warp has one, and the fewer than
+//     kWarpsPerCta*TR rows left are split along K (warp w takes the w-th
+//     eighth of the blocks), their partial sums added in shared memory in
+//     warp order.  Chosen by the host when round-robin would leave a sparse
+//     last round with most warps idle (fewer than ~1.75 tasks per warp).
+struct WarpRows {
+    int start, step, count, tail_begin, ntail;
+};
+template <int TR>
+__device__ __forceinline__ WarpRows warp_rows(int rows, bool balanced, int warp)
+{
+    WarpRows c;
+    if (balanced) {
+        const int lo = rows / static_cast<int>(gridDim.x), extra = rows % static_cast<int>(gridDim.x);
+        const int b = static_cast<int>(blockIdx.x);
+        const int begin = b * lo + min(b, extra);
+        const int n = lo + (b < extra ? 1 : 0);
+        c.count = n / (kWarpsPerCta * TR);
+        c.start = begin + warp * TR;
+        c.step = kWarpsPerCta * TR;
+        c.tail_begin = begin + c.count * kWarpsPerCta * TR;
+        c.ntail = n - c.count * kWarpsPerCta * TR;
+    } else {
+        const int ntasks = (rows + TR - 1) / TR;
+        const int first = static_cast<int>(blockIdx.x) * kWarpsPerCta + warp;
+        const int stride = static_cast<int>(gridDim.x) * kWarpsPerCta;
+        c.count = first < ntasks ? (ntasks - 1 - first) / stride + 1 : 0;
+        c.start = first * TR;
+        c.step = stride * TR;
+        c.tail_begin = 0;
+        c.ntail = 0;
+    }
+    return c;
+}
+// Blocks [lo, hi) of warp w for the tail rows; slice edges are multiples of
+// `align` blocks (nb % align == 0).
+__device__ __forceinline__ void tail_slice(int nb, int align, int w, int &lo, int &hi)
+{
+    const int units = nb / align;
+    lo = (units * w / kWarpsPerCta) * align;
+    hi = (units * (w + 1) / kWarpsPerCta) * align;
+}
+
 // Before waiting on the previous kernel, ask L2 to fetch the weight rows of
 // this warp's first task (weights never depend on the previous kernel).
 // One lane per row issues a bulk prefetch of the whole row.

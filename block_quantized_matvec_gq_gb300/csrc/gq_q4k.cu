@@ -11,55 +11,122 @@
 
 namespace gq {
 
-template <int LG, int R, int U, bool kEarly>
+template <int LG, int R, int U, int kMode>
 __global__ void __launch_bounds__(kThreadsPerCta, 2)
     k_q4k_matvec(const uint4 *__restrict__ nib, const uint4 *__restrict__ rec,
                  const float *__restrict__ x, float *__restrict__ y, int rows, int nsb)
 {
     extern __shared__ __align__(16) float xs[];
     constexpr int G = 32 / LG, TR = G * R;
+    // schedule (chosen by the host): 0 round-robin; 1 balanced; 2 balanced, first loads early
+    constexpr bool kBalanced = kMode >= 1, kEarly = kMode == 2;
+    __shared__ float part[kWarpsPerCta][kWarpsPerCta * TR];  // tail partial sums [warp][row]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane / LG, lp = lane % LG;
-    const int ntasks = (rows + TR - 1) / TR;
     const int ns = nsb >> 3;
-    const int first = blockIdx.x * kWarpsPerCta + warp;
-    const int stride = gridDim.x * kWarpsPerCta;
+    if constexpr (!kBalanced) {
+        // round-robin: task t of the grid goes to warp t % (warps in the grid)
+        const int ntasks = (rows + TR - 1) / TR;
+        const int first = blockIdx.x * kWarpsPerCta + warp;
+        const int stride = gridDim.x * kWarpsPerCta;
 
-    Q4KStream<LG, R, U> st;
-    auto setup = [&](int task) {
-#pragma unroll
-        for (int i = 0; i < R; ++i) {
-            const int r = min(task * TR + g * R + i, rows - 1);
-            st.wp[i] = nib + static_cast<size_t>(r) * nsb;
-            st.rp[i] = rec + static_cast<size_t>(r) * ns;
+        Q4KStream<LG, R, U> st;
+        auto setup = [&](int task) {
+    #pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const int r = min(task * TR + g * R + i, rows - 1);
+                st.wp[i] = nib + static_cast<size_t>(r) * nsb;
+                st.rp[i] = rec + static_cast<size_t>(r) * ns;
+            }
+            st.prime(nsb, lp);
+        };
+        // Weights never depend on the previous kernel: prefetch this warp's first
+        // rows into L2 before waiting for it and, when warps have about one task
+        // each (kEarly, chosen by the host), issue that task's first loads too.
+        // (Measured: with several tasks per warp the early loads cost more than
+        // they save.)
+        if (first < ntasks) {
+            const void *rp[TR];
+    #pragma unroll
+            for (int i = 0; i < TR; ++i) rp[i] = nib + static_cast<size_t>(min(first * TR + i, rows - 1)) * nsb;
+            prefetch_rows_l2<TR>(rp, static_cast<uint32_t>(nsb) * 16u, lane);
+            /* no early loads in this mode */
         }
-        st.prime(nsb, lp);
-    };
-    // Weights never depend on the previous kernel: prefetch this warp's first
-    // rows into L2 before waiting for it and, when warps have about one task
-    // each (kEarly, chosen by the host), issue that task's first loads too.
-    // (Measured: with several tasks per warp the early loads cost more than
-    // they save.)
-    if (first < ntasks) {
-        const void *rp[TR];
-#pragma unroll
-        for (int i = 0; i < TR; ++i) rp[i] = nib + static_cast<size_t>(min(first * TR + i, rows - 1)) * nsb;
-        prefetch_rows_l2<TR>(rp, static_cast<uint32_t>(nsb) * 16u, lane);
-        if (kEarly) setup(first);
-    }
-    pdl_wait();
-    stage_x_q4<true>(xs, x, nsb * 32);
-    pdl_launch_dependents();
+        pdl_wait();
+        stage_x_q4<true>(xs, x, nsb * 32);
+        pdl_launch_dependents();
 
-    for (int task = first; task < ntasks; task += stride) {
-        if (task != first || !kEarly) setup(task);
-        float out[R];
-        st.run(xs, nsb, lp, out);
-        const int r0 = task * TR + g * R;
-#pragma unroll
-        for (int i = 0; i < R; ++i) {
-            const float s = group_sum<LG>(out[i]);
-            if (lp == 0 && r0 + i < rows) y[r0 + i] = s;
+        for (int task = first; task < ntasks; task += stride) {
+            setup(task);
+            float out[R];
+            st.run(xs, nsb, lp, out);
+            const int r0 = task * TR + g * R;
+    #pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const float s = group_sum<LG>(out[i]);
+                if (lp == 0 && r0 + i < rows) y[r0 + i] = s;
+            }
+        }
+    } else {
+        const WarpRows cr = warp_rows<TR>(rows, kBalanced, warp);
+
+        Q4KStream<LG, R, U> st;
+        // rows r0 + g*R + i of a TR-row task, sub-blocks [blo, bhi) (blo % 8 == 0,
+        // so a lane's sub-block position stays lp % 8)
+        auto setup = [&](int r0, int blo, int bhi) {
+    #pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const int r = min(r0 + g * R + i, rows - 1);
+                st.wp[i] = nib + static_cast<size_t>(r) * nsb + blo;
+                st.rp[i] = rec + static_cast<size_t>(r) * ns + (blo >> 3);
+            }
+            st.prime(bhi - blo, lp);
+        };
+        // Weights never depend on the previous kernel: prefetch this warp's first
+        // rows into L2 before waiting for it and, when warps have about one task
+        // each (kEarly, chosen by the host), issue that task's first loads too.
+        if (cr.count > 0) {
+            const void *rp[TR];
+    #pragma unroll
+            for (int i = 0; i < TR; ++i) rp[i] = nib + static_cast<size_t>(min(cr.start + i, rows - 1)) * nsb;
+            prefetch_rows_l2<TR>(rp, static_cast<uint32_t>(nsb) * 16u, lane);
+            if (kEarly) setup(cr.start, 0, nsb);
+        }
+        pdl_wait();
+        stage_x_q4<true>(xs, x, nsb * 32);
+        pdl_launch_dependents();
+
+        for (int j = 0; j < cr.count; ++j) {
+            const int r0 = cr.start + j * cr.step;
+            if (j > 0 || !kEarly) setup(r0, 0, nsb);
+            float out[R];
+            st.run(xs, nsb, lp, out);
+    #pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const float s = group_sum<LG>(out[i]);
+                if (lp == 0 && r0 + g * R + i < rows) y[r0 + g * R + i] = s;
+            }
+        }
+        if (kBalanced && cr.ntail > 0) {
+            int blo, bhi;
+            tail_slice(nsb, 8, warp, blo, bhi);
+            for (int t0 = 0; t0 < cr.ntail; t0 += TR) {
+                setup(cr.tail_begin + t0, blo, bhi);
+                float out[R];
+                st.run(xs + blo * kXBlk, bhi - blo, lp, out);
+    #pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    const float s = group_sum<LG>(out[i]);
+                    if (lp == 0) part[warp][t0 + g * R + i] = s;
+                }
+            }
+            __syncthreads();
+            for (int r = threadIdx.x; r < cr.ntail; r += kThreadsPerCta) {
+                float s = 0.f;
+    #pragma unroll
+                for (int w = 0; w < kWarpsPerCta; ++w) s += part[w][r];
+                y[cr.tail_begin + r] = s;
+            }
         }
     }
 }
@@ -75,20 +142,21 @@ int launch_q4k_matvec(const void *W, const float *x, float *y, int rows, int K, 
     if (geo.p != 1) return GQ_ERR_SHAPE;
 #define CASE(LG, R, U)                                                                                  \
     {                                                                                                   \
-        auto late = k_q4k_matvec<LG, R, U, false>;                                                              \
-        int grid = persistent_grid(reinterpret_cast<const void *>(late), kThreadsPerCta, smem, ntasks); \
+        auto rr = k_q4k_matvec<LG, R, U, 0>;                                                                     \
+        int grid = persistent_grid(reinterpret_cast<const void *>(rr), kThreadsPerCta, smem, ntasks);  \
         if (grid <= 0) return GQ_ERR_SHAPE;                                                             \
-        /* first loads before the dependency wait only when warps have about one task */               \
-        const bool early = ntasks * 4 <= static_cast<long long>(grid) * kWarpsPerCta * 5;               \
-        auto kern = early ? k_q4k_matvec<LG, R, U, true> : late;                                                 \
-        if (early) { /* size through the launched instantiation too (raises its shared-memory limit) */ \
+        /* tasks per warp: < 1.75 balanced schedule, <= 1.25 also first loads early */                 \
+        const long long w5 = static_cast<long long>(grid) * kWarpsPerCta;                               \
+        const int mode = ntasks * 4 <= w5 * 5 ? 2 : (ntasks * 4 < w5 * 7 ? 1 : 0);                      \
+        auto kern = mode == 2 ? k_q4k_matvec<LG, R, U, 2> : (mode == 1 ? k_q4k_matvec<LG, R, U, 1> : rr);                 \
+        if (mode != 0) { /* size through the launched instantiation too (raises its shared-memory limit) */ \
             const int g2 = persistent_grid(reinterpret_cast<const void *>(kern), kThreadsPerCta, smem, ntasks); \
             if (g2 <= 0) return GQ_ERR_SHAPE;                                                           \
             if (g2 < grid) grid = g2;                                                                   \
         }                                                                                               \
-        return status_from(launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, nib, rec, x, y, rows, nsb));        \
+        return status_from(launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, nib, rec, x, y, rows, nsb));       \
     }
-    GQ_GEO_SWITCH(geo, CASE);
+    GQ_GEO_SWITCH_R12(geo, CASE);
 #undef CASE
 }
 
