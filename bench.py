@@ -83,7 +83,7 @@ class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,clocks.mem,clocks.max.mem")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -132,8 +132,11 @@ class ClockSampler:
         mx = [float(p[2]) for p in sel if p[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for p in sel for n, v in zip(names, p[5:9]) if v.lower() == "active"})
+        mem = [float(p[9]) for p in sel if len(p) > 9 and p[9].replace(".", "").isdigit()]
+        mem_mx = [float(p[10]) for p in sel if len(p) > 10 and p[10].replace(".", "").isdigit()]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(sel), "window": where}
+                "reasons": reasons, "samples": len(sel), "window": where,
+                "mem_mhz": statistics.median(mem) if mem else None, "mem_max_mhz": max(mem_mx) if mem_mx else None}
 
 
 # ---------------------------------------------------------------- workloads
