@@ -271,6 +271,46 @@ __device__ __forceinline__ uint32_t key_row(unsigned long long key)
 
 // A warp-resident sorted list of the k best keys (k <= 64): lane j holds
 // entries j (e0) and j + 32 (e1), in descending order.
+// Sort 128 keys held 4 per lane (key i = lane + 32*j in e[j]) into
+// descending order with a bitonic network: strides 64 and 32 exchange within
+// a lane, smaller strides between lanes.  28 parallel compare-exchange
+// stages.
+__device__ __forceinline__ void warp_sort128_desc(unsigned long long (&e)[4])
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 128; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            if (stride >= 32) {
+                const int js = stride >> 5;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if ((j & js) == 0) {
+                        const int i = lane + 32 * j;
+                        const bool desc = (i & size) == 0;  // this block of `size` sorts descending
+                        const unsigned long long a = e[j], b = e[j | js];
+                        const bool swap = desc ? (a < b) : (a > b);
+                        e[j] = swap ? b : a;
+                        e[j | js] = swap ? a : b;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int i = lane + 32 * j;
+                    const bool desc = (i & size) == 0;
+                    const unsigned long long other = __shfl_xor_sync(0xffffffffu, e[j], stride);
+                    const bool lower = (lane & stride) == 0;  // this key is the lower index of the pair
+                    // lower index keeps the larger key when the block is descending
+                    const bool keep_max = (lower == desc);
+                    e[j] = keep_max ? (e[j] > other ? e[j] : other) : (e[j] < other ? e[j] : other);
+                }
+            }
+        }
+    }
+}
+
 struct WarpTopK {
     unsigned long long e0, e1;
     __device__ __forceinline__ void init() { e0 = 0ull; e1 = 0ull; }

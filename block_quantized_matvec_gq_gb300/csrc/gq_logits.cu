@@ -54,10 +54,32 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     __shared__ unsigned long long cta_keys[kWarpsPerCta * GQ_MAX_TOPK];
     __shared__ unsigned long long wmax[kWarpsPerCta];
     __shared__ int s_last;
+    // Candidates for a merge: every key >= the merge's threshold, gathered in
+    // shared memory and sorted by one warp (the usual case: at most k keys
+    // per list can reach the threshold, and only a few lists do).
+    constexpr int kMaxCand = 128;
+    __shared__ unsigned long long cand[kMaxCand];
+    __shared__ int s_cnt;
     unsigned int *counter = reinterpret_cast<unsigned int *>(ws);
     unsigned long long *keys = ws + kLogitsWsHeaderWords;
     constexpr int G = 32 / LG, TR = G * R;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    auto gather_candidate = [&](unsigned long long key, unsigned long long T) {
+        if (key != 0ull && key >= T) {
+            const int pos = atomicAdd(&s_cnt, 1);
+            if (pos < kMaxCand) cand[pos] = key;
+        }
+    };
+    // warp-wide: the s_cnt candidates sorted descending, entry i in
+    // e[i / 32] of lane i % 32 (entries past s_cnt are 0)
+    auto sort_candidates = [&](unsigned long long (&e)[4]) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = lane + 32 * j;
+            e[j] = i < s_cnt ? cand[i] : 0ull;
+        }
+        warp_sort128_desc(e);
+    };
     const int g = lane / LG, lp = lane % LG;
     const int ntasks = (rows + TR - 1) / TR;
     const bool cap = softcap > 0.f;
@@ -102,16 +124,35 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
 
     // merge the warps' lists (lane j holds entry j in e0 and entry j+32 in e1)
     for (int j = lane; j < k; j += 32) cta_keys[warp * k + j] = (j < 32) ? top.e0 : top.e1;
+    if (threadIdx.x == 0) s_cnt = 0;
+    __syncthreads();
+    {
+        // every key of this CTA's top k is >= the largest k-th key of a warp list
+        unsigned long long T = 0ull;
+#pragma unroll
+        for (int w = 0; w < kWarpsPerCta; ++w) {
+            const unsigned long long v = cta_keys[w * k + k - 1];
+            T = v > T ? v : T;
+        }
+        for (int j = threadIdx.x; j < kWarpsPerCta * k; j += kThreadsPerCta) gather_candidate(cta_keys[j], T);
+    }
     __syncthreads();
     if (warp == 0) {
-        top.init();
-        thr = 0ull;
-        for (int base = 0; base < kWarpsPerCta * k; base += 32) {
-            const int j = base + lane;
-            offer(top, thr, 0ull, (j < kWarpsPerCta * k) ? cta_keys[j] : 0ull, k);
+        unsigned long long e[4];
+        if (s_cnt <= kMaxCand) {
+            sort_candidates(e);
+        } else {  // more than kMaxCand keys at or above the threshold (ties): insert one by one
+            top.init();
+            thr = 0ull;
+            for (int base = 0; base < kWarpsPerCta * k; base += 32) {
+                const int j = base + lane;
+                offer(top, thr, 0ull, (j < kWarpsPerCta * k) ? cta_keys[j] : 0ull, k);
+            }
+            e[0] = top.e0;
+            e[1] = top.e1;
         }
-        if (lane < k) keys[static_cast<size_t>(blockIdx.x) * k + lane] = top.e0;
-        if (lane + 32 < k) keys[static_cast<size_t>(blockIdx.x) * k + lane + 32] = top.e1;
+        if (lane < k) keys[static_cast<size_t>(blockIdx.x) * k + lane] = e[0];
+        if (lane + 32 < k) keys[static_cast<size_t>(blockIdx.x) * k + lane + 32] = e[1];
         // this CTA's keys are visible device-wide before it counts itself
         __threadfence();
         __syncwarp();
@@ -134,36 +175,64 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
         t = v > t ? v : t;
     }
     if (lane == 0) wmax[warp] = t;
+    if (threadIdx.x == 0) s_cnt = 0;
     __syncthreads();
     unsigned long long T = 0ull;
 #pragma unroll
     for (int w = 0; w < kWarpsPerCta; ++w) T = wmax[w] > T ? wmax[w] : T;
     const unsigned long long floor_thr = T > 0ull ? T - 1ull : 0ull;  // admit keys >= T
-
-    top.init();
-    thr = floor_thr;
     const int nkeys = nlists * k;
-    for (int base = warp * 32; base < nkeys; base += kThreadsPerCta) {
-        const int j = base + lane;
-        offer(top, thr, floor_thr, (j < nkeys) ? __ldcg(keys + j) : 0ull, k);
+    // gather the candidates (keys >= T), four loads per lane in flight
+    constexpr int kBatch = 4;
+    for (int base = threadIdx.x; base < nkeys; base += kBatch * kThreadsPerCta) {
+        unsigned long long kk[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = base + u * kThreadsPerCta;
+            kk[u] = (j < nkeys) ? __ldcg(keys + j) : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) gather_candidate(kk[u], T);
     }
-    for (int j = lane; j < k; j += 32) cta_keys[warp * k + j] = (j < 32) ? top.e0 : top.e1;
     __syncthreads();
-    if (warp == 0) {
+    unsigned long long e[4];
+    if (s_cnt <= kMaxCand) {
+        if (warp != 0) return;
+        sort_candidates(e);
+    } else {
+        // more than kMaxCand keys at or above the threshold (ties): per-warp
+        // insertion, then warp 0 merges the warp lists
+        top.init();
+        thr = floor_thr;
+        for (int base = warp * 32; base < nkeys; base += kBatch * kThreadsPerCta) {
+            unsigned long long kk[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int j = base + u * kThreadsPerCta + lane;
+                kk[u] = (j < nkeys) ? __ldcg(keys + j) : 0ull;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) offer(top, thr, floor_thr, kk[u], k);
+        }
+        for (int j = lane; j < k; j += 32) cta_keys[warp * k + j] = (j < 32) ? top.e0 : top.e1;
+        __syncthreads();
+        if (warp != 0) return;
         top.init();
         thr = floor_thr;
         for (int base = 0; base < kWarpsPerCta * k; base += 32) {
             const int j = base + lane;
             offer(top, thr, floor_thr, (j < kWarpsPerCta * k) ? cta_keys[j] : 0ull, k);
         }
-        if (lane < k) {
-            idx[lane] = static_cast<int>(key_row(top.e0));
-            val[lane] = key_value(top.e0);
-        }
-        if (lane + 32 < k) {
-            idx[lane + 32] = static_cast<int>(key_row(top.e1));
-            val[lane + 32] = key_value(top.e1);
-        }
+        e[0] = top.e0;
+        e[1] = top.e1;
+    }
+    if (lane < k) {
+        idx[lane] = static_cast<int>(key_row(e[0]));
+        val[lane] = key_value(e[0]);
+    }
+    if (lane + 32 < k) {
+        idx[lane + 32] = static_cast<int>(key_row(e[1]));
+        val[lane + 32] = key_value(e[1]);
     }
 }
 
