@@ -1,48 +1,51 @@
 // gq_gemm_split.cu -- the prefill contraction with both block scales folded
 // into the tensor-core operands, so Y accumulates in tensor memory across
-// the whole of K (no per-block read-out).
+// 8 blocks at a time (one read-out per 8 blocks instead of one per block).
 //
 // "Gemma 4 M4 Max kernel roadmap", K3 "prefill path" (batched Q4_0
 // matrix-matrix):  Y[t][r] = sum_b d_w[r][b] * dx[t][b] * D[t][r][b]
-// with D the integer dot of block b.  Written as one sum over k,
-//   Y[t][r] = sum_k A'[t][k] * B'[r][k],
-//   A'[t][k] = dx[t][k/32] * Xq[t][k]          (f32: one rounding, 2^-24)
-//   B'[r][k] = d_w[r][k/32] * (q_w[r][k] - 8)  (exact in f32: 11 x 4 bits)
-// and fed to kind::f16 MMAs with bf16 operands, each operand split into
-// bf16 pieces: B' = B1 + B2 exactly (at most 15 significant bits), A' =
-// A1 + A2 + A3 to 24 bits.  Five products per K step (A1B1, A1B2, A2B1,
-// A2B2, A3B1) leave out only A3*B2, of relative size 2^-24; every piece
-// product is exact.  The tensor core's f32 accumulation truncates (each add
-// errs toward zero, so the error grows with the number of adds), hence the
-// accumulator is read out every 8 blocks (80 MMAs) and the chunks are summed
-// in f32 registers with round-to-nearest.  The result equals the
-// block-scaled sum up to f32 rounding, like the per-block fold, at five
-// times the tensor work and one eighth of the read-outs, with no scale
-// arithmetic on the CUDA cores.
+// with D the integer dot of block b.  Over one chunk c of 8 blocks
+// (256 values of k) this is one sum over k,
+//   Y_c[t][r] = 2^-(s_t + u_r) * sum_k A'[t][k] * B'[r][k],
+//   A'[t][k] = (dx[t][k/32] * 2^s_t) * Xq[t][k]       (f32: one rounding, 2^-24)
+//   B'[r][k] = (d_w[r][k/32] * 2^u_r) * (q_w[r][k] - 8) (exact: 11 x 3 bits)
+// with power-of-two exponents s_t (per token and chunk) and u_r (per row and
+// chunk) chosen from the chunk's largest scale so that |A'| < 2^15 and
+// |B'| < 2^15 (f16 range, normal numbers down to the chunk's small values).
+// The operands are fed to kind::f16 MMAs as f16 pieces: B' = B1 + B2
+// exactly (14 significant bits), A' = A1 + A2 to 22 bits.  Three products
+// per K step (A1B1, A1B2, A2B1) leave out A2*B2 and the A remainder, both
+// below 2^-22 relative; every piece product is exact.  The tensor core's
+// f32 accumulation truncates (each add errs toward zero), so each chunk's
+// accumulator is read out (24 MMAs per 128 K) and added into f32 registers
+// with round-to-nearest, times its power-of-two factor 2^-(s_t + u_r).
+// The result equals the block-scaled sum up to f32 rounding, like the
+// per-block fold, at three times the tensor work and one eighth of the
+// read-outs.
 //
-// Requires K % 256 == 0 (8-block scale tiles); other K use the per-block
-// fold in gq_gemm_tc.cu.
+// Requires K % 256 == 0 (8-block chunks and scale tiles); other K use the
+// per-block fold in gq_gemm_tc.cu.
 //
 // Kernels:
-//   k_xq_split   writes A1, A2, A3 into the caller's workspace, one 24 KB
-//                chunk per (128-token tile, 32-block) in the UMMA K-major
-//                layout (bf16, 8-element groups in the order 0,4,1,5,2,6,3,7).
+//   k_xq_split   writes A1, A2 into the caller's workspace, one 16 KB chunk
+//                per (128-token tile, 32-block) in the UMMA K-major layout
+//                (f16, 8-element groups in the order 0,4,1,5,2,6,3,7).
 //   k_gemm_split one 480-thread CTA per SM, persistent over 128-token x
 //                192-row tiles, two 8-block chunk accumulators in TMEM:
 //   warps 0-11  workers: for each block, build B1, B2 from the nibbles and
 //               the d_w scale tile into the operand stage the MMA of block
 //               g-S has released; after each 8-block chunk, add its
-//               accumulator into f32 registers (warp w: TMEM lanes
-//               32*(w%4).., 64 of the 192 columns) and store Y after a
-//               tile's last chunk.
+//               accumulator times 2^-(s_t + u_r) into f32 registers (warp w:
+//               TMEM lanes 32*(w%4).., 64 of the 192 columns) and store Y
+//               after a tile's last chunk.
 //   warp 12     one lane: TMA loads of the 192 x 16 B nibbles per block
 //               and, every 8 blocks, of the 8 x 192 d_w scale tile.
-//   warp 13     one lane: 10 MMAs (M128 N192 K16) per block into the
+//   warp 13     one lane: 6 MMAs (M128 N192 K16) per block into the
 //               chunk's accumulator; owns TMEM.
-//   warp 14     one lane: bulk copy of each block's 24 KB A chunk.
+//   warp 14     one lane: bulk copy of each block's 16 KB A chunk.
 // Every mbarrier wait is bounded (see gq_tc.cuh): on timeout the kernel
 // records GQ_ERR_TIMEOUT, every role leaves its loop, TMEM is released.
-#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "gq_tc.cuh"
 
@@ -69,51 +72,93 @@ constexpr int NACC = 2;          // chunk accumulators (a chunk = SG blocks)
 constexpr int ACC_STRIDE = 256;  // TMEM column offset between them
 constexpr int TMEM_COLS = 512;
 
-constexpr int APIECE = TM * KB * 2;   // 8192: one bf16 piece of A
-constexpr int A_BYTES = 3 * APIECE;   // 24576: one workspace chunk
-constexpr int BPIECE = TN * KB * 2;   // 12288: one bf16 piece of B
+constexpr int APIECE = TM * KB * 2;   // 8192: one f16 piece of A
+constexpr int A_BYTES = 2 * APIECE;   // 16384: one workspace chunk
+constexpr int BPIECE = TN * KB * 2;   // 12288: one f16 piece of B
 constexpr int B_BYTES = 2 * BPIECE;   // 24576
 constexpr int RB_BYTES = TN * 16;     // 3072: nibbles (TMA box 16 x 192)
 constexpr int STW_BYTES = TN * SG * 2;  // 3072: d_w fp16 [192 rows][8 blocks]
+constexpr int NSR = 4;                  // chunks of row factors in flight
+constexpr int SR_BYTES = TN * 4;        // 2^-u_r of the tile's 192 rows for one chunk
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + S * A_BYTES;
 constexpr int OFF_RAW = OFF_B + S * B_BYTES;
 constexpr int OFF_STILE = OFF_RAW + RAW * RB_BYTES;
-constexpr int OFF_BAR = OFF_STILE + STG * STW_BYTES;
+constexpr int OFF_SR = OFF_STILE + STG * STW_BYTES;
+constexpr int OFF_BAR = OFF_SR + NSR * SR_BYTES;
 // afull, opempty, full per operand stage; rfull, rempty per raw stage;
-// cfull, cempty per chunk accumulator; sfull, sempty per scale tile stage; drain
-constexpr int N_BARS = 3 * S + 2 * RAW + 2 * NACC + 2 * STG + 1;
+// cfull, cempty per chunk accumulator; sfull, sempty per scale tile stage;
+// srdy per row-factor slot; drain
+constexpr int N_BARS = 3 * S + 2 * RAW + 2 * NACC + 2 * STG + NSR + 1;
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16;
 
 static_assert((S & (S - 1)) == 0 && (RAW & (RAW - 1)) == 0 && (SG & (SG - 1)) == 0 && (STG & (STG - 1)) == 0 &&
-                  (NACC & (NACC - 1)) == 0,
+                  (NACC & (NACC - 1)) == 0 && (NSR & (NSR - 1)) == 0,
               "ring sizes are powers of two");
-static_assert(OFF_B % 1024 == 0 && OFF_RAW % 1024 == 0 && OFF_STILE % 128 == 0 && OFF_BAR % 8 == 0 &&
-                  SMEM_BYTES <= 232448,
+static_assert(OFF_B % 1024 == 0 && OFF_RAW % 1024 == 0 && OFF_STILE % 128 == 0 && OFF_SR % 16 == 0 &&
+                  OFF_BAR % 8 == 0 && SMEM_BYTES <= 232448,
               "shared memory layout");
 static_assert(NWORK * 2 == TN * 4, "two 8-element nibble groups per worker thread");
 
-constexpr uint32_t kIdesc = idesc_f16(TM, TN, true);  // bf16 A and B
+constexpr uint32_t kIdesc = idesc_f16(TM, TN, false);  // f16 A and B
+
+// ---------------------------------------------------------------- chunk exponents
+// Exponents of the power-of-two chunk factors: for m > 0 (the chunk's
+// largest scale), m * 2^e lies in [2^(T-1), 2^T); e = 0 for m = 0, NaN or
+// infinity.  Read from the IEEE bits (subnormal m counts as 2^-126) and
+// clamped to [-60, 60], so 2^e, 2^-e and 2^-(s_t + u_r) are normal floats.
+constexpr int kTokExp = 8;    // max |A'| < 127 * 2^8 < 2^15
+constexpr int kRowExp = 12;   // max |B'| <= 8 * 2^12 = 2^15
+__device__ __forceinline__ int chunk_exp(float m, int T)
+{
+    const uint32_t bits = __float_as_uint(m);
+    const int be = static_cast<int>((bits >> 23) & 0xFFu);
+    if (!(m > 0.f) || be == 0xFF) return 0;
+    const int e = (be == 0 ? 1 : be) - 126;  // m in [2^(e-1), 2^e)
+    const int x = T - e;
+    return x < -60 ? -60 : (x > 60 ? 60 : x);
+}
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
+
+// Largest of 8 block scales: dx f32 (non-negative, from amax / 127) or d_w fp16 (|d|).
+__device__ __forceinline__ float max8_f32(float4 a, float4 b)
+{
+    return fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w)));
+}
+__device__ __forceinline__ float max8_f16(uint4 v)
+{
+    float m = 0.f;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m = fmaxf(m, fabsf(__half2float(__ushort_as_half(static_cast<uint16_t>(w[i] & 0xFFFFu)))));
+        m = fmaxf(m, fabsf(__half2float(__ushort_as_half(static_cast<uint16_t>(w[i] >> 16)))));
+    }
+    return m;
+}
 
 // ---------------------------------------------------------------- operand pieces
-__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
-// (a, b) -> bf16x2 hi = RN(a, b) and the exact remainders (a - hi.x, b - hi.y).
-__device__ __forceinline__ uint32_t split_bf2(float a, float b, float &ra, float &rb)
+// (a, b) -> f16x2 hi = RN(a, b) and the exact remainders (a - hi.x, b - hi.y).
+__device__ __forceinline__ uint32_t split_h2(float a, float b, float &ra, float &rb)
 {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const __half2 h = __floats2half2_rn(a, b);
     ra = a - __low2float(h);
     rb = b - __high2float(h);
-    return bf2_bits(h);
+    return h2_bits(h);
 }
 
 // Activation pieces: thread p writes 16 bytes of each piece of chunk p/512
 // = (token tile T, block b), T-major, at 8-element group position p % 512
-// (= op_off(row, kg) / 16).  Tokens past M are zeros.
+// (= op_off(row, kg) / 16).  Tokens past M are zeros.  The thread of group
+// 0 of a chunk's first block also writes the token's chunk factor 2^-s_t
+// to tokf[token][chunk] (1 for tokens past M).
 __global__ void __launch_bounds__(256) k_xq_split(const int8_t *__restrict__ Xq, const float *__restrict__ dx,
-                                                  uint4 *__restrict__ Xh, int K, int M, long long npieces)
+                                                  uint4 *__restrict__ Xh, float *__restrict__ tokf, int K, int M,
+                                                  long long npieces)
 {
     pdl_launch_dependents();  // the GEMM's prologue may overlap; it waits for this grid before reading Xh
     pdl_wait();
@@ -125,69 +170,77 @@ __global__ void __launch_bounds__(256) k_xq_split(const int8_t *__restrict__ Xq,
         const long long T = chunk / nb;
         const int b = static_cast<int>(chunk - T * nb);
         const long long t = T * TM + row;
-        uint4 o1 = make_uint4(0u, 0u, 0u, 0u), o2 = o1, o3 = o1;
+        uint4 o1 = make_uint4(0u, 0u, 0u, 0u), o2 = o1;
+        const bool fac = kg == 0 && (b & (SG - 1)) == 0;
+        if (fac && t >= M) tokf[t * (nb / SG) + b / SG] = 1.f;
         if (t < M) {
             const uint2 v = __ldg(reinterpret_cast<const uint2 *>(Xq + t * K + b * KB + kg * 8));
-            const float d = __ldg(dx + t * nb + b);
+            const float4 *dc = reinterpret_cast<const float4 *>(dx + t * nb + (b & ~(SG - 1)));
+            const int st = chunk_exp(max8_f32(__ldg(dc), __ldg(dc + 1)), kTokExp);
+            if (fac) tokf[t * (nb / SG) + b / SG] = exp2i(-st);
+            const float d = __ldg(dx + t * nb + b) * exp2i(st);  // exact (both normal or zero)
             float e[8];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 e[j] = d * static_cast<float>(static_cast<int8_t>(v.x >> (8 * j)));
                 e[j + 4] = d * static_cast<float>(static_cast<int8_t>(v.y >> (8 * j)));
             }
-            uint32_t w1[4], w2[4], w3[4];
+            uint32_t w1[4], w2[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {  // word i holds elements (i, i+4)
-                float r1a, r1b, r2a, r2b, r3a, r3b;
-                w1[i] = split_bf2(e[i], e[i + 4], r1a, r1b);
-                w2[i] = split_bf2(r1a, r1b, r2a, r2b);
-                w3[i] = split_bf2(r2a, r2b, r3a, r3b);
+                float r1a, r1b, r2a, r2b;
+                w1[i] = split_h2(e[i], e[i + 4], r1a, r1b);
+                w2[i] = split_h2(r1a, r1b, r2a, r2b);
             }
             o1 = make_uint4(w1[0], w1[1], w1[2], w1[3]);
             o2 = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-            o3 = make_uint4(w3[0], w3[1], w3[2], w3[3]);
         }
         uint4 *dst = Xh + chunk * (A_BYTES / 16) + within;
         dst[0] = o1;
         dst[APIECE / 16] = o2;
-        dst[2 * APIECE / 16] = o3;
     }
 }
 
 // Weight pieces of one 8-element group: nibbles of w (element order) and
-// the block's d_w -> B1 and B2 chunks (16 bytes each, order 0,4,1,5,...).
-// Pair i = (nibble i, nibble i+4): OR-ed into the 2^23 pattern (exact
-// 2^23 + q*16^i), one packed FMA by 16^-i gives q - 8 exactly, one packed
-// multiply by d_w gives B' exactly (4 x 11 bits); cvt.rn.bf16x2 gives B1,
-// the exact remainder B' - B1 (at most 7 bits) converts exactly to B2.  One
-// asm block per pair keeps the temporaries in 64-bit register pairs.
-#define GQ_SPLIT_PAIR(MASK, SCALE, BIAS)                                                                      \
-    "{\n"                                                                                                     \
-    " .reg .b32 a, b, hx, hy, rx, ry, vx, vy;\n"                                                              \
-    " .reg .b64 p, v, hp, r, s2, c2, d2;\n"                                                                   \
-    " shr.u32 b, %2, 16;\n"                                                                                   \
-    " lop3.b32 a, %2, " MASK ", 0x4B000000, 0xEA;\n"                                                          \
-    " lop3.b32 b, b, " MASK ", 0x4B000000, 0xEA;\n"                                                           \
-    " mov.b64 p, {a, b};\n"                                                                                   \
-    " mov.b64 s2, {%4, %4};\n mov.b64 c2, {%5, %5};\n mov.b64 d2, {%3, %3};\n"                               \
-    " fma.rn.f32x2 p, p, s2, c2;\n"                                                                           \
-    " mul.rn.f32x2 v, p, d2;\n"                                                                               \
-    " mov.b64 {vx, vy}, v;\n"                                                                                 \
-    " cvt.rn.bf16x2.f32 %0, vy, vx;\n"                                                                        \
-    " shl.b32 hx, %0, 16;\n"                                                                                  \
-    " and.b32 hy, %0, 0xFFFF0000;\n"                                                                          \
-    " mov.b64 hp, {hx, hy};\n"                                                                                \
-    " sub.rn.f32x2 r, v, hp;\n"                                                                               \
-    " mov.b64 {rx, ry}, r;\n"                                                                                 \
-    " cvt.rn.bf16x2.f32 %1, ry, rx;\n"                                                                        \
-    "}"
-
-__device__ __forceinline__ void nib8_split(uint32_t w, float dw, uint4 &b1, uint4 &b2)
+// the block's scale d = d_w * 2^u_r as f16x2 {d, d} -> B1 and B2 chunks
+// (16 bytes each, word i = elements (i, i+4)), all in packed f16:
+// pair i is OR-ed into the f16 pattern of 1024 (exact 1024 + q*16^(i%2),
+// after a shift by 8 for i >= 2), one FMA gives q - 8 exactly, B1 =
+// RN(d * (q - 8)) and B2 = d * (q - 8) - B1 by one FMA, exact because
+// d * (q - 8) has at most 14 significant bits (11 x 3), so the remainder
+// fits in f16 (in the normal range; d is at most 2^12, so |B1| <= 2^15).
+__device__ __forceinline__ void nib8_split(uint32_t w, uint32_t d2, uint4 &b1, uint4 &b2)
 {
-    asm(GQ_SPLIT_PAIR("0x0000000F", "", "") : "=r"(b1.x), "=r"(b2.x) : "r"(w), "f"(dw), "f"(1.0f), "f"(-8388616.0f));
-    asm(GQ_SPLIT_PAIR("0x000000F0", "", "") : "=r"(b1.y), "=r"(b2.y) : "r"(w), "f"(dw), "f"(0.0625f), "f"(-524296.0f));
-    asm(GQ_SPLIT_PAIR("0x00000F00", "", "") : "=r"(b1.z), "=r"(b2.z) : "r"(w), "f"(dw), "f"(0.00390625f), "f"(-32776.0f));
-    asm(GQ_SPLIT_PAIR("0x0000F000", "", "") : "=r"(b1.w), "=r"(b2.w) : "r"(w), "f"(dw), "f"(0.000244140625f), "f"(-2056.0f));
+    asm("{\n"
+        " .reg .b32 s, x0, x1, x2, x3, q0, q1, q2, q3, n0, n1, n2, n3, one, m1032, sixteenth, m72;\n"
+        " mov.b32 one, 0x3C003C00;\n"        // 1
+        " mov.b32 m1032, 0xE408E408;\n"      // -1032
+        " mov.b32 sixteenth, 0x2C002C00;\n"  // 1/16
+        " mov.b32 m72, 0xD480D480;\n"        // -72
+        " shr.u32 s, %8, 8;\n"
+        " lop3.b32 x0, %8, 0x000F000F, 0x64006400, 0xEA;\n"
+        " lop3.b32 x1, %8, 0x00F000F0, 0x64006400, 0xEA;\n"
+        " lop3.b32 x2, s, 0x000F000F, 0x64006400, 0xEA;\n"
+        " lop3.b32 x3, s, 0x00F000F0, 0x64006400, 0xEA;\n"
+        " fma.rn.f16x2 q0, x0, one, m1032;\n"  // x * 1 - 1032
+        " fma.rn.f16x2 q1, x1, sixteenth, m72;\n"  // x / 16 - 72
+        " fma.rn.f16x2 q2, x2, one, m1032;\n"
+        " fma.rn.f16x2 q3, x3, sixteenth, m72;\n"
+        " mul.rn.f16x2 %0, q0, %9;\n"
+        " mul.rn.f16x2 %1, q1, %9;\n"
+        " mul.rn.f16x2 %2, q2, %9;\n"
+        " mul.rn.f16x2 %3, q3, %9;\n"
+        " xor.b32 n0, %0, 0x80008000;\n"
+        " xor.b32 n1, %1, 0x80008000;\n"
+        " xor.b32 n2, %2, 0x80008000;\n"
+        " xor.b32 n3, %3, 0x80008000;\n"
+        " fma.rn.f16x2 %4, q0, %9, n0;\n"
+        " fma.rn.f16x2 %5, q1, %9, n1;\n"
+        " fma.rn.f16x2 %6, q2, %9, n2;\n"
+        " fma.rn.f16x2 %7, q3, %9, n3;\n"
+        "}"
+        : "=r"(b1.x), "=r"(b1.y), "=r"(b1.z), "=r"(b1.w), "=r"(b2.x), "=r"(b2.y), "=r"(b2.z), "=r"(b2.w)
+        : "r"(w), "r"(d2));
 }
 
 struct Work {
@@ -203,8 +256,8 @@ __device__ __forceinline__ void tile_origin(const Work &w, int tile, int &t0, in
 // ---------------------------------------------------------------- the kernel
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_gemm_split(const uint8_t *__restrict__ Xh, const __grid_constant__ CUtensorMap mapB,
-                 const __grid_constant__ CUtensorMap mapW, float *__restrict__ Y, int rows, int K, int M,
-                 int *__restrict__ status)
+                 const __grid_constant__ CUtensorMap mapW, const float *__restrict__ tokf,
+                 float *__restrict__ Y, int rows, int K, int M, int *__restrict__ status)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -213,7 +266,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t bar_rfull = bar_full + 8 * S, bar_rempty = bar_rfull + 8 * RAW;
     const uint32_t bar_cfull = bar_rempty + 8 * RAW, bar_cempty = bar_cfull + 8 * NACC;
     const uint32_t bar_sfull = bar_cempty + 8 * NACC, bar_sempty = bar_sfull + 8 * STG;
-    const uint32_t bar_drain = bar_sempty + 8 * STG;
+    const uint32_t bar_srdy = bar_sempty + 8 * STG;
+    const uint32_t bar_drain = bar_srdy + 8 * NSR;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
@@ -244,6 +298,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(bar_sfull + 8 * i, 1);
             mbar_init(bar_sempty + 8 * i, WORK_WARPS);
         }
+        for (int i = 0; i < NSR; ++i) mbar_init(bar_srdy + 8 * i, WORK_WARPS);
         mbar_init(bar_drain, 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -347,14 +402,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
                     const uint32_t ka = a0 + ks * 256, kb = b0 + ks * 256;
-                    const uint64_t A1 = smem_desc(ka, 128, 512), A2 = smem_desc(ka + APIECE, 128, 512),
-                                   A3 = smem_desc(ka + 2 * APIECE, 128, 512);
+                    const uint64_t A1 = smem_desc(ka, 128, 512), A2 = smem_desc(ka + APIECE, 128, 512);
                     const uint64_t B1 = smem_desc(kb, 128, 512), B2 = smem_desc(kb + BPIECE, 128, 512);
                     mma_f16(d, A1, B1, kIdesc, (cfirst && ks == 0) ? 0u : 1u);
                     mma_f16(d, A1, B2, kIdesc, 1u);
                     mma_f16(d, A2, B1, kIdesc, 1u);
-                    mma_f16(d, A2, B2, kIdesc, 1u);
-                    mma_f16(d, A3, B1, kIdesc, 1u);
                 }
                 mma_commit(bar_opempty + 8 * s);
                 if ((gb & (SG - 1)) == SG - 1) mma_commit(bar_cfull + 8 * acc);
@@ -370,8 +422,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncwarp();
     } else if (warp < WORK_WARPS) {
         // ------------------------------------------------ workers
-        const int tid = threadIdx.x;  // 0..NWORK-1
-        const int q = warp & 3;       // TMEM lane quarter
+        const int q = warp & 3;  // TMEM lane quarter
         const int c0 = (warp >> 2) * EPI_COLS;
         // this thread's two nibble groups: warp w covers rows 32*(w/2).. and K
         // groups 2*(w%2), 2*(w%2)+1, so the 16-byte stores of 8 consecutive
@@ -385,12 +436,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int cpt = w.nb / SG;  // chunks per tile
         float acc[EPI_COLS];        // written first by each tile's first chunk
         // Add chunk c's accumulator into acc; after a tile's last chunk store Y.
+        // 2^-s_t of this lane's token for the chunks c with c % 2 == 0 / 1,
+        // loaded from the pre-pass's table when the chunk's conversion starts
+        float ft0 = 1.f, ft1 = 1.f;
         auto readout = [&](int c) {
             const int ab = c & (NACC - 1);
+            const int ct = c % cpt;  // chunk within its tile
+            int t0, r0;
+            tile_origin(w, static_cast<int>(blockIdx.x) + (c / cpt) * static_cast<int>(gridDim.x), t0, r0);
+            const int t = t0 + q * 32 + lane;
+            const float ft = (c & 1) ? ft1 : ft0;
+            // 2^-u_r of the chunk's rows, written by the converters at its start
+            ok = wait_warp(bar_srdy + 8 * (c & (NSR - 1)), static_cast<uint32_t>(c / NSR) & 1u, abort, status);
+            if (!ok) return;
+            const float *sr = reinterpret_cast<const float *>(smem + OFF_SR + (c & (NSR - 1)) * SR_BYTES) + c0;
             ok = wait_warp(bar_cfull + 8 * ab, static_cast<uint32_t>(c / NACC) & 1u, abort, status);
             if (!ok) return;
             tc_fence_after();
-            const int ct = c % cpt;  // chunk within its tile
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + ab * ACC_STRIDE + c0;
 #pragma unroll
             for (int part = 0; part < EPI_COLS / 16; ++part) {
@@ -402,19 +464,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (lane == 0) mbar_arrive(bar_cempty + 8 * ab);
                 }
 #pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    float2 v = make_float2(d[e], d[e + 1]);
-                    if (ct != 0) v = __fadd2_rn(v, make_float2(acc[part * 16 + e], acc[part * 16 + e + 1]));
-                    acc[part * 16 + e] = v.x;
-                    acc[part * 16 + e + 1] = v.y;
+                for (int e = 0; e < 16; e += 4) {
+                    const float4 f4 = *reinterpret_cast<const float4 *>(sr + part * 16 + e);
+                    const float2 f01 = __fmul2_rn(make_float2(ft, ft), make_float2(f4.x, f4.y));  // exact
+                    const float2 f23 = __fmul2_rn(make_float2(ft, ft), make_float2(f4.z, f4.w));
+                    float2 v01, v23;
+                    if (ct != 0) {
+                        v01 = __ffma2_rn(make_float2(d[e], d[e + 1]), f01,
+                                         make_float2(acc[part * 16 + e], acc[part * 16 + e + 1]));
+                        v23 = __ffma2_rn(make_float2(d[e + 2], d[e + 3]), f23,
+                                         make_float2(acc[part * 16 + e + 2], acc[part * 16 + e + 3]));
+                    } else {
+                        v01 = __fmul2_rn(make_float2(d[e], d[e + 1]), f01);
+                        v23 = __fmul2_rn(make_float2(d[e + 2], d[e + 3]), f23);
+                    }
+                    acc[part * 16 + e] = v01.x;
+                    acc[part * 16 + e + 1] = v01.y;
+                    acc[part * 16 + e + 2] = v23.x;
+                    acc[part * 16 + e + 3] = v23.y;
                 }
 #pragma unroll
                 for (int e = 0; e < 16; ++e) asm volatile("" : "+f"(acc[part * 16 + e]));
             }
             if (ct == cpt - 1) {
-                int t0, r0;
-                tile_origin(w, static_cast<int>(blockIdx.x) + (c / cpt) * static_cast<int>(gridDim.x), t0, r0);
-                const int t = t0 + q * 32 + lane;
                 if (t < M) {
                     float *yrow = Y + static_cast<size_t>(t) * rows + r0 + c0;
                     const int nvalid = rows - (r0 + c0);
@@ -434,6 +506,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         };
 
+        float wsc = 1.f;  // 2^u_r of the converted row for the current chunk
         int rc = 0;  // next chunk to read out
         const int nchunks = nblocks / SG;
         for (int g = 0; g < nblocks && ok; ++g) {
@@ -444,10 +517,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 ok = wait_warp(bar_sfull + 8 * sg, static_cast<uint32_t>(g / (SG * STG)) & 1u, abort, status);
             if (ok) ok = wait_warp(bar_rfull + 8 * rs, static_cast<uint32_t>(g / RAW) & 1u, abort, status);
             if (!ok) break;
+            const uint8_t *stile = smem + OFF_STILE + sg * STW_BYTES;
+            const int cg = g / SG;  // chunk of this block
+            if ((g & (SG - 1)) == 0) {
+                // 2^u_r of this row for the chunk (rows past the end load zeros: 1),
+                // and 2^-u_r into the chunk's row-factor slot for the read-out
+                const int u = chunk_exp(max8_f16(*reinterpret_cast<const uint4 *>(stile + crow * 16)), kRowExp);
+                wsc = exp2i(u);
+                if (chalf == 0) reinterpret_cast<float *>(smem + OFF_SR + (cg & (NSR - 1)) * SR_BYTES)[crow] = exp2i(-u);
+                // this lane's token factor for the chunk
+                int t0, r0;
+                tile_origin(w, static_cast<int>(blockIdx.x) + (cg / cpt) * static_cast<int>(gridDim.x), t0, r0);
+                const float f = __ldg(tokf + static_cast<size_t>(t0 + q * 32 + lane) * cpt + cg % cpt);
+                if (cg & 1)
+                    ft1 = f;
+                else
+                    ft0 = f;
+            }
             {
-                const uint16_t dwb =
-                    reinterpret_cast<const uint16_t *>(smem + OFF_STILE + sg * STW_BYTES)[crow * SG + (g & (SG - 1))];
-                const float dw = __half2float(__ushort_as_half(dwb));
+                const uint16_t dwb = reinterpret_cast<const uint16_t *>(stile)[crow * SG + (g & (SG - 1))];
+                // d_w * 2^u_r: exact in f32, and in f16 down to 2^-14 (at most 2^12)
+                const uint32_t dh = __half_as_ushort(__float2half_rn(__half2float(__ushort_as_half(dwb)) * wsc));
+                const uint32_t dw = dh | (dh << 16);
                 const uint2 v = *reinterpret_cast<const uint2 *>(smem + OFF_RAW + rs * RB_BYTES + csrc);
                 uint8_t *dst = smem + OFF_B + s * B_BYTES + cdst;
                 uint4 h, l;
@@ -463,6 +554,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (lane == 0) {
                 mbar_arrive(bar_full + 8 * s);
                 mbar_arrive(bar_rempty + 8 * rs);
+                if ((g & (SG - 1)) == 0) mbar_arrive(bar_srdy + 8 * (cg & (NSR - 1)));
                 if ((g & (SG - 1)) == SG - 1) mbar_arrive(bar_sempty + 8 * sg);
             }
             // chunk rc ends at block SG*(rc+1) - 1; once S more blocks have been
@@ -490,10 +582,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }  // namespace tcs
 
 // ---------------------------------------------------------------- host side
+// Workspace: the A chunks, then the token factors f32 [ntm * 128][K / 256].
+static size_t split_chunks_bytes(int K, int M)
+{
+    return static_cast<size_t>((M + tcs::TM - 1) / tcs::TM) * static_cast<size_t>(K / tcs::KB) * tcs::A_BYTES;
+}
 size_t gemm_split_workspace_bytes(int K, int M)
 {
-    if (K < tcs::KB || K % tcs::KB != 0 || M < 1) return 0;
-    return static_cast<size_t>((M + tcs::TM - 1) / tcs::TM) * static_cast<size_t>(K / tcs::KB) * tcs::A_BYTES;
+    if (!gemm_split_supported(K) || M < 1) return 0;
+    return split_chunks_bytes(K, M) +
+           static_cast<size_t>((M + tcs::TM - 1) / tcs::TM) * tcs::TM * static_cast<size_t>(K / (tcs::KB * tcs::SG)) * 4;
 }
 
 bool gemm_split_supported(int K) { return K >= 256 && K % 256 == 0; }
@@ -519,13 +617,15 @@ int launch_gemm_split(const void *W, const int8_t *Xq, const float *dx, float *Y
                   static_cast<uint64_t>(nb) * 2, tcs::SG, tcs::TN))
         return GQ_ERR_CUDA;
 
-    // activation codes x scales -> bf16 operand pieces
-    const long long npieces = static_cast<long long>(need / tcs::A_BYTES) * 512;
+    // activation codes x scales -> f16 operand pieces
+    const size_t chunks_bytes = split_chunks_bytes(K, M);
+    float *tokf = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + chunks_bytes);
+    const long long npieces = static_cast<long long>(chunks_bytes / tcs::A_BYTES) * 512;
     long long pgrid = (npieces + 255) / 256;
     const long long pmax = static_cast<long long>(sm_count()) * 8;
     if (pgrid > pmax) pgrid = pmax;
     int rc = status_from(launch_pdl(tcs::k_xq_split, dim3(static_cast<unsigned>(pgrid)), dim3(256), 0, s, Xq, dx,
-                                    static_cast<uint4 *>(ws), K, M, npieces));
+                                    static_cast<uint4 *>(ws), tokf, K, M, npieces));
     if (rc != GQ_OK) return rc;
 
     const int occ = ctas_per_sm(reinterpret_cast<const void *>(tcs::k_gemm_split), tcs::NTHREADS, tcs::SMEM_BYTES);
@@ -534,7 +634,7 @@ int launch_gemm_split(const void *W, const int8_t *Xq, const float *dx, float *Y
     if (grid > ntiles) grid = ntiles;
     return status_from(launch_pdl(tcs::k_gemm_split, dim3(grid), dim3(tcs::NTHREADS),
                                   static_cast<size_t>(tcs::SMEM_BYTES), s, static_cast<const uint8_t *>(ws), mapB,
-                                  mapW, Y, rows, K, M, status_word()));
+                                  mapW, static_cast<const float *>(tokf), Y, rows, K, M, status_word()));
 }
 
 }  // namespace gq

@@ -1,5 +1,17 @@
 """GPU parity of the Q8_0 activation quantizer (bit-exact) and the Q4_0 x Q8_0
-prefill contraction (|Y - Y_ref| <= 1e-5 * sum_b |d_w d_x D|)."""
+prefill contraction.
+
+Two bounds for Y[t][r]:
+  element level  |Y - Y_ref| <= 1e-5 * sum_k |d_w (q_w - 8)| * |dx Xq|
+                 (the matvec bound, on the dequantized operands): guaranteed
+                 for any inputs, and the one the scale-folded path (operands
+                 dx*Xq and d_w*(q_w-8) rounded per element) is built to;
+  block level    |Y - Y_ref| <= 1e-5 * sum_b |d_w dx D_b|, tighter when a
+                 block's integer dot cancels; it holds on the pages-shaped
+                 inputs and is asserted there, but no f32 evaluation that
+                 rounds dx*Xq per element can promise it under heavy
+                 cancellation inside a block (the spread-scale test below).
+"""
 
 import numpy as np
 import pytest
@@ -38,6 +50,14 @@ def workspace(K, M):
     n = gq.gq_q4_0_gemm_workspace_bytes(K, M)
     # stale contents must not matter: the pre-pass overwrites every byte the GEMM reads
     return t.full((n,), 0x7B, dtype=t.uint8, device="cuda"), n
+
+
+def element_bound(W, Xq, dx, K):
+    """sum_k |w[r][k]| * |x[t][k]| with w = d_w (q_w - 8) (the oracle's dequantization)
+    and x = dx * Xq, as (tokens, rows)."""
+    w = np.abs(oracle.dequant(oracle.FORMAT_Q4_0, W, K))
+    x = np.abs(np.repeat(dx.astype(np.float64), 32, axis=1) * Xq.astype(np.float64))
+    return x @ w.T
 
 
 def run_gemm(W, Xq_np, dx_np, rows, K, M):
@@ -87,7 +107,33 @@ def test_gemm_full_512x21504x5376_sampled():
     assert np.all(np.abs(Yg - Y_ref) <= 1e-5 * A)
 
 
-@pytest.mark.parametrize("K", [128, 256])  # per-block fold; scale-folded bf16 pieces
+def test_gemm_scales_spread_over_many_octaves():
+    """Block scales spread over many octaves inside each 8-block chunk (weight
+    scales down to f16 subnormals, activation blocks 2^-12..2^12 apart, an
+    all-zero block and an all-zero chunk): the power-of-two chunk factors of
+    the f16 operand pieces keep every output within the bound."""
+    rows, K, M = 200, 512, 40
+    nb = K // 32
+    rng = np.random.default_rng(77)
+    W = synth.q4_0_weights(rows, K, synth.stream(77, 0))
+    e = rng.integers(-24, 9, size=(rows, nb))
+    d = np.ldexp(rng.uniform(0.5, 1.0, size=(rows, nb)), e).astype(np.float16)
+    d[7, :] = np.float16(2.0 ** -24)  # a row of the smallest subnormal scale
+    W.reshape(rows, nb, 18)[:, :, 0:2] = d.view(np.uint8).reshape(rows, nb, 2)
+    X = synth.normal((M, K), synth.stream(77, 1)).astype(np.float64)
+    X *= np.repeat(np.ldexp(1.0, rng.integers(-12, 13, size=(M, nb))), 32, axis=1)
+    X[3, 64:96] = 0.0
+    X[5, 256:512] = 0.0
+    X = X.astype(np.float32)
+    Xq, dx = oracle.quantize_q8_0(X, M, K)
+    Y = run_gemm(W, Xq, dx, rows, K, M)
+    Y_ref, _ = oracle.gemm_q8act(W, Xq, dx, rows, K, M)
+    err = np.abs(Y.astype(np.float64) - Y_ref)
+    A_el = element_bound(W, Xq, dx, K)
+    assert np.all(err <= 1e-5 * A_el), float(np.max(err / np.maximum(A_el, 1e-300)))
+
+
+@pytest.mark.parametrize("K", [128, 256])  # per-block fold; scale-folded f16 pieces
 def test_gemm_all_eight_weights_exact_zero(K):
     import blockenc as be
     rows, M = 70, 9
