@@ -30,19 +30,24 @@
 //   k_xq_split   writes A1, A2 into the caller's workspace, one 16 KB chunk
 //                per (128-token tile, 32-block) in the UMMA K-major layout
 //                (f16, 8-element groups in the order 0,4,1,5,2,6,3,7).
-//   k_gemm_split one 480-thread CTA per SM, persistent over 128-token x
+//   k_gemm_split one 608-thread CTA per SM, persistent over 128-token x
 //                192-row tiles, two 8-block chunk accumulators in TMEM:
-//   warps 0-11  workers: for each block, build B1, B2 from the nibbles and
-//               the d_w scale tile into the operand stage the MMA of block
-//               g-S has released; after each 8-block chunk, add its
-//               accumulator times 2^-(s_t + u_r) into f32 registers (warp w:
-//               TMEM lanes 32*(w%4).., 64 of the 192 columns) and store Y
-//               after a tile's last chunk.
-//   warp 12     one lane: TMA loads of the 192 x 16 B nibbles per block
+//   warps 0-11  read-out: after each 8-block chunk, add its accumulator
+//               times 2^-(s_t + u_r) into f32 registers (warp w: TMEM lanes
+//               32*(w%4).., 64 of the 192 columns) and store Y after a
+//               tile's last chunk.
+//   warps 12-15 converters: for each block, build B1, B2 from the nibbles
+//               and the d_w scale tile into the operand stage the MMA of
+//               block g-S has released (each thread: 3 rows x 16 weights);
+//               at a chunk's start, its rows' 2^-u_r for the read-out.
+//   warp 16     one lane: TMA loads of the 192 x 16 B nibbles per block
 //               and, every 8 blocks, of the 8 x 192 d_w scale tile.
-//   warp 13     one lane: 6 MMAs (M128 N192 K16) per block into the
+//   warp 17     one lane: 6 MMAs (M128 N192 K16) per block into the
 //               chunk's accumulator; owns TMEM.
-//   warp 14     one lane: bulk copy of each block's 16 KB A chunk.
+//   warp 18     one lane: bulk copy of each block's 16 KB A chunk.
+// The read-out runs on its own warps, so the conversion (the path's
+// limiter: it is latency-bound, one converter warp per scheduler) never
+// waits for it.
 // Every mbarrier wait is bounded (see gq_tc.cuh): on timeout the kernel
 // records GQ_ERR_TIMEOUT, every role leaves its loop, TMEM is released.
 #include <cuda_fp16.h>
@@ -61,13 +66,15 @@ constexpr int S = 4;      // operand stages
 constexpr int RAW = 8;    // raw nibble stages
 constexpr int SG = 8;     // blocks per scale tile
 constexpr int STG = 2;    // scale tile stages
-constexpr int WORK_WARPS = 12;
-constexpr int NWORK = WORK_WARPS * 32;
-constexpr int TMA_WARP = 12;
-constexpr int MMA_WARP = 13;
-constexpr int ACOPY_WARP = 14;
-constexpr int NTHREADS = 15 * 32;  // 480: up to 128 registers per thread
-constexpr int EPI_COLS = TN / (WORK_WARPS / 4);  // 64
+constexpr int RO_WARPS = 12;    // read-out warps: 4 TMEM lane quarters x 3 column groups
+constexpr int CONV_WARPS = 4;   // converter warps (weight pieces)
+constexpr int CONV0 = RO_WARPS; // first converter warp
+constexpr int TMA_WARP = RO_WARPS + CONV_WARPS;
+constexpr int MMA_WARP = TMA_WARP + 1;
+constexpr int ACOPY_WARP = TMA_WARP + 2;
+constexpr int NTHREADS = (ACOPY_WARP + 1) * 32;  // 608: up to 104 registers per thread
+constexpr int EPI_COLS = TN / (RO_WARPS / 4);    // 64
+constexpr int CROWS = TN / 64;                   // rows per converter thread (two nibble words each)
 constexpr int NACC = 2;          // chunk accumulators (a chunk = SG blocks)
 constexpr int ACC_STRIDE = 256;  // TMEM column offset between them
 constexpr int TMEM_COLS = 512;
@@ -100,7 +107,7 @@ static_assert((S & (S - 1)) == 0 && (RAW & (RAW - 1)) == 0 && (SG & (SG - 1)) ==
 static_assert(OFF_B % 1024 == 0 && OFF_RAW % 1024 == 0 && OFF_STILE % 128 == 0 && OFF_SR % 16 == 0 &&
                   OFF_BAR % 8 == 0 && SMEM_BYTES <= 232448,
               "shared memory layout");
-static_assert(NWORK * 2 == TN * 4, "two 8-element nibble groups per worker thread");
+static_assert(CONV_WARPS == 4 && TN % 64 == 0, "converter warp v: words 2h, 2h+1 (h = v % 2), rows 32 * (v / 2) + 64 * k + lane");
 
 constexpr uint32_t kIdesc = idesc_f16(TM, TN, false);  // f16 A and B
 
@@ -284,21 +291,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int i = 0; i < S; ++i) {
             mbar_init(bar_afull + 8 * i, 1);
             mbar_init(bar_opempty + 8 * i, 1);
-            mbar_init(bar_full + 8 * i, WORK_WARPS);
+            mbar_init(bar_full + 8 * i, CONV_WARPS);
         }
         for (int i = 0; i < RAW; ++i) {
             mbar_init(bar_rfull + 8 * i, 1);
-            mbar_init(bar_rempty + 8 * i, WORK_WARPS);
+            mbar_init(bar_rempty + 8 * i, CONV_WARPS);
         }
         for (int i = 0; i < NACC; ++i) {
             mbar_init(bar_cfull + 8 * i, 1);
-            mbar_init(bar_cempty + 8 * i, WORK_WARPS);
+            mbar_init(bar_cempty + 8 * i, RO_WARPS);
         }
         for (int i = 0; i < STG; ++i) {
             mbar_init(bar_sfull + 8 * i, 1);
-            mbar_init(bar_sempty + 8 * i, WORK_WARPS);
+            mbar_init(bar_sempty + 8 * i, CONV_WARPS);
         }
-        for (int i = 0; i < NSR; ++i) mbar_init(bar_srdy + 8 * i, WORK_WARPS);
+        for (int i = 0; i < NSR; ++i) mbar_init(bar_srdy + 8 * i, CONV_WARPS);
         mbar_init(bar_drain, 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -420,38 +427,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             wait_bounded(bar_drain, 0u, abort, status);
         }
         __syncwarp();
-    } else if (warp < WORK_WARPS) {
-        // ------------------------------------------------ workers
+    } else if (warp < RO_WARPS) {
+        // ------------------------------------------------ read-out warps
         const int q = warp & 3;  // TMEM lane quarter
         const int c0 = (warp >> 2) * EPI_COLS;
-        // this thread's two nibble groups: warp w covers rows 32*(w/2).. and K
-        // groups 2*(w%2), 2*(w%2)+1, so the 16-byte stores of 8 consecutive
-        // lanes fall on distinct bank groups
-        const int crow = 32 * (warp >> 1) + lane, chalf = warp & 1;
-        const uint32_t csrc = crow * 16 + chalf * 8;
-        const uint32_t cdst = op_off(crow, 2 * chalf);
         bool ok = true;
-
         // Chunks hold SG consecutive blocks of one tile (nb % SG == 0).
         const int cpt = w.nb / SG;  // chunks per tile
-        float acc[EPI_COLS];        // written first by each tile's first chunk
-        // Add chunk c's accumulator into acc; after a tile's last chunk store Y.
-        // 2^-s_t of this lane's token for the chunks c with c % 2 == 0 / 1,
-        // loaded from the pre-pass's table when the chunk's conversion starts
-        float ft0 = 1.f, ft1 = 1.f;
-        auto readout = [&](int c) {
-            const int ab = c & (NACC - 1);
-            const int ct = c % cpt;  // chunk within its tile
+        const int nchunks = nblocks / SG;
+        float acc[EPI_COLS];  // written first by each tile's first chunk
+        // 2^-s_t of this lane's token, loaded one chunk ahead
+        auto token_factor = [&](int c) -> float {
             int t0, r0;
             tile_origin(w, static_cast<int>(blockIdx.x) + (c / cpt) * static_cast<int>(gridDim.x), t0, r0);
-            const int t = t0 + q * 32 + lane;
-            const float ft = (c & 1) ? ft1 : ft0;
+            return __ldg(tokf + static_cast<size_t>(t0 + q * 32 + lane) * cpt + c % cpt);
+        };
+        float ft_next = nchunks > 0 ? token_factor(0) : 1.f;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int ab = c & (NACC - 1);
+            const int ct = c % cpt;  // chunk within its tile
+            const float ft = ft_next;
+            if (c + 1 < nchunks) ft_next = token_factor(c + 1);
             // 2^-u_r of the chunk's rows, written by the converters at its start
             ok = wait_warp(bar_srdy + 8 * (c & (NSR - 1)), static_cast<uint32_t>(c / NSR) & 1u, abort, status);
-            if (!ok) return;
+            if (!ok) break;
             const float *sr = reinterpret_cast<const float *>(smem + OFF_SR + (c & (NSR - 1)) * SR_BYTES) + c0;
             ok = wait_warp(bar_cfull + 8 * ab, static_cast<uint32_t>(c / NACC) & 1u, abort, status);
-            if (!ok) return;
+            if (!ok) break;
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + ab * ACC_STRIDE + c0;
 #pragma unroll
@@ -483,10 +485,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     acc[part * 16 + e + 2] = v23.x;
                     acc[part * 16 + e + 3] = v23.y;
                 }
-#pragma unroll
-                for (int e = 0; e < 16; ++e) asm volatile("" : "+f"(acc[part * 16 + e]));
             }
             if (ct == cpt - 1) {
+                int t0, r0;
+                tile_origin(w, static_cast<int>(blockIdx.x) + (c / cpt) * static_cast<int>(gridDim.x), t0, r0);
+                const int t = t0 + q * 32 + lane;
                 if (t < M) {
                     float *yrow = Y + static_cast<size_t>(t) * rows + r0 + c0;
                     const int nvalid = rows - (r0 + c0);
@@ -504,11 +507,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                 }
             }
-        };
-
-        float wsc = 1.f;  // 2^u_r of the converted row for the current chunk
-        int rc = 0;  // next chunk to read out
-        const int nchunks = nblocks / SG;
+        }
+    } else if (warp < CONV0 + CONV_WARPS) {
+        // ------------------------------------------------ converter warps
+        // warp v: nibble words 2h, 2h+1 (h = v % 2) of rows 32*(v/2) + 64k + lane,
+        // so the 16-byte stores of 8 consecutive lanes fall on distinct bank groups
+        const int v = warp - CONV0, h = v & 1;
+        int crow[CROWS];
+#pragma unroll
+        for (int k = 0; k < CROWS; ++k) crow[k] = 32 * (v >> 1) + 64 * k + lane;
+        bool ok = true;
+        float wsc[CROWS];  // 2^u_r of each converted row for the current chunk
+#pragma unroll
+        for (int k = 0; k < CROWS; ++k) wsc[k] = 1.f;
         for (int g = 0; g < nblocks && ok; ++g) {
             const int s = g & (S - 1), rs = g & (RAW - 1), sg = (g / SG) & (STG - 1);
             // the stage's previous block (g - S) must be done in the tensor core
@@ -520,34 +531,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint8_t *stile = smem + OFF_STILE + sg * STW_BYTES;
             const int cg = g / SG;  // chunk of this block
             if ((g & (SG - 1)) == 0) {
-                // 2^u_r of this row for the chunk (rows past the end load zeros: 1),
+                // 2^u_r of each row for the chunk (rows past the end load zeros: 1),
                 // and 2^-u_r into the chunk's row-factor slot for the read-out
-                const int u = chunk_exp(max8_f16(*reinterpret_cast<const uint4 *>(stile + crow * 16)), kRowExp);
-                wsc = exp2i(u);
-                if (chalf == 0) reinterpret_cast<float *>(smem + OFF_SR + (cg & (NSR - 1)) * SR_BYTES)[crow] = exp2i(-u);
-                // this lane's token factor for the chunk
-                int t0, r0;
-                tile_origin(w, static_cast<int>(blockIdx.x) + (cg / cpt) * static_cast<int>(gridDim.x), t0, r0);
-                const float f = __ldg(tokf + static_cast<size_t>(t0 + q * 32 + lane) * cpt + cg % cpt);
-                if (cg & 1)
-                    ft1 = f;
-                else
-                    ft0 = f;
+                float *srs = reinterpret_cast<float *>(smem + OFF_SR + (cg & (NSR - 1)) * SR_BYTES);
+#pragma unroll
+                for (int k = 0; k < CROWS; ++k) {
+                    const int u =
+                        chunk_exp(max8_f16(*reinterpret_cast<const uint4 *>(stile + crow[k] * 16)), kRowExp);
+                    wsc[k] = exp2i(u);
+                    if (h == 0) srs[crow[k]] = exp2i(-u);
+                }
             }
-            {
-                const uint16_t dwb = reinterpret_cast<const uint16_t *>(stile)[crow * SG + (g & (SG - 1))];
+            uint8_t *stage = smem + OFF_B + s * B_BYTES;
+            const uint8_t *raw = smem + OFF_RAW + rs * RB_BYTES;
+#pragma unroll
+            for (int k = 0; k < CROWS; ++k) {
+                const uint16_t dwb = reinterpret_cast<const uint16_t *>(stile)[crow[k] * SG + (g & (SG - 1))];
                 // d_w * 2^u_r: exact in f32, and in f16 down to 2^-14 (at most 2^12)
-                const uint32_t dh = __half_as_ushort(__float2half_rn(__half2float(__ushort_as_half(dwb)) * wsc));
+                const uint32_t dh =
+                    __half_as_ushort(__float2half_rn(__half2float(__ushort_as_half(dwb)) * wsc[k]));
                 const uint32_t dw = dh | (dh << 16);
-                const uint2 v = *reinterpret_cast<const uint2 *>(smem + OFF_RAW + rs * RB_BYTES + csrc);
-                uint8_t *dst = smem + OFF_B + s * B_BYTES + cdst;
-                uint4 h, l;
-                nib8_split(v.x, dw, h, l);
-                *reinterpret_cast<uint4 *>(dst) = h;
-                *reinterpret_cast<uint4 *>(dst + BPIECE) = l;
-                nib8_split(v.y, dw, h, l);
-                *reinterpret_cast<uint4 *>(dst + 128) = h;
-                *reinterpret_cast<uint4 *>(dst + BPIECE + 128) = l;
+                const uint2 nv = *reinterpret_cast<const uint2 *>(raw + crow[k] * 16 + h * 8);
+                uint8_t *dst = stage + op_off(crow[k], 2 * h);
+                uint4 b1, b2;
+                nib8_split(nv.x, dw, b1, b2);
+                *reinterpret_cast<uint4 *>(dst) = b1;
+                *reinterpret_cast<uint4 *>(dst + BPIECE) = b2;
+                nib8_split(nv.y, dw, b1, b2);
+                *reinterpret_cast<uint4 *>(dst + 128) = b1;
+                *reinterpret_cast<uint4 *>(dst + BPIECE + 128) = b2;
             }
             fence_async_smem();
             __syncwarp();
@@ -557,16 +569,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if ((g & (SG - 1)) == 0) mbar_arrive(bar_srdy + 8 * (cg & (NSR - 1)));
                 if ((g & (SG - 1)) == SG - 1) mbar_arrive(bar_sempty + 8 * sg);
             }
-            // chunk rc ends at block SG*(rc+1) - 1; once S more blocks have been
-            // converted the tensor core has started on that block
-            if (rc < nchunks && g >= SG * (rc + 1) + S) {
-                readout(rc);
-                ++rc;
-            }
-        }
-        while (ok && rc < nchunks) {
-            readout(rc);
-            ++rc;
         }
     }
 
