@@ -24,7 +24,8 @@
 // read-outs.
 //
 // Requires K % 256 == 0 (8-block chunks and scale tiles); other K use the
-// per-block fold in gq_gemm_tc.cu.
+// per-block fold in gq_gemm_tc.cu.  With more than 128 tokens the CTA-pair
+// kernel (k_gemm_pair, one M = 256 MMA per pair of SMs) is used.
 //
 // Kernels:
 //   k_xq_split   writes A1, A2 into the caller's workspace, one 16 KB chunk
@@ -581,22 +582,450 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------- the CTA-pair kernel
+// Same operands and chunking as k_gemm_split, with one M = 256 MMA per CTA
+// pair (cta_group::2): a cluster of two CTAs takes 256-token x 192-row
+// tiles; CTA rank c holds tokens 128c.. of the tile as its half of A (and of
+// D in its tensor memory) and rows 96c.. as its half of B, so each CTA
+// converts 96 rows per block instead of 192 and the tensor core reads half
+// of B from each SM.  Rank 0 issues the MMAs; the peer's converters and
+// read-out warps arrive on rank 0's barriers, and rank 0's commits signal
+// both CTAs.
+namespace pair {
+constexpr int HN = TN / 2;               // rows of B per CTA
+constexpr int BPIECE = HN * KB * 2;      // 6144: one f16 piece of this CTA's B half
+constexpr int B_BYTES = 2 * BPIECE;      // 12288
+constexpr int RB_BYTES = HN * 16;        // 1536: nibbles (TMA box 16 x 96)
+constexpr int STW_BYTES = TN * SG * 2;   // 3072: d_w of all 192 rows (TMA box 8 x 192)
+constexpr int CONV_WARPS = 6;            // one row (16 B of nibbles) per lane, two threads per row
+constexpr int CONV0 = RO_WARPS;
+constexpr int TMA_WARP = RO_WARPS + CONV_WARPS;
+constexpr int MMA_WARP = TMA_WARP + 1;
+constexpr int ACOPY_WARP = TMA_WARP + 2;
+constexpr int NTHREADS = (ACOPY_WARP + 1) * 32;  // 672
+
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + S * A_BYTES;
+constexpr int OFF_RAW = OFF_B + S * B_BYTES;
+constexpr int OFF_STILE = OFF_RAW + RAW * RB_BYTES;
+constexpr int OFF_SR = OFF_STILE + STG * STW_BYTES;
+constexpr int OFF_BAR = OFF_SR + NSR * SR_BYTES;
+constexpr int N_BARS = 4 * S + 2 * RAW + 2 * NACC + 2 * STG + NSR + 1;
+constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
+constexpr int OFF_RELAY = (OFF_MISC + 16 + 15) / 16 * 16;  // S x 16 B: rank 0's landing slots of the relay copies
+constexpr int RELAY_BYTES = 16;
+constexpr int SMEM_BYTES = OFF_RELAY + S * RELAY_BYTES;
+static_assert(OFF_B % 1024 == 0 && OFF_RAW % 1024 == 0 && OFF_STILE % 128 == 0 && OFF_SR % 16 == 0 &&
+                  OFF_BAR % 8 == 0 && SMEM_BYTES <= 232448,
+              "shared memory layout");
+static_assert(CONV_WARPS * 32 == 2 * HN && CONV_WARPS * 32 == TN, "converter threads: 2 per B row, 1 per tile row");
+constexpr uint32_t kIdesc = idesc_f16(2 * TM, TN, false);  // M = 256 over the pair
+
+struct Work {
+    int ntm2, ntiles, nb;  // 256-token tiles, tiles, blocks per row
+};
+__device__ __forceinline__ void tile_origin(const Work &w, int tile, int &t0, int &r0)
+{
+    const int tr = tile / w.ntm2;
+    t0 = (tile - tr * w.ntm2) * 2 * TM;
+    r0 = tr * TN;
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_gemm_pair(const uint8_t *__restrict__ Xh, const __grid_constant__ CUtensorMap mapB,
+                const __grid_constant__ CUtensorMap mapW, const float *__restrict__ tokf, float *__restrict__ Y,
+                int rows, int K, int M, int *__restrict__ status)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_afull = sbase + OFF_BAR, bar_opempty = bar_afull + 8 * S, bar_full = bar_opempty + 8 * S;
+    const uint32_t bar_rfull = bar_full + 8 * S, bar_rempty = bar_rfull + 8 * RAW;
+    const uint32_t bar_cfull = bar_rempty + 8 * RAW, bar_cempty = bar_cfull + 8 * NACC;
+    const uint32_t bar_sfull = bar_cempty + 8 * NACC, bar_sempty = bar_sfull + 8 * STG;
+    const uint32_t bar_srdy = bar_sempty + 8 * STG;
+    const uint32_t bar_drain = bar_srdy + 8 * NSR;
+    const uint32_t bar_pfull = bar_drain + 8;  // rank 1: its converters, relayed to rank 0's full
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+
+    Work w;
+    w.nb = K / KB;
+    w.ntm2 = (M + 2 * TM - 1) / (2 * TM);
+    w.ntiles = w.ntm2 * ((rows + TN - 1) / TN);
+    const int cid = static_cast<int>(blockIdx.x >> 1), ncl = static_cast<int>(gridDim.x >> 1);
+    const int my_tiles = (w.ntiles > cid) ? (w.ntiles - 1 - cid) / ncl + 1 : 0;
+    const int nblocks = my_tiles * w.nb;  // the same in both CTAs of the pair
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(bar_afull + 8 * i, 1);
+            mbar_init(bar_opempty + 8 * i, 1);
+            // rank 0's: its converters, plus RELAY_BYTES of transaction from the peer's relay copy
+            mbar_init(bar_full + 8 * i, CONV_WARPS);
+            mbar_init(bar_pfull + 8 * i, CONV_WARPS);
+        }
+        for (int i = 0; i < RAW; ++i) {
+            mbar_init(bar_rfull + 8 * i, 1);
+            mbar_init(bar_rempty + 8 * i, CONV_WARPS);
+        }
+        for (int i = 0; i < NACC; ++i) {
+            mbar_init(bar_cfull + 8 * i, 1);
+            mbar_init(bar_cempty + 8 * i, 2 * RO_WARPS);  // rank 0's: both CTAs' read-out warps
+        }
+        for (int i = 0; i < STG; ++i) {
+            mbar_init(bar_sfull + 8 * i, 1);
+            mbar_init(bar_sempty + 8 * i, CONV_WARPS);
+        }
+        for (int i = 0; i < NSR; ++i) mbar_init(bar_srdy + 8 * i, CONV_WARPS);
+        mbar_init(bar_drain, 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == MMA_WARP) {  // one warp of each CTA of the pair
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync_all();  // both CTAs' barriers initialized before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();
+
+    if (warp == TMA_WARP) {
+        // ------------------------------------------------ nibble (this CTA's 96 rows) and scale (192 rows) tiles
+        if (lane == 0) {
+            int tile = cid, b = 0, t0, r0;
+            tile_origin(w, tile, t0, r0);
+            int rs = 0, nr = 0, gi = 0;
+            uint32_t rph = 0;
+            for (int gb = 0; gb < nblocks; ++gb) {
+                if ((b & (SG - 1)) == 0) {
+                    const int sg = gi & (STG - 1);
+                    if (!wait_bounded(bar_sempty + 8 * sg, (static_cast<uint32_t>(gi / STG) & 1u) ^ 1u, abort, status))
+                        break;
+                    mbar_expect_tx(bar_sfull + 8 * sg, STW_BYTES);
+                    tma_load_2d(sbase + OFF_STILE + sg * STW_BYTES, &mapW, b, r0, bar_sfull + 8 * sg);
+                    ++gi;
+                }
+                if (!wait_bounded(bar_rempty + 8 * rs, rph ^ 1u, abort, status)) break;
+                mbar_expect_tx(bar_rfull + 8 * rs, RB_BYTES);
+                tma_load_2d(sbase + OFF_RAW + rs * RB_BYTES, &mapB, b * 16, r0 + static_cast<int>(rank) * HN,
+                            bar_rfull + 8 * rs);
+                ++nr;
+                if (++rs == RAW) {
+                    rs = 0;
+                    rph ^= 1u;
+                }
+                if (++b == w.nb) {
+                    b = 0;
+                    tile += ncl;
+                    tile_origin(w, tile, t0, r0);
+                }
+            }
+            volatile int no_abort = 0;
+            for (int g = (nr > RAW ? nr - RAW : 0); g < nr; ++g)
+                wait_bounded(bar_rfull + 8 * (g % RAW), static_cast<uint32_t>((g / RAW) & 1), &no_abort, status);
+            for (int g = (gi > STG ? gi - STG : 0); g < gi; ++g)
+                wait_bounded(bar_sfull + 8 * (g % STG), static_cast<uint32_t>((g / STG) & 1), &no_abort, status);
+        }
+        __syncwarp();
+    } else if (warp == ACOPY_WARP) {
+        // ------------------------------------------------ this CTA's half of A
+        if (lane == 0) {
+            int tile = cid, b = 0, t0, r0;
+            tile_origin(w, tile, t0, r0);
+            int s = 0, na = 0;
+            uint32_t sph = 0;
+            for (int gb = 0; gb < nblocks; ++gb) {
+                if (!wait_bounded<true>(bar_opempty + 8 * s, sph ^ 1u, abort, status)) break;
+                mbar_expect_tx(bar_afull + 8 * s, A_BYTES);
+                const size_t T = static_cast<size_t>(t0 / TM) + rank;  // 128-token tile
+                bulk_load(sbase + OFF_A + s * A_BYTES,
+                          Xh + (T * w.nb + b) * static_cast<size_t>(A_BYTES), A_BYTES, bar_afull + 8 * s);
+                ++na;
+                if (++s == S) {
+                    s = 0;
+                    sph ^= 1u;
+                }
+                if (++b == w.nb) {
+                    b = 0;
+                    tile += ncl;
+                    tile_origin(w, tile, t0, r0);
+                }
+            }
+            volatile int no_abort = 0;
+            for (int g = (na > S ? na - S : 0); g < na; ++g)
+                wait_bounded(bar_afull + 8 * (g % S), static_cast<uint32_t>((g / S) & 1), &no_abort, status);
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        // ------------------------------------------------ MMA issuer (rank 0)
+        if (lane == 0 && rank == 0) {
+            int s = 0;
+            uint32_t sph = 0;
+            for (int gb = 0; gb < nblocks; ++gb) {
+                const int ci = gb / SG, acc = ci & (NACC - 1);
+                const bool cfirst = (gb & (SG - 1)) == 0;
+                if (!wait_bounded(bar_afull + 8 * s, sph, abort, status)) break;
+                if (!wait_bounded<true>(bar_full + 8 * s, sph, abort, status)) break;
+                if (cfirst && !wait_bounded<true>(bar_cempty + 8 * acc, (static_cast<uint32_t>(ci / NACC) & 1u) ^ 1u,
+                                                  abort, status))
+                    break;
+                tc_fence_after();
+                const uint32_t a0 = sbase + OFF_A + s * A_BYTES, b0 = sbase + OFF_B + s * B_BYTES;
+                const uint32_t d = tmem + acc * ACC_STRIDE;
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const uint32_t ka = a0 + ks * 256, kb = b0 + ks * 256;
+                    const uint64_t A1 = smem_desc(ka, 128, 512), A2 = smem_desc(ka + APIECE, 128, 512);
+                    const uint64_t B1 = smem_desc(kb, 128, 512), B2 = smem_desc(kb + BPIECE, 128, 512);
+                    mma_f16_pair(d, A1, B1, kIdesc, (cfirst && ks == 0) ? 0u : 1u);
+                    mma_f16_pair(d, A1, B2, kIdesc, 1u);
+                    mma_f16_pair(d, A2, B1, kIdesc, 1u);
+                }
+                mma_commit_pair(bar_opempty + 8 * s);
+                if ((gb & (SG - 1)) == SG - 1) mma_commit_pair(bar_cfull + 8 * acc);
+                if (++s == S) {
+                    s = 0;
+                    sph ^= 1u;
+                }
+            }
+            // every issued MMA has completed before either CTA releases tensor memory
+            mma_commit_pair(bar_drain);
+        }
+        if (lane == 0 && rank != 0) {
+            // relay: once this CTA's B half (its converters) and A half (its
+            // bulk copy) of a stage are in shared memory, a 16-byte copy into
+            // rank 0's shared memory completes RELAY_BYTES of rank 0's full
+            // barrier for the stage (an async-proxy signal: the thread does not
+            // wait for it to land)
+            const uint32_t full0 = mapa_shared(bar_full, 0);
+            const uint32_t slot0 = mapa_shared(sbase + OFF_RELAY, 0);
+            for (int g = 0; g < nblocks; ++g) {
+                const int s = g & (S - 1);
+                const uint32_t ph = static_cast<uint32_t>(g / S) & 1u;
+                if (!wait_bounded(bar_pfull + 8 * s, ph, abort, status)) break;
+                if (!wait_bounded(bar_afull + 8 * s, ph, abort, status)) break;
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                        slot0 + s * RELAY_BYTES),
+                    "r"(sbase + OFF_RELAY + s * RELAY_BYTES), "r"(RELAY_BYTES), "r"(full0 + 8 * s)
+                    : "memory");
+            }
+            // every relay copy has landed before rank 0's MMAs of its stage were
+            // issued, so the drain wait below also covers them
+        }
+        if (lane == 0) {
+            volatile int no_abort = 0;
+            wait_bounded<true>(bar_drain, 0u, &no_abort, status);
+        }
+        __syncwarp();
+    } else if (warp < RO_WARPS) {
+        // ------------------------------------------------ read-out warps (this CTA's 128 tokens)
+        const int q = warp & 3;
+        const int c0 = (warp >> 2) * EPI_COLS;
+        const uint32_t cempty0 = mapa_shared(bar_cempty, 0);  // rank 0's barrier (for rank 1)
+        bool ok = true;
+        const int cpt = w.nb / SG;
+        const int nchunks = nblocks / SG;
+        float acc[EPI_COLS];
+        auto token_factor = [&](int c) -> float {
+            int t0, r0;
+            tile_origin(w, cid + (c / cpt) * ncl, t0, r0);
+            return __ldg(tokf + static_cast<size_t>(t0 + static_cast<int>(rank) * TM + q * 32 + lane) * cpt + c % cpt);
+        };
+        float ft_next = nchunks > 0 ? token_factor(0) : 1.f;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int ab = c & (NACC - 1);
+            const int ct = c % cpt;
+            const float ft = ft_next;
+            if (c + 1 < nchunks) ft_next = token_factor(c + 1);
+            ok = wait_warp(bar_srdy + 8 * (c & (NSR - 1)), static_cast<uint32_t>(c / NSR) & 1u, abort, status);
+            if (!ok) break;
+            const float *sr = reinterpret_cast<const float *>(smem + OFF_SR + (c & (NSR - 1)) * SR_BYTES) + c0;
+            ok = wait_warp<true>(bar_cfull + 8 * ab, static_cast<uint32_t>(c / NACC) & 1u, abort, status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + ab * ACC_STRIDE + c0;
+#pragma unroll
+            for (int part = 0; part < EPI_COLS / 16; ++part) {
+                float d[16];
+                tmem_ld16(taddr + part * 16, d);
+                if (part == EPI_COLS / 16 - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (rank == 0)
+                            mbar_arrive(bar_cempty + 8 * ab);
+                        else
+                            mbar_arrive_cluster(cempty0 + 8 * ab);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 16; e += 4) {
+                    const float4 f4 = *reinterpret_cast<const float4 *>(sr + part * 16 + e);
+                    const float2 f01 = __fmul2_rn(make_float2(ft, ft), make_float2(f4.x, f4.y));  // exact
+                    const float2 f23 = __fmul2_rn(make_float2(ft, ft), make_float2(f4.z, f4.w));
+                    float2 v01, v23;
+                    if (ct != 0) {
+                        v01 = __ffma2_rn(make_float2(d[e], d[e + 1]), f01,
+                                         make_float2(acc[part * 16 + e], acc[part * 16 + e + 1]));
+                        v23 = __ffma2_rn(make_float2(d[e + 2], d[e + 3]), f23,
+                                         make_float2(acc[part * 16 + e + 2], acc[part * 16 + e + 3]));
+                    } else {
+                        v01 = __fmul2_rn(make_float2(d[e], d[e + 1]), f01);
+                        v23 = __fmul2_rn(make_float2(d[e + 2], d[e + 3]), f23);
+                    }
+                    acc[part * 16 + e] = v01.x;
+                    acc[part * 16 + e + 1] = v01.y;
+                    acc[part * 16 + e + 2] = v23.x;
+                    acc[part * 16 + e + 3] = v23.y;
+                }
+            }
+            if (ct == cpt - 1) {
+                int t0, r0;
+                tile_origin(w, cid + (c / cpt) * ncl, t0, r0);
+                const int t = t0 + static_cast<int>(rank) * TM + q * 32 + lane;
+                if (t < M) {
+                    float *yrow = Y + static_cast<size_t>(t) * rows + r0 + c0;
+                    const int nvalid = rows - (r0 + c0);
+                    const bool vec = (rows & 3) == 0;
+#pragma unroll
+                    for (int cc = 0; cc < EPI_COLS; cc += 4) {
+                        if (vec && cc + 4 <= nvalid) {
+                            *reinterpret_cast<float4 *>(yrow + cc) =
+                                make_float4(acc[cc], acc[cc + 1], acc[cc + 2], acc[cc + 3]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (cc + e < nvalid) yrow[cc + e] = acc[cc + e];
+                        }
+                    }
+                }
+            }
+        }
+    } else if (warp < CONV0 + CONV_WARPS) {
+        // ------------------------------------------------ converter warps (this CTA's 96 rows)
+        // warp v: nibble words 2h, 2h+1 (h = v % 2) of half-tile row 32*(v/2) + lane;
+        // for the read-out, the chunk factor of tile row 32*v + lane
+        const int v = warp - CONV0, h = v & 1;
+        const int crow = 32 * (v >> 1) + lane;                   // row of this CTA's B half
+        const int trow = static_cast<int>(rank) * HN + crow;    // the same row in the tile
+        const int frow = 32 * v + lane;                          // row whose factor this thread writes
+        // rank 0: its own full barrier; rank 1: the local one its relay forwards
+        const uint32_t bar_mine = rank == 0 ? bar_full : bar_pfull;
+        bool ok = true;
+        float wsc = 1.f;
+        for (int g = 0; g < nblocks && ok; ++g) {
+            const int s = g & (S - 1), rs = g & (RAW - 1), sg = (g / SG) & (STG - 1);
+            if (g >= S)
+                ok = wait_warp<true>(bar_opempty + 8 * s, static_cast<uint32_t>(g / S - 1) & 1u, abort, status);
+            if (ok && (g & (SG - 1)) == 0)
+                ok = wait_warp(bar_sfull + 8 * sg, static_cast<uint32_t>(g / (SG * STG)) & 1u, abort, status);
+            if (ok) ok = wait_warp(bar_rfull + 8 * rs, static_cast<uint32_t>(g / RAW) & 1u, abort, status);
+            if (!ok) break;
+            const uint8_t *stile = smem + OFF_STILE + sg * STW_BYTES;
+            const int cg = g / SG;
+            if ((g & (SG - 1)) == 0) {
+                wsc = exp2i(chunk_exp(max8_f16(*reinterpret_cast<const uint4 *>(stile + trow * 16)), kRowExp));
+                const int uf = chunk_exp(max8_f16(*reinterpret_cast<const uint4 *>(stile + frow * 16)), kRowExp);
+                reinterpret_cast<float *>(smem + OFF_SR + (cg & (NSR - 1)) * SR_BYTES)[frow] = exp2i(-uf);
+            }
+            {
+                const uint16_t dwb = reinterpret_cast<const uint16_t *>(stile)[trow * SG + (g & (SG - 1))];
+                // d_w * 2^u_r: exact in f32, and in f16 down to 2^-14 (at most 2^12)
+                const uint32_t dh = __half_as_ushort(__float2half_rn(__half2float(__ushort_as_half(dwb)) * wsc));
+                const uint32_t dw = dh | (dh << 16);
+                const uint2 nv = *reinterpret_cast<const uint2 *>(smem + OFF_RAW + rs * RB_BYTES + crow * 16 + h * 8);
+                uint8_t *dst = smem + OFF_B + s * B_BYTES + op_off(crow, 2 * h);
+                uint4 b1, b2;
+                nib8_split(nv.x, dw, b1, b2);
+                *reinterpret_cast<uint4 *>(dst) = b1;
+                *reinterpret_cast<uint4 *>(dst + BPIECE) = b2;
+                nib8_split(nv.y, dw, b1, b2);
+                *reinterpret_cast<uint4 *>(dst + 128) = b1;
+                *reinterpret_cast<uint4 *>(dst + BPIECE + 128) = b2;
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (rank == 0 && v == 0)
+                    mbar_expect_tx(bar_full + 8 * s, RELAY_BYTES);  // arrive + the peer's relay bytes
+                else
+                    mbar_arrive(bar_mine + 8 * s);
+                mbar_arrive(bar_rempty + 8 * rs);
+                if ((g & (SG - 1)) == 0) mbar_arrive(bar_srdy + 8 * (cg & (NSR - 1)));
+                if ((g & (SG - 1)) == SG - 1) mbar_arrive(bar_sempty + 8 * sg);
+            }
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync_all();  // no remote arrive or MMA operand read is still pending on either CTA
+    pdl_launch_dependents();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+}  // namespace pair
+
 }  // namespace tcs
 
 // ---------------------------------------------------------------- host side
-// Workspace: the A chunks, then the token factors f32 [ntm * 128][K / 256].
+// Workspace: the A chunks, then the token factors f32 [ntm * 128][K / 256],
+// with ntm = the number of 128-token tiles rounded up to even (the pair
+// kernel takes 256 tokens per tile; the pre-pass zero-fills the padding).
+static int split_ntm(int M) { return 2 * ((M + 2 * tcs::TM - 1) / (2 * tcs::TM)); }
 static size_t split_chunks_bytes(int K, int M)
 {
-    return static_cast<size_t>((M + tcs::TM - 1) / tcs::TM) * static_cast<size_t>(K / tcs::KB) * tcs::A_BYTES;
+    return static_cast<size_t>(split_ntm(M)) * static_cast<size_t>(K / tcs::KB) * tcs::A_BYTES;
 }
 size_t gemm_split_workspace_bytes(int K, int M)
 {
     if (!gemm_split_supported(K) || M < 1) return 0;
     return split_chunks_bytes(K, M) +
-           static_cast<size_t>((M + tcs::TM - 1) / tcs::TM) * tcs::TM * static_cast<size_t>(K / (tcs::KB * tcs::SG)) * 4;
+           static_cast<size_t>(split_ntm(M)) * tcs::TM * static_cast<size_t>(K / (tcs::KB * tcs::SG)) * 4;
 }
 
 bool gemm_split_supported(int K) { return K >= 256 && K % 256 == 0; }
+
+// Clusters of two k_gemm_pair CTAs that can be resident at once (0 if none).
+static int pair_clusters()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] != 0) return cache[dev] > 0 ? cache[dev] : 0;
+    if (ctas_per_sm(reinterpret_cast<const void *>(tcs::pair::k_gemm_pair), tcs::pair::NTHREADS,
+                    tcs::pair::SMEM_BYTES) <= 0) {
+        cache[dev] = -1;
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(sm_count()));
+    cfg.blockDim = dim3(tcs::pair::NTHREADS);
+    cfg.dynamicSmemBytes = tcs::pair::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tcs::pair::k_gemm_pair, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        cache[dev] = -1;
+        return 0;
+    }
+    cache[dev] = n;
+    return n;
+}
 
 int launch_gemm_split(const void *W, const int8_t *Xq, const float *dx, float *Y, void *ws, size_t ws_bytes,
                       int rows, int K, int M, cudaStream_t s)
@@ -606,15 +1035,18 @@ int launch_gemm_split(const void *W, const int8_t *Xq, const float *dx, float *Y
     const size_t need = gemm_split_workspace_bytes(K, M);
     if (need == 0) return GQ_ERR_SHAPE;
     if (ws_bytes < need) return GQ_ERR_WORKSPACE;
-    const long long ntiles_ll =
-        static_cast<long long>((M + tcs::TM - 1) / tcs::TM) * ((rows + tcs::TN - 1) / tcs::TN);
+    // two CTAs per tile when there are at least two 128-token tiles
+    const bool use_pair = M > tcs::TM && pair_clusters() > 0;
+    const int tm = use_pair ? 2 * tcs::TM : tcs::TM;
+    const long long ntiles_ll = static_cast<long long>((M + tm - 1) / tm) * ((rows + tcs::TN - 1) / tcs::TN);
     if (ntiles_ll * nb > 0x7FFFFFFFll) return GQ_ERR_SHAPE;  // per-CTA block counts are ints
     const int ntiles = static_cast<int>(ntiles_ll);
     const uint8_t *nib = static_cast<const uint8_t *>(W);
     const uint16_t *dsc = reinterpret_cast<const uint16_t *>(nib + static_cast<size_t>(rows) * nb * 16);
     CUtensorMap mapB, mapW;
     if (!make_map(&mapB, CU_TENSOR_MAP_DATA_TYPE_UINT8, nib, static_cast<uint64_t>(nb) * 16,
-                  static_cast<uint64_t>(rows), static_cast<uint64_t>(nb) * 16, 16, tcs::TN) ||
+                  static_cast<uint64_t>(rows), static_cast<uint64_t>(nb) * 16, 16,
+                  use_pair ? tcs::pair::HN : tcs::TN) ||
         !make_map(&mapW, CU_TENSOR_MAP_DATA_TYPE_UINT16, dsc, static_cast<uint64_t>(nb), static_cast<uint64_t>(rows),
                   static_cast<uint64_t>(nb) * 2, tcs::SG, tcs::TN))
         return GQ_ERR_CUDA;
@@ -630,6 +1062,27 @@ int launch_gemm_split(const void *W, const int8_t *Xq, const float *dx, float *Y
                                     static_cast<uint4 *>(ws), tokf, K, M, npieces));
     if (rc != GQ_OK) return rc;
 
+    if (use_pair) {
+        int ncl = pair_clusters();
+        if (ncl > ntiles) ncl = ntiles;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * static_cast<unsigned>(ncl));
+        cfg.blockDim = dim3(tcs::pair::NTHREADS);
+        cfg.dynamicSmemBytes = tcs::pair::SMEM_BYTES;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        return status_from(cudaLaunchKernelEx(&cfg, tcs::pair::k_gemm_pair, static_cast<const uint8_t *>(ws), mapB,
+                                              mapW, static_cast<const float *>(tokf), Y, rows, K, M,
+                                              status_word()));
+    }
     const int occ = ctas_per_sm(reinterpret_cast<const void *>(tcs::k_gemm_split), tcs::NTHREADS, tcs::SMEM_BYTES);
     if (occ <= 0) return GQ_ERR_CUDA;
     int grid = sm_count();

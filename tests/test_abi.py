@@ -108,8 +108,9 @@ def test_ffn_logits_quant_gemm_pack_validation(lib):
     assert call("gq_quantize_q8_0", A, A, A, 64, 0, None) == gq.GQ_ERR_SHAPE
     gws = gq.gq_q4_0_gemm_workspace_bytes(64, 4)
     assert gws == 8192 * 2  # one 128-token tile x two 32-blocks of f16 codes (K % 256 != 0: per-block fold)
-    # 8 blocks x two f16 operand pieces, then one chunk factor per padded token
-    assert gq.gq_q4_0_gemm_workspace_bytes(256, 4) == 8 * 2 * 8192 + 128 * 4
+    # two 128-token tiles (an even count: 256-token tiles for CTA pairs) x 8 blocks
+    # x two f16 operand pieces, then one chunk factor per padded token
+    assert gq.gq_q4_0_gemm_workspace_bytes(256, 4) == 2 * 8 * 2 * 8192 + 256 * 4
     assert gq.gq_q4_0_gemm_workspace_bytes(48, 4) == 0 and gq.gq_q4_0_gemm_workspace_bytes(64, 0) == 0
     assert call("gq_q4_0_gemm_q8act", A, A, A, None, A, gws, 8, 64, 4, None) == gq.GQ_ERR_NULL
     assert call("gq_q4_0_gemm_q8act", A, A, A, A, None, gws, 8, 64, 4, None) == gq.GQ_ERR_NULL
