@@ -593,9 +593,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // both CTAs.
 namespace pair {
 constexpr int HN = TN / 2;               // rows of B per CTA
+constexpr int PS = 6;                    // operand stages (A half + B half = 28 KB each)
 constexpr int BPIECE = HN * KB * 2;      // 6144: one f16 piece of this CTA's B half
 constexpr int B_BYTES = 2 * BPIECE;      // 12288
-constexpr int RB_BYTES = HN * 16;        // 1536: nibbles (TMA box 16 x 96)
+constexpr int RBP_BYTES = HN * 32;       // 3072: nibbles of two blocks (TMA box 32 x 96)
+constexpr int RAWP = 4;                  // raw stages (block pairs)
 constexpr int STW_BYTES = TN * SG * 2;   // 3072: d_w of all 192 rows (TMA box 8 x 192)
 constexpr int CONV_WARPS = 6;            // one row (16 B of nibbles) per lane, two threads per row
 constexpr int CONV0 = RO_WARPS;
@@ -605,20 +607,21 @@ constexpr int ACOPY_WARP = TMA_WARP + 2;
 constexpr int NTHREADS = (ACOPY_WARP + 1) * 32;  // 672
 
 constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + S * A_BYTES;
-constexpr int OFF_RAW = OFF_B + S * B_BYTES;
-constexpr int OFF_STILE = OFF_RAW + RAW * RB_BYTES;
+constexpr int OFF_B = OFF_A + PS * A_BYTES;
+constexpr int OFF_RAW = OFF_B + PS * B_BYTES;
+constexpr int OFF_STILE = OFF_RAW + RAWP * RBP_BYTES;
 constexpr int OFF_SR = OFF_STILE + STG * STW_BYTES;
 constexpr int OFF_BAR = OFF_SR + NSR * SR_BYTES;
-constexpr int N_BARS = 4 * S + 2 * RAW + 2 * NACC + 2 * STG + NSR + 1;
+constexpr int N_BARS = 3 * PS + 2 * RAWP + 2 * NACC + 2 * STG + NSR + 1;
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
-constexpr int OFF_RELAY = (OFF_MISC + 16 + 15) / 16 * 16;  // S x 16 B: rank 0's landing slots of the relay copies
+constexpr int OFF_RELAY = (OFF_MISC + 16 + 15) / 16 * 16;  // PS x 16 B: rank 0's landing slots of the relay copies
 constexpr int RELAY_BYTES = 16;
-constexpr int SMEM_BYTES = OFF_RELAY + S * RELAY_BYTES;
+constexpr int SMEM_BYTES = OFF_RELAY + PS * RELAY_BYTES;
 static_assert(OFF_B % 1024 == 0 && OFF_RAW % 1024 == 0 && OFF_STILE % 128 == 0 && OFF_SR % 16 == 0 &&
                   OFF_BAR % 8 == 0 && SMEM_BYTES <= 232448,
               "shared memory layout");
 static_assert(CONV_WARPS * 32 == 2 * HN && CONV_WARPS * 32 == TN, "converter threads: 2 per B row, 1 per tile row");
+static_assert(PS % 2 == 0 && SG % 2 == 0, "block pairs never straddle a stage wrap, a chunk or a tile (nb % 8 == 0)");
 constexpr uint32_t kIdesc = idesc_f16(2 * TM, TN, false);  // M = 256 over the pair
 
 struct Work {
@@ -640,13 +643,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_afull = sbase + OFF_BAR, bar_opempty = bar_afull + 8 * S, bar_full = bar_opempty + 8 * S;
-    const uint32_t bar_rfull = bar_full + 8 * S, bar_rempty = bar_rfull + 8 * RAW;
-    const uint32_t bar_cfull = bar_rempty + 8 * RAW, bar_cempty = bar_cfull + 8 * NACC;
+    // full (rank 0): its converters, its A copy and the peer's relay bytes;
+    // pfull (rank 1): its converters and its A copy, forwarded by the relay
+    const uint32_t bar_pfull = sbase + OFF_BAR, bar_opempty = bar_pfull + 8 * PS, bar_full = bar_opempty + 8 * PS;
+    const uint32_t bar_rfull = bar_full + 8 * PS, bar_rempty = bar_rfull + 8 * RAWP;
+    const uint32_t bar_cfull = bar_rempty + 8 * RAWP, bar_cempty = bar_cfull + 8 * NACC;
     const uint32_t bar_sfull = bar_cempty + 8 * NACC, bar_sempty = bar_sfull + 8 * STG;
     const uint32_t bar_srdy = bar_sempty + 8 * STG;
     const uint32_t bar_drain = bar_srdy + 8 * NSR;
-    const uint32_t bar_pfull = bar_drain + 8;  // rank 1: its converters, relayed to rank 0's full
+    const uint32_t bar_mine = rank == 0 ? bar_full : bar_pfull;  // where this CTA's stage producers arrive
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
@@ -659,14 +664,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int nblocks = my_tiles * w.nb;  // the same in both CTAs of the pair
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < S; ++i) {
-            mbar_init(bar_afull + 8 * i, 1);
+        for (int i = 0; i < PS; ++i) {
             mbar_init(bar_opempty + 8 * i, 1);
-            // rank 0's: its converters, plus RELAY_BYTES of transaction from the peer's relay copy
-            mbar_init(bar_full + 8 * i, CONV_WARPS);
-            mbar_init(bar_pfull + 8 * i, CONV_WARPS);
+            // converters + the A copy's arrival (with its bytes); rank 0's full
+            // also expects RELAY_BYTES from the peer's relay copy
+            mbar_init(bar_full + 8 * i, CONV_WARPS + 1);
+            mbar_init(bar_pfull + 8 * i, CONV_WARPS + 1);
         }
-        for (int i = 0; i < RAW; ++i) {
+        for (int i = 0; i < RAWP; ++i) {
             mbar_init(bar_rfull + 8 * i, 1);
             mbar_init(bar_rempty + 8 * i, CONV_WARPS);
         }
@@ -702,7 +707,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tile_origin(w, tile, t0, r0);
             int rs = 0, nr = 0, gi = 0;
             uint32_t rph = 0;
-            for (int gb = 0; gb < nblocks; ++gb) {
+            for (int gb = 0; gb < nblocks; gb += 2) {
                 if ((b & (SG - 1)) == 0) {
                     const int sg = gi & (STG - 1);
                     if (!wait_bounded(bar_sempty + 8 * sg, (static_cast<uint32_t>(gi / STG) & 1u) ^ 1u, abort, status))
@@ -712,23 +717,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     ++gi;
                 }
                 if (!wait_bounded(bar_rempty + 8 * rs, rph ^ 1u, abort, status)) break;
-                mbar_expect_tx(bar_rfull + 8 * rs, RB_BYTES);
-                tma_load_2d(sbase + OFF_RAW + rs * RB_BYTES, &mapB, b * 16, r0 + static_cast<int>(rank) * HN,
+                mbar_expect_tx(bar_rfull + 8 * rs, RBP_BYTES);
+                tma_load_2d(sbase + OFF_RAW + rs * RBP_BYTES, &mapB, b * 16, r0 + static_cast<int>(rank) * HN,
                             bar_rfull + 8 * rs);
                 ++nr;
-                if (++rs == RAW) {
+                if (++rs == RAWP) {
                     rs = 0;
                     rph ^= 1u;
                 }
-                if (++b == w.nb) {
+                b += 2;
+                if (b == w.nb) {
                     b = 0;
                     tile += ncl;
                     tile_origin(w, tile, t0, r0);
                 }
             }
             volatile int no_abort = 0;
-            for (int g = (nr > RAW ? nr - RAW : 0); g < nr; ++g)
-                wait_bounded(bar_rfull + 8 * (g % RAW), static_cast<uint32_t>((g / RAW) & 1), &no_abort, status);
+            for (int g = (nr > RAWP ? nr - RAWP : 0); g < nr; ++g)
+                wait_bounded(bar_rfull + 8 * (g % RAWP), static_cast<uint32_t>((g / RAWP) & 1), &no_abort, status);
             for (int g = (gi > STG ? gi - STG : 0); g < gi; ++g)
                 wait_bounded(bar_sfull + 8 * (g % STG), static_cast<uint32_t>((g / STG) & 1), &no_abort, status);
         }
@@ -742,12 +748,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             uint32_t sph = 0;
             for (int gb = 0; gb < nblocks; ++gb) {
                 if (!wait_bounded<true>(bar_opempty + 8 * s, sph ^ 1u, abort, status)) break;
-                mbar_expect_tx(bar_afull + 8 * s, A_BYTES);
+                mbar_expect_tx(bar_mine + 8 * s, A_BYTES);
                 const size_t T = static_cast<size_t>(t0 / TM) + rank;  // 128-token tile
                 bulk_load(sbase + OFF_A + s * A_BYTES,
-                          Xh + (T * w.nb + b) * static_cast<size_t>(A_BYTES), A_BYTES, bar_afull + 8 * s);
+                          Xh + (T * w.nb + b) * static_cast<size_t>(A_BYTES), A_BYTES, bar_mine + 8 * s);
                 ++na;
-                if (++s == S) {
+                if (++s == PS) {
                     s = 0;
                     sph ^= 1u;
                 }
@@ -757,9 +763,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tile_origin(w, tile, t0, r0);
                 }
             }
+            // no copy may still be landing when the CTA exits (after an abort the
+            // stage's other arrivals may be missing: the waits then time out)
             volatile int no_abort = 0;
-            for (int g = (na > S ? na - S : 0); g < na; ++g)
-                wait_bounded(bar_afull + 8 * (g % S), static_cast<uint32_t>((g / S) & 1), &no_abort, status);
+            for (int g = (na > PS ? na - PS : 0); g < na; ++g)
+                wait_bounded<true>(bar_mine + 8 * (g % PS), static_cast<uint32_t>((g / PS) & 1), &no_abort, status);
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
@@ -770,7 +778,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int gb = 0; gb < nblocks; ++gb) {
                 const int ci = gb / SG, acc = ci & (NACC - 1);
                 const bool cfirst = (gb & (SG - 1)) == 0;
-                if (!wait_bounded(bar_afull + 8 * s, sph, abort, status)) break;
                 if (!wait_bounded<true>(bar_full + 8 * s, sph, abort, status)) break;
                 if (cfirst && !wait_bounded<true>(bar_cempty + 8 * acc, (static_cast<uint32_t>(ci / NACC) & 1u) ^ 1u,
                                                   abort, status))
@@ -789,7 +796,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 mma_commit_pair(bar_opempty + 8 * s);
                 if ((gb & (SG - 1)) == SG - 1) mma_commit_pair(bar_cfull + 8 * acc);
-                if (++s == S) {
+                if (++s == PS) {
                     s = 0;
                     sph ^= 1u;
                 }
@@ -806,10 +813,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint32_t full0 = mapa_shared(bar_full, 0);
             const uint32_t slot0 = mapa_shared(sbase + OFF_RELAY, 0);
             for (int g = 0; g < nblocks; ++g) {
-                const int s = g & (S - 1);
-                const uint32_t ph = static_cast<uint32_t>(g / S) & 1u;
+                const int s = g % PS;
+                const uint32_t ph = static_cast<uint32_t>(g / PS) & 1u;
                 if (!wait_bounded(bar_pfull + 8 * s, ph, abort, status)) break;
-                if (!wait_bounded(bar_afull + 8 * s, ph, abort, status)) break;
                 asm volatile(
                     "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                         slot0 + s * RELAY_BYTES),
@@ -916,17 +922,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int crow = 32 * (v >> 1) + lane;                   // row of this CTA's B half
         const int trow = static_cast<int>(rank) * HN + crow;    // the same row in the tile
         const int frow = 32 * v + lane;                          // row whose factor this thread writes
-        // rank 0: its own full barrier; rank 1: the local one its relay forwards
-        const uint32_t bar_mine = rank == 0 ? bar_full : bar_pfull;
         bool ok = true;
         float wsc = 1.f;
-        for (int g = 0; g < nblocks && ok; ++g) {
-            const int s = g & (S - 1), rs = g & (RAW - 1), sg = (g / SG) & (STG - 1);
-            if (g >= S)
-                ok = wait_warp<true>(bar_opempty + 8 * s, static_cast<uint32_t>(g / S - 1) & 1u, abort, status);
+        for (int g = 0; g < nblocks && ok; g += 2) {  // blocks g, g + 1: stages s, s + 1
+            const int s = g % PS, rs = (g >> 1) & (RAWP - 1), sg = (g / SG) & (STG - 1);
+            if (g >= PS) {
+                ok = wait_warp<true>(bar_opempty + 8 * s, static_cast<uint32_t>(g / PS - 1) & 1u, abort, status);
+                if (ok)
+                    ok = wait_warp<true>(bar_opempty + 8 * (s + 1), static_cast<uint32_t>(g / PS - 1) & 1u, abort,
+                                         status);
+            }
             if (ok && (g & (SG - 1)) == 0)
                 ok = wait_warp(bar_sfull + 8 * sg, static_cast<uint32_t>(g / (SG * STG)) & 1u, abort, status);
-            if (ok) ok = wait_warp(bar_rfull + 8 * rs, static_cast<uint32_t>(g / RAW) & 1u, abort, status);
+            if (ok) ok = wait_warp(bar_rfull + 8 * rs, static_cast<uint32_t>((g >> 1) / RAWP) & 1u, abort, status);
             if (!ok) break;
             const uint8_t *stile = smem + OFF_STILE + sg * STW_BYTES;
             const int cg = g / SG;
@@ -935,31 +943,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int uf = chunk_exp(max8_f16(*reinterpret_cast<const uint4 *>(stile + frow * 16)), kRowExp);
                 reinterpret_cast<float *>(smem + OFF_SR + (cg & (NSR - 1)) * SR_BYTES)[frow] = exp2i(-uf);
             }
-            {
-                const uint16_t dwb = reinterpret_cast<const uint16_t *>(stile)[trow * SG + (g & (SG - 1))];
-                // d_w * 2^u_r: exact in f32, and in f16 down to 2^-14 (at most 2^12)
-                const uint32_t dh = __half_as_ushort(__float2half_rn(__half2float(__ushort_as_half(dwb)) * wsc));
-                const uint32_t dw = dh | (dh << 16);
-                const uint2 nv = *reinterpret_cast<const uint2 *>(smem + OFF_RAW + rs * RB_BYTES + crow * 16 + h * 8);
-                uint8_t *dst = smem + OFF_B + s * B_BYTES + op_off(crow, 2 * h);
-                uint4 b1, b2;
-                nib8_split(nv.x, dw, b1, b2);
-                *reinterpret_cast<uint4 *>(dst) = b1;
-                *reinterpret_cast<uint4 *>(dst + BPIECE) = b2;
-                nib8_split(nv.y, dw, b1, b2);
-                *reinterpret_cast<uint4 *>(dst + 128) = b1;
-                *reinterpret_cast<uint4 *>(dst + BPIECE + 128) = b2;
-            }
+            // d_w * 2^u_r of both blocks: exact in f32, and in f16 down to 2^-14 (at most 2^12)
+            const uint32_t dwp = *reinterpret_cast<const uint32_t *>(stile + trow * 16 + (g & (SG - 1)) * 2);
+            const uint32_t dh0 = __half_as_ushort(
+                __float2half_rn(__half2float(__ushort_as_half(static_cast<uint16_t>(dwp & 0xFFFFu))) * wsc));
+            const uint32_t dh1 =
+                __half_as_ushort(__float2half_rn(__half2float(__ushort_as_half(static_cast<uint16_t>(dwp >> 16))) * wsc));
+            const uint8_t *raw = smem + OFF_RAW + rs * RBP_BYTES + crow * 32 + h * 8;
+            const uint2 n0 = *reinterpret_cast<const uint2 *>(raw);
+            const uint2 n1 = *reinterpret_cast<const uint2 *>(raw + 16);
+            uint8_t *dst0 = smem + OFF_B + s * B_BYTES + op_off(crow, 2 * h);
+            uint8_t *dst1 = dst0 + B_BYTES;
+            uint4 b1, b2, c1, c2;
+            nib8_split(n0.x, dh0 | (dh0 << 16), b1, b2);
+            nib8_split(n1.x, dh1 | (dh1 << 16), c1, c2);
+            *reinterpret_cast<uint4 *>(dst0) = b1;
+            *reinterpret_cast<uint4 *>(dst0 + BPIECE) = b2;
+            *reinterpret_cast<uint4 *>(dst1) = c1;
+            *reinterpret_cast<uint4 *>(dst1 + BPIECE) = c2;
+            nib8_split(n0.y, dh0 | (dh0 << 16), b1, b2);
+            nib8_split(n1.y, dh1 | (dh1 << 16), c1, c2);
+            *reinterpret_cast<uint4 *>(dst0 + 128) = b1;
+            *reinterpret_cast<uint4 *>(dst0 + BPIECE + 128) = b2;
+            *reinterpret_cast<uint4 *>(dst1 + 128) = c1;
+            *reinterpret_cast<uint4 *>(dst1 + BPIECE + 128) = c2;
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-                if (rank == 0 && v == 0)
+                if (rank == 0 && v == 0) {
                     mbar_expect_tx(bar_full + 8 * s, RELAY_BYTES);  // arrive + the peer's relay bytes
-                else
+                    mbar_expect_tx(bar_full + 8 * (s + 1), RELAY_BYTES);
+                } else {
                     mbar_arrive(bar_mine + 8 * s);
+                    mbar_arrive(bar_mine + 8 * (s + 1));
+                }
                 mbar_arrive(bar_rempty + 8 * rs);
                 if ((g & (SG - 1)) == 0) mbar_arrive(bar_srdy + 8 * (cg & (NSR - 1)));
-                if ((g & (SG - 1)) == SG - 1) mbar_arrive(bar_sempty + 8 * sg);
+                if ((g & (SG - 1)) == SG - 2) mbar_arrive(bar_sempty + 8 * sg);
             }
         }
     }
@@ -1045,7 +1065,7 @@ int launch_gemm_split(const void *W, const int8_t *Xq, const float *dx, float *Y
     const uint16_t *dsc = reinterpret_cast<const uint16_t *>(nib + static_cast<size_t>(rows) * nb * 16);
     CUtensorMap mapB, mapW;
     if (!make_map(&mapB, CU_TENSOR_MAP_DATA_TYPE_UINT8, nib, static_cast<uint64_t>(nb) * 16,
-                  static_cast<uint64_t>(rows), static_cast<uint64_t>(nb) * 16, 16,
+                  static_cast<uint64_t>(rows), static_cast<uint64_t>(nb) * 16, use_pair ? 32 : 16,
                   use_pair ? tcs::pair::HN : tcs::TN) ||
         !make_map(&mapW, CU_TENSOR_MAP_DATA_TYPE_UINT16, dsc, static_cast<uint64_t>(nb), static_cast<uint64_t>(rows),
                   static_cast<uint64_t>(nb) * 2, tcs::SG, tcs::TN))
