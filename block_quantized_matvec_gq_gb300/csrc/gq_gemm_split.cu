@@ -594,6 +594,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 namespace pair {
 constexpr int HN = TN / 2;               // rows of B per CTA
 constexpr int PS = 6;                    // operand stages (A half + B half = 28 KB each)
+constexpr int PS2 = PS / 2;              // pair stages: one barrier phase per two blocks
 constexpr int BPIECE = HN * KB * 2;      // 6144: one f16 piece of this CTA's B half
 constexpr int B_BYTES = 2 * BPIECE;      // 12288
 constexpr int RBP_BYTES = HN * 32;       // 3072: nibbles of two blocks (TMA box 32 x 96)
@@ -612,11 +613,11 @@ constexpr int OFF_RAW = OFF_B + PS * B_BYTES;
 constexpr int OFF_STILE = OFF_RAW + RAWP * RBP_BYTES;
 constexpr int OFF_SR = OFF_STILE + STG * STW_BYTES;
 constexpr int OFF_BAR = OFF_SR + NSR * SR_BYTES;
-constexpr int N_BARS = 3 * PS + 2 * RAWP + 2 * NACC + 2 * STG + NSR + 1;
+constexpr int N_BARS = 3 * PS2 + 2 * RAWP + 2 * NACC + 2 * STG + NSR + 1;
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
-constexpr int OFF_RELAY = (OFF_MISC + 16 + 15) / 16 * 16;  // PS x 16 B: rank 0's landing slots of the relay copies
+constexpr int OFF_RELAY = (OFF_MISC + 16 + 15) / 16 * 16;  // PS2 x 16 B: rank 0's landing slots of the relay copies
 constexpr int RELAY_BYTES = 16;
-constexpr int SMEM_BYTES = OFF_RELAY + PS * RELAY_BYTES;
+constexpr int SMEM_BYTES = OFF_RELAY + PS2 * RELAY_BYTES;
 static_assert(OFF_B % 1024 == 0 && OFF_RAW % 1024 == 0 && OFF_STILE % 128 == 0 && OFF_SR % 16 == 0 &&
                   OFF_BAR % 8 == 0 && SMEM_BYTES <= 232448,
               "shared memory layout");
@@ -645,8 +646,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t sbase = smem_u32(smem);
     // full (rank 0): its converters, its A copy and the peer's relay bytes;
     // pfull (rank 1): its converters and its A copy, forwarded by the relay
-    const uint32_t bar_pfull = sbase + OFF_BAR, bar_opempty = bar_pfull + 8 * PS, bar_full = bar_opempty + 8 * PS;
-    const uint32_t bar_rfull = bar_full + 8 * PS, bar_rempty = bar_rfull + 8 * RAWP;
+    // (per pair stage: blocks 2p and 2p + 1 of the CTA's sequence, p = pair index)
+    const uint32_t bar_pfull = sbase + OFF_BAR, bar_opempty = bar_pfull + 8 * PS2, bar_full = bar_opempty + 8 * PS2;
+    const uint32_t bar_rfull = bar_full + 8 * PS2, bar_rempty = bar_rfull + 8 * RAWP;
     const uint32_t bar_cfull = bar_rempty + 8 * RAWP, bar_cempty = bar_cfull + 8 * NACC;
     const uint32_t bar_sfull = bar_cempty + 8 * NACC, bar_sempty = bar_sfull + 8 * STG;
     const uint32_t bar_srdy = bar_sempty + 8 * STG;
@@ -664,7 +666,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int nblocks = my_tiles * w.nb;  // the same in both CTAs of the pair
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < PS; ++i) {
+        for (int i = 0; i < PS2; ++i) {
             mbar_init(bar_opempty + 8 * i, 1);
             // converters + the A copy's arrival (with its bytes); rank 0's full
             // also expects RELAY_BYTES from the peer's relay copy
@@ -744,20 +746,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) {
             int tile = cid, b = 0, t0, r0;
             tile_origin(w, tile, t0, r0);
-            int s = 0, na = 0;
+            int sp = 0, na = 0;
             uint32_t sph = 0;
-            for (int gb = 0; gb < nblocks; ++gb) {
-                if (!wait_bounded<true>(bar_opempty + 8 * s, sph ^ 1u, abort, status)) break;
-                mbar_expect_tx(bar_mine + 8 * s, A_BYTES);
+            for (int gb = 0; gb < nblocks; gb += 2) {
+                if (!wait_bounded<true>(bar_opempty + 8 * sp, sph ^ 1u, abort, status)) break;
+                mbar_expect_tx(bar_mine + 8 * sp, 2 * A_BYTES);
                 const size_t T = static_cast<size_t>(t0 / TM) + rank;  // 128-token tile
-                bulk_load(sbase + OFF_A + s * A_BYTES,
-                          Xh + (T * w.nb + b) * static_cast<size_t>(A_BYTES), A_BYTES, bar_mine + 8 * s);
+                const uint8_t *src = Xh + (T * w.nb + b) * static_cast<size_t>(A_BYTES);  // blocks b, b + 1
+                bulk_load(sbase + OFF_A + 2 * sp * A_BYTES, src, A_BYTES, bar_mine + 8 * sp);
+                bulk_load(sbase + OFF_A + (2 * sp + 1) * A_BYTES, src + A_BYTES, A_BYTES, bar_mine + 8 * sp);
                 ++na;
-                if (++s == PS) {
-                    s = 0;
+                if (++sp == PS2) {
+                    sp = 0;
                     sph ^= 1u;
                 }
-                if (++b == w.nb) {
+                b += 2;
+                if (b == w.nb) {
                     b = 0;
                     tile += ncl;
                     tile_origin(w, tile, t0, r0);
@@ -766,38 +770,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // no copy may still be landing when the CTA exits (after an abort the
             // stage's other arrivals may be missing: the waits then time out)
             volatile int no_abort = 0;
-            for (int g = (na > PS ? na - PS : 0); g < na; ++g)
-                wait_bounded<true>(bar_mine + 8 * (g % PS), static_cast<uint32_t>((g / PS) & 1), &no_abort, status);
+            for (int g = (na > PS2 ? na - PS2 : 0); g < na; ++g)
+                wait_bounded<true>(bar_mine + 8 * (g % PS2), static_cast<uint32_t>((g / PS2) & 1), &no_abort, status);
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------ MMA issuer (rank 0)
         if (lane == 0 && rank == 0) {
-            int s = 0;
+            int sp = 0;
             uint32_t sph = 0;
-            for (int gb = 0; gb < nblocks; ++gb) {
+            for (int gb = 0; gb < nblocks; gb += 2) {
                 const int ci = gb / SG, acc = ci & (NACC - 1);
                 const bool cfirst = (gb & (SG - 1)) == 0;
-                if (!wait_bounded<true>(bar_full + 8 * s, sph, abort, status)) break;
+                if (!wait_bounded<true>(bar_full + 8 * sp, sph, abort, status)) break;
                 if (cfirst && !wait_bounded<true>(bar_cempty + 8 * acc, (static_cast<uint32_t>(ci / NACC) & 1u) ^ 1u,
                                                   abort, status))
                     break;
                 tc_fence_after();
-                const uint32_t a0 = sbase + OFF_A + s * A_BYTES, b0 = sbase + OFF_B + s * B_BYTES;
                 const uint32_t d = tmem + acc * ACC_STRIDE;
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-                    const uint32_t ka = a0 + ks * 256, kb = b0 + ks * 256;
-                    const uint64_t A1 = smem_desc(ka, 128, 512), A2 = smem_desc(ka + APIECE, 128, 512);
-                    const uint64_t B1 = smem_desc(kb, 128, 512), B2 = smem_desc(kb + BPIECE, 128, 512);
-                    mma_f16_pair(d, A1, B1, kIdesc, (cfirst && ks == 0) ? 0u : 1u);
-                    mma_f16_pair(d, A1, B2, kIdesc, 1u);
-                    mma_f16_pair(d, A2, B1, kIdesc, 1u);
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t a0 = sbase + OFF_A + (2 * sp + j) * A_BYTES, b0 = sbase + OFF_B + (2 * sp + j) * B_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const uint32_t ka = a0 + ks * 256, kb = b0 + ks * 256;
+                        const uint64_t A1 = smem_desc(ka, 128, 512), A2 = smem_desc(ka + APIECE, 128, 512);
+                        const uint64_t B1 = smem_desc(kb, 128, 512), B2 = smem_desc(kb + BPIECE, 128, 512);
+                        mma_f16_pair(d, A1, B1, kIdesc, (cfirst && j == 0 && ks == 0) ? 0u : 1u);
+                        mma_f16_pair(d, A1, B2, kIdesc, 1u);
+                        mma_f16_pair(d, A2, B1, kIdesc, 1u);
+                    }
                 }
-                mma_commit_pair(bar_opempty + 8 * s);
-                if ((gb & (SG - 1)) == SG - 1) mma_commit_pair(bar_cfull + 8 * acc);
-                if (++s == PS) {
-                    s = 0;
+                mma_commit_pair(bar_opempty + 8 * sp);
+                if ((gb & (SG - 1)) == SG - 2) mma_commit_pair(bar_cfull + 8 * acc);
+                if (++sp == PS2) {
+                    sp = 0;
                     sph ^= 1u;
                 }
             }
@@ -812,14 +819,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // wait for it to land)
             const uint32_t full0 = mapa_shared(bar_full, 0);
             const uint32_t slot0 = mapa_shared(sbase + OFF_RELAY, 0);
-            for (int g = 0; g < nblocks; ++g) {
-                const int s = g % PS;
-                const uint32_t ph = static_cast<uint32_t>(g / PS) & 1u;
-                if (!wait_bounded(bar_pfull + 8 * s, ph, abort, status)) break;
+            for (int p = 0; p < nblocks / 2; ++p) {
+                const int sp = p % PS2;
+                const uint32_t ph = static_cast<uint32_t>(p / PS2) & 1u;
+                if (!wait_bounded(bar_pfull + 8 * sp, ph, abort, status)) break;
                 asm volatile(
                     "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                        slot0 + s * RELAY_BYTES),
-                    "r"(sbase + OFF_RELAY + s * RELAY_BYTES), "r"(RELAY_BYTES), "r"(full0 + 8 * s)
+                        slot0 + sp * RELAY_BYTES),
+                    "r"(sbase + OFF_RELAY + sp * RELAY_BYTES), "r"(RELAY_BYTES), "r"(full0 + 8 * sp)
                     : "memory");
             }
             // every relay copy has landed before rank 0's MMAs of its stage were
@@ -925,16 +932,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         bool ok = true;
         float wsc = 1.f;
         for (int g = 0; g < nblocks && ok; g += 2) {  // blocks g, g + 1: stages s, s + 1
-            const int s = g % PS, rs = (g >> 1) & (RAWP - 1), sg = (g / SG) & (STG - 1);
-            if (g >= PS) {
-                ok = wait_warp<true>(bar_opempty + 8 * s, static_cast<uint32_t>(g / PS - 1) & 1u, abort, status);
-                if (ok)
-                    ok = wait_warp<true>(bar_opempty + 8 * (s + 1), static_cast<uint32_t>(g / PS - 1) & 1u, abort,
-                                         status);
-            }
+            const int p = g >> 1, sp = p % PS2, s = 2 * sp, rs = p & (RAWP - 1), sg = (g / SG) & (STG - 1);
+            if (p >= PS2)
+                ok = wait_warp<true>(bar_opempty + 8 * sp, static_cast<uint32_t>(p / PS2 - 1) & 1u, abort, status);
             if (ok && (g & (SG - 1)) == 0)
                 ok = wait_warp(bar_sfull + 8 * sg, static_cast<uint32_t>(g / (SG * STG)) & 1u, abort, status);
-            if (ok) ok = wait_warp(bar_rfull + 8 * rs, static_cast<uint32_t>((g >> 1) / RAWP) & 1u, abort, status);
+            if (ok) ok = wait_warp(bar_rfull + 8 * rs, static_cast<uint32_t>(p / RAWP) & 1u, abort, status);
             if (!ok) break;
             const uint8_t *stile = smem + OFF_STILE + sg * STW_BYTES;
             const int cg = g / SG;
@@ -970,13 +973,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-                if (rank == 0 && v == 0) {
-                    mbar_expect_tx(bar_full + 8 * s, RELAY_BYTES);  // arrive + the peer's relay bytes
-                    mbar_expect_tx(bar_full + 8 * (s + 1), RELAY_BYTES);
-                } else {
-                    mbar_arrive(bar_mine + 8 * s);
-                    mbar_arrive(bar_mine + 8 * (s + 1));
-                }
+                if (rank == 0 && v == 0)
+                    mbar_expect_tx(bar_full + 8 * sp, RELAY_BYTES);  // arrive + the peer's relay bytes
+                else
+                    mbar_arrive(bar_mine + 8 * sp);
                 mbar_arrive(bar_rempty + 8 * rs);
                 if ((g & (SG - 1)) == 0) mbar_arrive(bar_srdy + 8 * (cg & (NSR - 1)));
                 if ((g & (SG - 1)) == SG - 2) mbar_arrive(bar_sempty + 8 * sg);
