@@ -600,7 +600,7 @@ constexpr int B_BYTES = 2 * BPIECE;      // 12288
 constexpr int RBP_BYTES = HN * 32;       // 3072: nibbles of two blocks (TMA box 32 x 96)
 constexpr int RAWP = 4;                  // raw stages (block pairs)
 constexpr int STW_BYTES = TN * SG * 2;   // 3072: d_w of all 192 rows (TMA box 8 x 192)
-constexpr int CONV_WARPS = 6;            // one row (16 B of nibbles) per lane, two threads per row
+constexpr int CONV_WARPS = 6;            // one row of one block (16 B of nibbles) per lane per block pair
 constexpr int CONV0 = RO_WARPS;
 constexpr int TMA_WARP = RO_WARPS + CONV_WARPS;
 constexpr int MMA_WARP = TMA_WARP + 1;
@@ -621,7 +621,7 @@ constexpr int SMEM_BYTES = OFF_RELAY + PS2 * RELAY_BYTES;
 static_assert(OFF_B % 1024 == 0 && OFF_RAW % 1024 == 0 && OFF_STILE % 128 == 0 && OFF_SR % 16 == 0 &&
                   OFF_BAR % 8 == 0 && SMEM_BYTES <= 232448,
               "shared memory layout");
-static_assert(CONV_WARPS * 32 == 2 * HN && CONV_WARPS * 32 == TN, "converter threads: 2 per B row, 1 per tile row");
+static_assert(CONV_WARPS * 32 == 2 * HN && CONV_WARPS * 32 == TN, "converter threads: 2 per B row (one per block of a pair), 1 per tile row");
 static_assert(PS % 2 == 0 && SG % 2 == 0, "block pairs never straddle a stage wrap, a chunk or a tile (nb % 8 == 0)");
 constexpr uint32_t kIdesc = idesc_f16(2 * TM, TN, false);  // M = 256 over the pair
 
@@ -923,8 +923,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     } else if (warp < CONV0 + CONV_WARPS) {
         // ------------------------------------------------ converter warps (this CTA's 96 rows)
-        // warp v: nibble words 2h, 2h+1 (h = v % 2) of half-tile row 32*(v/2) + lane;
-        // for the read-out, the chunk factor of tile row 32*v + lane
+        // warp v: all four nibble words of half-tile row 32*(v/2) + lane in block
+        // g + h (h = v % 2) of each pair g, g + 1; for the read-out, the chunk
+        // factor of tile row 32*v + lane
         const int v = warp - CONV0, h = v & 1;
         const int crow = 32 * (v >> 1) + lane;                   // row of this CTA's B half
         const int trow = static_cast<int>(rank) * HN + crow;    // the same row in the tile
@@ -946,30 +947,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int uf = chunk_exp(max8_f16(*reinterpret_cast<const uint4 *>(stile + frow * 16)), kRowExp);
                 reinterpret_cast<float *>(smem + OFF_SR + (cg & (NSR - 1)) * SR_BYTES)[frow] = exp2i(-uf);
             }
-            // d_w * 2^u_r of both blocks: exact in f32, and in f16 down to 2^-14 (at most 2^12)
-            const uint32_t dwp = *reinterpret_cast<const uint32_t *>(stile + trow * 16 + (g & (SG - 1)) * 2);
-            const uint32_t dh0 = __half_as_ushort(
-                __float2half_rn(__half2float(__ushort_as_half(static_cast<uint16_t>(dwp & 0xFFFFu))) * wsc));
-            const uint32_t dh1 =
-                __half_as_ushort(__float2half_rn(__half2float(__ushort_as_half(static_cast<uint16_t>(dwp >> 16))) * wsc));
-            const uint8_t *raw = smem + OFF_RAW + rs * RBP_BYTES + crow * 32 + h * 8;
-            const uint2 n0 = *reinterpret_cast<const uint2 *>(raw);
-            const uint2 n1 = *reinterpret_cast<const uint2 *>(raw + 16);
-            uint8_t *dst0 = smem + OFF_B + s * B_BYTES + op_off(crow, 2 * h);
-            uint8_t *dst1 = dst0 + B_BYTES;
-            uint4 b1, b2, c1, c2;
-            nib8_split(n0.x, dh0 | (dh0 << 16), b1, b2);
-            nib8_split(n1.x, dh1 | (dh1 << 16), c1, c2);
-            *reinterpret_cast<uint4 *>(dst0) = b1;
-            *reinterpret_cast<uint4 *>(dst0 + BPIECE) = b2;
-            *reinterpret_cast<uint4 *>(dst1) = c1;
-            *reinterpret_cast<uint4 *>(dst1 + BPIECE) = c2;
-            nib8_split(n0.y, dh0 | (dh0 << 16), b1, b2);
-            nib8_split(n1.y, dh1 | (dh1 << 16), c1, c2);
-            *reinterpret_cast<uint4 *>(dst0 + 128) = b1;
-            *reinterpret_cast<uint4 *>(dst0 + BPIECE + 128) = b2;
-            *reinterpret_cast<uint4 *>(dst1 + 128) = c1;
-            *reinterpret_cast<uint4 *>(dst1 + BPIECE + 128) = c2;
+            // d_w * 2^u_r of block g + h: exact in f32, and in f16 down to 2^-14 (at most 2^12)
+            const uint16_t dwb = reinterpret_cast<const uint16_t *>(stile)[trow * SG + (g & (SG - 1)) + h];
+            const uint32_t dh = __half_as_ushort(__float2half_rn(__half2float(__ushort_as_half(dwb)) * wsc));
+            const uint32_t dw = dh | (dh << 16);
+            const uint4 nv = *reinterpret_cast<const uint4 *>(smem + OFF_RAW + rs * RBP_BYTES + crow * 32 + h * 16);
+            uint8_t *dst = smem + OFF_B + (s + h) * B_BYTES + op_off(crow, 0);
+            uint4 b1, b2;
+            nib8_split(nv.x, dw, b1, b2);
+            *reinterpret_cast<uint4 *>(dst) = b1;
+            *reinterpret_cast<uint4 *>(dst + BPIECE) = b2;
+            nib8_split(nv.y, dw, b1, b2);
+            *reinterpret_cast<uint4 *>(dst + 128) = b1;
+            *reinterpret_cast<uint4 *>(dst + BPIECE + 128) = b2;
+            nib8_split(nv.z, dw, b1, b2);
+            *reinterpret_cast<uint4 *>(dst + 256) = b1;
+            *reinterpret_cast<uint4 *>(dst + BPIECE + 256) = b2;
+            nib8_split(nv.w, dw, b1, b2);
+            *reinterpret_cast<uint4 *>(dst + 384) = b1;
+            *reinterpret_cast<uint4 *>(dst + BPIECE + 384) = b2;
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
