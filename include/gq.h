@@ -188,10 +188,13 @@ int gq_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, gq_str
  * Y is f32[M][rows] row-major (one row of Y per token).
  *
  * Y is computed on the tensor cores in one of two ways, both equal to the
- * sum above up to f32 rounding: for K % 256 == 0 both block scales are
- * folded into bf16 operand pieces (dx*Xq as three, d_w*(q_w-8) as two exact
- * pieces) and Y accumulates across all of K in tensor memory; otherwise
- * each block's exact integer D is read out and folded in f32.
+ * sum above up to f32 rounding (|Y - Y_ref| <= 1e-5 * sum_k |w x| over the
+ * dequantized operands w = d_w*(q_w-8), x = dx*Xq): for K % 256 == 0 both
+ * block scales are folded, per 8-block chunk and with power-of-two chunk
+ * factors, into f16 operand pieces (dx*Xq as two, d_w*(q_w-8) as two exact
+ * pieces) and Y accumulates a chunk at a time in tensor memory (with more
+ * than 128 tokens on pairs of SMs); otherwise each block's exact integer D
+ * is read out and folded in f32.
  *
  * The workspace (device memory, 16-byte aligned, at least
  * gq_q4_0_gemm_workspace_bytes(K, M) bytes, owned by the caller) receives
