@@ -111,6 +111,7 @@ static_assert(OFF_B % 1024 == 0 && OFF_RAW % 1024 == 0 && OFF_STILE % 128 == 0 &
 static_assert(CONV_WARPS == 4 && TN % 64 == 0, "converter warp v: words 2h, 2h+1 (h = v % 2), rows 32 * (v / 2) + 64 * k + lane");
 
 constexpr uint32_t kIdesc = idesc_f16(TM, TN, false);  // f16 A and B
+constexpr uint32_t kNegB = 1u << 14;  // instruction descriptor: negate B (the stored second weight piece is -B2)
 
 // ---------------------------------------------------------------- chunk exponents
 // Exponents of the power-of-two chunk factors: for m > 0 (the chunk's
@@ -210,17 +211,18 @@ __global__ void __launch_bounds__(256) k_xq_split(const int8_t *__restrict__ Xq,
 }
 
 // Weight pieces of one 8-element group: nibbles of w (element order) and
-// the block's scale d = d_w * 2^u_r as f16x2 {d, d} -> B1 and B2 chunks
-// (16 bytes each, word i = elements (i, i+4)), all in packed f16:
+// the block's scale d = d_w * 2^u_r as f16x2 {d, d} (and -d) -> B1 and -B2
+// chunks (16 bytes each, word i = elements (i, i+4)), all in packed f16:
 // pair i is OR-ed into the f16 pattern of 1024 (exact 1024 + q*16^(i%2),
 // after a shift by 8 for i >= 2), one FMA gives q - 8 exactly, B1 =
-// RN(d * (q - 8)) and B2 = d * (q - 8) - B1 by one FMA, exact because
+// RN(d * (q - 8)) and -B2 = B1 - d * (q - 8) by one FMA, exact because
 // d * (q - 8) has at most 14 significant bits (11 x 3), so the remainder
 // fits in f16 (in the normal range; d is at most 2^12, so |B1| <= 2^15).
-__device__ __forceinline__ void nib8_split(uint32_t w, uint32_t d2, uint4 &b1, uint4 &b2)
+// The MMA of the second piece negates B (kNegB).
+__device__ __forceinline__ void nib8_split(uint32_t w, uint32_t d2, uint32_t nd2, uint4 &b1, uint4 &b2)
 {
     asm("{\n"
-        " .reg .b32 s, x0, x1, x2, x3, q0, q1, q2, q3, n0, n1, n2, n3, one, m1032, sixteenth, m72;\n"
+        " .reg .b32 s, x0, x1, x2, x3, q0, q1, q2, q3, one, m1032, sixteenth, m72;\n"
         " mov.b32 one, 0x3C003C00;\n"        // 1
         " mov.b32 m1032, 0xE408E408;\n"      // -1032
         " mov.b32 sixteenth, 0x2C002C00;\n"  // 1/16
@@ -238,17 +240,14 @@ __device__ __forceinline__ void nib8_split(uint32_t w, uint32_t d2, uint4 &b1, u
         " mul.rn.f16x2 %1, q1, %9;\n"
         " mul.rn.f16x2 %2, q2, %9;\n"
         " mul.rn.f16x2 %3, q3, %9;\n"
-        " xor.b32 n0, %0, 0x80008000;\n"
-        " xor.b32 n1, %1, 0x80008000;\n"
-        " xor.b32 n2, %2, 0x80008000;\n"
-        " xor.b32 n3, %3, 0x80008000;\n"
-        " fma.rn.f16x2 %4, q0, %9, n0;\n"
-        " fma.rn.f16x2 %5, q1, %9, n1;\n"
-        " fma.rn.f16x2 %6, q2, %9, n2;\n"
-        " fma.rn.f16x2 %7, q3, %9, n3;\n"
+        " fma.rn.f16x2 %4, q0, %10, %0;\n"
+        " fma.rn.f16x2 %5, q1, %10, %1;\n"
+        " fma.rn.f16x2 %6, q2, %10, %2;\n"
+        " fma.rn.f16x2 %7, q3, %10, %3;\n"
         "}"
-        : "=r"(b1.x), "=r"(b1.y), "=r"(b1.z), "=r"(b1.w), "=r"(b2.x), "=r"(b2.y), "=r"(b2.z), "=r"(b2.w)
-        : "r"(w), "r"(d2));
+        // every output is written before the last read of an input: early-clobber
+        : "=&r"(b1.x), "=&r"(b1.y), "=&r"(b1.z), "=&r"(b1.w), "=&r"(b2.x), "=&r"(b2.y), "=&r"(b2.z), "=&r"(b2.w)
+        : "r"(w), "r"(d2), "r"(nd2));
 }
 
 struct Work {
@@ -413,7 +412,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint64_t A1 = smem_desc(ka, 128, 512), A2 = smem_desc(ka + APIECE, 128, 512);
                     const uint64_t B1 = smem_desc(kb, 128, 512), B2 = smem_desc(kb + BPIECE, 128, 512);
                     mma_f16(d, A1, B1, kIdesc, (cfirst && ks == 0) ? 0u : 1u);
-                    mma_f16(d, A1, B2, kIdesc, 1u);
+                    mma_f16(d, A1, B2, kIdesc | kNegB, 1u);
                     mma_f16(d, A2, B1, kIdesc, 1u);
                 }
                 mma_commit(bar_opempty + 8 * s);
@@ -551,14 +550,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 // d_w * 2^u_r: exact in f32, and in f16 down to 2^-14 (at most 2^12)
                 const uint32_t dh =
                     __half_as_ushort(__float2half_rn(__half2float(__ushort_as_half(dwb)) * wsc[k]));
-                const uint32_t dw = dh | (dh << 16);
+                const uint32_t dw = dh | (dh << 16), ndw = dw ^ 0x80008000u;
                 const uint2 nv = *reinterpret_cast<const uint2 *>(raw + crow[k] * 16 + h * 8);
                 uint8_t *dst = stage + op_off(crow[k], 2 * h);
                 uint4 b1, b2;
-                nib8_split(nv.x, dw, b1, b2);
+                nib8_split(nv.x, dw, ndw, b1, b2);
                 *reinterpret_cast<uint4 *>(dst) = b1;
                 *reinterpret_cast<uint4 *>(dst + BPIECE) = b2;
-                nib8_split(nv.y, dw, b1, b2);
+                nib8_split(nv.y, dw, ndw, b1, b2);
                 *reinterpret_cast<uint4 *>(dst + 128) = b1;
                 *reinterpret_cast<uint4 *>(dst + BPIECE + 128) = b2;
             }
@@ -797,7 +796,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const uint64_t A1 = smem_desc(ka, 128, 512), A2 = smem_desc(ka + APIECE, 128, 512);
                         const uint64_t B1 = smem_desc(kb, 128, 512), B2 = smem_desc(kb + BPIECE, 128, 512);
                         mma_f16_pair(d, A1, B1, kIdesc, (cfirst && j == 0 && ks == 0) ? 0u : 1u);
-                        mma_f16_pair(d, A1, B2, kIdesc, 1u);
+                        mma_f16_pair(d, A1, B2, kIdesc | kNegB, 1u);
                         mma_f16_pair(d, A2, B1, kIdesc, 1u);
                     }
                 }
@@ -950,20 +949,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // d_w * 2^u_r of block g + h: exact in f32, and in f16 down to 2^-14 (at most 2^12)
             const uint16_t dwb = reinterpret_cast<const uint16_t *>(stile)[trow * SG + (g & (SG - 1)) + h];
             const uint32_t dh = __half_as_ushort(__float2half_rn(__half2float(__ushort_as_half(dwb)) * wsc));
-            const uint32_t dw = dh | (dh << 16);
+            const uint32_t dw = dh | (dh << 16), ndw = dw ^ 0x80008000u;
             const uint4 nv = *reinterpret_cast<const uint4 *>(smem + OFF_RAW + rs * RBP_BYTES + crow * 32 + h * 16);
             uint8_t *dst = smem + OFF_B + (s + h) * B_BYTES + op_off(crow, 0);
             uint4 b1, b2;
-            nib8_split(nv.x, dw, b1, b2);
+            nib8_split(nv.x, dw, ndw, b1, b2);
             *reinterpret_cast<uint4 *>(dst) = b1;
             *reinterpret_cast<uint4 *>(dst + BPIECE) = b2;
-            nib8_split(nv.y, dw, b1, b2);
+            nib8_split(nv.y, dw, ndw, b1, b2);
             *reinterpret_cast<uint4 *>(dst + 128) = b1;
             *reinterpret_cast<uint4 *>(dst + BPIECE + 128) = b2;
-            nib8_split(nv.z, dw, b1, b2);
+            nib8_split(nv.z, dw, ndw, b1, b2);
             *reinterpret_cast<uint4 *>(dst + 256) = b1;
             *reinterpret_cast<uint4 *>(dst + BPIECE + 256) = b2;
-            nib8_split(nv.w, dw, b1, b2);
+            nib8_split(nv.w, dw, ndw, b1, b2);
             *reinterpret_cast<uint4 *>(dst + 384) = b1;
             *reinterpret_cast<uint4 *>(dst + BPIECE + 384) = b2;
             fence_async_smem();

@@ -87,6 +87,22 @@ def test_gemm_matches_oracle(M, rows, K):
     assert np.all(err <= 1e-5 * A), float(np.max(err / np.maximum(A, 1e-300)))
 
 
+# Shapes for the CTA-pair kernel (K % 256 == 0, M > 128): the peer CTA's half of
+# B entirely past the last row (rows <= 96), its tokens all padding but one
+# (M = 129), one 8-block chunk per tile (K = 256), ragged row and token tiles,
+# and more tiles than CTA pairs.
+@pytest.mark.parametrize("M,rows,K", [(129, 50, 256), (129, 96, 512), (257, 200, 768), (384, 97, 256),
+                                      (1000, 193, 512), (300, 31000, 256)])
+def test_gemm_cta_pair_shapes(M, rows, K):
+    W = synth.q4_0_weights(rows, K, synth.stream(800 + M, rows))
+    X = synth.normal((M, K), synth.stream(800 + M, K))
+    Xq, dx = oracle.quantize_q8_0(X, M, K)
+    Y = run_gemm(W, Xq, dx, rows, K, M)
+    Y_ref, A = oracle.gemm_q8act(W, Xq, dx, rows, K, M)
+    err = np.abs(Y.astype(np.float64) - Y_ref)
+    assert np.all(err <= 1e-5 * A), float(np.max(err / np.maximum(A, 1e-300)))
+
+
 def test_gemm_full_512x21504x5376_sampled():
     rows, K, M = 21504, 5376, 512
     W, X = synth.gemm_inputs()
