@@ -197,3 +197,22 @@ def test_gemm_extreme_block_dots_exact():
     got = D.cpu().numpy()
     assert np.all(got[0, :, 0] == 32 * 7 * 127) and np.all(got[0, :, 1] == -32 * 8 * 127)
     assert np.all(got[1, :, 0] == -32 * 7 * 127) and np.all(got[1, :, 1] == 32 * 8 * 127)
+
+
+@pytest.mark.parametrize("M,rows,K", [(100, 2000, 5376), (512, 3000, 5376)])  # one CTA per tile; CTA pairs
+def test_gemm_repeat_runs_bitwise_identical(M, rows, K):
+    """The chunk read-out adds in a fixed order: the same inputs give the same bits."""
+    t = torch()
+    W = synth.q4_0_weights(rows, K, synth.stream(900 + M, 0))
+    X = synth.normal((M, K), synth.stream(900 + M, 1))
+    Xq, dx = oracle.quantize_q8_0(X, M, K)
+    Wp = packed(oracle.FORMAT_Q4_0, W, rows, K)
+    ws, n = workspace(K, M)
+    outs = []
+    for _ in range(3):
+        Y = t.full((M, rows), float("nan"), dtype=t.float32, device="cuda")
+        gq.gq_q4_0_gemm_q8act(Wp, dev(Xq), dev(dx), Y, ws, n, rows, K, M)
+        t.cuda.synchronize()
+        outs.append(Y.cpu().numpy().view(np.uint32))
+    assert gq.gq_device_status() == gq.GQ_OK
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
