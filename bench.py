@@ -324,7 +324,23 @@ class Gemm(Workload):
                                    self.M)
 
 
-WORKLOADS = {w.name: w for w in (LogitsTopK, Q40Matvec, Q4KMatvec, FFN, Gemm)}
+class GemmSmallBatch8(Gemm):
+    """The same contraction at a small batch (a verifier's eight tokens): every
+    weight is decoded once on the CUDA cores and applied to all eight tokens."""
+    name = "q4_0_gemm_q8act_8x21504x5376"
+    kernel = "k_gemm_small"
+    bound = "hbm"  # reported as bytes per step (weights, X, Y) over the step time
+    M = 8
+
+
+class GemmSmallBatch32(GemmSmallBatch8):
+    """32 tokens: past the CUDA-core kernel's 16, one 128-token tile per CTA on the tensor cores."""
+    name = "q4_0_gemm_q8act_32x21504x5376"
+    kernel = "k_gemm_split"
+    M = 32
+
+
+WORKLOADS = {w.name: w for w in (LogitsTopK, Q40Matvec, Q4KMatvec, FFN, Gemm, GemmSmallBatch8, GemmSmallBatch32)}
 
 
 # ---------------------------------------------------------------- timing

@@ -168,6 +168,8 @@ int gq_q4_0_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *
     if (rows < 1 || M < 1 || K < 32 || K % 32 != 0) return GQ_ERR_SHAPE;
     if (workspace_bytes < gq_q4_0_gemm_workspace_bytes(K, M)) return GQ_ERR_WORKSPACE;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // few tokens: decode each weight once on the CUDA cores and apply it to every token
+    if (gemm_small_supported(K, M)) return launch_gemm_small(W, Xq, dx, Y, rows, K, M, st);
     if (gemm_split_supported(K)) return launch_gemm_split(W, Xq, dx, Y, workspace, workspace_bytes, rows, K, M, st);
     return launch_gemm_q8act_tc(W, Xq, dx, Y, workspace, workspace_bytes, rows, K, M, st);
 }

@@ -140,6 +140,9 @@ size_t gemm_workspace_bytes(int K, int M);
 // scale-folded bf16 tensor-core path (gq_gemm_split.cu): K % 256 == 0
 size_t gemm_split_workspace_bytes(int K, int M);
 bool gemm_split_supported(int K);
+bool gemm_small_supported(int K, int M);
+int launch_gemm_small(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows, int K, int M,
+                      cudaStream_t s);
 int launch_gemm_split(const void *W, const int8_t *Xq, const float *dx, float *Y, void *ws, size_t ws_bytes,
                       int rows, int K, int M, cudaStream_t s);
 int launch_gemm_q8act_tc(const void *W, const int8_t *Xq, const float *dx, float *Y, void *ws, size_t ws_bytes,

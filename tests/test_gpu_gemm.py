@@ -103,6 +103,22 @@ def test_gemm_cta_pair_shapes(M, rows, K):
     assert np.all(err <= 1e-5 * A), float(np.max(err / np.maximum(A, 1e-300)))
 
 
+# Small batches (M <= 16, staged codes fit in shared memory) run on the
+# CUDA-core kernel: odd rows, one block, the largest K each token tile size
+# still stages; just past that the tensor-core path takes over.
+@pytest.mark.parametrize("M,rows,K", [(2, 1, 32), (3, 77, 96), (4, 100, 21504), (8, 300, 5376), (13, 1001, 256),
+                                      (16, 3001, 5376), (16, 64, 7680),
+                                      (16, 50, 8192), (8, 40, 21504)])  # staging too large: tensor cores
+def test_gemm_small_batches(M, rows, K):
+    W = synth.q4_0_weights(rows, K, synth.stream(1000 + M, rows))
+    X = synth.normal((M, K), synth.stream(1000 + M, K))
+    Xq, dx = oracle.quantize_q8_0(X, M, K)
+    Y = run_gemm(W, Xq, dx, rows, K, M)
+    Y_ref, A = oracle.gemm_q8act(W, Xq, dx, rows, K, M)
+    err = np.abs(Y.astype(np.float64) - Y_ref)
+    assert np.all(err <= 1e-5 * A), float(np.max(err / np.maximum(A, 1e-300)))
+
+
 def test_gemm_full_512x21504x5376_sampled():
     rows, K, M = 21504, 5376, 512
     W, X = synth.gemm_inputs()
@@ -199,7 +215,7 @@ def test_gemm_extreme_block_dots_exact():
     assert np.all(got[1, :, 0] == -32 * 7 * 127) and np.all(got[1, :, 1] == 32 * 8 * 127)
 
 
-@pytest.mark.parametrize("M,rows,K", [(100, 2000, 5376), (512, 3000, 5376)])  # one CTA per tile; CTA pairs
+@pytest.mark.parametrize("M,rows,K", [(8, 2000, 5376), (100, 2000, 5376), (512, 3000, 5376)])  # small; one CTA; pairs
 def test_gemm_repeat_runs_bitwise_identical(M, rows, K):
     """The chunk read-out adds in a fixed order: the same inputs give the same bits."""
     t = torch()
