@@ -334,7 +334,8 @@ class GemmSmallBatch8(Gemm):
 
 
 class GemmSmallBatch32(GemmSmallBatch8):
-    """32 tokens: past the CUDA-core kernel's 16, one 128-token tile per CTA on the tensor cores."""
+    """32 tokens (a short prompt): past the CUDA-core kernel's 24, one
+    128-token tile per CTA on the tensor cores."""
     name = "q4_0_gemm_q8act_32x21504x5376"
     kernel = "k_gemm_split"
     M = 32

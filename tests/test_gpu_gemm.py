@@ -103,12 +103,14 @@ def test_gemm_cta_pair_shapes(M, rows, K):
     assert np.all(err <= 1e-5 * A), float(np.max(err / np.maximum(A, 1e-300)))
 
 
-# Small batches (M <= 16, staged codes fit in shared memory) run on the
-# CUDA-core kernel: odd rows, one block, the largest K each token tile size
-# still stages; just past that the tensor-core path takes over.
+# Small batches (M <= 24 in passes of up to 8 tokens whose staged codes fit
+# in shared memory) run on the CUDA-core kernel: odd rows, one block, the
+# largest K an 8-token pass still stages, several passes with a short last
+# one; just past those limits the tensor-core paths take over.
 @pytest.mark.parametrize("M,rows,K", [(2, 1, 32), (3, 77, 96), (4, 100, 21504), (8, 300, 5376), (13, 1001, 256),
-                                      (16, 3001, 5376), (16, 64, 7680),
-                                      (16, 50, 8192), (8, 40, 21504)])  # staging too large: tensor cores
+                                      (16, 3001, 5376), (17, 77, 96), (24, 300, 5376), (6, 50, 15744),
+                                      # staging too large or too many tokens: tensor cores
+                                      (8, 50, 15872), (8, 40, 21504), (25, 200, 256), (32, 300, 5376)])
 def test_gemm_small_batches(M, rows, K):
     W = synth.q4_0_weights(rows, K, synth.stream(1000 + M, rows))
     X = synth.normal((M, K), synth.stream(1000 + M, K))
