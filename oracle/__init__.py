@@ -26,6 +26,9 @@ _LIB = os.path.join(_HERE, "libgq_oracle.so")
 FORMAT_Q4_0 = 0
 FORMAT_Q8_0 = 1
 FORMAT_Q4_K = 2
+FORMAT_Q6_K = 3
+_SUPER = (FORMAT_Q4_K, FORMAT_Q6_K)  # 256-weight super-block formats
+_BLOCK_BYTES = {0: 18, 1: 34, 2: 144, 3: 210}
 
 _lib = None
 
@@ -61,7 +64,7 @@ def lib():
         I64 = ctypes.c_int64
         L.gqo_half_to_double.argtypes = [ctypes.c_uint16]
         L.gqo_half_to_double.restype = ctypes.c_double
-        for name in ("gqo_dequant_q4_0", "gqo_dequant_q8_0", "gqo_dequant_q4_k"):
+        for name in ("gqo_dequant_q4_0", "gqo_dequant_q8_0", "gqo_dequant_q4_k", "gqo_dequant_q6_k"):
             getattr(L, name).argtypes = [P, I64, P]
             getattr(L, name).restype = None
         L.gqo_q4_k_scale_min.argtypes = [P, ctypes.c_int, P, P]
@@ -100,10 +103,11 @@ def half_to_double(h: int) -> float:
 def dequant(fmt: int, blocks: np.ndarray, K: int) -> np.ndarray:
     """Decode canonical rows (rows x row_bytes uint8) to float64 (rows x K)."""
     blocks = _c(blocks, np.uint8)
-    rows = blocks.size // (K // (256 if fmt == FORMAT_Q4_K else 32) * {0: 18, 1: 34, 2: 144}[fmt])
+    rows = blocks.size // (K // (256 if fmt in _SUPER else 32) * _BLOCK_BYTES[fmt])
     out = np.empty((rows, K), dtype=np.float64)
-    fn = {0: lib().gqo_dequant_q4_0, 1: lib().gqo_dequant_q8_0, 2: lib().gqo_dequant_q4_k}[fmt]
-    nblk = rows * K // (256 if fmt == FORMAT_Q4_K else 32)
+    fn = {0: lib().gqo_dequant_q4_0, 1: lib().gqo_dequant_q8_0, 2: lib().gqo_dequant_q4_k,
+          3: lib().gqo_dequant_q6_k}[fmt]
+    nblk = rows * K // (256 if fmt in _SUPER else 32)
     fn(_ptr(blocks), nblk, _ptr(out))
     return out
 

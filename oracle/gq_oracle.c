@@ -32,9 +32,17 @@
  *        sub-scales sc[8] and mins m[8], then 128 bytes of nibbles in four
  *        32-byte chunks; chunk c holds sub-block 2c in its low nibbles and
  *        sub-block 2c+1 in its high nibbles; w = d*sc*q - dmin*m.
+ *   Q6_K (210 B / 256 weights; [LARQL] section 1 "Q6_K 210B"): 128 bytes ql
+ *        (low 4 bits of the codes), 64 bytes qh (top 2 bits), 16 int8
+ *        sub-scales (one per 16 weights), then fp16 d.  Each half of 128
+ *        weights uses 64 bytes of ql and 32 of qh; in a half, weight 32*c + l
+ *        (c = 0..3, l = 0..31) takes its low bits from ql byte l + 32*(c%2)
+ *        (low nibble for c < 2, high nibble otherwise) and its top bits from
+ *        bits 2c, 2c+1 of qh byte l; w = d * sc[weight/16] * (q - 32).
  *
  * Parity unpinned: bit compatibility with real GGUF files (nibble order of
- * Q4_0, 6-bit packing of Q4_K) -- no GGUF file is available to compare with.
+ * Q4_0, 6-bit packing of Q4_K, bit placement of Q6_K) -- no GGUF file is
+ * available to compare with.
  */
 #include <math.h>
 #include <stdint.h>
@@ -44,6 +52,7 @@
 #define GQO_Q4_0 0
 #define GQO_Q8_0 1
 #define GQO_Q4_K 2
+#define GQO_Q6_K 3
 
 /* IEEE binary16 -> double, exact (every half is a double). */
 static double half_to_double(uint16_t h)
@@ -132,12 +141,32 @@ void gqo_dequant_q4_k(const uint8_t *blocks, int64_t nsuper, double *out)
     }
 }
 
+/* Q6_K: w = d * sc[e/16] * (q_e - 32), q_e from 4 bits of ql and 2 of qh. */
+void gqo_dequant_q6_k(const uint8_t *blocks, int64_t nsuper, double *out)
+{
+    for (int64_t b = 0; b < nsuper; ++b) {
+        const uint8_t *blk = blocks + b * 210;
+        const uint8_t *ql = blk, *qh = blk + 128;
+        const int8_t *sc = (const int8_t *)(blk + 192);
+        double d = half_to_double(rd16(blk + 208));
+        for (int e = 0; e < 256; ++e) {
+            int half = e / 128, c = (e % 128) / 32, l = e % 32;
+            int lowbyte = ql[64 * half + l + 32 * (c % 2)];
+            int lo = (c < 2) ? (lowbyte & 0x0f) : (lowbyte >> 4);
+            int hi = (qh[32 * half + l] >> (2 * c)) & 3;
+            int q = lo | (hi << 4);
+            out[b * 256 + e] = d * (double)sc[e / 16] * (double)(q - 32);
+        }
+    }
+}
+
 static int64_t row_bytes(int fmt, int64_t K)
 {
     switch (fmt) {
     case GQO_Q4_0: return K / 32 * 18;
     case GQO_Q8_0: return K / 32 * 34;
     case GQO_Q4_K: return K / 256 * 144;
+    case GQO_Q6_K: return K / 256 * 210;
     }
     return -1;
 }
@@ -149,6 +178,7 @@ static void dequant_row(int fmt, const uint8_t *row, int64_t K, double *w)
     case GQO_Q4_0: gqo_dequant_q4_0(row, K / 32, w); break;
     case GQO_Q8_0: gqo_dequant_q8_0(row, K / 32, w); break;
     case GQO_Q4_K: gqo_dequant_q4_k(row, K / 256, w); break;
+    case GQO_Q6_K: gqo_dequant_q6_k(row, K / 256, w); break;
     }
 }
 
@@ -162,7 +192,7 @@ int gqo_matvec(int fmt, const uint8_t *W, int64_t rows, int64_t K, const float *
                const int64_t *row_idx, int64_t n_sel, double *y, double *a)
 {
     int64_t rb = row_bytes(fmt, K);
-    if (rb < 0 || K <= 0 || K % (fmt == GQO_Q4_K ? 256 : 32) != 0)
+    if (rb < 0 || K <= 0 || K % ((fmt == GQO_Q4_K || fmt == GQO_Q6_K) ? 256 : 32) != 0)
         return -1;
     (void)rows;
 #pragma omp parallel

@@ -19,6 +19,10 @@ How each field is drawn:
 * Q4_K: 12 uniform random bytes for the packed 6-bit sub-scales and mins
   (every 6-bit field is then an independent uniform integer 0..63, whatever
   the bit packing) and 128 uniform random bytes of nibbles.
+* Q6_K: 192 uniform random bytes for the low and high code bits (every 6-bit
+  code is then an independent uniform integer 0..63, whatever the bit
+  placement), 16 sub-scales uniform on -128..127, and the fp16 scale in the
+  last two bytes.
 * fp16 scales: the f32 value 2**e * U(0.5, 1.5), rounded to nearest-even
   fp16, stored little-endian in the first bytes of the block.
 * Activations: standard normal f32.
@@ -36,15 +40,18 @@ import numpy as np
 Q4_0_BYTES = 18
 Q8_0_BYTES = 34
 Q4_K_BYTES = 144
+Q6_K_BYTES = 210
 QK = 32  # weights per Q4_0 / Q8_0 block
 QK_K = 256  # weights per Q4_K super-block
 
 FORMAT_Q4_0 = 0
 FORMAT_Q8_0 = 1
 FORMAT_Q4_K = 2
+FORMAT_Q6_K = 3
 
-_BLOCK_BYTES = {FORMAT_Q4_0: Q4_0_BYTES, FORMAT_Q8_0: Q8_0_BYTES, FORMAT_Q4_K: Q4_K_BYTES}
-_BLOCK_WEIGHTS = {FORMAT_Q4_0: QK, FORMAT_Q8_0: QK, FORMAT_Q4_K: QK_K}
+_BLOCK_BYTES = {FORMAT_Q4_0: Q4_0_BYTES, FORMAT_Q8_0: Q8_0_BYTES, FORMAT_Q4_K: Q4_K_BYTES,
+                FORMAT_Q6_K: Q6_K_BYTES}
+_BLOCK_WEIGHTS = {FORMAT_Q4_0: QK, FORMAT_Q8_0: QK, FORMAT_Q4_K: QK_K, FORMAT_Q6_K: QK_K}
 
 
 def block_bytes(fmt: int) -> int:
@@ -111,6 +118,21 @@ def q4_k_weights(rows: int, K: int, rng: np.random.Generator, d_exp2: int = -8) 
     return out.reshape(rows, ns * Q4_K_BYTES)
 
 
+def q6_k_weights(rows: int, K: int, rng: np.random.Generator, d_exp2: int = -10) -> np.ndarray:
+    """Canonical Q6_K rows: uint8 array (rows, K//256*210).
+
+    Bytes 0..191 hold the code bits, 192..207 the int8 sub-scales, 208..209 d.
+    """
+    assert K % QK_K == 0
+    ns = K // QK_K
+    out = np.empty((rows, ns, Q6_K_BYTES), dtype=np.uint8)
+    out[:, :, 0:192] = rng.integers(0, 256, size=(rows, ns, 192), dtype=np.uint8)
+    out[:, :, 192:208] = rng.integers(-128, 128, size=(rows, ns, 16), dtype=np.int8).view(np.uint8)
+    d = _fp16_scales(rng, rows * ns, d_exp2).reshape(rows, ns)
+    out[:, :, 208:210] = d.view(np.uint8).reshape(rows, ns, 2)
+    return out.reshape(rows, ns * Q6_K_BYTES)
+
+
 def weights(fmt: int, rows: int, K: int, rng: np.random.Generator) -> np.ndarray:
     if fmt == FORMAT_Q4_0:
         return q4_0_weights(rows, K, rng)
@@ -118,6 +140,8 @@ def weights(fmt: int, rows: int, K: int, rng: np.random.Generator) -> np.ndarray
         return q8_0_weights(rows, K, rng)
     if fmt == FORMAT_Q4_K:
         return q4_k_weights(rows, K, rng)
+    if fmt == FORMAT_Q6_K:
+        return q6_k_weights(rows, K, rng)
     raise ValueError(fmt)
 
 

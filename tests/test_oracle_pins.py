@@ -56,6 +56,7 @@ def test_half_to_double_matches_numpy_for_every_finite_pattern():
     (oracle.FORMAT_Q4_0, "q4_0_handbuilt.txt", 32),
     (oracle.FORMAT_Q8_0, "q8_0_handbuilt.txt", 32),
     (oracle.FORMAT_Q4_K, "q4_k_handbuilt.txt", 256),
+    (oracle.FORMAT_Q6_K, "q6_k_handbuilt.txt", 256),
 ])
 def test_golden_handbuilt_blocks(fmt, name, K):
     blk, expect = _golden(name)
@@ -105,6 +106,24 @@ def test_q4_k_special_sub_blocks():
     assert np.all(w[0:32] == -dmin * 3)
 
 
+def test_q6_k_special_codes_and_scales():
+    # q = 32 -> 0 for any scale; q = 63 -> 31 d sc; q = 0 -> -32 d sc; sc = 0, -128, 127
+    d = 0.25
+    q = np.full(256, 32)
+    q[16:32] = 63
+    q[32:48] = 0
+    q[48:64] = 63
+    q[64:80] = 0
+    sc = [7, -3, 5, -128, 127, 0] + [1] * 10
+    w = oracle.dequant(oracle.FORMAT_Q6_K, np.frombuffer(be.enc_q6_k(q, sc, d), np.uint8), 256)[0]
+    assert np.all(w[0:16] == 0.0) and np.all(w[80:] == 0.0)
+    assert np.all(w[16:32] == 31 * d * -3) and np.all(w[32:48] == -32 * d * 5)
+    assert np.all(w[48:64] == 31 * d * -128) and np.all(w[64:80] == -32 * d * 127)
+    q[80:96] = 63
+    w = oracle.dequant(oracle.FORMAT_Q6_K, np.frombuffer(be.enc_q6_k(q, sc, d), np.uint8), 256)[0]
+    assert np.all(w[80:96] == 0.0)  # sc = 0
+
+
 def test_q4_k_scale_min_unpacking_every_field():
     rng = np.random.default_rng(3)
     for _ in range(200):
@@ -133,9 +152,14 @@ def test_q4_k_decode_matches_intended_values():
     assert np.array_equal(oracle.dequant(oracle.FORMAT_Q4_K, W, 512), dense)
 
 
+def test_q6_k_decode_matches_intended_values():
+    W, dense = be.random_q6_k_matrix(3, 512, np.random.default_rng(17))
+    assert np.array_equal(oracle.dequant(oracle.FORMAT_Q6_K, W, 512), dense)
+
+
 # ---------------------------------------------------------------- one-hot / all-ones
 
-@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K])
+@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K, oracle.FORMAT_Q6_K])
 def test_one_hot_x_reproduces_a_column(fmt):
     rng = np.random.default_rng(8)
     rows, K = 3, 512
@@ -143,8 +167,10 @@ def test_one_hot_x_reproduces_a_column(fmt):
         W, dense, _, _ = be.random_q4_0_matrix(rows, K, rng)
     elif fmt == oracle.FORMAT_Q8_0:
         W, dense = be.random_q8_0_matrix(rows, K, rng)
-    else:
+    elif fmt == oracle.FORMAT_Q4_K:
         W, dense = be.random_q4_k_matrix(rows, K, rng)
+    else:
+        W, dense = be.random_q6_k_matrix(rows, K, rng)
     for j in (0, 1, 15, 16, 17, 31, 33, 255, 256, 300, 511):
         x = np.zeros(K, np.float32)
         x[j] = 1.0
@@ -173,15 +199,17 @@ def _exact_dot(dense_row, x):
 
 
 @pytest.mark.parametrize("fmt,K", [(oracle.FORMAT_Q4_0, 64), (oracle.FORMAT_Q8_0, 64),
-                                   (oracle.FORMAT_Q4_K, 256)])
+                                   (oracle.FORMAT_Q4_K, 256), (oracle.FORMAT_Q6_K, 256)])
 def test_brute_force_exact_rational_2xK(fmt, K):
     rng = np.random.default_rng(21 + fmt)
     if fmt == oracle.FORMAT_Q4_0:
         W, dense, _, _ = be.random_q4_0_matrix(2, K, rng)
     elif fmt == oracle.FORMAT_Q8_0:
         W, dense = be.random_q8_0_matrix(2, K, rng)
-    else:
+    elif fmt == oracle.FORMAT_Q4_K:
         W, dense = be.random_q4_k_matrix(2, K, rng)
+    else:
+        W, dense = be.random_q6_k_matrix(2, K, rng)
     x = rng.standard_normal(K).astype(np.float32)
     y, a = oracle.matvec(fmt, W, x, 2, K)
     for r in range(2):
@@ -197,6 +225,8 @@ def test_matvec_rejects_partial_blocks():
         oracle.matvec(oracle.FORMAT_Q4_0, np.zeros(18, np.uint8), np.zeros(48, np.float32), 1, 48)
     with pytest.raises(ValueError):
         oracle.matvec(oracle.FORMAT_Q4_K, np.zeros(144, np.uint8), np.zeros(128, np.float32), 1, 128)
+    with pytest.raises(ValueError):
+        oracle.matvec(oracle.FORMAT_Q6_K, np.zeros(210, np.uint8), np.zeros(128, np.float32), 1, 128)
 
 
 def test_row_selection_matches_full_rows():
@@ -426,3 +456,27 @@ def test_planted_nibble_order_mistake_is_caught_by_golden_fixture():
     for j in range(16):
         wrong += [(qs[j] & 15) - 8, (qs[j] >> 4) - 8]
     assert not np.array_equal(np.array(wrong, float), expect)
+
+
+def test_planted_q6_k_bit_placement_mistakes_are_caught_by_golden_fixture():
+    """Decoders that take a weight's top bits from the wrong qh bit pair, or
+    its low bits from the other nibble, must disagree with the hand-built
+    fixture (whose weights were derived from the intended codes)."""
+    blk, expect = _golden("q6_k_handbuilt.txt")
+    ql, qh = blk[:128], blk[128:192]
+    sc = np.frombuffer(blk[192:208], dtype=np.int8).astype(int)
+    d = float(np.frombuffer(blk[208:210], dtype=np.float16)[0])
+
+    def decode(hi_shift, lo_high):
+        out = []
+        for e in range(256):
+            half, c, l = e // 128, (e % 128) // 32, e % 32
+            b = ql[64 * half + l + 32 * (c % 2)]
+            lo = (b >> 4) if lo_high(c) else (b & 15)
+            hi = (qh[32 * half + l] >> hi_shift(c)) & 3
+            out.append(d * sc[e // 16] * ((lo | (hi << 4)) - 32))
+        return np.array(out)
+
+    assert np.array_equal(decode(lambda c: 2 * c, lambda c: c >= 2), expect)  # the reading itself
+    assert not np.array_equal(decode(lambda c: 6 - 2 * c, lambda c: c >= 2), expect)  # qh pairs reversed
+    assert not np.array_equal(decode(lambda c: 2 * c, lambda c: c % 2 == 1), expect)  # nibble by c parity
