@@ -266,6 +266,31 @@ class Q4KMatvec(Rotating):
         self.gq.gq_q4k_matvec(self.copies[i % len(self.copies)], self.x, self.y, self.rows, self.K)
 
 
+class Q6KMatvec(Rotating):
+    """Q6_K at the FFN shape (21 super-blocks per row, 4410 B per row)."""
+    name = "q6_k_matvec_21504x5376"
+    kernel = "k_q6k_matvec"
+    rows, K = 21504, 5376
+
+    def setup(self, torch, gq):
+        W = synth.q6_k_weights(self.rows, self.K, synth.stream(6, 0))
+        x = synth.normal(self.K, synth.stream(6, 1))
+        nbytes = gq.gq_packed_bytes(3, self.rows, self.K)
+        R = self._rotate(torch, nbytes)
+        Wp = gq.pack(3, _to_dev(torch, W.reshape(-1)), self.rows, self.K)
+        self.copies = [Wp] + [Wp.clone() for _ in range(R - 1)]
+        self.x = _to_dev(torch, x)
+        self.y = torch.empty(self.rows, dtype=torch.float32, device="cuda")
+        self.gq = gq
+        self.bytes_per_step = nbytes + 4 * self.K + 4 * self.rows
+        self.weight_bytes = nbytes
+        self.working_set = nbytes * R
+        self.l2_policy = f"{R} rotating weight copies ({nbytes * R / 2**20:.0f} MiB > 4x L2)"
+
+    def step(self, i):
+        self.gq.gq_q6k_matvec(self.copies[i % len(self.copies)], self.x, self.y, self.rows, self.K)
+
+
 class FFN(Rotating):
     name = "q4_0_ffn_gelu_21504x5376"
     kernel = "k_ffn_gate_up"
@@ -341,7 +366,8 @@ class GemmSmallBatch32(GemmSmallBatch8):
     M = 32
 
 
-WORKLOADS = {w.name: w for w in (LogitsTopK, Q40Matvec, Q4KMatvec, FFN, Gemm, GemmSmallBatch8, GemmSmallBatch32)}
+WORKLOADS = {w.name: w for w in (LogitsTopK, Q40Matvec, Q4KMatvec, Q6KMatvec, FFN, Gemm, GemmSmallBatch8,
+                                  GemmSmallBatch32)}
 
 
 # ---------------------------------------------------------------- timing

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(HERE, "libgq.so")
 GQ_FORMAT_Q4_0 = 0
 GQ_FORMAT_Q8_0 = 1
 GQ_FORMAT_Q4_K = 2
+GQ_FORMAT_Q6_K = 3
 GQ_MAX_K = 49152
 GQ_MAX_TOPK = 64
 
@@ -53,6 +54,7 @@ def _declare(L):
         "gq_q4_0_matvec": ([P, P, P, I, I, I, P], I),
         "gq_q8_0_matvec": ([P, P, P, I, I, I, P], I),
         "gq_q4k_matvec": ([P, P, P, I, I, I, P], I),
+        "gq_q6k_matvec": ([P, P, P, I, I, I, P], I),
         "gq_ffn_gate_up_gelu": ([P, P, P, P, I, I, I, P], I),
         "gq_logits_topk_workspace_bytes": ([I, I, I], S),
         "gq_logits_topk": ([P, P, ctypes.c_float, I, P, P, P, P, S, I, I, I, P], I),
@@ -139,6 +141,10 @@ def gq_q8_0_matvec(W, x, y, rows, K, M=1, stream=None):
 
 def gq_q4k_matvec(W, x, y, rows, K, M=1, stream=None):
     _check(lib().gq_q4k_matvec(_ptr(W), _ptr(x), _ptr(y), rows, K, M, _stream(stream)), "gq_q4k_matvec")
+
+
+def gq_q6k_matvec(W, x, y, rows, K, M=1, stream=None):
+    _check(lib().gq_q6k_matvec(_ptr(W), _ptr(x), _ptr(y), rows, K, M, _stream(stream)), "gq_q6k_matvec")
 
 
 def gq_ffn_gate_up_gelu(W_gate, W_up, x, h, rows, K, M=1, stream=None):

@@ -11,7 +11,7 @@ using namespace gq;
 
 namespace {
 
-int block_weights(int format) { return format == GQ_FORMAT_Q4_K ? 256 : 32; }
+int block_weights(int format) { return (format == GQ_FORMAT_Q4_K || format == GQ_FORMAT_Q6_K) ? 256 : 32; }
 
 int block_bytes(int format)
 {
@@ -19,13 +19,15 @@ int block_bytes(int format)
     case GQ_FORMAT_Q4_0: return 18;
     case GQ_FORMAT_Q8_0: return 34;
     case GQ_FORMAT_Q4_K: return 144;
+    case GQ_FORMAT_Q6_K: return 210;
     }
     return 0;
 }
 
 bool valid_format(int format)
 {
-    return format == GQ_FORMAT_Q4_0 || format == GQ_FORMAT_Q8_0 || format == GQ_FORMAT_Q4_K;
+    return format == GQ_FORMAT_Q4_0 || format == GQ_FORMAT_Q8_0 || format == GQ_FORMAT_Q4_K ||
+           format == GQ_FORMAT_Q6_K;
 }
 
 int check_matvec(int format, const void *W, const float *x, const float *y, int rows, int K, int M)
@@ -106,6 +108,13 @@ int gq_q4k_matvec(const void *W, const float *x, float *y, int rows, int K, int 
     if (st != GQ_OK) return st;
     return launch_q4k_matvec(W, x, y, rows, K, choose_matvec_geo(GQ_FORMAT_Q4_K, rows, K / 32, aligned32(W)),
                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gq_q6k_matvec(const void *W, const float *x, float *y, int rows, int K, int M, gq_stream_t stream)
+{
+    int st = check_matvec(GQ_FORMAT_Q6_K, W, x, y, rows, K, M);
+    if (st != GQ_OK) return st;
+    return launch_q6k_matvec(W, x, y, rows, K, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int gq_ffn_gate_up_gelu(const void *W_gate, const void *W_up, const float *x, float *h, int rows, int K,

@@ -12,6 +12,10 @@
 //   Q8_0: [rows*nb x 32 B, byte = q XOR 0x80]     [rows*nb x fp16 d]
 //   Q4_K: [rows*ns x 128 B, sub-block s at 16 s, element order]
 //         [rows*ns x 16 B {d, dmin, 12 scale bytes}]
+//   Q6_K: [rows*ns x 128 B low 4 code bits, element order]
+//         [rows*ns x 64 B top 2 code bits: byte i holds elements 4i..4i+3 at
+//          bits 0, 2, 4, 6]
+//         [rows*ns x 18 B {16 int8 sub-scales, fp16 d}]
 // "Element order" means byte i of a 32-element group holds element 2i in
 // its low nibble and element 2i+1 in its high nibble.
 #include "gq_host.h"
@@ -139,9 +143,52 @@ __global__ void k_pack_q4_k(const uint8_t *__restrict__ src, uint8_t *__restrict
     }
 }
 
+// Q6_K canonical block (ql[128], qh[64], sc[16], d): in each 128-weight half
+// h, weight 32c + l has its low bits in ql[64h + l + 32(c % 2)] (low nibble
+// for c < 2, high nibble otherwise) and its top bits at bit 2c of qh[32h + l].
+__global__ void k_pack_q6_k(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, long long nsup,
+                            bool unpack)
+{
+    for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nsup;
+         b += (long long)gridDim.x * blockDim.x) {
+        if (!unpack) {
+            const uint8_t *blk = src + b * 210;
+            uint8_t *lo = dst + b * 128;
+            uint8_t *hi = dst + nsup * 128 + b * 64;
+            uint8_t *rec = dst + nsup * 192 + b * 18;
+            for (int j = 0; j < 18; ++j) rec[j] = blk[192 + j];
+            for (int i = 0; i < 128; ++i) lo[i] = 0;
+            for (int i = 0; i < 64; ++i) hi[i] = 0;
+            for (int e = 0; e < 256; ++e) {
+                const int h = e >> 7, c = (e >> 5) & 3, l = e & 31;
+                const uint8_t qlb = blk[64 * h + l + 32 * (c & 1)];
+                const int q_lo = (c < 2) ? (qlb & 15) : (qlb >> 4);
+                const int q_hi = (blk[128 + 32 * h + l] >> (2 * c)) & 3;
+                lo[e >> 1] |= static_cast<uint8_t>(q_lo << (4 * (e & 1)));
+                hi[e >> 2] |= static_cast<uint8_t>(q_hi << (2 * (e & 3)));
+            }
+        } else {
+            const uint8_t *lo = src + b * 128;
+            const uint8_t *hi = src + nsup * 128 + b * 64;
+            const uint8_t *rec = src + nsup * 192 + b * 18;
+            uint8_t *blk = dst + b * 210;
+            for (int j = 0; j < 18; ++j) blk[192 + j] = rec[j];
+            for (int i = 0; i < 192; ++i) blk[i] = 0;
+            for (int e = 0; e < 256; ++e) {
+                const int h = e >> 7, c = (e >> 5) & 3, l = e & 31;
+                const int q_lo = (lo[e >> 1] >> (4 * (e & 1))) & 15;
+                const int q_hi = (hi[e >> 2] >> (2 * (e & 3))) & 3;
+                blk[64 * h + l + 32 * (c & 1)] |= static_cast<uint8_t>(q_lo << ((c < 2) ? 0 : 4));
+                blk[128 + 32 * h + l] |= static_cast<uint8_t>(q_hi << (2 * c));
+            }
+        }
+    }
+}
+
 int launch_pack(int format, const void *src, void *dst, int rows, int K, bool unpack, cudaStream_t s)
 {
-    const long long n = (format == GQ_FORMAT_Q4_K) ? (long long)rows * (K / 256) : (long long)rows * (K / 32);
+    const long long n = (format == GQ_FORMAT_Q4_K || format == GQ_FORMAT_Q6_K) ? (long long)rows * (K / 256)
+                                                                               : (long long)rows * (K / 32);
     const int threads = 256;
     long long blocks = (n + threads - 1) / threads;
     const long long cap = (long long)sm_count() * 16;
@@ -153,6 +200,7 @@ int launch_pack(int format, const void *src, void *dst, int rows, int K, bool un
     case GQ_FORMAT_Q4_0: k_pack_q4_0<<<(unsigned)blocks, threads, 0, s>>>(a, b, n, unpack); break;
     case GQ_FORMAT_Q8_0: k_pack_q8_0<<<(unsigned)blocks, threads, 0, s>>>(a, b, n, unpack); break;
     case GQ_FORMAT_Q4_K: k_pack_q4_k<<<(unsigned)blocks, threads, 0, s>>>(a, b, n, unpack); break;
+    case GQ_FORMAT_Q6_K: k_pack_q6_k<<<(unsigned)blocks, threads, 0, s>>>(a, b, n, unpack); break;
     default: return GQ_ERR_FORMAT;
     }
     return status_from(cudaGetLastError());

@@ -62,8 +62,10 @@ typedef enum {
 enum {
     GQ_FORMAT_Q4_0 = 0, /* 18 B / 32 weights: fp16 d, 16 B nibbles; w = (q - 8) d   */
     GQ_FORMAT_Q8_0 = 1, /* 34 B / 32 weights: fp16 d, 32 int8 q;     w = q d        */
-    GQ_FORMAT_Q4_K = 2  /* 144 B / 256 weights: fp16 d, dmin, 12 B 6-bit sc/m,
+    GQ_FORMAT_Q4_K = 2, /* 144 B / 256 weights: fp16 d, dmin, 12 B 6-bit sc/m,
                            128 B nibbles;                       w = d sc q - dmin m */
+    GQ_FORMAT_Q6_K = 3  /* 210 B / 256 weights: 128 B low 4 code bits, 64 B top 2
+                           bits, 16 int8 sub-scales, fp16 d; w = d sc (q - 32) */
 };
 
 /* Largest K accepted by the single-pass matvec kernels (the whole activation
@@ -81,7 +83,10 @@ const char *gq_status_string(int status);
  * The canonical blocks are the GGUF byte order: Q4_0 byte j holds element j
  * (low nibble) and element j+16 (high nibble); Q4_K's 128 nibble bytes are
  * four 32-byte chunks, chunk c holding sub-block 2c in the low nibbles and
- * 2c+1 in the high nibbles.  The packed layout keeps every bit of every
+ * 2c+1 in the high nibbles; Q6_K's code bits follow the GGUF placement (in
+ * each 128-weight half, weight 32c + l has its low 4 bits in ql byte
+ * l + 32(c % 2) of the half, low nibble for c < 2, and its top 2 bits at bit
+ * 2c of qh byte l of the half).  The packed layout keeps every bit of every
  * block and the same total byte count; it is a bijection, undone exactly by
  * gq_unpack.  Packed layout of a rows x K matrix with nb blocks per row:
  *   Q4_0: plane 0 = rows*nb 16-byte payloads, row-major, nibbles in element
@@ -93,6 +98,10 @@ const char *gq_status_string(int status);
  *         sub-block s at bytes 16s..16s+15, nibbles in element order;
  *         plane 1 = rows*ns 16-byte records {d, dmin, 12 scale bytes}
  *         copied unchanged.
+ *   Q6_K: plane 0 = rows*ns 128-byte low-bit payloads in element order;
+ *         plane 1 = rows*ns 64-byte top-bit payloads (byte i = elements
+ *         4i..4i+3 at bits 0, 2, 4, 6); plane 2 = rows*ns 18-byte records
+ *         {16 int8 sub-scales, fp16 d} copied unchanged.
  * W_canon and W_packed must not overlap.  Both are device pointers.
  * ------------------------------------------------------------------------ */
 size_t gq_packed_bytes(int format, int rows, int K); /* 0 if invalid */
@@ -114,6 +123,11 @@ int gq_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K, int
 int gq_q8_0_matvec(const void *W, const float *x, float *y, int rows, int K, int M,
                    gq_stream_t stream);
 int gq_q4k_matvec(const void *W, const float *x, float *y, int rows, int K, int M,
+                  gq_stream_t stream);
+/* Q6_K ("Metal kernel capability table", section 1, q6k_matvec row: 210-byte
+ * super-blocks, K % 256): w = d * sc[j / 16] * (q_j - 32) within a
+ * super-block.  Same contract as the other matvecs. */
+int gq_q6k_matvec(const void *W, const float *x, float *y, int rows, int K, int M,
                   gq_stream_t stream);
 
 /* ---------------------------------------------------------------------------

@@ -44,6 +44,8 @@ def test_packed_bytes(lib):
     assert gq.gq_packed_bytes(0, 4096, 4096) == 9437184
     assert gq.gq_packed_bytes(1, 262144, 5376) == 1497366528
     assert gq.gq_packed_bytes(2, 21504, 5376) == 65028096
+    assert gq.gq_packed_bytes(3, 21504, 5376) == 21504 * 21 * 210
+    assert gq.gq_packed_bytes(3, 1, 512 + 32) == 0
     assert gq.gq_packed_bytes(0, 21504, 5376) == 65028096
     assert gq.gq_packed_bytes(0, 1, 48) == 0
     assert gq.gq_packed_bytes(2, 1, 512 + 32) == 0
@@ -68,7 +70,7 @@ def call(name, *args):
 
 
 def test_matvec_argument_validation(lib):
-    for name in ("gq_q4_0_matvec", "gq_q8_0_matvec", "gq_q4k_matvec"):
+    for name in ("gq_q4_0_matvec", "gq_q8_0_matvec", "gq_q4k_matvec", "gq_q6k_matvec"):
         assert call(name, None, A, A, 4, 256, 1, None) == gq.GQ_ERR_NULL
         assert call(name, A, None, A, 4, 256, 1, None) == gq.GQ_ERR_NULL
         assert call(name, A, A, None, 4, 256, 1, None) == gq.GQ_ERR_NULL
@@ -82,6 +84,7 @@ def test_matvec_argument_validation(lib):
         assert call(name, A, A, A, 4, 256, 0, None) == gq.GQ_ERR_SHAPE
         assert call(name, A, A, A, 4, gq.GQ_MAX_K + 256, 1, None) == gq.GQ_ERR_SHAPE
     assert call("gq_q4k_matvec", A, A, A, 4, 288, 1, None) == gq.GQ_ERR_SHAPE
+    assert call("gq_q6k_matvec", A, A, A, 4, 288, 1, None) == gq.GQ_ERR_SHAPE
     assert call("gq_q8_0_matvec", A + 16, A, A, 4, 256, 1, None) == gq.GQ_ERR_ALIGN   # needs 32 B
     assert call("gq_q4_0_matvec", A + 16, None, A, 4, 256, 1, None) == gq.GQ_ERR_NULL
 

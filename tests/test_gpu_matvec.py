@@ -1,4 +1,4 @@
-"""GPU parity of the decode matvecs (Q4_0, Q8_0, Q4_K) against the fp64 oracle.
+"""GPU parity of the decode matvecs (Q4_0, Q8_0, Q4_K, Q6_K) against the fp64 oracle.
 
 Bound (per row): |y - y_ref| <= 1e-5 * sum_j |w_ij x_j|.  Cases span several
 tiles and a ragged row tail, K at the block minimum, the lane-group widths
@@ -21,6 +21,7 @@ FMT_FN = {
     oracle.FORMAT_Q4_0: gq.gq_q4_0_matvec,
     oracle.FORMAT_Q8_0: gq.gq_q8_0_matvec,
     oracle.FORMAT_Q4_K: gq.gq_q4k_matvec,
+    oracle.FORMAT_Q6_K: gq.gq_q6k_matvec,
 }
 
 
@@ -38,11 +39,11 @@ SHAPES = [(1, 32), (3, 64), (37, 96), (257, 256), (1000, 512), (129, 4096), (515
           (33, 2304), (250, 800), (8, 49152)]
 
 
-@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K])
+@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K, oracle.FORMAT_Q6_K])
 @pytest.mark.parametrize("rows,K", SHAPES)
 def test_matvec_matches_oracle(fmt, rows, K):
-    if fmt == oracle.FORMAT_Q4_K and K % 256:
-        pytest.skip("Q4_K needs K % 256 == 0")
+    if fmt in (oracle.FORMAT_Q4_K, oracle.FORMAT_Q6_K) and K % 256:
+        pytest.skip("K-quants need K % 256 == 0")
     seed = 1000 + rows + K
     W = synth.weights(fmt, rows, K, synth.stream(seed, 0))
     x = synth.normal(K, synth.stream(seed, 1))
@@ -58,6 +59,16 @@ def test_q4_0_full_4096x4096_workload():
     assert_within(y, y_ref, a_ref, what="q4_0 4096x4096")
 
 
+def test_q6_k_21504x5376_sampled_rows():
+    rows, K = 21504, 5376
+    W = synth.q6_k_weights(rows, K, synth.stream(70, 0))
+    x = synth.normal(K, synth.stream(70, 1))
+    y = run_matvec(oracle.FORMAT_Q6_K, W, x, rows, K)
+    sel = np.concatenate([[0, 1, 2, 3, rows - 1], np.random.default_rng(0).choice(rows, 400, replace=False)])
+    y_ref, a_ref = oracle.matvec(oracle.FORMAT_Q6_K, W, x, rows, K, row_idx=sel)
+    assert_within(y[sel], y_ref, a_ref, what="q6_k 21504x5376")
+
+
 def test_q4_k_full_21504x5376_workload():
     W, x = synth.q4_k_matvec_inputs()
     y = run_matvec(oracle.FORMAT_Q4_K, W, x, 21504, 5376)
@@ -65,7 +76,7 @@ def test_q4_k_full_21504x5376_workload():
     assert_within(y, y_ref, a_ref, what="q4_k 21504x5376")
 
 
-@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K])
+@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K, oracle.FORMAT_Q6_K])
 def test_one_hot_x_is_bit_exact(fmt):
     rows, K = 70, 512
     W = synth.weights(fmt, rows, K, synth.stream(5, fmt))
@@ -118,7 +129,7 @@ def test_q4_k_zero_scales_and_mins():
     assert y[0] == 0.0 and y[6] == 0.0     # sc = 0 and m = 0
 
 
-@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K])
+@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K, oracle.FORMAT_Q6_K])
 def test_repeat_runs_are_bitwise_identical(fmt):
     rows, K = 3001, 5376 if fmt != oracle.FORMAT_Q4_0 else 4096
     W = synth.weights(fmt, rows, K, synth.stream(8, 0))

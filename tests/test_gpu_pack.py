@@ -13,7 +13,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("fmt,rows,K", [(0, 1, 32), (0, 37, 4096), (1, 5, 96), (1, 300, 5376),
-                                        (2, 1, 256), (2, 77, 5376)])
+                                        (2, 1, 256), (2, 77, 5376), (3, 1, 256), (3, 77, 5376)])
 def test_pack_unpack_round_trip(fmt, rows, K):
     t = torch()
     W = synth.weights(fmt, rows, K, synth.stream(600 + fmt, rows))
@@ -40,12 +40,25 @@ def _decode_packed_host(fmt, P, rows, K):
         u = P[:rows * nb * 32].reshape(rows, nb, 32).astype(np.int64)
         d = P[rows * nb * 32:].copy().view(np.float16).reshape(rows, nb).astype(np.float64)
         return ((u - 128) * d[:, :, None]).reshape(rows, K)
+    if fmt == oracle.FORMAT_Q6_K:
+        ns = K // 256
+        lo = P[:rows * ns * 128].reshape(rows, ns, 128)
+        hi = P[rows * ns * 128:rows * ns * 192].reshape(rows, ns, 64)
+        rec = P[rows * ns * 192:].reshape(rows, ns, 18)
+        q = np.empty((rows, ns, 256), np.int64)
+        q[:, :, 0::2] = lo & 15
+        q[:, :, 1::2] = lo >> 4
+        for k in range(4):
+            q[:, :, k::4] |= ((hi >> (2 * k)) & 3).astype(np.int64) << 4
+        sc = rec[:, :, :16].copy().view(np.int8).astype(np.float64)
+        d = rec[:, :, 16:18].copy().view(np.float16).reshape(rows, ns).astype(np.float64)
+        return (d[:, :, None] * np.repeat(sc, 16, axis=2) * (q - 32)).reshape(rows, K)
     raise ValueError(fmt)
 
 
-@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0])
+@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q6_K])
 def test_packed_layout_is_as_documented(fmt):
-    rows, K = 9, 160
+    rows, K = 9, (512 if fmt == oracle.FORMAT_Q6_K else 160)
     W = synth.weights(fmt, rows, K, synth.stream(610, fmt))
     P = packed(fmt, W, rows, K).cpu().numpy()
     assert np.array_equal(_decode_packed_host(fmt, P, rows, K), oracle.dequant(fmt, W, K))
