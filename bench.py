@@ -436,10 +436,7 @@ def run_gpu(wl_cls, args, rank, world, torch, dist):
         sampler.stop()
         clocks = sampler.summary(t0, t1)
 
-    if dist is not None:
-        tt = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, dist, "cuda")
 
     # end to end through the public API with host buffers (default workload only)
     e2e = None
@@ -457,6 +454,22 @@ def run_gpu(wl_cls, args, rank, world, torch, dist):
                "h2d_bytes_per_step": wl.h2d, "d2h_bytes_per_step": wl.d2h,
                "ms_per_step": round(e2e_ms, 4)}
     return wl, ms, clocks, e2e
+
+
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time: the job ends when its last rank does."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step, ms_per_step, world):
+    """Whole-job rate (weak scaling): the units every rank processed in one
+    step, over the slowest rank's step time."""
+    return units_per_rank_step * world / (ms_per_step * 1e-3)
 
 
 def cpu_baseline(wl_cls, sample_rows):
@@ -511,7 +524,7 @@ def main():
         ms_step = ms / args.steps
         sec = ms_step * 1e-3
         if wl.bound == "tensor":
-            value = wl.ops_per_step / sec / 1e12 * world
+            value = job_throughput(wl.ops_per_step, ms_step, world) / 1e12
             unit = "TOPS"
             achieved = wl.ops_per_step / sec / 1e12
             roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16, "unit": "TFLOP/s",
@@ -519,7 +532,7 @@ def main():
                     "peak_source": f"{peak_src} bf16 dense (f16 MMAs run at the same rate; achieved counts "
                                    "useful ops, the exact f16-piece products make the tensor pipe do 3x that)"}
         else:
-            value = wl.bytes_per_step / sec / 1e9 * world
+            value = job_throughput(wl.bytes_per_step, ms_step, world) / 1e9
             unit = "GB/s"
             roof = {"bound": "hbm", "achieved": round(wl.bytes_per_step / sec / 1e9, 2), "peak": hbm,
                     "unit": "GB/s", "frac": round(wl.bytes_per_step / sec / 1e9 / hbm, 4),
