@@ -64,6 +64,7 @@ def _declare(L):
         "gq_q4_0_gemm_q8act": ([P, P, P, P, P, S, I, I, I, P], I),
         "gq_q4_0_gemm_block_dots": ([P, P, P, P, S, I, I, I, P], I),
         "gq_device_status": ([I], I),
+        "gq_selftest_bounded_wait": ([P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -186,6 +187,10 @@ def gq_q4_0_gemm_q8act(W, Xq, dx, Y, workspace, workspace_bytes, rows, K, M, str
 def gq_q4_0_gemm_block_dots(W, Xq, D, workspace, workspace_bytes, rows, K, M, stream=None):
     _check(lib().gq_q4_0_gemm_block_dots(_ptr(W), _ptr(Xq), _ptr(D), _ptr(workspace), int(workspace_bytes),
                                          rows, K, M, _stream(stream)), "gq_q4_0_gemm_block_dots")
+
+
+def gq_selftest_bounded_wait(stream=None):
+    _check(lib().gq_selftest_bounded_wait(_stream(stream)), "gq_selftest_bounded_wait")
 
 
 def gq_device_status(reset: bool = True) -> int:

@@ -196,4 +196,9 @@ int gq_q4_0_gemm_block_dots(const void *W, const int8_t *Xq, int32_t *D, void *w
 
 int gq_device_status(int reset) { return read_device_status(reset != 0); }
 
+int gq_selftest_bounded_wait(gq_stream_t stream)
+{
+    return launch_selftest_bounded_wait(reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -123,6 +123,7 @@ int launch_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K,
 int launch_q8_0_matvec(const void *W, const float *x, float *y, int rows, int K, MatvecGeo g,
                        cudaStream_t s);
 int launch_q6k_matvec(const void *W, const float *x, float *y, int rows, int K, cudaStream_t s);
+int launch_selftest_bounded_wait(cudaStream_t s);
 int launch_q4k_matvec(const void *W, const float *x, float *y, int rows, int K, MatvecGeo g,
                       cudaStream_t s);
 int launch_ffn_gate_up(const void *Wg, const void *Wu, const float *x, float *h, int rows, int K,

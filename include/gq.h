@@ -235,6 +235,14 @@ int gq_q4_0_gemm_block_dots(const void *W, const int8_t *Xq, int32_t *D, void *w
  * ------------------------------------------------------------------------ */
 int gq_device_status(int reset);
 
+/* Self-check of the bounded-wait path of the tensor-core kernels: launches
+ * one CTA whose thread waits, with the kernels' wait helper and time limit
+ * (about 2 s), on an mbarrier phase that nothing completes.  The wait gives
+ * up, records GQ_ERR_TIMEOUT in the device status (read it with
+ * gq_device_status) and the kernel returns normally; the context stays
+ * usable.  Returns the launch status.  For tests. */
+int gq_selftest_bounded_wait(gq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
