@@ -25,6 +25,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -55,18 +56,51 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def kernel_source_hash():
+_CSRC = os.path.join(ROOT, "block_quantized_matvec_gq_gb300", "csrc")
+_INCLUDE = os.path.join(ROOT, "include")
+
+
+def _kernel_unit(kernel: str):
+    """The csrc translation unit that defines the __global__ function `kernel`."""
+    pat = re.compile(r"__global__[^;{]*?\b" + re.escape(kernel) + r"\s*\(", re.S)
+    for name in sorted(os.listdir(_CSRC)):
+        if name.endswith(".cu"):
+            with open(os.path.join(_CSRC, name)) as f:
+                if pat.search(f.read()):
+                    return os.path.join(_CSRC, name)
+    return None
+
+
+def kernel_source_hash(kernel: str):
+    """Digest of the sources a kernel's machine code depends on: its
+    translation unit and every file it includes, transitively, from csrc/
+    and include/ (None if no unit defines it)."""
+    unit = _kernel_unit(kernel)
+    if unit is None:
+        return None
+    seen, todo = set(), [unit]
+    while todo:
+        p = todo.pop()
+        if p in seen:
+            continue
+        seen.add(p)
+        with open(p) as f:
+            for inc in re.findall(r'^\s*#\s*include\s*"([^"]+)"', f.read(), re.M):
+                for d in (os.path.dirname(p), _CSRC, _INCLUDE):
+                    q = os.path.join(d, inc)
+                    if os.path.exists(q):
+                        todo.append(os.path.normpath(q))
+                        break
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "block_quantized_matvec_gq_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode())
+    for p in sorted(seen):
+        h.update(os.path.relpath(p, ROOT).encode())
+        with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
     sources are unchanged since the capture; otherwise None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
@@ -74,7 +108,8 @@ def recorded_traffic(kernel: str, workload: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload)
-    if not e or e.get("kernel") != kernel or e.get("source_hash") != kernel_source_hash():
+    h = kernel_source_hash(kernel)
+    if not e or e.get("kernel") != kernel or h is None or e.get("source_hash") != h:
         return None
     return e.get("dram_bytes_per_launch")
 
