@@ -76,6 +76,8 @@ def lib():
         L.gqo_softcap.restype = ctypes.c_double
         L.gqo_ffn_gate_up.argtypes = [P, P, I64, I64, P, P, I64, P, P, P, P, P]
         L.gqo_ffn_gate_up.restype = ctypes.c_int
+        L.gqo_geglu_down.argtypes = [ctypes.c_int, P, I64, I64, P, P, P, I64, P, P, P]
+        L.gqo_geglu_down.restype = ctypes.c_int
         L.gqo_topk.argtypes = [P, I64, I64, P, P]
         L.gqo_topk.restype = ctypes.c_int
         L.gqo_quantize_q8_0.argtypes = [P, I64, I64, P, P]
@@ -156,6 +158,21 @@ def ffn_gate_up(Wg, Wu, x, rows: int, K: int, row_idx=None):
     if rc != 0:
         raise ValueError("oracle ffn rejected the shape")
     return out
+
+
+def geglu_down(fmt: int, W, g, u, rows: int, K: int, row_idx=None):
+    """(y, a, b) float64 for the selected rows: y = W h with h = gelu_tanh(g) * u,
+    a = sum |w h|, b = sum |w| (|g u| + |h|)."""
+    W = _c(W, np.uint8)
+    g = _c(g, np.float32)
+    u = _c(u, np.float32)
+    idx = None if row_idx is None else _c(row_idx, np.int64)
+    n = rows if idx is None else idx.size
+    y, a, b = (np.empty(n, dtype=np.float64) for _ in range(3))
+    rc = lib().gqo_geglu_down(fmt, _ptr(W), rows, K, _ptr(g), _ptr(u), _ptr(idx), n, _ptr(y), _ptr(a), _ptr(b))
+    if rc != 0:
+        raise ValueError("oracle geglu_down rejected the shape")
+    return y, a, b
 
 
 def topk(values: np.ndarray, k: int):

@@ -263,6 +263,53 @@ int gqo_ffn_gate_up(const uint8_t *Wg, const uint8_t *Wu, int64_t rows, int64_t 
     return rc;
 }
 
+/* Down projection of a gated GELU FFN with the gate applied to its input
+ * ([LARQL] section 4: the fused GELU-tanh down kernels, which take the gate
+ * and up vectors; finding F1: the tanh argument is clamped, as
+ * gqo_gelu_tanh does):
+ *   h_j = gelu_tanh(g_j) * u_j,   y_i = sum_j w_ij h_j   (double, ascending j)
+ * for the selected rows, with the tolerance scales
+ *   a_i = sum_j |w_ij h_j|,   b_i = sum_j |w_ij| (|g_j u_j| + |h_j|)
+ * (a or b may be NULL).  Returns 0, or -1 as gqo_matvec. */
+int gqo_geglu_down(int fmt, const uint8_t *W, int64_t rows, int64_t K, const float *g,
+                   const float *u, const int64_t *row_idx, int64_t n_sel, double *y, double *a,
+                   double *b)
+{
+    int64_t rb = row_bytes(fmt, K);
+    if (rb < 0 || K <= 0 || K % ((fmt == GQO_Q4_K || fmt == GQO_Q6_K) ? 256 : 32) != 0)
+        return -1;
+    (void)rows;
+    double *h = (double *)malloc(sizeof(double) * (size_t)K);
+    double *e = (double *)malloc(sizeof(double) * (size_t)K);
+    for (int64_t j = 0; j < K; ++j) {
+        h[j] = gqo_gelu_tanh((double)g[j]) * (double)u[j];
+        e[j] = fabs((double)g[j] * (double)u[j]) + fabs(h[j]);
+    }
+#pragma omp parallel
+    {
+        double *w = (double *)malloc(sizeof(double) * (size_t)K);
+#pragma omp for schedule(static)
+        for (int64_t i = 0; i < n_sel; ++i) {
+            int64_t r = row_idx ? row_idx[i] : i;
+            dequant_row(fmt, W + r * rb, K, w);
+            double acc = 0.0, aacc = 0.0, bacc = 0.0;
+            for (int64_t j = 0; j < K; ++j) {
+                double p = w[j] * h[j];
+                acc += p;
+                aacc += fabs(p);
+                bacc += fabs(w[j]) * e[j];
+            }
+            y[i] = acc;
+            if (a) a[i] = aacc;
+            if (b) b[i] = bacc;
+        }
+        free(w);
+    }
+    free(h);
+    free(e);
+    return 0;
+}
+
 /* ---- top-k ------------------------------------------------------------- */
 
 typedef struct {

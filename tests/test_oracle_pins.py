@@ -445,6 +445,96 @@ def test_ffn_gate_up_combines_two_matvecs():
         assert out["h"][i] == oracle.gelu_tanh(g[i]) * u[i]
 
 
+# ---------------------------------------------------------------- GELU-gated down projection
+
+def _matrix(fmt, rows, K, seed):
+    rng = np.random.default_rng(seed)
+    if fmt == oracle.FORMAT_Q4_0:
+        W, dense, _, _ = be.random_q4_0_matrix(rows, K, rng)
+    elif fmt == oracle.FORMAT_Q4_K:
+        W, dense = be.random_q4_k_matrix(rows, K, rng)
+    else:
+        W, dense = be.random_q6_k_matrix(rows, K, rng)
+    return W, dense
+
+
+def test_geglu_down_zero_gate_or_zero_up_gives_zero():
+    rows, K = 5, 256
+    W, _ = _matrix(oracle.FORMAT_Q4_0, rows, K, 40)
+    rng = np.random.default_rng(41)
+    v = rng.standard_normal(K).astype(np.float32)
+    z = np.zeros(K, np.float32)
+    for g, u in ((v, z), (z, v)):
+        y, a, b = oracle.geglu_down(oracle.FORMAT_Q4_0, W, g, u, rows, K)
+        assert np.all(y == 0.0) and np.all(a == 0.0)
+
+
+@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q4_K, oracle.FORMAT_Q6_K])
+def test_geglu_down_one_hot_up_gives_a_gated_column(fmt):
+    # u = e_j: one nonzero term, y_i = w_ij gelu(g_j) exactly.  The gate, not
+    # the up value, goes through GELU (gelu(2.5) * 1 != gelu(1) * 2.5), and
+    # the other gate values must not leak in.
+    rows, K = 3, 512
+    W, dense = _matrix(fmt, rows, K, 42 + fmt)
+    g = np.random.default_rng(43).standard_normal(K).astype(np.float32) * 4
+    for j in (0, 1, 31, 32, 255, 256, 511):
+        for c in (2.5, -0.75, 9.0):
+            gg = g.copy()
+            gg[j] = c
+            u = np.zeros(K, np.float32)
+            u[j] = 1.0
+            y, a, b = oracle.geglu_down(fmt, W, gg, u, rows, K)
+            gel = oracle.gelu_tanh(c)
+            assert np.array_equal(y, dense[:, j] * gel)
+            assert np.array_equal(a, np.abs(dense[:, j] * gel))
+            assert np.array_equal(b, np.abs(dense[:, j]) * (abs(c) + abs(gel)))
+
+
+def test_geglu_down_clamped_gate_is_a_scaled_matvec():
+    # For a >= 6 the clamp holds the tanh argument at 15, so
+    # gelu(a) = a (1 + tanh(15)) / 2 and y = gelu(a) * (W u).
+    rows, K = 7, 1024
+    W, _ = _matrix(oracle.FORMAT_Q4_0, rows, K, 44)
+    u = np.random.default_rng(45).standard_normal(K).astype(np.float32)
+    g = np.full(K, 8.0, np.float32)
+    y, a, _ = oracle.geglu_down(oracle.FORMAT_Q4_0, W, g, u, rows, K)
+    ymv, amv = oracle.matvec(oracle.FORMAT_Q4_0, W, u, rows, K)
+    s = 8.0 * (1.0 + math.tanh(15.0)) / 2.0
+    assert np.all(np.abs(y - s * ymv) <= 1e-13 * s * amv)
+    assert np.all(np.abs(a - s * amv) <= 1e-13 * s * amv)
+
+
+@pytest.mark.parametrize("fmt,K", [(oracle.FORMAT_Q4_0, 64), (oracle.FORMAT_Q4_K, 256), (oracle.FORMAT_Q6_K, 256)])
+def test_geglu_down_brute_force_exact_rational(fmt, K):
+    # h_j = gelu(g_j) u_j as one double product; the sum over j then checked
+    # exactly with rationals.
+    W, dense = _matrix(fmt, 2, K, 46 + fmt)
+    rng = np.random.default_rng(47)
+    g = (rng.standard_normal(K) * 3).astype(np.float32)
+    u = rng.standard_normal(K).astype(np.float32)
+    y, a, _ = oracle.geglu_down(fmt, W, g, u, 2, K)
+    h = [oracle.gelu_tanh(float(gv)) * float(uv) for gv, uv in zip(g, u)]
+    for r in range(2):
+        exact = sum(Fraction(float(w)) * Fraction(hv) for w, hv in zip(dense[r], h))
+        absum = sum(abs(Fraction(float(w)) * Fraction(hv)) for w, hv in zip(dense[r], h))
+        assert abs(Fraction(y[r]) - exact) <= Fraction(K) * Fraction(2) ** -52 * absum
+        assert abs(Fraction(a[r]) - absum) <= Fraction(K) * Fraction(2) ** -52 * absum
+
+
+def test_geglu_down_row_selection_and_partial_blocks():
+    rows, K = 9, 256
+    W, _ = _matrix(oracle.FORMAT_Q4_0, rows, K, 48)
+    rng = np.random.default_rng(49)
+    g, u = (rng.standard_normal(K).astype(np.float32) for _ in range(2))
+    y, a, b = oracle.geglu_down(oracle.FORMAT_Q4_0, W, g, u, rows, K)
+    idx = np.array([8, 0, 3, 3])
+    ys, as_, bs = oracle.geglu_down(oracle.FORMAT_Q4_0, W, g, u, rows, K, row_idx=idx)
+    assert np.array_equal(ys, y[idx]) and np.array_equal(as_, a[idx]) and np.array_equal(bs, b[idx])
+    with pytest.raises(ValueError):
+        oracle.geglu_down(oracle.FORMAT_Q4_0, np.zeros(18, np.uint8), np.zeros(48, np.float32),
+                          np.zeros(48, np.float32), 1, 48)
+
+
 # ---------------------------------------------------------------- planted mistakes are caught
 
 def test_planted_nibble_order_mistake_is_caught_by_golden_fixture():
