@@ -326,6 +326,34 @@ class Q6KMatvec(Rotating):
         self.gq.gq_q6k_matvec(self.copies[i % len(self.copies)], self.x, self.y, self.rows, self.K)
 
 
+class GegluDown(Rotating):
+    """The FFN's down projection (5376 x 21504, Q4_0) taking the gate and up
+    outputs, with gelu_tanh(g) * u formed while the input is staged."""
+    name = "q4_0_geglu_down_5376x21504"
+    kernel = "k_q4_0_matvec"
+    rows, K = 5376, 21504
+
+    def setup(self, torch, gq):
+        W = synth.q4_0_weights(self.rows, self.K, synth.stream(7, 0))
+        g = (synth.normal(self.K, synth.stream(7, 1)) * 2).astype(np.float32)
+        u = synth.normal(self.K, synth.stream(7, 2))
+        nbytes = gq.gq_packed_bytes(0, self.rows, self.K)
+        R = self._rotate(torch, nbytes)
+        Wp = gq.pack(0, _to_dev(torch, W.reshape(-1)), self.rows, self.K)
+        self.copies = [Wp] + [Wp.clone() for _ in range(R - 1)]
+        self.g = _to_dev(torch, g)
+        self.u = _to_dev(torch, u)
+        self.y = torch.empty(self.rows, dtype=torch.float32, device="cuda")
+        self.gq = gq
+        self.bytes_per_step = nbytes + 2 * 4 * self.K + 4 * self.rows
+        self.weight_bytes = nbytes
+        self.working_set = nbytes * R
+        self.l2_policy = f"{R} rotating weight copies ({nbytes * R / 2**20:.0f} MiB > 4x L2)"
+
+    def step(self, i):
+        self.gq.gq_q4_0_geglu_down(self.copies[i % len(self.copies)], self.g, self.u, self.y, self.rows, self.K)
+
+
 class FFN(Rotating):
     name = "q4_0_ffn_gelu_21504x5376"
     kernel = "k_ffn_gate_up"
@@ -401,7 +429,7 @@ class GemmSmallBatch32(GemmSmallBatch8):
     M = 32
 
 
-WORKLOADS = {w.name: w for w in (LogitsTopK, Q40Matvec, Q4KMatvec, Q6KMatvec, FFN, Gemm, GemmSmallBatch8,
+WORKLOADS = {w.name: w for w in (LogitsTopK, Q40Matvec, Q4KMatvec, Q6KMatvec, FFN, GegluDown, Gemm, GemmSmallBatch8,
                                   GemmSmallBatch32)}
 
 

@@ -56,6 +56,7 @@ def _declare(L):
         "gq_q4k_matvec": ([P, P, P, I, I, I, P], I),
         "gq_q6k_matvec": ([P, P, P, I, I, I, P], I),
         "gq_ffn_gate_up_gelu": ([P, P, P, P, I, I, I, P], I),
+        "gq_q4_0_geglu_down": ([P, P, P, P, I, I, I, P], I),
         "gq_logits_topk_workspace_bytes": ([I, I, I], S),
         "gq_logits_topk": ([P, P, ctypes.c_float, I, P, P, P, P, S, I, I, I, P], I),
         "gq_logits_topk_noalloc": ([P, P, ctypes.c_float, I, P, P, P, I, I, I, P], I),
@@ -118,7 +119,7 @@ def _check(status: int, what: str):
         raise GQError(status, what)
 
 
-# ---------------------------------------------------------------- entry points (same names as gq.h)
+# ---------------------------------------------------------------- entry points (same names as gq.h, gq_geglu.h)
 
 def gq_packed_bytes(format: int, rows: int, K: int) -> int:
     return int(lib().gq_packed_bytes(format, rows, K))
@@ -151,6 +152,11 @@ def gq_q6k_matvec(W, x, y, rows, K, M=1, stream=None):
 def gq_ffn_gate_up_gelu(W_gate, W_up, x, h, rows, K, M=1, stream=None):
     _check(lib().gq_ffn_gate_up_gelu(_ptr(W_gate), _ptr(W_up), _ptr(x), _ptr(h), rows, K, M,
                                      _stream(stream)), "gq_ffn_gate_up_gelu")
+
+
+def gq_q4_0_geglu_down(W_down, g, u, y, rows, K, M=1, stream=None):
+    _check(lib().gq_q4_0_geglu_down(_ptr(W_down), _ptr(g), _ptr(u), _ptr(y), rows, K, M, _stream(stream)),
+           "gq_q4_0_geglu_down")
 
 
 def gq_logits_topk_workspace_bytes(rows, K, k) -> int:

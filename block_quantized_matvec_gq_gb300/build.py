@@ -39,7 +39,7 @@ def _sources():
 
 def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + [
-        os.path.join(INCLUDE, "gq.h"), os.path.abspath(__file__)]
+        os.path.abspath(__file__)] + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
 def up_to_date() -> bool:

@@ -5,9 +5,16 @@
 // F6, F17: a silent no-op or a silently truncated K is a defect.  Every
 // entry point here rejects what its kernels cannot compute exactly, before
 // launching anything.
+#include "gq_geglu.h"
 #include "gq_host.h"
 
 using namespace gq;
+
+namespace gq {
+// gq_q4_0.cu: the Q4_0 matvec staging gelu_tanh(g) * u as its input vector
+int launch_q4_0_geglu_down(const void *W, const float *g, const float *u, float *y, int rows, int K, MatvecGeo geo,
+                           cudaStream_t s);
+}  // namespace gq
 
 namespace {
 
@@ -126,6 +133,18 @@ int gq_ffn_gate_up_gelu(const void *W_gate, const void *W_up, const float *x, fl
     if (st != GQ_OK) return st;
     return launch_ffn_gate_up(W_gate, W_up, x, h, rows, K, choose_ffn_geo(rows, K / 32, aligned32(W_gate) && aligned32(W_up)),
                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gq_q4_0_geglu_down(const void *W_down, const float *g, const float *u, float *y, int rows, int K, int M,
+                       gq_stream_t stream)
+{
+    if (!u) return GQ_ERR_NULL;
+    int st = check_matvec(GQ_FORMAT_Q4_0, W_down, g, y, rows, K, M);
+    if (st != GQ_OK) return st;
+    if (!aligned16(u)) return GQ_ERR_ALIGN;
+    return launch_q4_0_geglu_down(W_down, g, u, y, rows, K,
+                                  choose_matvec_geo(GQ_FORMAT_Q4_0, rows, K / 32, aligned32(W_down)),
+                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t gq_logits_topk_workspace_bytes(int rows, int K, int k)

@@ -5,18 +5,58 @@
 // accumulation.  "Metal kernel capability table (Phase B ground truth)",
 // section 1, q4_f32_matvec (rows masked; here K is never truncated).
 //
-// Persistent kernel: each CTA stages x once (padded 144-byte blocks), then its
-// warps stream packed Q4_0 rows (16-byte nibble loads + fp16 scales); see
-// gq_matvec.cuh for the lane geometry and the exact nibble-to-f32 step.
+// Persistent kernel: each CTA stages its input vector once (padded 144-byte
+// blocks), then its warps stream packed Q4_0 rows (16-byte nibble loads +
+// fp16 scales); see gq_matvec.cuh for the lane geometry and the exact
+// nibble-to-f32 step.
+//
+// The input vector is x itself, or -- the down projection of a gated GELU
+// FFN with the gate applied while the input is read ("Metal kernel
+// capability table (Phase B ground truth)", section 4, the fused GELU-tanh
+// down kernels that take the gate and up vectors) -- h = gelu_tanh(g) * u,
+// formed in f32 as the vector is staged, with the tanh argument clamped to
+// +-15 (finding F1: the pages' fused kernels lacked the clamp their
+// separated twins carry, and gave NaN for large gate values).
 #include "gq_host.h"
 #include "gq_matvec.cuh"
 
 namespace gq {
 
-template <int LG, int R, int U, int kMode>
+// Input: x.
+struct InX {
+    const float *__restrict__ x;
+    __device__ __forceinline__ void stage(float *xs, int K) const { stage_x_q4<false>(xs, x, K); }
+};
+
+// Input: gelu_tanh(g) * u, in the staged layout of stage_x_q4 (8-element
+// group i at block i / 4, offset 8 (i % 4), as elements 0,4,1,5 | 2,6,3,7).
+// All threads of the CTA take part; ends with a CTA barrier.
+struct InGeglu {
+    const float *__restrict__ g;
+    const float *__restrict__ u;
+    __device__ __forceinline__ void stage(float *xs, int K) const
+    {
+        for (int i = threadIdx.x; i < (K >> 3); i += blockDim.x) {
+            const float4 g0 = *reinterpret_cast<const float4 *>(g + 8 * i);
+            const float4 g1 = *reinterpret_cast<const float4 *>(g + 8 * i + 4);
+            const float4 u0 = *reinterpret_cast<const float4 *>(u + 8 * i);
+            const float4 u1 = *reinterpret_cast<const float4 *>(u + 8 * i + 4);
+            const float4 a = make_float4(gelu_tanh(g0.x) * u0.x, gelu_tanh(g0.y) * u0.y, gelu_tanh(g0.z) * u0.z,
+                                         gelu_tanh(g0.w) * u0.w);
+            const float4 b = make_float4(gelu_tanh(g1.x) * u1.x, gelu_tanh(g1.y) * u1.y, gelu_tanh(g1.z) * u1.z,
+                                         gelu_tanh(g1.w) * u1.w);
+            float *dst = xs + (i >> 2) * kXBlk + 8 * (i & 3);
+            *reinterpret_cast<float4 *>(dst) = make_float4(a.x, b.x, a.y, b.y);
+            *reinterpret_cast<float4 *>(dst + 4) = make_float4(a.z, b.z, a.w, b.w);
+        }
+        __syncthreads();
+    }
+};
+
+template <int LG, int R, int U, int kMode, class In>
 __global__ void __launch_bounds__(kThreadsPerCta, 2)
-    k_q4_0_matvec(const uint4 *__restrict__ nib, const uint16_t *__restrict__ dsc,
-                  const float *__restrict__ x, float *__restrict__ y, int rows, int nb)
+    k_q4_0_matvec(const uint4 *__restrict__ nib, const uint16_t *__restrict__ dsc, In in, float *__restrict__ y,
+                  int rows, int nb)
 {
     extern __shared__ __align__(16) float xs[];
     constexpr int G = 32 / LG, TR = G * R;
@@ -54,7 +94,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
             /* no early loads in this mode */
         }
         pdl_wait();
-        stage_x_q4<false>(xs, x, nb * 32);
+        in.stage(xs, nb * 32);
         pdl_launch_dependents();
 
         for (int task = first; task < ntasks; task += stride) {
@@ -95,7 +135,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
             if (kEarly) setup(cr.start, 0, nb);
         }
         pdl_wait();
-        stage_x_q4<false>(xs, x, nb * 32);
+        in.stage(xs, nb * 32);
         pdl_launch_dependents();
 
         for (int j = 0; j < cr.count; ++j) {
@@ -133,8 +173,8 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     }
 }
 
-int launch_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K, MatvecGeo geo,
-                       cudaStream_t s)
+template <class In>
+static int launch_q4_0(const void *W, In in, float *y, int rows, int K, MatvecGeo geo, cudaStream_t s)
 {
     const int nb = K / 32;
     const uint4 *nib = static_cast<const uint4 *>(W);
@@ -144,22 +184,33 @@ int launch_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K,
     if (geo.p != 1) return GQ_ERR_SHAPE;
 #define CASE(LG, R, U)                                                                                  \
     {                                                                                                   \
-        auto rr = k_q4_0_matvec<LG, R, U, 0>;                                                                     \
+        auto rr = k_q4_0_matvec<LG, R, U, 0, In>;                                                                     \
         int grid = persistent_grid(reinterpret_cast<const void *>(rr), kThreadsPerCta, smem, ntasks);  \
         if (grid <= 0) return GQ_ERR_SHAPE;                                                             \
         /* tasks per warp: < 1.75 balanced schedule, <= 1.25 also first loads early */                 \
         const long long w5 = static_cast<long long>(grid) * kWarpsPerCta;                               \
         const int mode = ntasks * 4 <= w5 * 5 ? 2 : (ntasks * 4 < w5 * 7 ? 1 : 0);                      \
-        auto kern = mode == 2 ? k_q4_0_matvec<LG, R, U, 2> : (mode == 1 ? k_q4_0_matvec<LG, R, U, 1> : rr);                 \
+        auto kern = mode == 2 ? k_q4_0_matvec<LG, R, U, 2, In> : (mode == 1 ? k_q4_0_matvec<LG, R, U, 1, In> : rr);                 \
         if (mode != 0) { /* size through the launched instantiation too (raises its shared-memory limit) */ \
             const int g2 = persistent_grid(reinterpret_cast<const void *>(kern), kThreadsPerCta, smem, ntasks); \
             if (g2 <= 0) return GQ_ERR_SHAPE;                                                           \
             if (g2 < grid) grid = g2;                                                                   \
         }                                                                                               \
-        return status_from(launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, nib, dsc, x, y, rows, nb));       \
+        return status_from(launch_pdl(kern, dim3(grid), dim3(kThreadsPerCta), smem, s, nib, dsc, in, y, rows, nb));       \
     }
     GQ_GEO_SWITCH_R12(geo, CASE);
 #undef CASE
+}
+
+int launch_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K, MatvecGeo geo, cudaStream_t s)
+{
+    return launch_q4_0(W, InX{x}, y, rows, K, geo, s);
+}
+
+int launch_q4_0_geglu_down(const void *W, const float *g, const float *u, float *y, int rows, int K, MatvecGeo geo,
+                           cudaStream_t s)
+{
+    return launch_q4_0(W, InGeglu{g, u}, y, rows, K, geo, s);
 }
 
 }  // namespace gq

@@ -1,5 +1,6 @@
 """Host-side checks of the C ABI (no GPU needed): the library loads, exports
-every function gq.h declares, and rejects bad arguments before launching."""
+every function include/*.h declares, and rejects bad arguments before
+launching."""
 
 import ctypes
 import os
@@ -20,7 +21,8 @@ def lib():
 
 
 def declared_functions():
-    src = open(os.path.join(ROOT, "include", "gq.h")).read()
+    inc = os.path.join(ROOT, "include")
+    src = "".join(open(os.path.join(inc, n)).read() for n in sorted(os.listdir(inc)) if n.endswith(".h"))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(gq_[a-z0-9_]+)\s*\(", src)))
 
@@ -87,6 +89,22 @@ def test_matvec_argument_validation(lib):
     assert call("gq_q6k_matvec", A, A, A, 4, 288, 1, None) == gq.GQ_ERR_SHAPE
     assert call("gq_q8_0_matvec", A + 16, A, A, 4, 256, 1, None) == gq.GQ_ERR_ALIGN   # needs 32 B
     assert call("gq_q4_0_matvec", A + 16, None, A, 4, 256, 1, None) == gq.GQ_ERR_NULL
+
+
+def test_geglu_down_validation(lib):
+    name = "gq_q4_0_geglu_down"
+    assert call(name, None, A, A, A, 4, 256, 1, None) == gq.GQ_ERR_NULL
+    assert call(name, A, None, A, A, 4, 256, 1, None) == gq.GQ_ERR_NULL
+    assert call(name, A, A, None, A, 4, 256, 1, None) == gq.GQ_ERR_NULL
+    assert call(name, A, A, A, None, 4, 256, 1, None) == gq.GQ_ERR_NULL
+    assert call(name, U, A, A, A, 4, 256, 1, None) == gq.GQ_ERR_ALIGN
+    assert call(name, A, U, A, A, 4, 256, 1, None) == gq.GQ_ERR_ALIGN
+    assert call(name, A, A, U, A, 4, 256, 1, None) == gq.GQ_ERR_ALIGN
+    assert call(name, A, A, A, U, 4, 256, 1, None) == gq.GQ_ERR_ALIGN
+    assert call(name, A, A, A, A, 0, 256, 1, None) == gq.GQ_ERR_SHAPE
+    assert call(name, A, A, A, A, 4, 256 + 16, 1, None) == gq.GQ_ERR_SHAPE   # not whole blocks (F16)
+    assert call(name, A, A, A, A, 4, 256, 2, None) == gq.GQ_ERR_SHAPE
+    assert call(name, A, A, A, A, 4, gq.GQ_MAX_K + 32, 1, None) == gq.GQ_ERR_SHAPE
 
 
 def test_ffn_logits_quant_gemm_pack_validation(lib):
