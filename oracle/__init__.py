@@ -1,4 +1,6 @@
-"""ctypes wrapper for the plain-C fp64 oracle (gq_oracle.c).
+"""ctypes wrapper for the plain-C fp64 oracle (gq_oracle.c), and the RMS
+norm, written here in numpy: its sum of squares is math.fsum, the correctly
+rounded sum, and its other steps are single IEEE operations.
 
 TEST INFRASTRUCTURE: only the test suite, the smoke check and the benchmark's
 CPU-baseline leg may import this package.  It shares no code with the CUDA
@@ -12,6 +14,7 @@ files, which no function here can be checked against).
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import shutil
 import subprocess
@@ -193,6 +196,37 @@ def quantize_q8_0(X: np.ndarray, M: int, K: int):
     if rc != 0:
         raise ValueError("oracle quantize rejected the shape")
     return q, d
+
+
+def rmsnorm(X, w, offset: float, eps: float, M: int, K: int):
+    """RMS normalization of each token's row ("Metal kernel capability table
+    (Phase B ground truth)", section 6: rms_norm scales by the inverse RMS
+    and by (w + offset)), with every rounding fixed so that the Q8 codes
+    that follow are a function of the inputs alone:
+      ss  = sum_j x_j^2 rounded once to double (each x_j^2 is exact in
+            double; math.fsum returns the correctly rounded sum),
+      r   = sqrt(ss / K + eps), in double, each operation rounded,
+      inv = f32(1 / r),
+      y_j = f32(f32(x_j * inv) * f32(w_j + offset)).
+    Returns (y f32[M][K], ss float64[M], r float64[M])."""
+    X = np.ascontiguousarray(X, dtype=np.float32).reshape(M, K)
+    wo = np.ascontiguousarray(w, dtype=np.float32) + np.float32(offset)   # f32 addition
+    y = np.empty((M, K), dtype=np.float32)
+    ss = np.empty(M, dtype=np.float64)
+    r = np.empty(M, dtype=np.float64)
+    for t in range(M):
+        x64 = X[t].astype(np.float64)
+        ss[t] = math.fsum((x64 * x64).tolist())
+        r[t] = math.sqrt(ss[t] / K + float(np.float32(eps)))
+        inv = np.float32(1.0 / r[t])
+        y[t] = (X[t] * inv) * wo        # two f32 multiplications, each rounded
+    return y, ss, r
+
+
+def rmsnorm_quantize_q8_0(X, w, offset: float, eps: float, M: int, K: int):
+    """rmsnorm, then the Q8_0 quantization of its f32 output: (q, d)."""
+    y, _, _ = rmsnorm(X, w, offset, eps, M, K)
+    return quantize_q8_0(y, M, K)
 
 
 def block_dots(W, Xq, rows: int, K: int, M: int, t0: int, nt: int, r0: int, nr: int):

@@ -535,6 +535,80 @@ def test_geglu_down_row_selection_and_partial_blocks():
                           np.zeros(48, np.float32), 1, 48)
 
 
+# ---------------------------------------------------------------- RMS norm (Q8 prologue)
+
+def _wide_rows(K, rng):
+    normal = rng.standard_normal(K)
+    wide = rng.standard_normal(K) * 2.0 ** rng.integers(-140, 120, K)
+    sub = rng.integers(1, 1 << 23, K).astype(np.uint32).view(np.float32).astype(np.float64)   # subnormals
+    spike = np.concatenate([[1.0 + 2.0 ** -23 * rng.integers(0, 1 << 23)], 2.0 ** rng.integers(-149, -20, K - 1)])
+    return [r.astype(np.float32) for r in (normal, wide, sub, spike)]
+
+
+def test_rmsnorm_sum_of_squares_is_the_exact_sum_rounded_once():
+    rng = np.random.default_rng(60)
+    K = 256
+    for x in _wide_rows(K, rng):
+        _, ss, _ = oracle.rmsnorm(x[None], np.zeros(K, np.float32), 1.0, 1e-6, 1, K)
+        exact = sum((Fraction(float(v)) ** 2 for v in x), Fraction(0))
+        assert ss[0] == float(exact)   # float(Fraction) rounds to nearest
+
+
+def test_rmsnorm_closed_form_perfect_square():
+    # x = 3 everywhere and eps = 7: ss / K = 9, r = sqrt(16) = 4, inv = 1/4,
+    # y = 0.75 (w + offset)
+    K = 256
+    X = np.full((1, K), 3.0, np.float32)
+    w = (np.arange(K) % 5 - 2).astype(np.float32)
+    y, ss, r = oracle.rmsnorm(X, w, 1.0, 7.0, 1, K)
+    assert ss[0] == 9.0 * K and r[0] == 4.0
+    assert np.array_equal(y[0], (0.75 * (w + 1.0)).astype(np.float32))
+
+
+def test_rmsnorm_power_of_two_scale_invariance():
+    # eps far below the rounding of ss / K: scaling x by 4 scales ss by 16 and
+    # r by 4 exactly, so y is unchanged bit for bit
+    rng = np.random.default_rng(61)
+    M, K = 3, 512
+    X = rng.standard_normal((M, K)).astype(np.float32)
+    w = rng.standard_normal(K).astype(np.float32)
+    y1, _, r1 = oracle.rmsnorm(X, w, 1.0, 1e-30, M, K)
+    y2, _, r2 = oracle.rmsnorm(X * np.float32(4), w, 1.0, 1e-30, M, K)
+    assert np.array_equal(r2, 4 * r1) and np.array_equal(y1, y2)
+
+
+def test_rmsnorm_against_high_precision_formula():
+    # y_j against x_j (w_j + offset) / sqrt(mean x^2 + eps) in 50-digit
+    # decimals: the fixed roundings (four f32, a few double) stay below
+    # 5 * 2^-24 relative, plus the f32 underflow step (2^-149) of the two
+    # products for elements far below the RMS
+    from decimal import Decimal, getcontext
+    getcontext().prec = 50
+    rng = np.random.default_rng(62)
+    K = 256
+    w = rng.standard_normal(K).astype(np.float32)
+    for x in _wide_rows(K, rng)[:2]:
+        y, _, _ = oracle.rmsnorm(x[None], w, 1.0, 1e-6, 1, K)
+        mean = sum((Decimal(float(v)) ** 2 for v in x), Decimal(0)) / K
+        rms = (mean + Decimal(float(np.float32(1e-6)))).sqrt()
+        for j in range(K):
+            exact = Decimal(float(x[j])) * (Decimal(float(w[j])) + 1) / rms
+            tiny = Decimal(2) ** -149 * (1 + abs(Decimal(float(w[j])) + 1))
+            assert abs(Decimal(float(y[0, j])) - exact) <= abs(exact) * Decimal(5) / Decimal(2 ** 24) + tiny
+
+
+def test_rmsnorm_quantize_is_the_quantizer_on_the_normalized_row():
+    rng = np.random.default_rng(63)
+    M, K = 4, 128
+    X = rng.standard_normal((M, K)).astype(np.float32)
+    w = rng.standard_normal(K).astype(np.float32)
+    q, d = oracle.rmsnorm_quantize_q8_0(X, w, 1.0, 1e-6, M, K)
+    y, _, _ = oracle.rmsnorm(X, w, 1.0, 1e-6, M, K)
+    q2, d2 = oracle.quantize_q8_0(y, M, K)
+    assert np.array_equal(q, q2) and np.array_equal(d, d2)
+    assert np.all(np.abs(q) <= 127) and np.any(np.abs(q) == 127)
+
+
 # ---------------------------------------------------------------- planted mistakes are caught
 
 def test_planted_nibble_order_mistake_is_caught_by_golden_fixture():
