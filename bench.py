@@ -354,6 +354,34 @@ class GegluDown(Rotating):
         self.gq.gq_q4_0_geglu_down(self.copies[i % len(self.copies)], self.g, self.u, self.y, self.rows, self.K)
 
 
+class RMSNormQ8(Rotating):
+    """The prefill activations (512 tokens x 5376) normalized and quantized to
+    Q8_0 in one kernel: X is read, Xq and dx are written."""
+    name = "rmsnorm_q8_0_512x5376"
+    kernel = "k_rmsnorm_q8_0"
+    M, K = 512, 5376
+
+    def setup(self, torch, gq):
+        X = synth.normal((self.M, self.K), synth.stream(8, 0))
+        w = (synth.normal(self.K, synth.stream(8, 1)) * 0.1).astype(np.float32)
+        xbytes = 4 * self.M * self.K
+        R = self._rotate(torch, xbytes)
+        X0 = _to_dev(torch, X)
+        self.copies = [X0] + [X0.clone() for _ in range(R - 1)]
+        self.w = _to_dev(torch, w)
+        self.Xq = torch.empty((self.M, self.K), dtype=torch.int8, device="cuda")
+        self.dx = torch.empty((self.M, self.K // 32), dtype=torch.float32, device="cuda")
+        self.gq = gq
+        self.bytes_per_step = xbytes + 4 * self.K + self.M * self.K + 4 * self.M * (self.K // 32)
+        self.weight_bytes = xbytes
+        self.working_set = xbytes * R
+        self.l2_policy = f"{R} rotating activation copies ({xbytes * R / 2**20:.0f} MiB > 4x L2)"
+
+    def step(self, i):
+        self.gq.gq_rmsnorm_quantize_q8_0(self.copies[i % len(self.copies)], self.w, 1.0, 1e-6, self.Xq, self.dx,
+                                         self.K, self.M)
+
+
 class FFN(Rotating):
     name = "q4_0_ffn_gelu_21504x5376"
     kernel = "k_ffn_gate_up"
@@ -429,8 +457,8 @@ class GemmSmallBatch32(GemmSmallBatch8):
     M = 32
 
 
-WORKLOADS = {w.name: w for w in (LogitsTopK, Q40Matvec, Q4KMatvec, Q6KMatvec, FFN, GegluDown, Gemm, GemmSmallBatch8,
-                                  GemmSmallBatch32)}
+WORKLOADS = {w.name: w for w in (LogitsTopK, Q40Matvec, Q4KMatvec, Q6KMatvec, FFN, GegluDown, RMSNormQ8, Gemm,
+                                  GemmSmallBatch8, GemmSmallBatch32)}
 
 
 # ---------------------------------------------------------------- timing

@@ -61,6 +61,7 @@ def _declare(L):
         "gq_logits_topk": ([P, P, ctypes.c_float, I, P, P, P, P, S, I, I, I, P], I),
         "gq_logits_topk_noalloc": ([P, P, ctypes.c_float, I, P, P, P, I, I, I, P], I),
         "gq_quantize_q8_0": ([P, P, P, I, I, P], I),
+        "gq_rmsnorm_quantize_q8_0": ([P, P, ctypes.c_float, ctypes.c_float, P, P, I, I, P], I),
         "gq_q4_0_gemm_workspace_bytes": ([I, I], S),
         "gq_q4_0_gemm_q8act": ([P, P, P, P, P, S, I, I, I, P], I),
         "gq_q4_0_gemm_block_dots": ([P, P, P, P, S, I, I, I, P], I),
@@ -119,7 +120,7 @@ def _check(status: int, what: str):
         raise GQError(status, what)
 
 
-# ---------------------------------------------------------------- entry points (same names as gq.h, gq_geglu.h)
+# ---------------------------------------------------------------- entry points (same names as include/*.h)
 
 def gq_packed_bytes(format: int, rows: int, K: int) -> int:
     return int(lib().gq_packed_bytes(format, rows, K))
@@ -179,6 +180,11 @@ def gq_logits_topk_noalloc(W, x, softcap, k, idx, val, logits_or_null, rows, K, 
 
 def gq_quantize_q8_0(X, Xq, dx, K, M, stream=None):
     _check(lib().gq_quantize_q8_0(_ptr(X), _ptr(Xq), _ptr(dx), K, M, _stream(stream)), "gq_quantize_q8_0")
+
+
+def gq_rmsnorm_quantize_q8_0(X, w, offset, eps, Xq, dx, K, M, stream=None):
+    _check(lib().gq_rmsnorm_quantize_q8_0(_ptr(X), _ptr(w), float(offset), float(eps), _ptr(Xq), _ptr(dx), K, M,
+                                          _stream(stream)), "gq_rmsnorm_quantize_q8_0")
 
 
 def gq_q4_0_gemm_workspace_bytes(K, M) -> int:

@@ -5,8 +5,11 @@
 // F6, F17: a silent no-op or a silently truncated K is a defect.  Every
 // entry point here rejects what its kernels cannot compute exactly, before
 // launching anything.
+#include <math.h>
+
 #include "gq_geglu.h"
 #include "gq_host.h"
+#include "gq_norm.h"
 
 using namespace gq;
 
@@ -14,6 +17,9 @@ namespace gq {
 // gq_q4_0.cu: the Q4_0 matvec staging gelu_tanh(g) * u as its input vector
 int launch_q4_0_geglu_down(const void *W, const float *g, const float *u, float *y, int rows, int K, MatvecGeo geo,
                            cudaStream_t s);
+// gq_norm.cu: RMS normalization fused with Q8_0 quantization, one CTA per token
+int launch_rmsnorm_q8_0(const float *X, const float *w, float offset, float eps, int8_t *Xq, float *dx, int K,
+                        int M, cudaStream_t s);
 }  // namespace gq
 
 namespace {
@@ -178,6 +184,16 @@ int gq_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, gq_str
     if (!aligned16(X) || !aligned16(Xq) || !aligned16(dx)) return GQ_ERR_ALIGN;
     if (M < 1 || K < 32 || K % 32 != 0) return GQ_ERR_SHAPE;
     return launch_quantize_q8_0(X, Xq, dx, K, M, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gq_rmsnorm_quantize_q8_0(const float *X, const float *w, float offset, float eps, int8_t *Xq, float *dx,
+                             int K, int M, gq_stream_t stream)
+{
+    if (!X || !w || !Xq || !dx) return GQ_ERR_NULL;
+    if (!aligned16(X) || !aligned16(w) || !aligned16(Xq) || !aligned16(dx)) return GQ_ERR_ALIGN;
+    if (M < 1 || K < 32 || K % 32 != 0 || K > GQ_MAX_K) return GQ_ERR_SHAPE;
+    if (!(eps > 0.0f) || !isfinite(eps) || !isfinite(offset)) return GQ_ERR_SHAPE;
+    return launch_rmsnorm_q8_0(X, w, offset, eps, Xq, dx, K, M, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t gq_q4_0_gemm_workspace_bytes(int K, int M)

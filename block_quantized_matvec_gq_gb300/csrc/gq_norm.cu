@@ -1,0 +1,204 @@
+// gq_norm.cu -- RMS normalization fused with the Q8_0 quantization of the
+// normalized activations, one CTA per token.
+//
+// "Metal kernel capability table (Phase B ground truth)", section 6:
+// rms_norm scales a row by 1 / RMS and by (w + offset); rms_norm_q8 fuses
+// the Q8 quantization of the normalized row into the same kernel (there the
+// block scales came out wrong unless the threadgroup size and the row
+// length were multiples of 32; here K % 32 == 0 is required and every
+// 32-block is one group of eight lanes, as in the quantizer).
+//
+// The codes are integers decided by floating point, so the statistic is
+// made a function of the inputs alone, independent of any summation order:
+//   ss  = sum_j x_j^2, rounded once to double
+//   r   = sqrt(ss / K + eps), each double operation rounded to nearest
+//   inv = f32(1 / r)
+//   y_j = f32(f32(x_j * inv) * f32(w_j + offset))
+// followed by the Q8_0 rule of gq_quantize_q8_0 on each 32-block of y.
+//
+// Exact sum of squares: x = m 2^(e - 150) with m the 24-bit significand
+// (e the biased exponent; subnormals take e = 1 and no hidden bit), so
+// x^2 = m^2 2^(2e - 300) with m^2 < 2^48.  Squares with the same e add
+// exactly in a 64-bit integer bucket (K < 2^16 terms), in any order; the
+// buckets then add exactly as B_e << 2(e - 1) into a 608-bit integer, which
+// is rounded once, to nearest even, into the double ss = N 2^-298.
+#include "gq_host.h"
+#include "gq_internal.cuh"
+
+namespace gq {
+namespace norm {
+
+constexpr int kThreads = 256;
+constexpr int kLimbs = 19;  // 32-bit limbs; the largest sum needs 571 bits
+
+// One element's square into its exponent bucket (non-finite values only set
+// a flag: bit 0 for an infinity, bit 1 for a NaN).
+__device__ __forceinline__ void add_square(unsigned long long *bucket, int *nonfinite, float f)
+{
+    const uint32_t b = __float_as_uint(f) & 0x7FFFFFFFu;
+    uint32_t e = b >> 23, m = b & 0x7FFFFFu;
+    if (e == 255u) {
+        atomicOr(nonfinite, m ? 2 : 1);
+        return;
+    }
+    if (e == 0u) {
+        if (m == 0u) return;
+        e = 1u;
+    } else {
+        m |= 0x800000u;
+    }
+    atomicAdd(&bucket[e], static_cast<unsigned long long>(m) * m);
+}
+// sum_e bucket[e] 2^(2e - 300), rounded to nearest even (one thread); occ
+// marks the nonzero buckets (bit e % 32 of occ[e / 32]).
+__device__ double exact_sum(const unsigned long long *bucket, const uint32_t (&occ)[8])
+{
+    uint32_t n[kLimbs];
+    for (int i = 0; i < kLimbs; ++i) n[i] = 0u;
+    for (int wd = 0; wd < 8; ++wd) {
+        for (uint32_t bits = occ[wd]; bits != 0u; bits &= bits - 1u) {
+            const int e = 32 * wd + __ffs(bits) - 1;
+            const unsigned long long B = bucket[e];
+            const int s = 2 * (e - 1), l = s >> 5, o = s & 31;  // B << s spans limbs l .. l + 2
+            const unsigned long long lo = B << o;
+            const uint32_t p[3] = {static_cast<uint32_t>(lo), static_cast<uint32_t>(lo >> 32),
+                                   o ? static_cast<uint32_t>(B >> (64 - o)) : 0u};
+            unsigned long long c = 0ull;
+            for (int k = 0; k < 3; ++k) {
+                c += static_cast<unsigned long long>(n[l + k]) + p[k];
+                n[l + k] = static_cast<uint32_t>(c);
+                c >>= 32;
+            }
+            for (int k = l + 3; c != 0ull && k < kLimbs; ++k) {
+                c += n[k];
+                n[k] = static_cast<uint32_t>(c);
+                c >>= 32;
+            }
+        }
+    }
+    int top = kLimbs - 1;
+    while (top >= 0 && n[top] == 0u) --top;
+    if (top < 0) return 0.0;
+    // the 64 bits from the leading one down, and whether anything below is set
+    const uint32_t a = n[top];
+    const uint32_t b1 = top >= 1 ? n[top - 1] : 0u;
+    const uint32_t b2 = top >= 2 ? n[top - 2] : 0u;
+    bool sticky = false;
+    for (int k = 0; k < top - 2; ++k) sticky |= n[k] != 0u;
+    const int lz = __clz(a);
+    unsigned long long v = (static_cast<unsigned long long>(a) << 32) | b1;
+    if (lz) {
+        v = (v << lz) | (b2 >> (32 - lz));
+        sticky |= static_cast<uint32_t>(b2 << lz) != 0u;
+    } else {
+        sticky |= b2 != 0u;
+    }
+    unsigned long long m = v >> 11;  // 53 bits, leading one at bit 52
+    const bool half = ((v >> 10) & 1ull) != 0ull;
+    sticky |= (v & 0x3FFull) != 0ull;
+    int pos = 32 * top + 31 - lz;  // bit index of the leading one of N
+    if (half && (sticky || (m & 1ull))) {
+        ++m;
+        if (m >> 53) {  // rounded up to the next power of two
+            m >>= 1;
+            ++pos;
+        }
+    }
+    // ss = m 2^(pos - 52) 2^-298: biased exponent pos - 298 + 1023, always normal
+    const long long be = static_cast<long long>(pos) - 298 + 1023;
+    return __longlong_as_double((be << 52) | static_cast<long long>(m & 0xFFFFFFFFFFFFFull));
+}
+
+__global__ void __launch_bounds__(kThreads)
+    k_rmsnorm_q8_0(const float4 *__restrict__ X, const float4 *__restrict__ w, float offset, float eps,
+                   uint32_t *__restrict__ Xq, float *__restrict__ dx, int K)
+{
+    __shared__ unsigned long long bucket[256];
+    __shared__ int nonfinite;
+    __shared__ float s_inv;
+    const int t = blockIdx.x;
+    const int nq = K >> 2, nblk = K >> 5;
+    const float4 *xr = X + static_cast<size_t>(t) * nq;
+    for (int i = threadIdx.x; i < 256; i += kThreads) bucket[i] = 0ull;
+    if (threadIdx.x == 0) nonfinite = 0;
+    // dependents launch once every CTA has started; they still wait for this
+    // grid's completion before reading Xq and dx
+    pdl_launch_dependents();
+    pdl_wait();
+    __syncthreads();
+
+    for (int i = threadIdx.x; i < nq; i += kThreads) {
+        const float4 v = xr[i];
+        add_square(bucket, &nonfinite, v.x);
+        add_square(bucket, &nonfinite, v.y);
+        add_square(bucket, &nonfinite, v.z);
+        add_square(bucket, &nonfinite, v.w);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {  // warp 0: which buckets are occupied, then lane 0 adds them
+        uint32_t occ[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) occ[k] = __ballot_sync(0xffffffffu, bucket[32 * k + threadIdx.x] != 0ull);
+        if (threadIdx.x == 0) {
+            double ss;
+            if (nonfinite & 2)
+                ss = __longlong_as_double(0x7FF8000000000000ll);  // NaN
+            else if (nonfinite & 1)
+                ss = __longlong_as_double(0x7FF0000000000000ll);  // +infinity
+            else
+                ss = exact_sum(bucket, occ);
+            const double r =
+                __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(K)), static_cast<double>(eps)));
+            s_inv = __double2float_rn(__ddiv_rn(1.0, r));
+        }
+    }
+    __syncthreads();
+    const float inv = s_inv;
+
+    // Q8_0 of y: eight lanes per 32-block (four elements each), four blocks
+    // per warp in a warp-uniform loop so the full-mask shuffles never diverge
+    const int sub = threadIdx.x & 7;
+    uint32_t *qr = Xq + static_cast<size_t>(t) * (nblk * 8);
+    float *dr = dx + static_cast<size_t>(t) * nblk;
+    for (int wb = (threadIdx.x >> 5) * 4; wb < nblk; wb += (kThreads >> 5) * 4) {
+        const int blk = wb + ((threadIdx.x & 31) >> 3);
+        const bool active = blk < nblk;
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+        if (active) {
+            const float4 x4 = xr[blk * 8 + sub];
+            const float4 w4 = __ldg(w + blk * 8 + sub);
+            e[0] = __fmul_rn(__fmul_rn(x4.x, inv), __fadd_rn(w4.x, offset));
+            e[1] = __fmul_rn(__fmul_rn(x4.y, inv), __fadd_rn(w4.y, offset));
+            e[2] = __fmul_rn(__fmul_rn(x4.z, inv), __fadd_rn(w4.z, offset));
+            e[3] = __fmul_rn(__fmul_rn(x4.w, inv), __fadd_rn(w4.w, offset));
+        }
+        float amax = fmaxf(fmaxf(fabsf(e[0]), fabsf(e[1])), fmaxf(fabsf(e[2]), fabsf(e[3])));
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float d = __fdiv_rn(amax, 127.0f);
+        uint32_t packed = 0;
+        if (d != 0.0f) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float q = fminf(fmaxf(roundf(__fdiv_rn(e[i], d)), -127.0f), 127.0f);
+                packed |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xFFu) << (8 * i);
+            }
+        }
+        if (active) {
+            qr[blk * 8 + sub] = packed;
+            if (sub == 0) dr[blk] = d;
+        }
+    }
+}
+
+}  // namespace norm
+
+int launch_rmsnorm_q8_0(const float *X, const float *w, float offset, float eps, int8_t *Xq, float *dx, int K,
+                        int M, cudaStream_t s)
+{
+    return status_from(launch_pdl(norm::k_rmsnorm_q8_0, dim3(static_cast<unsigned>(M)), dim3(norm::kThreads), 0, s,
+                                  reinterpret_cast<const float4 *>(X), reinterpret_cast<const float4 *>(w), offset,
+                                  eps, reinterpret_cast<uint32_t *>(Xq), dx, K));
+}
+
+}  // namespace gq

@@ -107,6 +107,28 @@ def test_geglu_down_validation(lib):
     assert call(name, A, A, A, A, 4, gq.GQ_MAX_K + 32, 1, None) == gq.GQ_ERR_SHAPE
 
 
+def test_rmsnorm_quantize_validation(lib):
+    name = "gq_rmsnorm_quantize_q8_0"
+    f = ctypes.c_float
+    one, eps = f(1.0), f(1e-6)
+    assert call(name, None, A, one, eps, A, A, 64, 2, None) == gq.GQ_ERR_NULL
+    assert call(name, A, None, one, eps, A, A, 64, 2, None) == gq.GQ_ERR_NULL
+    assert call(name, A, A, one, eps, None, A, 64, 2, None) == gq.GQ_ERR_NULL
+    assert call(name, A, A, one, eps, A, None, 64, 2, None) == gq.GQ_ERR_NULL
+    for i in range(4):
+        p = [A, A, A, A]
+        p[i] = U
+        assert call(name, p[0], p[1], one, eps, p[2], p[3], 64, 2, None) == gq.GQ_ERR_ALIGN
+    assert call(name, A, A, one, eps, A, A, 65, 2, None) == gq.GQ_ERR_SHAPE
+    assert call(name, A, A, one, eps, A, A, 0, 2, None) == gq.GQ_ERR_SHAPE
+    assert call(name, A, A, one, eps, A, A, 64, 0, None) == gq.GQ_ERR_SHAPE
+    assert call(name, A, A, one, eps, A, A, gq.GQ_MAX_K + 32, 2, None) == gq.GQ_ERR_SHAPE
+    for bad in (0.0, -1e-6, float("nan"), float("inf")):
+        assert call(name, A, A, one, f(bad), A, A, 64, 2, None) == gq.GQ_ERR_SHAPE
+    for bad in (float("nan"), float("inf")):
+        assert call(name, A, A, f(bad), eps, A, A, 64, 2, None) == gq.GQ_ERR_SHAPE
+
+
 def test_ffn_logits_quant_gemm_pack_validation(lib):
     assert call("gq_ffn_gate_up_gelu", A, None, A, A, 4, 64, 1, None) == gq.GQ_ERR_NULL
     assert call("gq_ffn_gate_up_gelu", A, U, A, A, 4, 64, 1, None) == gq.GQ_ERR_ALIGN
