@@ -19,7 +19,8 @@
 // Exact sum of squares: x = m 2^(e - 150) with m the 24-bit significand
 // (e the biased exponent; subnormals take e = 1 and no hidden bit), so
 // x^2 = m^2 2^(2e - 300) with m^2 < 2^48.  Squares with the same e add
-// exactly in a 64-bit integer bucket (K < 2^16 terms), in any order; the
+// exactly in a 64-bit integer bucket (K <= 49152 < 2^16 terms), in any order
+// (per warp, then across the warps); the
 // buckets then add exactly as B_e << 2(e - 1) into a 608-bit integer, which
 // is rounded once, to nearest even, into the double ss = N 2^-298.
 #include "gq_host.h"
@@ -31,24 +32,41 @@ namespace norm {
 constexpr int kThreads = 256;
 constexpr int kLimbs = 19;  // 32-bit limbs; the largest sum needs 571 bits
 
-// One element's square into its exponent bucket (non-finite values only set
-// a flag: bit 0 for an infinity, bit 1 for a NaN).
-__device__ __forceinline__ void add_square(unsigned long long *bucket, int *nonfinite, float f)
+constexpr int kWarps = kThreads / 32;
+
+// The squares of one element per lane into this warp's exponent buckets wb
+// (non-finite values only set a flag: bit 0 for an infinity, bit 1 for a
+// NaN).  Lanes with the same exponent are summed first -- the 48-bit squares
+// as two 24-bit halves, whose sums over 32 lanes fit 32 bits, by full-warp
+// reductions -- and lane 0 adds each exponent's sum to its bucket, so every
+// bucket update is one thread's read-modify-write (no atomics, no
+// same-address conflicts).
+__device__ __forceinline__ void add_squares_warp(unsigned long long *wb, int *nonfinite, float f, int lane)
 {
     const uint32_t b = __float_as_uint(f) & 0x7FFFFFFFu;
     uint32_t e = b >> 23, m = b & 0x7FFFFFu;
     if (e == 255u) {
         atomicOr(nonfinite, m ? 2 : 1);
-        return;
-    }
-    if (e == 0u) {
-        if (m == 0u) return;
-        e = 1u;
+        m = 0u;
+    } else if (e == 0u) {
+        e = 1u;  // subnormal: m 2^(1 - 150); a zero adds nothing
     } else {
         m |= 0x800000u;
     }
-    atomicAdd(&bucket[e], static_cast<unsigned long long>(m) * m);
+    const unsigned long long v = static_cast<unsigned long long>(m) * m;
+    const uint32_t lo = static_cast<uint32_t>(v) & 0xFFFFFFu, hi = static_cast<uint32_t>(v >> 24);
+    // one exponent per round, the lowest pending lane's; every lane leaves
+    // the loop together (pending is warp-uniform and loses a bit each round)
+    for (uint32_t pending = __ballot_sync(0xffffffffu, v != 0ull); pending != 0u;) {
+        const uint32_t key = __shfl_sync(0xffffffffu, e, __ffs(pending) - 1);
+        const bool mine = ((pending >> lane) & 1u) != 0u && e == key;
+        const uint32_t slo = __reduce_add_sync(0xffffffffu, mine ? lo : 0u);
+        const uint32_t shi = __reduce_add_sync(0xffffffffu, mine ? hi : 0u);
+        if (lane == 0) wb[key] += (static_cast<unsigned long long>(shi) << 24) + slo;
+        pending &= ~__ballot_sync(0xffffffffu, mine);
+    }
 }
+
 // sum_e bucket[e] 2^(2e - 300), rounded to nearest even (one thread); occ
 // marks the nonzero buckets (bit e % 32 of occ[e / 32]).
 __device__ double exact_sum(const unsigned long long *bucket, const uint32_t (&occ)[8])
@@ -113,13 +131,15 @@ __global__ void __launch_bounds__(kThreads)
     k_rmsnorm_q8_0(const float4 *__restrict__ X, const float4 *__restrict__ w, float offset, float eps,
                    uint32_t *__restrict__ Xq, float *__restrict__ dx, int K)
 {
+    __shared__ unsigned long long wbk[kWarps][256];  // per-warp exponent buckets
     __shared__ unsigned long long bucket[256];
     __shared__ int nonfinite;
     __shared__ float s_inv;
     const int t = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nq = K >> 2, nblk = K >> 5;
     const float4 *xr = X + static_cast<size_t>(t) * nq;
-    for (int i = threadIdx.x; i < 256; i += kThreads) bucket[i] = 0ull;
+    for (int i = threadIdx.x; i < kWarps * 256; i += kThreads) (&wbk[0][0])[i] = 0ull;
     if (threadIdx.x == 0) nonfinite = 0;
     // dependents launch once every CTA has started; they still wait for this
     // grid's completion before reading Xq and dx
@@ -127,12 +147,22 @@ __global__ void __launch_bounds__(kThreads)
     pdl_wait();
     __syncthreads();
 
-    for (int i = threadIdx.x; i < nq; i += kThreads) {
-        const float4 v = xr[i];
-        add_square(bucket, &nonfinite, v.x);
-        add_square(bucket, &nonfinite, v.y);
-        add_square(bucket, &nonfinite, v.z);
-        add_square(bucket, &nonfinite, v.w);
+    // warp-uniform loop (the reductions use the full warp); lanes past the
+    // row contribute zeros
+    for (int i0 = warp * 32; i0 < nq; i0 += kThreads) {
+        const int i = i0 + lane;
+        const float4 v = i < nq ? xr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        add_squares_warp(wbk[warp], &nonfinite, v.x, lane);
+        add_squares_warp(wbk[warp], &nonfinite, v.y, lane);
+        add_squares_warp(wbk[warp], &nonfinite, v.z, lane);
+        add_squares_warp(wbk[warp], &nonfinite, v.w, lane);
+    }
+    __syncthreads();
+    {  // the warps' buckets, added exactly (each total stays below K 2^48 < 2^64)
+        unsigned long long s = 0ull;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) s += wbk[w][threadIdx.x];
+        bucket[threadIdx.x] = s;
     }
     __syncthreads();
     if (threadIdx.x < 32) {  // warp 0: which buckets are occupied, then lane 0 adds them
