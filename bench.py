@@ -180,6 +180,7 @@ class Workload:
     name = ""
     kernel = ""           # dominant kernel (for the roofline)
     bound = "hbm"
+    cpu_unit, cpu_scale = "GB/s", 1e9   # unit of the oracle's timing (cpu_reference amounts per second)
 
     def setup(self, torch, gq):
         raise NotImplementedError
@@ -249,6 +250,15 @@ class Rotating(Workload):
     """A matvec-like workload over R independent weight copies (working set > 4x L2)."""
     launches_per_step = 1
 
+    def _matvec_reference(self, oracle, fmt, W, x, rows_sample):
+        n = min(rows_sample, self.rows)
+        sel = np.arange(n, dtype=np.int64)
+        row_bytes = W.shape[1]
+
+        def run():
+            oracle.matvec(fmt, W, x, self.rows, self.K, row_idx=sel)
+        return run, n * row_bytes + 4 * self.K + 4 * n, f"{n} of {self.rows} rows (fp64 decode and dot)"
+
     def _rotate(self, torch, one_copy_bytes):
         l2 = torch.cuda.get_device_properties(0).L2_cache_size
         need = max(4 * l2, 256 << 20)
@@ -277,6 +287,10 @@ class Q40Matvec(Rotating):
     def step(self, i):
         self.gq.gq_q4_0_matvec(self.copies[i % len(self.copies)], self.x, self.y, self.rows, self.K)
 
+    def cpu_reference(self, oracle, rows_sample):
+        W, x = synth.q4_0_matvec_inputs(self.rows, self.K)
+        return self._matvec_reference(oracle, oracle.FORMAT_Q4_0, W, x, rows_sample)
+
 
 class Q4KMatvec(Rotating):
     name = "q4_k_matvec_21504x5376"
@@ -299,6 +313,10 @@ class Q4KMatvec(Rotating):
 
     def step(self, i):
         self.gq.gq_q4k_matvec(self.copies[i % len(self.copies)], self.x, self.y, self.rows, self.K)
+
+    def cpu_reference(self, oracle, rows_sample):
+        W, x = synth.q4_k_matvec_inputs(self.rows, self.K)
+        return self._matvec_reference(oracle, oracle.FORMAT_Q4_K, W, x, rows_sample)
 
 
 class Q6KMatvec(Rotating):
@@ -324,6 +342,11 @@ class Q6KMatvec(Rotating):
 
     def step(self, i):
         self.gq.gq_q6k_matvec(self.copies[i % len(self.copies)], self.x, self.y, self.rows, self.K)
+
+    def cpu_reference(self, oracle, rows_sample):
+        W = synth.q6_k_weights(self.rows, self.K, synth.stream(6, 0))
+        x = synth.normal(self.K, synth.stream(6, 1))
+        return self._matvec_reference(oracle, oracle.FORMAT_Q6_K, W, x, rows_sample)
 
 
 class GegluDown(Rotating):
@@ -353,6 +376,17 @@ class GegluDown(Rotating):
     def step(self, i):
         self.gq.gq_q4_0_geglu_down(self.copies[i % len(self.copies)], self.g, self.u, self.y, self.rows, self.K)
 
+    def cpu_reference(self, oracle, rows_sample):
+        W = synth.q4_0_weights(self.rows, self.K, synth.stream(7, 0))
+        g = (synth.normal(self.K, synth.stream(7, 1)) * 2).astype(np.float32)
+        u = synth.normal(self.K, synth.stream(7, 2))
+        n = min(rows_sample, self.rows)
+        sel = np.arange(n, dtype=np.int64)
+
+        def run():
+            oracle.geglu_down(oracle.FORMAT_Q4_0, W, g, u, self.rows, self.K, row_idx=sel)
+        return run, n * W.shape[1] + 8 * self.K + 4 * n, f"{n} of {self.rows} rows (fp64 gated input, decode, dot)"
+
 
 class RMSNormQ8(Rotating):
     """The prefill activations (512 tokens x 5376) normalized and quantized to
@@ -360,6 +394,7 @@ class RMSNormQ8(Rotating):
     name = "rmsnorm_q8_0_512x5376"
     kernel = "k_rmsnorm_q8_0"
     M, K = 512, 5376
+    rows = M   # the rows of X
 
     def setup(self, torch, gq):
         X = synth.normal((self.M, self.K), synth.stream(8, 0))
@@ -380,6 +415,17 @@ class RMSNormQ8(Rotating):
     def step(self, i):
         self.gq.gq_rmsnorm_quantize_q8_0(self.copies[i % len(self.copies)], self.w, 1.0, 1e-6, self.Xq, self.dx,
                                          self.K, self.M)
+
+    def cpu_reference(self, oracle, rows_sample):
+        X = synth.normal((self.M, self.K), synth.stream(8, 0))
+        w = (synth.normal(self.K, synth.stream(8, 1)) * 0.1).astype(np.float32)
+        n = min(rows_sample, self.M)
+        Xs = np.ascontiguousarray(X[:n])
+
+        def run():
+            oracle.rmsnorm_quantize_q8_0(Xs, w, 1.0, 1e-6, n, self.K)
+        amount = n * (4 * self.K + self.K + 4 * (self.K // 32)) + 4 * self.K
+        return run, amount, f"{n} of {self.M} tokens (exact sum of squares by math.fsum, f32 scaling, Q8_0)"
 
 
 class FFN(Rotating):
@@ -410,6 +456,16 @@ class FFN(Rotating):
         self.gq.gq_ffn_gate_up_gelu(g, u, self.x, self.h, self.rows, self.K)
         self.gq.gq_q4_0_matvec(d, self.h, self.y, self.K, self.rows)
 
+    def cpu_reference(self, oracle, rows_sample):
+        Wg, Wu, Wd, x = synth.ffn_inputs(self.rows, self.K)
+        nb = Wg.shape[1]
+
+        def run():
+            h = oracle.ffn_gate_up(Wg, Wu, x, self.rows, self.K)["h"]
+            oracle.matvec(oracle.FORMAT_Q4_0, Wd, h.astype(np.float32), self.K, self.rows)
+        amount = 3 * self.rows * nb + 4 * self.K + 2 * 4 * self.rows + 4 * self.K
+        return run, amount, "the whole step (fp64 gate/up with GELU, then the down matvec)"
+
 
 class Gemm(Workload):
     name = "q4_0_gemm_q8act_512x21504x5376"
@@ -439,6 +495,24 @@ class Gemm(Workload):
         self.gq.gq_q4_0_gemm_q8act(self.Wp, self.Xq, self.dx, self.Y, self.ws, self.ws_bytes, self.rows, self.K,
                                    self.M)
 
+    cpu_unit, cpu_scale = "TOPS", 1e12
+    cpu_tokens = 16   # the oracle's bounded sample: this many tokens against every row
+
+    def cpu_reference(self, oracle, rows_sample):
+        W, X = synth.gemm_inputs(self.rows, self.K, self.M)
+        nt = min(self.M, self.cpu_tokens)
+        Xs = np.ascontiguousarray(X[:nt])
+
+        def run():
+            q, d = oracle.quantize_q8_0(Xs, nt, self.K)
+            oracle.gemm_q8act(W, q, d, self.rows, self.K, nt)
+        if self.cpu_unit == "TOPS":
+            amount = 2 * nt * self.rows * self.K
+        else:
+            amount = W.size + 4 * nt * self.K + 4 * nt * self.rows
+        return run, amount, (f"{nt} of {self.M} tokens against all {self.rows} rows (Q8_0 quantization, "
+                             "fp64 block-scaled contraction)")
+
 
 class GemmSmallBatch8(Gemm):
     """The same contraction at a small batch (a verifier's eight tokens): every
@@ -447,6 +521,8 @@ class GemmSmallBatch8(Gemm):
     kernel = "k_gemm_small"
     bound = "hbm"  # reported as bytes per step (weights, X, Y) over the step time
     M = 8
+    cpu_unit, cpu_scale = "GB/s", 1e9
+    cpu_tokens = 32
 
 
 class GemmSmallBatch32(GemmSmallBatch8):
@@ -569,11 +645,11 @@ def cpu_baseline(wl_cls, sample_rows):
     wl = wl_cls()
     if not hasattr(wl, "cpu_reference"):
         return None
-    run, nbytes, desc = wl.cpu_reference(oracle, sample_rows)
+    run, amount, desc = wl.cpu_reference(oracle, sample_rows)
     t = time.perf_counter()
     run()
     dt = time.perf_counter() - t
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.threads(),
+    return {"value": round(amount / dt / wl.cpu_scale, 4), "unit": wl.cpu_unit, "cores": oracle.threads(),
             "kind": "oracle", "sample": desc, "seconds": round(dt, 3)}
 
 
@@ -663,23 +739,24 @@ def run_reference(args, rank):
         print(json.dumps({"impl": "reference", "unavailable": f"no oracle timing for {wl.name}"}))
         return
     sample = 32768
-    run, nbytes, desc = wl.cpu_reference(oracle, sample)
+    run, amount, desc = wl.cpu_reference(oracle, sample)
     for _ in range(args.warmup):
         run()
     t = time.perf_counter()
     for _ in range(args.steps):
         run()
     dt = (time.perf_counter() - t) / args.steps
-    value = nbytes / dt / 1e9
+    value = amount / dt / wl.cpu_scale
+    unit = wl.cpu_unit
     cores = oracle.threads()
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 0,
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": wl.name},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": desc},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
 

@@ -51,3 +51,20 @@ def test_digest_follows_the_include_graph(tmp_path, monkeypatch):
         f.write("\n/* edit */\n")
     assert bench.kernel_source_hash("k_q4_0_matvec") != h_q4
     assert bench.kernel_source_hash("k_gemm_pair") != h_gemm
+
+
+def test_reference_arm_runs_for_every_workload(capsys):
+    """--impl reference: the oracle, timed on the host for each workload (the
+    1.5 GB logits matrix aside), prints one line in the workload's unit."""
+    import argparse
+    import json
+    for name, wl in sorted(bench.WORKLOADS.items()):
+        if name == bench.DEFAULT_WORKLOAD:
+            continue
+        bench.run_reference(argparse.Namespace(config=name, steps=1, warmup=1), rank=0)
+        line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+        assert line["impl"] == "reference" and line["config"]["workload"] == name
+        assert line["unit"] == wl.cpu_unit and line["value"] > 0
+        assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    bench.run_reference(argparse.Namespace(config=bench.DEFAULT_WORKLOAD, steps=1, warmup=1), rank=1)
+    assert capsys.readouterr().out == ""   # ranks other than 0 print nothing
