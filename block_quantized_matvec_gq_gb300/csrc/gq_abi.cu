@@ -13,6 +13,10 @@
 
 using namespace gq;
 
+// Launchers of the entry points declared in gq_geglu.h and gq_norm.h.  They
+// are declared here rather than in gq_host.h, which every kernel includes,
+// so that adding them changed no other kernel's sources (whose recorded DRAM
+// counters are keyed to a digest of those sources).
 namespace gq {
 // gq_q4_0.cu: the Q4_0 matvec staging gelu_tanh(g) * u as its input vector
 int launch_q4_0_geglu_down(const void *W, const float *g, const float *u, float *y, int rows, int K, MatvecGeo geo,
