@@ -662,6 +662,8 @@ def main():
     ap.add_argument("--config", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--suite", action="store_true", help="every workload, one line each")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tensor-peaks", action="store_true",
+                    help="build and run the tensor-path peak probes and print their JSON (no bench line)")
     ap.add_argument("--rows", type=int, default=0,
                     help="logits workload only: vocabulary rows (default 262144; smaller for profiling)")
     args = ap.parse_args()
@@ -672,6 +674,8 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, rank)
+    if args.tensor_peaks:
+        sys.exit(tensor_peaks())
 
     import torch
     dist = None
@@ -725,6 +729,22 @@ def main():
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def tensor_peaks():
+    """Build and run the tensor-path peak probes (block_quantized_matvec_gq_gb300/peaks/tensor_peaks.cu):
+    tcgen05 kind::f16, tcgen05.ld read-out, mma.sync f16 and s8, f32 FMA (scalar and packed).
+    Prints the probe's JSON object."""
+    from block_quantized_matvec_gq_gb300 import build as gqbuild
+    src = os.path.join(ROOT, "block_quantized_matvec_gq_gb300", "peaks", "tensor_peaks.cu")
+    os.makedirs(gqbuild.BUILD, exist_ok=True)
+    exe = os.path.join(gqbuild.BUILD, "tensor_peaks")
+    cmd = [gqbuild.nvcc()] + gqbuild.ARCH + ["-O3", "-std=c++17", "-I", gqbuild.INCLUDE, "-I", gqbuild.CSRC,
+                                             "--expt-relaxed-constexpr", "-o", exe, src]
+    subprocess.run(cmd, check=True)
+    r = subprocess.run([exe], capture_output=True, text=True)
+    sys.stdout.write(r.stdout)
+    return r.returncode
 
 
 def run_reference(args, rank):

@@ -62,6 +62,7 @@ def _declare(L):
         "gq_logits_topk_noalloc": ([P, P, ctypes.c_float, I, P, P, P, I, I, I, P], I),
         "gq_quantize_q8_0": ([P, P, P, I, I, P], I),
         "gq_rmsnorm_quantize_q8_0": ([P, P, ctypes.c_float, ctypes.c_float, P, P, I, I, P], I),
+        "gq_rmsnorm_sum_squares": ([P, P, I, I, P], I),
         "gq_q4_0_gemm_workspace_bytes": ([I, I], S),
         "gq_q4_0_gemm_q8act": ([P, P, P, P, P, S, I, I, I, P], I),
         "gq_q4_0_gemm_block_dots": ([P, P, P, P, S, I, I, I, P], I),
@@ -185,6 +186,10 @@ def gq_quantize_q8_0(X, Xq, dx, K, M, stream=None):
 def gq_rmsnorm_quantize_q8_0(X, w, offset, eps, Xq, dx, K, M, stream=None):
     _check(lib().gq_rmsnorm_quantize_q8_0(_ptr(X), _ptr(w), float(offset), float(eps), _ptr(Xq), _ptr(dx), K, M,
                                           _stream(stream)), "gq_rmsnorm_quantize_q8_0")
+
+
+def gq_rmsnorm_sum_squares(X, ss, K, M, stream=None):
+    _check(lib().gq_rmsnorm_sum_squares(_ptr(X), _ptr(ss), K, M, _stream(stream)), "gq_rmsnorm_sum_squares")
 
 
 def gq_q4_0_gemm_workspace_bytes(K, M) -> int:

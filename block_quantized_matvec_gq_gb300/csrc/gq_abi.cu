@@ -24,6 +24,8 @@ int launch_q4_0_geglu_down(const void *W, const float *g, const float *u, float 
 // gq_norm.cu: RMS normalization fused with Q8_0 quantization, one CTA per token
 int launch_rmsnorm_q8_0(const float *X, const float *w, float offset, float eps, int8_t *Xq, float *dx, int K,
                         int M, cudaStream_t s);
+// gq_norm.cu: the exact sum of squares of every row
+int launch_row_sum_squares(const float *X, double *ss, int K, int M, cudaStream_t s);
 }  // namespace gq
 
 namespace {
@@ -106,6 +108,11 @@ int gq_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K, int
 {
     int st = check_matvec(GQ_FORMAT_Q4_0, W, x, y, rows, K, M);
     if (st != GQ_OK) return st;
+    // rows of whole 8-block groups stream through the shared-memory ring; other K take the register path
+    if (ring_preferred(rows) && ring_q4_0_supported(K / 32)) {
+        st = launch_ring_q4_0(W, x, nullptr, nullptr, y, rows, K, reinterpret_cast<cudaStream_t>(stream));
+        if (st != GQ_ERR_SHAPE) return st;
+    }
     return launch_q4_0_matvec(W, x, y, rows, K, choose_matvec_geo(GQ_FORMAT_Q4_0, rows, K / 32, aligned32(W)),
                               reinterpret_cast<cudaStream_t>(stream));
 }
@@ -123,6 +130,10 @@ int gq_q4k_matvec(const void *W, const float *x, float *y, int rows, int K, int 
 {
     int st = check_matvec(GQ_FORMAT_Q4_K, W, x, y, rows, K, M);
     if (st != GQ_OK) return st;
+    if (ring_preferred(rows)) {
+        st = launch_ring_q4k(W, x, y, rows, K, reinterpret_cast<cudaStream_t>(stream));
+        if (st != GQ_ERR_SHAPE) return st;
+    }
     return launch_q4k_matvec(W, x, y, rows, K, choose_matvec_geo(GQ_FORMAT_Q4_K, rows, K / 32, aligned32(W)),
                              reinterpret_cast<cudaStream_t>(stream));
 }
@@ -141,6 +152,10 @@ int gq_ffn_gate_up_gelu(const void *W_gate, const void *W_up, const float *x, fl
     if (!aligned16(W_up)) return GQ_ERR_ALIGN;
     int st = check_matvec(GQ_FORMAT_Q4_0, W_gate, x, h, rows, K, M);
     if (st != GQ_OK) return st;
+    if (ring_preferred(rows) && ring_q4_0_supported(K / 32)) {
+        st = launch_ring_ffn(W_gate, W_up, x, h, rows, K, reinterpret_cast<cudaStream_t>(stream));
+        if (st != GQ_ERR_SHAPE) return st;
+    }
     return launch_ffn_gate_up(W_gate, W_up, x, h, rows, K, choose_ffn_geo(rows, K / 32, aligned32(W_gate) && aligned32(W_up)),
                               reinterpret_cast<cudaStream_t>(stream));
 }
@@ -152,6 +167,10 @@ int gq_q4_0_geglu_down(const void *W_down, const float *g, const float *u, float
     int st = check_matvec(GQ_FORMAT_Q4_0, W_down, g, y, rows, K, M);
     if (st != GQ_OK) return st;
     if (!aligned16(u)) return GQ_ERR_ALIGN;
+    if (ring_preferred(rows) && ring_q4_0_supported(K / 32)) {
+        st = launch_ring_q4_0(W_down, nullptr, g, u, y, rows, K, reinterpret_cast<cudaStream_t>(stream));
+        if (st != GQ_ERR_SHAPE) return st;
+    }
     return launch_q4_0_geglu_down(W_down, g, u, y, rows, K,
                                   choose_matvec_geo(GQ_FORMAT_Q4_0, rows, K / 32, aligned32(W_down)),
                                   reinterpret_cast<cudaStream_t>(stream));
@@ -200,6 +219,14 @@ int gq_rmsnorm_quantize_q8_0(const float *X, const float *w, float offset, float
     return launch_rmsnorm_q8_0(X, w, offset, eps, Xq, dx, K, M, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int gq_rmsnorm_sum_squares(const float *X, double *ss, int K, int M, gq_stream_t stream)
+{
+    if (!X || !ss) return GQ_ERR_NULL;
+    if (!aligned16(X) || !aligned16(ss)) return GQ_ERR_ALIGN;
+    if (M < 1 || K < 32 || K % 32 != 0 || K > GQ_MAX_K) return GQ_ERR_SHAPE;
+    return launch_row_sum_squares(X, ss, K, M, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t gq_q4_0_gemm_workspace_bytes(int K, int M)
 {
     // enough for either contraction path (the split path needs the most)
@@ -218,7 +245,8 @@ int gq_q4_0_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // few tokens: decode each weight once on the CUDA cores and apply it to every token
     if (gemm_small_supported(K, M)) return launch_gemm_small(W, Xq, dx, Y, rows, K, M, st);
-    if (gemm_split_supported(K)) return launch_gemm_split(W, Xq, dx, Y, workspace, workspace_bytes, rows, K, M, st);
+    if (gemm_split_supported(K) && !gemm_force_block_path())
+        return launch_gemm_split(W, Xq, dx, Y, workspace, workspace_bytes, rows, K, M, st);
     return launch_gemm_q8act_tc(W, Xq, dx, Y, workspace, workspace_bytes, rows, K, M, st);
 }
 

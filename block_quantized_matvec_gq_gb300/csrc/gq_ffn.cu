@@ -66,6 +66,13 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
 
         for (int task = first; task < ntasks; task += stride) {
             setup(task);
+            // the next task's rows stream into L2 while this one computes
+            if (task + stride < ntasks) {
+                prefetch_task_l2<TR>(reinterpret_cast<const uint8_t *>(gnib), nb * 16u,
+                                     reinterpret_cast<const uint8_t *>(gsc), nb * 2u, (task + stride) * TR, rows, lane);
+                prefetch_task_l2<TR>(reinterpret_cast<const uint8_t *>(unib), nb * 16u,
+                                     reinterpret_cast<const uint8_t *>(usc), nb * 2u, (task + stride) * TR, rows, lane);
+            }
             float out[2 * R];
             st.run(xs, nb, lp, out);
             const int r0 = task * TR + g * R;
@@ -113,6 +120,13 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
         for (int j = 0; j < cr.count; ++j) {
             const int r0 = cr.start + j * cr.step;
             if (j > 0 || !kEarly) setup(r0, 0, nb);
+            // the next task's rows stream into L2 while this one computes
+            if (j + 1 < cr.count) {
+                prefetch_task_l2<TR>(reinterpret_cast<const uint8_t *>(gnib), nb * 16u,
+                                     reinterpret_cast<const uint8_t *>(gsc), nb * 2u, r0 + cr.step, rows, lane);
+                prefetch_task_l2<TR>(reinterpret_cast<const uint8_t *>(unib), nb * 16u,
+                                     reinterpret_cast<const uint8_t *>(usc), nb * 2u, r0 + cr.step, rows, lane);
+            }
             float out[2 * R];
             st.run(xs, nb, lp, out);
     #pragma unroll
@@ -163,7 +177,6 @@ int launch_ffn_gate_up(const void *Wg, const void *Wu, const float *x, float *h,
     const uint16_t *us = reinterpret_cast<const uint16_t *>(un + static_cast<size_t>(rows) * nb);
     const size_t smem = static_cast<size_t>(nb) * kXBlk * sizeof(float);
     const long long ntasks = (rows + (32 / geo.lg) * geo.r - 1) / ((32 / geo.lg) * geo.r);
-    if (geo.p != 1) return GQ_ERR_SHAPE;
 #define CASE(LG, R, U)                                                                                  \
     {                                                                                                   \
         auto rr = k_ffn_gate_up<LG, R, U, 0>;                                                                     \

@@ -1,29 +1,74 @@
 // gq_geo.cu -- geometry choice for the matvec-family kernels.
 //
 // Chosen by measurement on GB300 (sweeps over lane-group width LG, rows per
-// group R, loads in flight U, and blocks per lane load P at the workload
-// shapes).  With the register-lean 4-bit core, 16-byte loads (P = 1) beat
-// the 32-byte block-pair loads at every measured shape; LG = 32 when a row's
-// block count is a multiple of 32, else 16 (less idle lanes in the last
-// step); U = 2 (with the balanced K-split schedule, two loads in flight
-// also beat four on the 5376 x 21504 down projection: 20.6 vs 22.0 us).
+// group R and blocks per batch U at the workload shapes).  The 4-bit
+// streams load a batch of U blocks of every row before computing it:
+// LG = 32 when a row's block count is a multiple of 32, else 16 (fewer idle
+// lanes in the last step), R = 2, U = 4 (21504 x 5376 Q4_K: 21.3 us, against
+// 22.0 with LG 8 and 28-29 with eight-block batches; the 4096 x 4096 Q4_0:
+// 3.8 us).  The FFN pair: LG = 16, R = 1, U = 4 (two matrices per row).
+#include <stdio.h>
+#include <stdlib.h>
+
 #include "gq_host.h"
 
 namespace gq {
+
+#ifdef GQ_TUNING
+// Geometry sweeps: a tuning build reads overrides from the environment.
+static MatvecGeo tuned(const char *prefix, MatvecGeo g)
+{
+    char name[64];
+    const char *v;
+    snprintf(name, sizeof name, "%s_LG", prefix);
+    if ((v = getenv(name))) g.lg = atoi(v);
+    snprintf(name, sizeof name, "%s_R", prefix);
+    if ((v = getenv(name))) g.r = atoi(v);
+    snprintf(name, sizeof name, "%s_U", prefix);
+    if ((v = getenv(name))) g.u = atoi(v);
+    return g;
+}
+static int ring_override()
+{
+    const char *v = getenv("GQ_RING");
+    return v ? atoi(v) : -1;
+}
+bool gemm_force_block_path()
+{
+    const char *v = getenv("GQ_GEMM_BLOCK");
+    return v && atoi(v) != 0;
+}
+#else
+static MatvecGeo tuned(const char *, MatvecGeo g) { return g; }
+static int ring_override() { return -1; }
+bool gemm_force_block_path() { return false; }
+#endif
+
+// Short, wide matrices (fewer than four rows per SM) take the shared-memory
+// ring with a cluster split-K: the register streams would leave most SMs
+// idle (measured on Q4_0: 256 x 21504 in 5.1 instead of 13.6 us, 8 x 49152 in
+// 3.8 instead of 17.9 us).  Larger matrices keep the register streams, which
+// were as fast or faster at every shape measured.
+bool ring_preferred(int rows)
+{
+    const int o = ring_override();
+    if (o >= 0) return o != 0;
+    return rows < 4 * sm_count();
+}
 
 MatvecGeo choose_matvec_geo(int format, int rows, int nb, bool pair_ok)
 {
     (void)rows;
     (void)pair_ok;
-    if (format == GQ_FORMAT_Q8_0) return MatvecGeo{16, 2, 4, 8, 1};
-    return MatvecGeo{(nb % 32 == 0) ? 32 : 16, 2, 2, 8, 1};
+    if (format == GQ_FORMAT_Q8_0) return tuned("GQ_Q8", MatvecGeo{16, 2, 4, 8});
+    return tuned("GQ_Q4", MatvecGeo{(nb % 32 == 0) ? 32 : 16, 2, 4, 8});
 }
 
 MatvecGeo choose_logits_geo(int rows, int nb)
 {
     (void)rows;
     (void)nb;
-    return MatvecGeo{8, 2, 4, 8, 1};
+    return MatvecGeo{8, 2, 4, 8};
 }
 
 MatvecGeo choose_ffn_geo(int rows, int nb, bool pair_ok)
@@ -31,7 +76,7 @@ MatvecGeo choose_ffn_geo(int rows, int nb, bool pair_ok)
     (void)rows;
     (void)nb;
     (void)pair_ok;
-    return MatvecGeo{8, 1, 4, 8, 1};
+    return tuned("GQ_FFN", MatvecGeo{16, 1, 4, 8});
 }
 
 }  // namespace gq

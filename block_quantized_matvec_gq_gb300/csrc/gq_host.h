@@ -111,7 +111,6 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 // Matvec geometry: LG lanes per row group, R rows per group, U blocks in flight.
 struct MatvecGeo {
     int lg, r, u, warps;
-    int p;  // blocks per lane load: 1 (16/32-byte loads) or 2 (32-byte block pairs, Q4 formats)
 };
 
 MatvecGeo choose_matvec_geo(int format, int rows, int nb, bool pair_ok);
@@ -136,8 +135,6 @@ int launch_logits_topk(const void *W, const float *x, float softcap, int k, int 
 int launch_pack(int format, const void *src, void *dst, int rows, int K, bool unpack,
                 cudaStream_t s);
 int launch_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, cudaStream_t s);
-int launch_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows, int K,
-                      int M, cudaStream_t s);
 size_t gemm_workspace_bytes(int K, int M);
 // scale-folded bf16 tensor-core path (gq_gemm_split.cu): K % 256 == 0
 size_t gemm_split_workspace_bytes(int K, int M);
@@ -151,6 +148,14 @@ int launch_gemm_q8act_tc(const void *W, const int8_t *Xq, const float *dx, float
                          int rows, int K, int M, cudaStream_t s);
 int launch_block_dots_tc(const void *W, const int8_t *Xq, int32_t *D, void *ws, size_t ws_bytes, int rows, int K,
                          int M, cudaStream_t s);
+// ring-streamed 4-bit matvecs (gq_stream.cu)
+bool ring_preferred(int rows);
+bool gemm_force_block_path();
+bool ring_q4_0_supported(int nb);
+int launch_ring_q4_0(const void *W, const float *x, const float *g_or_null, const float *u, float *y, int rows,
+                     int K, cudaStream_t s);
+int launch_ring_ffn(const void *Wg, const void *Wu, const float *x, float *h, int rows, int K, cudaStream_t s);
+int launch_ring_q4k(const void *W, const float *x, float *y, int rows, int K, cudaStream_t s);
 int read_device_status(bool reset);
 int *status_word();  // device address of the status word (current device)
 

@@ -34,26 +34,30 @@ __device__ __forceinline__ void cp_async_wait_all()
 }
 
 // Streaming weight loads: read once, no L1 allocation.  (An L2 eviction
-// hint is accepted by sm_103a only on the 32-byte form.)
+// hint is accepted by sm_103a only on the 32-byte form.)  The asm is not
+// volatile: weights are read-only for the whole kernel, so the compiler may
+// schedule these loads like any other load -- a volatile form pinned them in
+// program order and cost the 4-bit matvecs a third of their issue rate
+// (measured: 7.0 against 10.0 T codes/s per GPU on the same core).
 __device__ __forceinline__ uint4 ld_stream16(const void *p)
 {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
     return v;
 }
 // 32-byte load (two 16-byte halves), evict-first in L2.
 __device__ __forceinline__ void ld_stream32(const void *p, uint4 &a, uint4 &b)
 {
-    asm volatile("ld.global.nc.L1::no_allocate.L2::evict_first.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
-                 : "l"(p));
+    asm("ld.global.nc.L1::no_allocate.L2::evict_first.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+        : "l"(p));
 }
 __device__ __forceinline__ uint16_t ld_stream_u16(const void *p)
 {
     uint16_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
     return v;
 }
 
@@ -100,10 +104,10 @@ __device__ __forceinline__ float group_sum(float v)
 
 // ---------------------------------------------------------------- exact code -> f32
 // Codes are turned into exact f32 values without an int-to-float
-// conversion: OR-ing a code (at bit position p < 20) into the bit pattern of
-// 2^23 gives the float 2^23 + q * 2^p exactly; one FMA with 2^-p and a
-// constant then removes 2^(23-p) (and an offset) without rounding, since the
-// exact result is a small integer.
+// conversion: OR-ing a code into the significand of a power of two 2^e, with
+// the code's lowest bit on the units place (bit 23 - e of the significand),
+// gives the float 2^e + q exactly; one add of -(2^e + offset) then leaves
+// (q - offset) without rounding, since the exact result is a small integer.
 constexpr uint32_t kMagic = 0x4B000000u;  // bit pattern of 2^23
 
 __device__ __forceinline__ float2 mk2(float a, float b) { return make_float2(a, b); }
@@ -113,9 +117,11 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return _
 // ---------------------------------------------------------------- 4-bit codes
 // One 32-bit word w holds the 8 nibbles of one 8-element group in element
 // order (nibble k = bits 4k..4k+3).  For i = 0..3 the pair (nibble i, nibble
-// i+4) is isolated in place by one LOP3 each: (w & 0xF<<4i) | 0x4B000000 is
-// the f32 2^23 + q*16^i, and the same on w>>16 gives element i+4.  One packed
-// f32x2 FMA by 16^-i minus (2^(23-4i) + OFF) turns the pair into
+// i+4) is isolated in place by one LOP3 each into an f32 whose exponent is
+// chosen per pair: OR-ing (w & 0xF<<4i) into the bit pattern of 2^(23-4i)
+// puts the nibble on the units bit of the significand, so the float is
+// exactly 2^(23-4i) + q (and the same on w>>16 gives element i+4).  One
+// packed f32x2 add of -(2^(23-4i) + OFF) turns the pair into
 // (q_i - OFF, q_{i+4} - OFF) exactly, and one packed FMA adds its products
 // with (x_i, x_{i+4}).  x is staged per 8-group in the order
 // x0,x4,x1,x5,x2,x6,x3,x7, so each pair of x values is one aligned 64-bit
@@ -124,23 +130,22 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return _
 #define GQ_NIB8_BODY(FIRST)                                                                                      \
     "{\n"                                                                                                        \
     " .reg .b32 h, l0, h0, l1, h1, l2, h2, l3, h3;\n"                                                           \
-    " .reg .b64 p0, p1, p2, p3, x0, x1, x2, x3, a, c0, c1, c2, c3, s1, s2, s3;\n"                               \
+    " .reg .b64 p0, p1, p2, p3, x0, x1, x2, x3, a, c0, c1, c2, c3;\n"                                           \
     " shr.u32 h, %2, 16;\n"                                                                                      \
     " lop3.b32 l0, %2, 0x0000000F, 0x4B000000, 0xEA;\n lop3.b32 h0, h, 0x0000000F, 0x4B000000, 0xEA;\n"         \
-    " lop3.b32 l1, %2, 0x000000F0, 0x4B000000, 0xEA;\n lop3.b32 h1, h, 0x000000F0, 0x4B000000, 0xEA;\n"         \
-    " lop3.b32 l2, %2, 0x00000F00, 0x4B000000, 0xEA;\n lop3.b32 h2, h, 0x00000F00, 0x4B000000, 0xEA;\n"         \
-    " lop3.b32 l3, %2, 0x0000F000, 0x4B000000, 0xEA;\n lop3.b32 h3, h, 0x0000F000, 0x4B000000, 0xEA;\n"         \
+    " lop3.b32 l1, %2, 0x000000F0, 0x49000000, 0xEA;\n lop3.b32 h1, h, 0x000000F0, 0x49000000, 0xEA;\n"         \
+    " lop3.b32 l2, %2, 0x00000F00, 0x47000000, 0xEA;\n lop3.b32 h2, h, 0x00000F00, 0x47000000, 0xEA;\n"         \
+    " lop3.b32 l3, %2, 0x0000F000, 0x45000000, 0xEA;\n lop3.b32 h3, h, 0x0000F000, 0x45000000, 0xEA;\n"         \
     " mov.b64 p0, {l0, h0};\n mov.b64 p1, {l1, h1};\n mov.b64 p2, {l2, h2};\n mov.b64 p3, {l3, h3};\n"         \
     " mov.b64 c0, {%13, %13};\n mov.b64 c1, {%14, %14};\n mov.b64 c2, {%15, %15};\n mov.b64 c3, {%16, %16};\n" \
-    " mov.b64 s1, {%17, %17};\n mov.b64 s2, {%18, %18};\n mov.b64 s3, {%19, %19};\n"                           \
-    " add.rn.f32x2 p0, p0, c0;\n"                                                                                \
-    " fma.rn.f32x2 p1, p1, s1, c1;\n fma.rn.f32x2 p2, p2, s2, c2;\n fma.rn.f32x2 p3, p3, s3, c3;\n"             \
+    " add.rn.f32x2 p0, p0, c0;\n add.rn.f32x2 p1, p1, c1;\n add.rn.f32x2 p2, p2, c2;\n add.rn.f32x2 p3, p3, c3;\n"  \
     " mov.b64 x0, {%3, %4};\n mov.b64 x1, {%5, %6};\n mov.b64 x2, {%7, %8};\n mov.b64 x3, {%9, %10};\n"         \
     " mov.b64 a, {%11, %12};\n" FIRST                                                                            \
     " fma.rn.f32x2 a, p1, x1, a;\n fma.rn.f32x2 a, p2, x2, a;\n fma.rn.f32x2 a, p3, x3, a;\n"                   \
     " mov.b64 {%0, %1}, a;\n"                                                                                    \
     "}"
 
+// -(2^(23-4i) + OFF): removes pair i's exponent term and the code offset.
 template <int OFF>
 struct NibConsts {
     static constexpr float c0 = -(8388608.0f + OFF);  // -(2^23 + OFF)
@@ -160,13 +165,13 @@ __device__ __forceinline__ float2 nib8_fma(uint32_t w, float4 xa, float4 xb, flo
             : "=f"(r.x), "=f"(r.y)
             : "r"(w), "f"(xa.x), "f"(xa.y), "f"(xa.z), "f"(xa.w), "f"(xb.x), "f"(xb.y), "f"(xb.z), "f"(xb.w),
               "f"(acc.x), "f"(acc.y), "f"(NibConsts<OFF>::c0), "f"(NibConsts<OFF>::c1), "f"(NibConsts<OFF>::c2),
-              "f"(NibConsts<OFF>::c3), "f"(0.0625f), "f"(0.00390625f), "f"(0.000244140625f));
+              "f"(NibConsts<OFF>::c3));
     } else {
         asm(GQ_NIB8_BODY(" fma.rn.f32x2 a, p0, x0, a;\n")
             : "=f"(r.x), "=f"(r.y)
             : "r"(w), "f"(xa.x), "f"(xa.y), "f"(xa.z), "f"(xa.w), "f"(xb.x), "f"(xb.y), "f"(xb.z), "f"(xb.w),
               "f"(acc.x), "f"(acc.y), "f"(NibConsts<OFF>::c0), "f"(NibConsts<OFF>::c1), "f"(NibConsts<OFF>::c2),
-              "f"(NibConsts<OFF>::c3), "f"(0.0625f), "f"(0.00390625f), "f"(0.000244140625f));
+              "f"(NibConsts<OFF>::c3));
     }
     return r;
 }

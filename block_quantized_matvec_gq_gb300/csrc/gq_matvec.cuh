@@ -55,19 +55,21 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t h)
 
 // ---------------------------------------------------------------- Q4_0
 // Packed Q4_0: nibble plane (16 B per block, element order) + fp16 scale plane.
-// One row task of NS rows: set the row pointers, prime() loads the first U
-// blocks of every row (a kernel may call it before waiting for the previous
-// kernel, since weights never depend on it), run() streams the rest.  Loads
-// of the next U blocks alternate between two register sets (the loop body
-// is written twice), so no copies are needed between iterations.
+// One row task of NS rows: set the row pointers, prime() issues the loads of
+// the first batch (U blocks of every row; a kernel may call it before
+// waiting for the previous kernel, since weights never depend on it), run()
+// computes each batch and then issues the next.  A batch is loaded whole
+// before any of it is used, so a lane keeps U*NS 16-byte loads in flight and
+// the SM as many bytes as its warps hold batches: HBM latency is covered by
+// the bytes in flight (Little's law), not by a second register set.
 template <int LG, int NS, int U>
 struct Q40Stream {
     const uint4 *wp[NS];
     const uint16_t *sp[NS];
-    uint4 wA[U][NS], wB[U][NS];
-    uint32_t dA[U][NS], dB[U][NS];
+    uint4 w[U][NS];
+    uint32_t d[U][NS];
 
-    __device__ __forceinline__ void load(uint4 (&w)[U][NS], uint32_t (&d)[U][NS], int b0, int nb) const
+    __device__ __forceinline__ void load(int b0, int nb)
     {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -80,8 +82,7 @@ struct Q40Stream {
             }
         }
     }
-    __device__ __forceinline__ void compute(const uint4 (&w)[U][NS], const uint32_t (&d)[U][NS], int b0, int nb,
-                                            const float *xs, float2 (&acc)[NS]) const
+    __device__ __forceinline__ void compute(int b0, int nb, const float *xs, float2 (&acc)[NS]) const
     {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -97,19 +98,18 @@ struct Q40Stream {
             }
         }
     }
-    __device__ __forceinline__ void prime(int nb, int lp) { load(wA, dA, lp, nb); }
+    __device__ __forceinline__ void prime(int nb, int lp) { load(lp, nb); }
     __device__ __forceinline__ void run(const float *xs, int nb, int lp, float (&out)[NS])
     {
         constexpr int STEP = LG * U;
         float2 acc[NS];
 #pragma unroll
         for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
-        for (int b0 = lp; b0 < nb; b0 += 2 * STEP) {
-            load(wB, dB, b0 + STEP, nb);
-            compute(wA, dA, b0, nb, xs, acc);
-            if (b0 + STEP >= nb) break;
-            load(wA, dA, b0 + 2 * STEP, nb);
-            compute(wB, dB, b0 + STEP, nb, xs, acc);
+        for (int b0 = lp;;) {
+            compute(b0, nb, xs, acc);
+            b0 += STEP;
+            if (b0 >= nb) break;
+            load(b0, nb);
         }
 #pragma unroll
         for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
@@ -209,15 +209,16 @@ __device__ __forceinline__ void q4k_dm(uint4 rec, const Q4KSub &c, float &dsc, f
     dm = half_bits_to_float(rec.x >> 16) * __uint2float_rn(imn);
 }
 
-// One row task of NS Q4_K rows, in the same prime() / run() form as Q40Stream.
+// One row task of NS Q4_K rows, in the same batched prime() / run() form as
+// Q40Stream.
 template <int LG, int NS, int U>
 struct Q4KStream {
     static_assert(LG % 8 == 0, "a lane's sub-block position must be fixed");
     const uint4 *wp[NS];
     const uint4 *rp[NS];
-    uint4 wA[U][NS], wB[U][NS], rA[U][NS], rB[U][NS];
+    uint4 w[U][NS], r[U][NS];
 
-    __device__ __forceinline__ void load(uint4 (&w)[U][NS], uint4 (&r)[U][NS], int b0, int nsb) const
+    __device__ __forceinline__ void load(int b0, int nsb)
     {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -231,8 +232,8 @@ struct Q4KStream {
             }
         }
     }
-    __device__ __forceinline__ void compute(const uint4 (&w)[U][NS], const uint4 (&r)[U][NS], int b0, int nsb,
-                                            const float *xs, const Q4KSub &sub, float2 (&acc)[NS]) const
+    __device__ __forceinline__ void compute(int b0, int nsb, const float *xs, const Q4KSub &sub,
+                                            float2 (&acc)[NS]) const
     {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -252,7 +253,7 @@ struct Q4KStream {
             }
         }
     }
-    __device__ __forceinline__ void prime(int nsb, int lp) { load(wA, rA, lp, nsb); }
+    __device__ __forceinline__ void prime(int nsb, int lp) { load(lp, nsb); }
     __device__ __forceinline__ void run(const float *xs, int nsb, int lp, float (&out)[NS])
     {
         constexpr int STEP = LG * U;
@@ -260,12 +261,11 @@ struct Q4KStream {
         float2 acc[NS];
 #pragma unroll
         for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
-        for (int b0 = lp; b0 < nsb; b0 += 2 * STEP) {
-            load(wB, rB, b0 + STEP, nsb);
-            compute(wA, rA, b0, nsb, xs, sub, acc);
-            if (b0 + STEP >= nsb) break;
-            load(wA, rA, b0 + 2 * STEP, nsb);
-            compute(wB, rB, b0 + STEP, nsb, xs, sub, acc);
+        for (int b0 = lp;;) {
+            compute(b0, nsb, xs, sub, acc);
+            b0 += STEP;
+            if (b0 >= nsb) break;
+            load(b0, nsb);
         }
 #pragma unroll
         for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
@@ -325,6 +325,28 @@ __device__ __forceinline__ void tail_slice(int nb, int align, int w, int &lo, in
     hi = (units * (w + 1) / kWarpsPerCta) * align;
 }
 
+// Ask L2 for the weights of the TR-row task starting at row r0: lane i < TR
+// prefetches row r0 + i of the payload plane (row_bytes each, a multiple of
+// 16); lane 31 prefetches the rows' scale records, one contiguous range of
+// the scale plane (row_sc bytes per row) rounded to 16-byte boundaries that
+// stay inside the plane.  A prefetch is only a hint: the loads that follow
+// read the same bytes whether or not it has landed.
+template <int TR>
+__device__ __forceinline__ void prefetch_task_l2(const uint8_t *pay, uint32_t row_bytes, const uint8_t *sc,
+                                                 uint32_t row_sc, int r0, int rows, int lane)
+{
+    if (lane < TR && r0 + lane < rows) prefetch_l2_bulk(pay + static_cast<size_t>(r0 + lane) * row_bytes, row_bytes);
+    if (lane == 31 && r0 < rows) {
+        const size_t plane = static_cast<size_t>(rows) * row_sc;
+        const size_t lo = (static_cast<size_t>(r0) * row_sc) & ~static_cast<size_t>(15);
+        size_t hi = static_cast<size_t>(min(r0 + TR, rows)) * row_sc;
+        hi = (hi + 15) & ~static_cast<size_t>(15);
+        const size_t cap = plane & ~static_cast<size_t>(15);
+        if (hi > cap) hi = cap;
+        if (hi > lo) prefetch_l2_bulk(sc + lo, static_cast<uint32_t>(hi - lo));
+    }
+}
+
 // Before waiting on the previous kernel, ask L2 to fetch the weight rows of
 // this warp's first task (weights never depend on the previous kernel).
 // One lane per row issues a bulk prefetch of the whole row.
@@ -354,6 +376,10 @@ __device__ __forceinline__ float gelu_tanh(float a)
 #define GQ_GEO_CASE1(geo, CASE, LG, R)                                  \
     if ((geo).lg == LG && (geo).r == R && (geo).u == 2) { CASE(LG, R, 2); } \
     if ((geo).lg == LG && (geo).r == R && (geo).u == 4) { CASE(LG, R, 4); }
+// the 4-bit streams also take eight-block batches
+#define GQ_GEO_CASE1B(geo, CASE, LG, R)                                 \
+    GQ_GEO_CASE1(geo, CASE, LG, R)                                      \
+    if ((geo).lg == LG && (geo).r == R && (geo).u == 8) { CASE(LG, R, 8); }
 #define GQ_GEO_SWITCH(geo, CASE)              \
     do {                                      \
         GQ_GEO_CASE1(geo, CASE, 32, 1)        \
@@ -367,13 +393,23 @@ __device__ __forceinline__ float gelu_tanh(float a)
         GQ_GEO_CASE1(geo, CASE, 8, 4)         \
         return GQ_ERR_SHAPE;                  \
     } while (0)
+#ifdef GQ_TUNING
+#define GQ_GEO_TUNING_CASES(geo, CASE)                                              \
+    if ((geo).lg == 8 && (geo).r == 4 && (geo).u == 4) { CASE(8, 4, 4); }          \
+    if ((geo).lg == 16 && (geo).r == 4 && (geo).u == 4) { CASE(16, 4, 4); }        \
+    if ((geo).lg == 32 && (geo).r == 4 && (geo).u == 4) { CASE(32, 4, 4); }        \
+    if ((geo).lg == 8 && (geo).r == 4 && (geo).u == 2) { CASE(8, 4, 2); }
+#else
+#define GQ_GEO_TUNING_CASES(geo, CASE)
+#endif
 #define GQ_GEO_SWITCH_R12(geo, CASE)          \
     do {                                      \
-        GQ_GEO_CASE1(geo, CASE, 32, 1)        \
-        GQ_GEO_CASE1(geo, CASE, 32, 2)        \
-        GQ_GEO_CASE1(geo, CASE, 16, 1)        \
-        GQ_GEO_CASE1(geo, CASE, 16, 2)        \
-        GQ_GEO_CASE1(geo, CASE, 8, 1)         \
-        GQ_GEO_CASE1(geo, CASE, 8, 2)         \
+        GQ_GEO_CASE1B(geo, CASE, 32, 1)        \
+        GQ_GEO_CASE1B(geo, CASE, 32, 2)        \
+        GQ_GEO_CASE1B(geo, CASE, 16, 1)        \
+        GQ_GEO_CASE1B(geo, CASE, 16, 2)        \
+        GQ_GEO_CASE1B(geo, CASE, 8, 1)         \
+        GQ_GEO_CASE1B(geo, CASE, 8, 2)         \
+        GQ_GEO_TUNING_CASES(geo, CASE)        \
         return GQ_ERR_SHAPE;                  \
     } while (0)

@@ -18,11 +18,26 @@
 //
 // Exact sum of squares: x = m 2^(e - 150) with m the 24-bit significand
 // (e the biased exponent; subnormals take e = 1 and no hidden bit), so
-// x^2 = m^2 2^(2e - 300) with m^2 < 2^48.  Squares with the same e add
-// exactly in a 64-bit integer bucket (K <= 49152 < 2^16 terms), in any order
-// (per warp, then across the warps); the
-// buckets then add exactly as B_e << 2(e - 1) into a 608-bit integer, which
-// is rounded once, to nearest even, into the double ss = N 2^-298.
+// x^2 = m^2 2^(2e - 300) with m^2 < 2^48.
+//
+// Fast path (every row but a vanishing fraction): with E the row's largest
+// exponent, each square is added to a 128-bit integer in units of
+// 2^(2E - 364) (m^2 shifted left by 2(e - E) + 64, i.e. 64 bits below the
+// largest square's last bit); bits shifted out below the unit are dropped,
+// and a sticky flag records whether any was nonzero.  The sum A is below
+// K 2^112 < 2^128, and its leading bit is at least bit 64, so the double's
+// rounding position lies at least 11 bits above the unit.  The dropped part
+// delta is below K units (one per term at most), so the rounding of the
+// exact sum is decided by A alone unless the bits of A below the rounding
+// position are within K units under the half-way point (then delta could
+// carry the remainder over it): exactly half-way, the sticky flag breaks the
+// tie; in the window below half-way, the row takes the slow path.
+//
+// Slow path: squares with the same e add exactly in a 64-bit integer bucket
+// (K <= 49152 < 2^16 terms), in any order (per warp, then across the
+// warps); the buckets then add exactly as B_e << 2(e - 1) into a 608-bit
+// integer, which is rounded once, to nearest even, into the double
+// ss = N 2^-298.
 #include "gq_host.h"
 #include "gq_internal.cuh"
 
@@ -127,63 +142,241 @@ __device__ double exact_sum(const unsigned long long *bucket, const uint32_t (&o
     return __longlong_as_double((be << 52) | static_cast<long long>(m & 0xFFFFFFFFFFFFFull));
 }
 
+// x = m 2^(e - 150): biased exponent (subnormals and zero: 1) and the
+// significand with its hidden bit (0 for zero); non-finite values are
+// reported through `bad` (bit 0 infinity, bit 1 NaN) and contribute zero.
+__device__ __forceinline__ void split_f32(float f, uint32_t &e, uint32_t &m, int &bad)
+{
+    const uint32_t b = __float_as_uint(f) & 0x7FFFFFFFu;
+    e = b >> 23;
+    m = b & 0x7FFFFFu;
+    if (e == 255u) {
+        bad |= m ? 2 : 1;
+        m = 0u;
+        e = 1u;
+    } else if (e == 0u) {
+        e = 1u;
+    } else {
+        m |= 0x800000u;
+    }
+}
+
+// (hi, lo) += m^2 2^(2(e - E) + 64), dropping (and flagging in `sticky`)
+// the bits below the unit.
+__device__ __forceinline__ void add_square_fixed(uint32_t e, uint32_t m, uint32_t E, unsigned long long &lo,
+                                                 unsigned long long &hi, bool &sticky)
+{
+    const unsigned long long sq = static_cast<unsigned long long>(m) * m;
+    const int s = 2 * (static_cast<int>(e) - static_cast<int>(E)) + 64;
+    unsigned long long tl, th;
+    if (s >= 64) {
+        tl = 0ull;
+        th = sq;  // s == 64 (e == E)
+    } else if (s > 0) {
+        tl = sq << s;
+        th = sq >> (64 - s);
+    } else if (s == 0) {
+        tl = sq;
+        th = 0ull;
+    } else if (s > -64) {
+        tl = sq >> (-s);
+        th = 0ull;
+        sticky |= (sq & ((1ull << (-s)) - 1ull)) != 0ull;
+    } else {
+        tl = 0ull;
+        th = 0ull;
+        sticky |= sq != 0ull;
+    }
+    lo += tl;
+    hi += th + (lo < tl ? 1ull : 0ull);
+}
+
+// The double nearest A 2^(2E - 364) given the dropped part's sticky flag,
+// or a negative value if the rounding is not decided by A (K terms: the
+// dropped part is below K units).
+__device__ __forceinline__ double round_fixed(unsigned long long lo, unsigned long long hi, uint32_t E, bool sticky,
+                                              int K)
+{
+    // leading bit p of A (A >= 2^64 whenever any x is nonzero; A == 0 otherwise)
+    if (hi == 0ull && lo == 0ull) return sticky ? -1.0 : 0.0;
+    const int p = hi ? 64 + 63 - __clzll(static_cast<long long>(hi)) : 63 - __clzll(static_cast<long long>(lo));
+    if (p < 53) return -1.0;  // cannot happen for a nonzero row; take the slow path
+    const int sh = p - 52;    // bits below the double's last bit
+    // mantissa m53 = A >> sh, remainder r = A mod 2^sh (sh <= 75)
+    unsigned long long m53, rhi, rlo;  // remainder as a 128-bit (rhi, rlo)
+    if (sh >= 64) {
+        m53 = hi >> (sh - 64);
+        rlo = lo;
+        rhi = (sh == 64) ? 0ull : (hi & ((1ull << (sh - 64)) - 1ull));
+    } else {
+        m53 = (lo >> sh) | (hi << (64 - sh));
+        rlo = lo & ((1ull << sh) - 1ull);
+        rhi = 0ull;
+    }
+    // half = 2^(sh - 1) as (hhi, hlo)
+    const int hb = sh - 1;
+    const unsigned long long hhi = hb >= 64 ? (1ull << (hb - 64)) : 0ull;
+    const unsigned long long hlo = hb >= 64 ? 0ull : (1ull << hb);
+    const bool r_gt = rhi > hhi || (rhi == hhi && rlo > hlo);
+    const bool r_eq = rhi == hhi && rlo == hlo;
+    bool up;
+    if (r_gt) {
+        up = true;
+    } else if (r_eq) {
+        up = sticky || (m53 & 1ull);
+    } else {
+        // below half: decided unless half - r <= K units (the dropped part could reach it)
+        const unsigned long long dlo = hlo - rlo;
+        const unsigned long long dhi = hhi - rhi - (hlo < rlo ? 1ull : 0ull);
+        if (dhi == 0ull && dlo <= static_cast<unsigned long long>(K)) return -1.0;
+        up = false;
+    }
+    int pos = p;
+    if (up) {
+        ++m53;
+        if (m53 >> 53) {
+            m53 >>= 1;
+            ++pos;
+        }
+    }
+    const long long be = static_cast<long long>(pos) + 2 * static_cast<long long>(E) - 364 + 1023;
+    return __longlong_as_double((be << 52) | static_cast<long long>(m53 & 0xFFFFFFFFFFFFFull));
+}
+
+// Shared memory of the sum of squares of one row.
+struct SumSqSmem {
+    unsigned long long wbk[kWarps][256];  // per-warp exponent buckets (slow path)
+    unsigned long long bucket[256];
+    unsigned long long part_lo[kThreads], part_hi[kThreads];
+    uint32_t emax[kWarps];
+    int nonfinite;
+    int slow;
+    double ss;
+};
+
+// The sum of the squares of row xr (K floats) rounded once to double
+// (+infinity if the row holds an infinity, NaN if it holds a NaN); every
+// thread of the CTA calls it and gets the result.
+__device__ double row_sum_squares(const float4 *__restrict__ xr, int K, SumSqSmem &sm)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nq = K >> 2;
+    if (threadIdx.x == 0) sm.nonfinite = 0;
+
+    // pass 1: the row's largest exponent (and whether it holds a non-finite value)
+    uint32_t emax = 1u;
+    int bad = 0;
+    for (int i = threadIdx.x; i < nq; i += kThreads) {
+        const float4 v = __ldg(xr + i);
+        const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t e, m;
+            split_f32(f[k], e, m, bad);
+            if (m != 0u && e > emax) emax = e;
+        }
+    }
+    emax = __reduce_max_sync(0xffffffffu, emax);
+    bad = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bad)));
+    if (lane == 0) sm.emax[warp] = emax;
+    __syncthreads();
+    if (lane == 0 && bad) atomicOr(&sm.nonfinite, bad);
+    uint32_t E = sm.emax[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) E = max(E, sm.emax[w]);
+
+    // pass 2: the squares in 128-bit fixed point anchored at E
+    unsigned long long lo = 0ull, hi = 0ull;
+    bool sticky = false;
+    for (int i = threadIdx.x; i < nq; i += kThreads) {
+        const float4 v = __ldg(xr + i);
+        const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t e, m;
+            int ignored = 0;
+            split_f32(f[k], e, m, ignored);
+            add_square_fixed(e, m, E, lo, hi, sticky);
+        }
+    }
+    sm.part_lo[threadIdx.x] = lo;
+    sm.part_hi[threadIdx.x] = hi;
+    const int any_sticky = __syncthreads_or(sticky ? 1 : 0);
+    if (threadIdx.x < 32) {  // warp 0 adds the partial sums (exactly: the total stays below 2^128)
+        unsigned long long a = 0ull, b = 0ull;
+        for (int j = threadIdx.x; j < kThreads; j += 32) {
+            a += sm.part_lo[j];
+            b += sm.part_hi[j] + (a < sm.part_lo[j] ? 1ull : 0ull);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long oa = __shfl_xor_sync(0xffffffffu, a, o);
+            const unsigned long long ob = __shfl_xor_sync(0xffffffffu, b, o);
+            a += oa;
+            b += ob + (a < oa ? 1ull : 0ull);
+        }
+        if (threadIdx.x == 0) {
+            double ss;
+            if (sm.nonfinite & 2)
+                ss = __longlong_as_double(0x7FF8000000000000ll);  // NaN
+            else if (sm.nonfinite & 1)
+                ss = __longlong_as_double(0x7FF0000000000000ll);  // +infinity
+            else
+                ss = round_fixed(a, b, E, any_sticky != 0, K);
+            sm.slow = ss < 0.0 ? 1 : 0;
+            sm.ss = ss;
+        }
+    }
+    __syncthreads();
+    if (sm.slow) {
+        // the rounding is not decided by the fixed-point sum: exact exponent buckets
+        for (int i = threadIdx.x; i < kWarps * 256; i += kThreads) (&sm.wbk[0][0])[i] = 0ull;
+        __syncthreads();
+        // warp-uniform loop (the reductions use the full warp); lanes past the
+        // row contribute zeros
+        for (int i0 = warp * 32; i0 < nq; i0 += kThreads) {
+            const int i = i0 + lane;
+            const float4 v = i < nq ? xr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            add_squares_warp(sm.wbk[warp], &sm.nonfinite, v.x, lane);
+            add_squares_warp(sm.wbk[warp], &sm.nonfinite, v.y, lane);
+            add_squares_warp(sm.wbk[warp], &sm.nonfinite, v.z, lane);
+            add_squares_warp(sm.wbk[warp], &sm.nonfinite, v.w, lane);
+        }
+        __syncthreads();
+        {  // the warps' buckets, added exactly (each total stays below K 2^48 < 2^64)
+            unsigned long long sb = 0ull;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) sb += sm.wbk[w][threadIdx.x];
+            sm.bucket[threadIdx.x] = sb;
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {  // warp 0: which buckets are occupied, then lane 0 adds them
+            uint32_t occ[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                occ[k] = __ballot_sync(0xffffffffu, sm.bucket[32 * k + threadIdx.x] != 0ull);
+            if (threadIdx.x == 0) sm.ss = exact_sum(sm.bucket, occ);
+        }
+        __syncthreads();
+    }
+    return sm.ss;
+}
+
 __global__ void __launch_bounds__(kThreads)
     k_rmsnorm_q8_0(const float4 *__restrict__ X, const float4 *__restrict__ w, float offset, float eps,
                    uint32_t *__restrict__ Xq, float *__restrict__ dx, int K)
 {
-    __shared__ unsigned long long wbk[kWarps][256];  // per-warp exponent buckets
-    __shared__ unsigned long long bucket[256];
-    __shared__ int nonfinite;
-    __shared__ float s_inv;
+    __shared__ SumSqSmem sm;
     const int t = blockIdx.x;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nq = K >> 2, nblk = K >> 5;
-    const float4 *xr = X + static_cast<size_t>(t) * nq;
-    for (int i = threadIdx.x; i < kWarps * 256; i += kThreads) (&wbk[0][0])[i] = 0ull;
-    if (threadIdx.x == 0) nonfinite = 0;
+    const int nblk = K >> 5;
+    const float4 *xr = X + static_cast<size_t>(t) * (K >> 2);
     // dependents launch once every CTA has started; they still wait for this
     // grid's completion before reading Xq and dx
     pdl_launch_dependents();
     pdl_wait();
-    __syncthreads();
-
-    // warp-uniform loop (the reductions use the full warp); lanes past the
-    // row contribute zeros
-    for (int i0 = warp * 32; i0 < nq; i0 += kThreads) {
-        const int i = i0 + lane;
-        const float4 v = i < nq ? xr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-        add_squares_warp(wbk[warp], &nonfinite, v.x, lane);
-        add_squares_warp(wbk[warp], &nonfinite, v.y, lane);
-        add_squares_warp(wbk[warp], &nonfinite, v.z, lane);
-        add_squares_warp(wbk[warp], &nonfinite, v.w, lane);
-    }
-    __syncthreads();
-    {  // the warps' buckets, added exactly (each total stays below K 2^48 < 2^64)
-        unsigned long long s = 0ull;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += wbk[w][threadIdx.x];
-        bucket[threadIdx.x] = s;
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {  // warp 0: which buckets are occupied, then lane 0 adds them
-        uint32_t occ[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) occ[k] = __ballot_sync(0xffffffffu, bucket[32 * k + threadIdx.x] != 0ull);
-        if (threadIdx.x == 0) {
-            double ss;
-            if (nonfinite & 2)
-                ss = __longlong_as_double(0x7FF8000000000000ll);  // NaN
-            else if (nonfinite & 1)
-                ss = __longlong_as_double(0x7FF0000000000000ll);  // +infinity
-            else
-                ss = exact_sum(bucket, occ);
-            const double r =
-                __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(K)), static_cast<double>(eps)));
-            s_inv = __double2float_rn(__ddiv_rn(1.0, r));
-        }
-    }
-    __syncthreads();
-    const float inv = s_inv;
+    const double ss = row_sum_squares(xr, K, sm);
+    const double r = __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(K)), static_cast<double>(eps)));
+    const float inv = __double2float_rn(__ddiv_rn(1.0, r));
 
     // Q8_0 of y: eight lanes per 32-block (four elements each), four blocks
     // per warp in a warp-uniform loop so the full-mask shuffles never diverge
@@ -221,7 +414,23 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// The statistic alone: ss[t] for every row (for tests of the exact sum).
+__global__ void __launch_bounds__(kThreads) k_row_sum_squares(const float4 *__restrict__ X, double *__restrict__ ss, int K)
+{
+    __shared__ SumSqSmem sm;
+    pdl_launch_dependents();
+    pdl_wait();
+    const double v = row_sum_squares(X + static_cast<size_t>(blockIdx.x) * (K >> 2), K, sm);
+    if (threadIdx.x == 0) ss[blockIdx.x] = v;
+}
+
 }  // namespace norm
+
+int launch_row_sum_squares(const float *X, double *ss, int K, int M, cudaStream_t s)
+{
+    return status_from(launch_pdl(norm::k_row_sum_squares, dim3(static_cast<unsigned>(M)), dim3(norm::kThreads), 0, s,
+                                  reinterpret_cast<const float4 *>(X), ss, K));
+}
 
 int launch_rmsnorm_q8_0(const float *X, const float *w, float offset, float eps, int8_t *Xq, float *dx, int K,
                         int M, cudaStream_t s)

@@ -77,6 +77,9 @@ __global__ void k_pack_q4_0(const uint8_t *__restrict__ src, uint8_t *__restrict
             for (int j = 0; j < 16; ++j) blk[2 + j] = tmp[j];
         }
     }
+    // The decode kernels read their weights before they wait for the preceding kernel
+    // (weights are model constants): make the packed bytes visible before this block exits.
+    __threadfence();
 }
 
 __global__ void k_pack_q8_0(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, long long nblk,
@@ -102,6 +105,9 @@ __global__ void k_pack_q8_0(const uint8_t *__restrict__ src, uint8_t *__restrict
             for (int j = 0; j < 32; ++j) blk[2 + j] = q[j] ^ 0x80u;
         }
     }
+    // The decode kernels read their weights before they wait for the preceding kernel
+    // (weights are model constants): make the packed bytes visible before this block exits.
+    __threadfence();
 }
 
 __global__ void k_pack_q4_k(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, long long nsup,
@@ -141,6 +147,9 @@ __global__ void k_pack_q4_k(const uint8_t *__restrict__ src, uint8_t *__restrict
             }
         }
     }
+    // The decode kernels read their weights before they wait for the preceding kernel
+    // (weights are model constants): make the packed bytes visible before this block exits.
+    __threadfence();
 }
 
 // Q6_K canonical block (ql[128], qh[64], sc[16], d): in each 128-weight half
@@ -183,6 +192,9 @@ __global__ void k_pack_q6_k(const uint8_t *__restrict__ src, uint8_t *__restrict
             }
         }
     }
+    // The decode kernels read their weights before they wait for the preceding kernel
+    // (weights are model constants): make the packed bytes visible before this block exits.
+    __threadfence();
 }
 
 int launch_pack(int format, const void *src, void *dst, int rows, int K, bool unpack, cudaStream_t s)

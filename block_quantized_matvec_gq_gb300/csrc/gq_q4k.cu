@@ -58,6 +58,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
 
         for (int task = first; task < ntasks; task += stride) {
             setup(task);
+            // the next task's rows stream into L2 while this one computes
+            if (task + stride < ntasks)
+                prefetch_task_l2<TR>(reinterpret_cast<const uint8_t *>(nib), nsb * 16u,
+                                     reinterpret_cast<const uint8_t *>(rec), ns * 16u, (task + stride) * TR, rows, lane);
             float out[R];
             st.run(xs, nsb, lp, out);
             const int r0 = task * TR + g * R;
@@ -99,6 +103,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
         for (int j = 0; j < cr.count; ++j) {
             const int r0 = cr.start + j * cr.step;
             if (j > 0 || !kEarly) setup(r0, 0, nsb);
+            // the next task's rows stream into L2 while this one computes
+            if (j + 1 < cr.count)
+                prefetch_task_l2<TR>(reinterpret_cast<const uint8_t *>(nib), nsb * 16u,
+                                     reinterpret_cast<const uint8_t *>(rec), ns * 16u, r0 + cr.step, rows, lane);
             float out[R];
             st.run(xs, nsb, lp, out);
     #pragma unroll
@@ -139,7 +147,6 @@ int launch_q4k_matvec(const void *W, const float *x, float *y, int rows, int K, 
     const uint4 *rec = nib + static_cast<size_t>(rows) * nsb;
     const size_t smem = static_cast<size_t>(nsb) * kXBlk * sizeof(float);
     const long long ntasks = (rows + (32 / geo.lg) * geo.r - 1) / ((32 / geo.lg) * geo.r);
-    if (geo.p != 1) return GQ_ERR_SHAPE;
 #define CASE(LG, R, U)                                                                                  \
     {                                                                                                   \
         auto rr = k_q4k_matvec<LG, R, U, 0>;                                                                     \

@@ -6,14 +6,21 @@ namespace gq {
 
 static __device__ int g_status_word = 0;
 
+// Device address of the status word on the current device (looked up once
+// per device, under a lock: launchers may run on several host threads).
 int *status_word()
 {
     static int *cache[64] = {nullptr};
+    static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
     if (cache[dev] == nullptr) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
         cache[dev] = static_cast<int *>(p);
     }
     return cache[dev];

@@ -34,6 +34,13 @@
  *     as the canonical GGUF-order blocks; see gq_pack).
  *   - Results are deterministic: the same inputs give bitwise the same
  *     outputs on the same GPU and launch configuration.
+ *   - The decode kernels may start while the preceding kernel in `stream`
+ *     is still running (programmatic dependent launch).  They read their
+ *     activation inputs and write their outputs only after that kernel has
+ *     completed, but they may read the packed weights W earlier: weights
+ *     are constants of the model.  W must therefore not be written by the
+ *     kernel that immediately precedes the call in `stream`, unless that
+ *     kernel is gq_pack's (which makes its writes visible before it exits).
  */
 #ifndef GQ_H
 #define GQ_H
@@ -178,6 +185,9 @@ int gq_logits_topk(const void *W, const float *x, float softcap, int k, int *idx
  * gq_logits_topk accepts fits, and a call that would not fit is rejected with
  * GQ_ERR_SHAPE.  The first call on a device looks the array's address up
  * (cudaGetSymbolAddress) -- make that first call before any stream capture.
+ * The address is kept for the life of the process: do not call this entry
+ * point again after cudaDeviceReset (or any other re-creation of the
+ * device's primary context), which would leave it stale.
  * Calls share the array: calls that may overlap on the GPU race on it.
  * Nothing is allocated. */
 int gq_logits_topk_noalloc(const void *W, const float *x, float softcap, int k, int *idx, float *val,

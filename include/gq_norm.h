@@ -45,6 +45,18 @@ extern "C" {
 int gq_rmsnorm_quantize_q8_0(const float *X, const float *w, float offset, float eps, int8_t *Xq, float *dx,
                              int K, int M, gq_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * The statistic of gq_rmsnorm_quantize_q8_0 alone: ss[t] = sum_j X[t][j]^2
+ * rounded once to double, for every token t < M (the same device code as
+ * the fused kernel's; exported so that the exact summation can be checked
+ * on its own).  +infinity for a row holding an infinity and no NaN, NaN for
+ * a row holding a NaN.
+ *   X  f32[M][K] row-major, 16-byte aligned; ss f64[M], 16-byte aligned.
+ *   1 <= M, 32 <= K <= GQ_MAX_K, K % 32 == 0.
+ * Errors as gq_rmsnorm_quantize_q8_0's.
+ * ------------------------------------------------------------------------ */
+int gq_rmsnorm_sum_squares(const float *X, double *ss, int K, int M, gq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,7 +36,7 @@ def run_matvec(fmt, W_canon, x, rows, K):
 
 
 SHAPES = [(1, 32), (3, 64), (37, 96), (257, 256), (1000, 512), (129, 4096), (515, 5376), (77, 21504),
-          (33, 2304), (250, 800), (8, 49152)]
+          (33, 2304), (250, 800), (8, 49152), (256, 21504), (5, 2048), (600, 1024), (2048, 49152)]
 
 
 @pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K, oracle.FORMAT_Q6_K])
@@ -143,6 +143,26 @@ def test_repeat_runs_are_bitwise_identical(fmt):
         ys.append(y)
     for y in ys[1:]:
         assert t.equal(y, ys[0])
+
+
+@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q4_K])
+@pytest.mark.parametrize("rows,K", [(8, 49152), (77, 21504), (256, 21504), (600, 4096)])
+def test_split_k_repeat_runs_are_bitwise_identical(fmt, rows, K):
+    """Short, wide shapes split K across the CTAs of a cluster; the partial
+    sums are added in a fixed order, so repeated runs agree bit for bit."""
+    W = synth.weights(fmt, rows, K, synth.stream(9, rows))
+    t = torch()
+    Wp = packed(fmt, W, rows, K)
+    x = dev(synth.normal(K, synth.stream(9, rows + 1)))
+    ys = []
+    for _ in range(4):
+        y = t.empty(rows, dtype=t.float32, device="cuda")
+        FMT_FN[fmt](Wp, x, y, rows, K)
+        ys.append(y)
+    for y in ys[1:]:
+        assert t.equal(y, ys[0])
+    y_ref, a_ref = oracle.matvec(fmt, W, x.cpu().numpy(), rows, K)
+    assert_within(ys[0].cpu().numpy(), y_ref, a_ref, what=f"fmt{fmt} {rows}x{K} split-K")
 
 
 def test_argument_errors_launch_nothing():

@@ -71,3 +71,51 @@ def test_rmsnorm_q8_offset_and_eps():
     check(X, w, 0.0, 1e-6, M, K)
     check(X, w, 1.0, 10.0, M, K)
     check(X * np.float32(1e-20), w, 1.0, np.float32(1e-38), M, K)
+
+
+def gpu_sum_squares(X, M, K):
+    t = torch()
+    fs, ss, cs = guarded(M, t.float64, fill=-7.25)
+    gq.gq_rmsnorm_sum_squares(dev(X), ss, K, M)
+    t.cuda.synchronize()
+    cs()
+    return ss.cpu().numpy()
+
+
+def midpoint_rows(K):
+    """Rows whose exact sum of squares lies on or next to a rounding boundary
+    of the double: 1 + 2^-53 (an exact tie: stays 1), the same plus a square
+    far below the fixed-point window (the tie broken upward), 1 + 3 2^-53
+    (a tie rounding up to even), and the tie plus a square just inside the
+    window."""
+    rows = []
+    base = np.zeros(K, np.float64)
+    r = base.copy(); r[0] = 1.0; r[1] = r[2] = 2.0 ** -27; rows.append(r)                   # 1 + 2^-53
+    r = rows[0].copy(); r[3] = 2.0 ** -100; rows.append(r)                                  # + 2^-200
+    r = base.copy(); r[0] = 1.0; r[1] = r[2] = 2.0 ** -27; r[3] = 2.0 ** -26.0; rows.append(r)  # 1 + 3 2^-53
+    r = rows[0].copy(); r[3] = 2.0 ** -50; rows.append(r)                                   # + 2^-100
+    r = base.copy(); r[0] = 2.0 ** 60; r[1] = r[2] = 2.0 ** 33; r[K - 1] = 2.0 ** -140; rows.append(r)
+    return np.stack(rows).astype(np.float32)
+
+
+@pytest.mark.parametrize("K", [32, 256, 5376, 49152])
+def test_sum_of_squares_is_the_correctly_rounded_sum(K):
+    """The statistic itself against math.fsum (the oracle's), bit for bit, on
+    normal rows, the special rows and rows on rounding boundaries."""
+    rng = np.random.default_rng(830 + K)
+    X = np.concatenate([synth.normal((3, K), synth.stream(830, K)), special_rows(K, rng), midpoint_rows(K)])
+    M = X.shape[0]
+    ss = gpu_sum_squares(X, M, K)
+    _, ss_ref, _ = oracle.rmsnorm(X, np.ones(K, np.float32), 0.0, 1e-6, M, K)
+    assert np.array_equal(ss.view(np.uint64), ss_ref.view(np.uint64)), (ss, ss_ref)
+
+
+def test_sum_of_squares_non_finite_rows():
+    K = 64
+    X = synth.normal((3, K), synth.stream(840, 0))
+    X[0, 5] = np.inf
+    X[1, 7] = np.nan
+    X[2, 9] = -np.inf
+    X[2, 10] = np.nan
+    ss = gpu_sum_squares(X, 3, K)
+    assert ss[0] == np.inf and np.isnan(ss[1]) and np.isnan(ss[2])
