@@ -188,6 +188,28 @@ class Workload:
     def step(self, i):
         raise NotImplementedError
 
+    # End to end through the public API: every step copies the step's inputs
+    # from pinned host memory, runs the step, and reads its outputs back.
+    def e2e_inputs(self):
+        return []
+
+    def e2e_outputs(self):
+        return []
+
+    def e2e_setup(self, torch):
+        self._e2e_in = [(d, d.cpu().pin_memory()) for d in self.e2e_inputs()]
+        self._e2e_out = [(d, torch.empty(d.shape, dtype=d.dtype).pin_memory()) for d in self.e2e_outputs()]
+        self.h2d = sum(h.numel() * h.element_size() for _, h in self._e2e_in)
+        self.d2h = sum(h.numel() * h.element_size() for _, h in self._e2e_out)
+
+    def e2e_step(self, torch):
+        for d, h in self._e2e_in:
+            d.copy_(h, non_blocking=True)
+        self.step(0)
+        for d, h in self._e2e_out:
+            h.copy_(d, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
 
 def _to_dev(torch, a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
@@ -287,6 +309,12 @@ class Q40Matvec(Rotating):
     def step(self, i):
         self.gq.gq_q4_0_matvec(self.copies[i % len(self.copies)], self.x, self.y, self.rows, self.K)
 
+    def e2e_inputs(self):
+        return [self.x]
+
+    def e2e_outputs(self):
+        return [self.y]
+
     def cpu_reference(self, oracle, rows_sample):
         W, x = synth.q4_0_matvec_inputs(self.rows, self.K)
         return self._matvec_reference(oracle, oracle.FORMAT_Q4_0, W, x, rows_sample)
@@ -313,6 +341,12 @@ class Q4KMatvec(Rotating):
 
     def step(self, i):
         self.gq.gq_q4k_matvec(self.copies[i % len(self.copies)], self.x, self.y, self.rows, self.K)
+
+    def e2e_inputs(self):
+        return [self.x]
+
+    def e2e_outputs(self):
+        return [self.y]
 
     def cpu_reference(self, oracle, rows_sample):
         W, x = synth.q4_k_matvec_inputs(self.rows, self.K)
@@ -342,6 +376,12 @@ class Q6KMatvec(Rotating):
 
     def step(self, i):
         self.gq.gq_q6k_matvec(self.copies[i % len(self.copies)], self.x, self.y, self.rows, self.K)
+
+    def e2e_inputs(self):
+        return [self.x]
+
+    def e2e_outputs(self):
+        return [self.y]
 
     def cpu_reference(self, oracle, rows_sample):
         W = synth.q6_k_weights(self.rows, self.K, synth.stream(6, 0))
@@ -375,6 +415,12 @@ class GegluDown(Rotating):
 
     def step(self, i):
         self.gq.gq_q4_0_geglu_down(self.copies[i % len(self.copies)], self.g, self.u, self.y, self.rows, self.K)
+
+    def e2e_inputs(self):
+        return [self.g, self.u]
+
+    def e2e_outputs(self):
+        return [self.y]
 
     def cpu_reference(self, oracle, rows_sample):
         W = synth.q4_0_weights(self.rows, self.K, synth.stream(7, 0))
@@ -416,6 +462,12 @@ class RMSNormQ8(Rotating):
         self.gq.gq_rmsnorm_quantize_q8_0(self.copies[i % len(self.copies)], self.w, 1.0, 1e-6, self.Xq, self.dx,
                                          self.K, self.M)
 
+    def e2e_inputs(self):
+        return [self.copies[0]]   # step(0) reads copy 0
+
+    def e2e_outputs(self):
+        return [self.Xq, self.dx]
+
     def cpu_reference(self, oracle, rows_sample):
         X = synth.normal((self.M, self.K), synth.stream(8, 0))
         w = (synth.normal(self.K, synth.stream(8, 1)) * 0.1).astype(np.float32)
@@ -456,6 +508,12 @@ class FFN(Rotating):
         self.gq.gq_ffn_gate_up_gelu(g, u, self.x, self.h, self.rows, self.K)
         self.gq.gq_q4_0_matvec(d, self.h, self.y, self.K, self.rows)
 
+    def e2e_inputs(self):
+        return [self.x]
+
+    def e2e_outputs(self):
+        return [self.y]
+
     def cpu_reference(self, oracle, rows_sample):
         Wg, Wu, Wd, x = synth.ffn_inputs(self.rows, self.K)
         nb = Wg.shape[1]
@@ -494,6 +552,12 @@ class Gemm(Workload):
         self.gq.gq_quantize_q8_0(self.X, self.Xq, self.dx, self.K, self.M)
         self.gq.gq_q4_0_gemm_q8act(self.Wp, self.Xq, self.dx, self.Y, self.ws, self.ws_bytes, self.rows, self.K,
                                    self.M)
+
+    def e2e_inputs(self):
+        return [self.X]
+
+    def e2e_outputs(self):
+        return [self.Y]
 
     cpu_unit, cpu_scale = "TOPS", 1e12
     cpu_tokens = 16   # the oracle's bounded sample: this many tokens against every row
@@ -605,7 +669,7 @@ def run_gpu(wl_cls, args, rank, world, torch, dist):
 
     ms = max_over_ranks(ms, dist, "cuda")
 
-    # end to end through the public API with host buffers (default workload only)
+    # end to end through the public API with host buffers (every workload)
     e2e = None
     if hasattr(wl, "e2e_setup") and rank == 0:
         wl.e2e_setup(torch)
@@ -617,7 +681,11 @@ def run_gpu(wl_cls, args, rank, world, torch, dist):
             wl.e2e_step(torch)
         t_b = time.perf_counter()
         e2e_ms = (t_b - t_a) * 1e3 / n
-        e2e = {"value": round(wl.bytes_per_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        if wl.bound == "tensor":
+            ev, eu = wl.ops_per_step / (e2e_ms * 1e-3) / 1e12, "TOPS"
+        else:
+            ev, eu = wl.bytes_per_step / (e2e_ms * 1e-3) / 1e9, "GB/s"
+        e2e = {"value": round(ev, 3), "unit": eu,
                "h2d_bytes_per_step": wl.h2d, "d2h_bytes_per_step": wl.d2h,
                "ms_per_step": round(e2e_ms, 4)}
     return wl, ms, clocks, e2e

@@ -49,6 +49,17 @@ bool gemm_force_block_path() { return false; }
 // idle (measured on Q4_0: 256 x 21504 in 5.1 instead of 13.6 us, 8 x 49152 in
 // 3.8 instead of 17.9 us).  Larger matrices keep the register streams, which
 // were as fast or faster at every shape measured.
+// Register-stream schedule from tasks per resident warp: < 1.75 balanced
+// (mode 1), <= 1.25 balanced with the first loads issued early (mode 2),
+// else round-robin (mode 0).
+int schedule_mode(long long ntasks, long long warps)
+{
+#ifdef GQ_TUNING
+    if (const char *v = getenv("GQ_MODE")) return atoi(v);
+#endif
+    return ntasks * 4 <= warps * 5 ? 2 : (ntasks * 4 < warps * 7 ? 1 : 0);
+}
+
 bool ring_preferred(int rows)
 {
     const int o = ring_override();

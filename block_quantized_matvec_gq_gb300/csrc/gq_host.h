@@ -150,6 +150,7 @@ int launch_block_dots_tc(const void *W, const int8_t *Xq, int32_t *D, void *ws, 
                          int M, cudaStream_t s);
 // ring-streamed 4-bit matvecs (gq_stream.cu)
 bool ring_preferred(int rows);
+int schedule_mode(long long ntasks, long long warps);
 bool gemm_force_block_path();
 bool ring_q4_0_supported(int nb);
 int launch_ring_q4_0(const void *W, const float *x, const float *g_or_null, const float *u, float *y, int rows,

@@ -161,32 +161,35 @@ __device__ __forceinline__ void split_f32(float f, uint32_t &e, uint32_t &m, int
     }
 }
 
+// 64-bit shifts whose amount may reach 64: PTX clamps the amount to the
+// register width, so a shift by 64 or more gives 0 (no branch needed).
+__device__ __forceinline__ unsigned long long shl64(unsigned long long a, uint32_t n)
+{
+    unsigned long long r;
+    asm("shl.b64 %0, %1, %2;" : "=l"(r) : "l"(a), "r"(n));
+    return r;
+}
+__device__ __forceinline__ unsigned long long shr64(unsigned long long a, uint32_t n)
+{
+    unsigned long long r;
+    asm("shr.b64 %0, %1, %2;" : "=l"(r) : "l"(a), "r"(n));
+    return r;
+}
+
 // (hi, lo) += m^2 2^(2(e - E) + 64), dropping (and flagging in `sticky`)
-// the bits below the unit.
+// the bits below the unit.  Branch-free: lanes whose values differ in
+// exponent take the same instructions.
 __device__ __forceinline__ void add_square_fixed(uint32_t e, uint32_t m, uint32_t E, unsigned long long &lo,
                                                  unsigned long long &hi, bool &sticky)
 {
     const unsigned long long sq = static_cast<unsigned long long>(m) * m;
-    const int s = 2 * (static_cast<int>(e) - static_cast<int>(E)) + 64;
-    unsigned long long tl, th;
-    if (s >= 64) {
-        tl = 0ull;
-        th = sq;  // s == 64 (e == E)
-    } else if (s > 0) {
-        tl = sq << s;
-        th = sq >> (64 - s);
-    } else if (s == 0) {
-        tl = sq;
-        th = 0ull;
-    } else if (s > -64) {
-        tl = sq >> (-s);
-        th = 0ull;
-        sticky |= (sq & ((1ull << (-s)) - 1ull)) != 0ull;
-    } else {
-        tl = 0ull;
-        th = 0ull;
-        sticky |= sq != 0ull;
-    }
+    const int s = 2 * (static_cast<int>(e) - static_cast<int>(E)) + 64;  // <= 64
+    const uint32_t sp = s > 0 ? static_cast<uint32_t>(s) : 0u;          // left shift (s >= 0)
+    const uint32_t sn = s < 0 ? static_cast<uint32_t>(-s) : 0u;         // right shift (s < 0)
+    const unsigned long long tl = s >= 0 ? shl64(sq, sp) : shr64(sq, sn);
+    const unsigned long long th = shr64(sq, 64u - sp);  // bits at 64 and above (0 unless s > 16)
+    // bits shifted out below the unit: the low min(sn, 64) bits of sq
+    sticky |= s < 0 && shl64(sq, 64u - min(sn, 64u)) != 0ull;
     lo += tl;
     hi += th + (lo < tl ? 1ull : 0ull);
 }
@@ -254,51 +257,33 @@ struct SumSqSmem {
     double ss;
 };
 
-// The sum of the squares of row xr (K floats) rounded once to double
-// (+infinity if the row holds an infinity, NaN if it holds a NaN); every
-// thread of the CTA calls it and gets the result.
-__device__ double row_sum_squares(const float4 *__restrict__ xr, int K, SumSqSmem &sm)
+// Block-wide: the row's largest exponent from every thread's own maximum
+// (and non-finite flags), returned to every thread.
+__device__ __forceinline__ uint32_t block_emax(uint32_t emax, int bad, SumSqSmem &sm)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nq = K >> 2;
-    if (threadIdx.x == 0) sm.nonfinite = 0;
-
-    // pass 1: the row's largest exponent (and whether it holds a non-finite value)
-    uint32_t emax = 1u;
-    int bad = 0;
-    for (int i = threadIdx.x; i < nq; i += kThreads) {
-        const float4 v = __ldg(xr + i);
-        const float f[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            uint32_t e, m;
-            split_f32(f[k], e, m, bad);
-            if (m != 0u && e > emax) emax = e;
-        }
-    }
     emax = __reduce_max_sync(0xffffffffu, emax);
     bad = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bad)));
-    if (lane == 0) sm.emax[warp] = emax;
+    if (lane == 0) {
+        sm.emax[warp] = emax;
+        if (bad) atomicOr(&sm.nonfinite, bad);
+    }
     __syncthreads();
-    if (lane == 0 && bad) atomicOr(&sm.nonfinite, bad);
     uint32_t E = sm.emax[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) E = max(E, sm.emax[w]);
+    return E;
+}
 
-    // pass 2: the squares in 128-bit fixed point anchored at E
-    unsigned long long lo = 0ull, hi = 0ull;
-    bool sticky = false;
-    for (int i = threadIdx.x; i < nq; i += kThreads) {
-        const float4 v = __ldg(xr + i);
-        const float f[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            uint32_t e, m;
-            int ignored = 0;
-            split_f32(f[k], e, m, ignored);
-            add_square_fixed(e, m, E, lo, hi, sticky);
-        }
-    }
+// Block-wide: ss from every thread's fixed-point partial (lo, hi, sticky)
+// anchored at E; rows whose rounding the partials do not decide take the
+// exact exponent buckets over the row in global memory.  Every thread gets
+// the result.
+__device__ double block_sum_squares(unsigned long long lo, unsigned long long hi, bool sticky, uint32_t E,
+                                    const float4 *__restrict__ xr, int K, SumSqSmem &sm)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nq = K >> 2;
     sm.part_lo[threadIdx.x] = lo;
     sm.part_hi[threadIdx.x] = hi;
     const int any_sticky = __syncthreads_or(sticky ? 1 : 0);
@@ -362,6 +347,101 @@ __device__ double row_sum_squares(const float4 *__restrict__ xr, int K, SumSqSme
     return sm.ss;
 }
 
+// The four squares of v into the fixed-point partial.
+__device__ __forceinline__ void add_chunk_fixed(const float4 &v, uint32_t E, unsigned long long &lo,
+                                                unsigned long long &hi, bool &sticky)
+{
+    const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint32_t e, m;
+        int ignored = 0;
+        split_f32(f[k], e, m, ignored);
+        add_square_fixed(e, m, E, lo, hi, sticky);
+    }
+}
+__device__ __forceinline__ void max_chunk_exp(const float4 &v, uint32_t &emax, int &bad)
+{
+    const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint32_t e, m;
+        split_f32(f[k], e, m, bad);
+        if (m != 0u && e > emax) emax = e;
+    }
+}
+
+// Rows of at most kRegChunks * kThreads float4 (K <= 8192) are read once:
+// thread t keeps chunks t, t + kThreads, ... in registers.
+constexpr int kRegChunks = 8;
+
+// The sum of the squares of row xr (K floats) rounded once to double
+// (+infinity if the row holds an infinity, NaN if it holds a NaN); every
+// thread of the CTA calls it and gets the result.  Reads the row from
+// global memory (twice; a third time on the slow path).
+__device__ double row_sum_squares(const float4 *__restrict__ xr, int K, SumSqSmem &sm)
+{
+    const int nq = K >> 2;
+    if (threadIdx.x == 0) sm.nonfinite = 0;
+    uint32_t emax = 1u;
+    int bad = 0;
+    for (int i = threadIdx.x; i < nq; i += kThreads) max_chunk_exp(__ldg(xr + i), emax, bad);
+    const uint32_t E = block_emax(emax, bad, sm);
+    unsigned long long lo = 0ull, hi = 0ull;
+    bool sticky = false;
+    for (int i = threadIdx.x; i < nq; i += kThreads) add_chunk_fixed(__ldg(xr + i), E, lo, hi, sticky);
+    return block_sum_squares(lo, hi, sticky, E, xr, K, sm);
+}
+
+// The same from the row's chunks already in registers (v[j] = chunk
+// threadIdx.x + j kThreads, valid below nq).
+__device__ double row_sum_squares_regs(const float4 (&v)[kRegChunks], const float4 *__restrict__ xr, int K,
+                                       SumSqSmem &sm)
+{
+    const int nq = K >> 2;
+    if (threadIdx.x == 0) sm.nonfinite = 0;
+    uint32_t emax = 1u;
+    int bad = 0;
+#pragma unroll
+    for (int j = 0; j < kRegChunks; ++j)
+        if (static_cast<int>(threadIdx.x) + j * kThreads < nq) max_chunk_exp(v[j], emax, bad);
+    const uint32_t E = block_emax(emax, bad, sm);
+    unsigned long long lo = 0ull, hi = 0ull;
+    bool sticky = false;
+#pragma unroll
+    for (int j = 0; j < kRegChunks; ++j)
+        if (static_cast<int>(threadIdx.x) + j * kThreads < nq) add_chunk_fixed(v[j], E, lo, hi, sticky);
+    return block_sum_squares(lo, hi, sticky, E, xr, K, sm);
+}
+
+// Q8_0 of the normalized chunk x4 (one of the eight chunks of its 32-block,
+// the eight lanes of a block being adjacent): the packed codes and, from
+// every lane, the block's d.  All lanes of the warp take part (shuffles).
+__device__ __forceinline__ uint32_t quant_chunk(float4 x4, float4 w4, float inv, float offset, bool active,
+                                                float &d)
+{
+    float e[4] = {0.f, 0.f, 0.f, 0.f};
+    if (active) {
+        e[0] = __fmul_rn(__fmul_rn(x4.x, inv), __fadd_rn(w4.x, offset));
+        e[1] = __fmul_rn(__fmul_rn(x4.y, inv), __fadd_rn(w4.y, offset));
+        e[2] = __fmul_rn(__fmul_rn(x4.z, inv), __fadd_rn(w4.z, offset));
+        e[3] = __fmul_rn(__fmul_rn(x4.w, inv), __fadd_rn(w4.w, offset));
+    }
+    float amax = fmaxf(fmaxf(fabsf(e[0]), fabsf(e[1])), fmaxf(fabsf(e[2]), fabsf(e[3])));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    d = __fdiv_rn(amax, 127.0f);
+    uint32_t packed = 0;
+    if (d != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float q = fminf(fmaxf(roundf(__fdiv_rn(e[i], d)), -127.0f), 127.0f);
+            packed |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xFFu) << (8 * i);
+        }
+    }
+    return packed;
+}
+
 __global__ void __launch_bounds__(kThreads)
     k_rmsnorm_q8_0(const float4 *__restrict__ X, const float4 *__restrict__ w, float offset, float eps,
                    uint32_t *__restrict__ Xq, float *__restrict__ dx, int K)
@@ -374,6 +454,36 @@ __global__ void __launch_bounds__(kThreads)
     // grid's completion before reading Xq and dx
     pdl_launch_dependents();
     pdl_wait();
+    const int nq = K >> 2;
+    uint32_t *qr = Xq + static_cast<size_t>(t) * (nblk * 8);
+    float *dr = dx + static_cast<size_t>(t) * nblk;
+    if (nq <= kRegChunks * kThreads) {
+        // the row is read once: chunk i = threadIdx.x + j kThreads is v[j];
+        // the eight chunks of a 32-block sit in eight adjacent lanes
+        float4 v[kRegChunks];
+#pragma unroll
+        for (int j = 0; j < kRegChunks; ++j) {
+            const int i = static_cast<int>(threadIdx.x) + j * kThreads;
+            v[j] = i < nq ? __ldg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const double ss = row_sum_squares_regs(v, xr, K, sm);
+        const double r = __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(K)), static_cast<double>(eps)));
+        const float inv = __double2float_rn(__ddiv_rn(1.0, r));
+#pragma unroll
+        for (int j = 0; j < kRegChunks; ++j) {
+            const int i = static_cast<int>(threadIdx.x) + j * kThreads;
+            if (j * kThreads >= nq) break;  // warp-uniform (kThreads is a multiple of 32)
+            const bool active = i < nq;
+            const float4 w4 = active ? __ldg(w + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            float d;
+            const uint32_t packed = quant_chunk(v[j], w4, inv, offset, active, d);
+            if (active) {
+                qr[i] = packed;
+                if ((i & 7) == 0) dr[i >> 3] = d;
+            }
+        }
+        return;
+    }
     const double ss = row_sum_squares(xr, K, sm);
     const double r = __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(K)), static_cast<double>(eps)));
     const float inv = __double2float_rn(__ddiv_rn(1.0, r));
@@ -381,32 +491,13 @@ __global__ void __launch_bounds__(kThreads)
     // Q8_0 of y: eight lanes per 32-block (four elements each), four blocks
     // per warp in a warp-uniform loop so the full-mask shuffles never diverge
     const int sub = threadIdx.x & 7;
-    uint32_t *qr = Xq + static_cast<size_t>(t) * (nblk * 8);
-    float *dr = dx + static_cast<size_t>(t) * nblk;
     for (int wb = (threadIdx.x >> 5) * 4; wb < nblk; wb += (kThreads >> 5) * 4) {
         const int blk = wb + ((threadIdx.x & 31) >> 3);
         const bool active = blk < nblk;
-        float e[4] = {0.f, 0.f, 0.f, 0.f};
-        if (active) {
-            const float4 x4 = xr[blk * 8 + sub];
-            const float4 w4 = __ldg(w + blk * 8 + sub);
-            e[0] = __fmul_rn(__fmul_rn(x4.x, inv), __fadd_rn(w4.x, offset));
-            e[1] = __fmul_rn(__fmul_rn(x4.y, inv), __fadd_rn(w4.y, offset));
-            e[2] = __fmul_rn(__fmul_rn(x4.z, inv), __fadd_rn(w4.z, offset));
-            e[3] = __fmul_rn(__fmul_rn(x4.w, inv), __fadd_rn(w4.w, offset));
-        }
-        float amax = fmaxf(fmaxf(fabsf(e[0]), fabsf(e[1])), fmaxf(fabsf(e[2]), fabsf(e[3])));
-#pragma unroll
-        for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float d = __fdiv_rn(amax, 127.0f);
-        uint32_t packed = 0;
-        if (d != 0.0f) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float q = fminf(fmaxf(roundf(__fdiv_rn(e[i], d)), -127.0f), 127.0f);
-                packed |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xFFu) << (8 * i);
-            }
-        }
+        const float4 x4 = active ? xr[blk * 8 + sub] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 w4 = active ? __ldg(w + blk * 8 + sub) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float d;
+        const uint32_t packed = quant_chunk(x4, w4, inv, offset, active, d);
         if (active) {
             qr[blk * 8 + sub] = packed;
             if (sub == 0) dr[blk] = d;
