@@ -61,13 +61,27 @@ _INCLUDE = os.path.join(ROOT, "include")
 
 
 def _kernel_unit(kernel: str):
-    """The csrc translation unit that defines the __global__ function `kernel`."""
+    """The csrc translation unit that defines the __global__ function `kernel`
+    (or, for a kernel template defined in a header, the unit that includes
+    that header and instantiates it)."""
     pat = re.compile(r"__global__[^;{]*?\b" + re.escape(kernel) + r"\s*\(", re.S)
-    for name in sorted(os.listdir(_CSRC)):
+    names = sorted(os.listdir(_CSRC))
+    for name in names:
         if name.endswith(".cu"):
             with open(os.path.join(_CSRC, name)) as f:
                 if pat.search(f.read()):
                     return os.path.join(_CSRC, name)
+    for header in names:
+        if header.endswith(".cuh"):
+            with open(os.path.join(_CSRC, header)) as f:
+                if not pat.search(f.read()):
+                    continue
+            inc = re.compile(r'^\s*#\s*include\s*"' + re.escape(header) + '"', re.M)
+            for name in names:
+                if name.endswith(".cu"):
+                    with open(os.path.join(_CSRC, name)) as f:
+                        if inc.search(f.read()):
+                            return os.path.join(_CSRC, name)
     return None
 
 
@@ -318,6 +332,15 @@ class Q40Matvec(Rotating):
     def cpu_reference(self, oracle, rows_sample):
         W, x = synth.q4_0_matvec_inputs(self.rows, self.K)
         return self._matvec_reference(oracle, oracle.FORMAT_Q4_0, W, x, rows_sample)
+
+
+class Q40MatvecShortWide(Q40Matvec):
+    """A short, wide Q4_0 matvec (256 rows, K = 21504: the FFN down
+    projection's width with few rows): too few rows to fill the GPU, so K is
+    split across the CTAs of a cluster (the shared-memory ring kernel)."""
+    name = "q4_0_matvec_256x21504"
+    kernel = "k_ring_matvec"
+    rows, K = 256, 21504
 
 
 class Q4KMatvec(Rotating):
@@ -597,8 +620,8 @@ class GemmSmallBatch32(GemmSmallBatch8):
     M = 32
 
 
-WORKLOADS = {w.name: w for w in (LogitsTopK, Q40Matvec, Q4KMatvec, Q6KMatvec, FFN, GegluDown, RMSNormQ8, Gemm,
-                                  GemmSmallBatch8, GemmSmallBatch32)}
+WORKLOADS = {w.name: w for w in (LogitsTopK, Q40Matvec, Q40MatvecShortWide, Q4KMatvec, Q6KMatvec, FFN, GegluDown,
+                                  RMSNormQ8, Gemm, GemmSmallBatch8, GemmSmallBatch32)}
 
 
 # ---------------------------------------------------------------- timing
