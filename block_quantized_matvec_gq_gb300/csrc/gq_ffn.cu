@@ -37,10 +37,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     #pragma unroll
             for (int i = 0; i < R; ++i) {
                 const int r = min(task * TR + g * R + i, rows - 1);
-                st.wp[i] = gnib + static_cast<size_t>(r) * nb;
-                st.sp[i] = gsc + static_cast<size_t>(r) * nb;
-                st.wp[R + i] = unib + static_cast<size_t>(r) * nb;
-                st.sp[R + i] = usc + static_cast<size_t>(r) * nb;
+                st.wp[i] = gnib + static_cast<size_t>(r) * nb + lp;
+                st.sp[i] = gsc + static_cast<size_t>(r) * nb + lp;
+                st.wp[R + i] = unib + static_cast<size_t>(r) * nb + lp;
+                st.sp[R + i] = usc + static_cast<size_t>(r) * nb + lp;
             }
             st.prime(nb, lp);
         };
@@ -92,10 +92,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     #pragma unroll
             for (int i = 0; i < R; ++i) {
                 const int r = min(r0 + g * R + i, rows - 1);
-                st.wp[i] = gnib + static_cast<size_t>(r) * nb + blo;
-                st.sp[i] = gsc + static_cast<size_t>(r) * nb + blo;
-                st.wp[R + i] = unib + static_cast<size_t>(r) * nb + blo;
-                st.sp[R + i] = usc + static_cast<size_t>(r) * nb + blo;
+                st.wp[i] = gnib + static_cast<size_t>(r) * nb + blo + lp;
+                st.sp[i] = gsc + static_cast<size_t>(r) * nb + blo + lp;
+                st.wp[R + i] = unib + static_cast<size_t>(r) * nb + blo + lp;
+                st.sp[R + i] = usc + static_cast<size_t>(r) * nb + blo + lp;
             }
             st.prime(bhi - blo, lp);
         };

@@ -176,6 +176,61 @@ __device__ __forceinline__ float2 nib8_fma(uint32_t w, float4 xa, float4 xb, flo
     return r;
 }
 
+// ---------------------------------------------------------------- offset-free 4-bit codes as subnormals
+// A code without offset (Q4_K: w = d*sc*q - dmin*m) need not be converted at
+// all: AND-ing nibble i (bits 4i..4i+3) out of a 16-bit half leaves, with a
+// zero exponent field, the bit pattern of the subnormal f32 q * 2^(4i-149).
+// If the staged x of that position holds x * 2^(149-4i-c) (stage_x_q4k), the
+// FMA forms q * x * 2^-c from the exact product and rounds once, as the
+// magic-number form does with (q - OFF) * x; the sum comes out scaled by
+// 2^-c.  Per 8 codes: one shift, eight ANDs and four packed FMAs, against
+// eight LOP3s, four packed adds and four packed FMAs.  Subnormal operands
+// are kept: the PTX operations carry no .ftz.
+#define GQ_NIB8_SUB_BODY(FIRST)                                                              \
+    "{\n"                                                                                    \
+    " .reg .b32 h, l0, h0, l1, h1, l2, h2, l3, h3;\n"                                       \
+    " .reg .b64 p0, p1, p2, p3, x0, x1, x2, x3, a;\n"                                       \
+    " shr.u32 h, %2, 16;\n"                                                                  \
+    " and.b32 l0, %2, 0x0000000F;\n and.b32 h0, h, 0x0000000F;\n"                           \
+    " and.b32 l1, %2, 0x000000F0;\n and.b32 h1, h, 0x000000F0;\n"                           \
+    " and.b32 l2, %2, 0x00000F00;\n and.b32 h2, h, 0x00000F00;\n"                           \
+    " and.b32 l3, %2, 0x0000F000;\n and.b32 h3, h, 0x0000F000;\n"                           \
+    " mov.b64 p0, {l0, h0};\n mov.b64 p1, {l1, h1};\n mov.b64 p2, {l2, h2};\n mov.b64 p3, {l3, h3};\n" \
+    " mov.b64 x0, {%3, %4};\n mov.b64 x1, {%5, %6};\n mov.b64 x2, {%7, %8};\n mov.b64 x3, {%9, %10};\n" \
+    " mov.b64 a, {%11, %12};\n" FIRST                                                        \
+    " fma.rn.f32x2 a, p1, x1, a;\n fma.rn.f32x2 a, p2, x2, a;\n fma.rn.f32x2 a, p3, x3, a;\n" \
+    " mov.b64 {%0, %1}, a;\n"                                                                \
+    "}"
+
+// Returns acc + sum over the word of q * xs (xs the position-scaled staged
+// x) as a packed pair of partial sums; kStart ignores acc.
+template <bool kStart>
+__device__ __forceinline__ float2 nib8_sub_fma(uint32_t w, float4 xa, float4 xb, float2 acc)
+{
+    float2 r;
+    if (kStart) {
+        asm(GQ_NIB8_SUB_BODY(" mul.rn.f32x2 a, p0, x0;\n")
+            : "=f"(r.x), "=f"(r.y)
+            : "r"(w), "f"(xa.x), "f"(xa.y), "f"(xa.z), "f"(xa.w), "f"(xb.x), "f"(xb.y), "f"(xb.z), "f"(xb.w),
+              "f"(acc.x), "f"(acc.y));
+    } else {
+        asm(GQ_NIB8_SUB_BODY(" fma.rn.f32x2 a, p0, x0, a;\n")
+            : "=f"(r.x), "=f"(r.y)
+            : "r"(w), "f"(xa.x), "f"(xa.y), "f"(xa.z), "f"(xa.w), "f"(xb.x), "f"(xb.y), "f"(xb.z), "f"(xb.w),
+              "f"(acc.x), "f"(acc.y));
+    }
+    return r;
+}
+
+// 2^k as f32 for -126 <= k <= 127.
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
+// v * 2^k for -252 <= k <= 254 in two exact power-of-two steps.
+__device__ __forceinline__ float scale_pow2(float v, int k)
+{
+    const int k1 = k >> 1;
+    return v * pow2i(k1) * pow2i(k - k1);
+}
+
 // ---------------------------------------------------------------- activation staging for 4-bit formats
 // x is kept in shared memory as K/32 blocks of kXBlk = 36 floats (144 bytes):
 // the block's 32 values, every 8-element group in the order
@@ -220,6 +275,69 @@ __device__ __forceinline__ void stage_x_q4(float *xs, const float *__restrict__ 
         }
     }
     __syncthreads();
+}
+
+// Bit pattern of |v| if v is finite, else 0 (the unsigned order of these
+// patterns is the order of the magnitudes).
+__device__ __forceinline__ uint32_t finite_mag_bits(float v)
+{
+    const uint32_t b = __float_as_uint(v) & 0x7FFFFFFFu;
+    return b < 0x7F800000u ? b : 0u;
+}
+
+// Staging for the subnormal-code core (nib8_sub_fma): the layout of
+// stage_x_q4<true>, with every value multiplied by 2^(149-4i-c), i its
+// nibble position (stored index t of an 8-group has i = t/2), and the block
+// sums (taken from the unscaled values, in stage_x_q4's order) by 2^-c.
+// c = e + 22, e the binary exponent of the largest finite |x| (at least
+// -126): the largest scaled value stays below 2^128, and a product
+// q * x * 2^-c is a normal number whenever |x| >= 2^(e-104).  Infinities
+// and NaNs stay what they are.  Returns c (the same in every thread); all
+// threads of the CTA take part; `red` holds one word per warp; ends with a
+// CTA barrier.
+__device__ __forceinline__ int stage_x_q4k(float *xs, const float *__restrict__ x, int K, uint32_t *red)
+{
+    const int ngroups = K >> 3;
+    uint32_t mx = 0u;
+    for (int g = threadIdx.x; g < ngroups; g += blockDim.x) {
+        const float4 a = *reinterpret_cast<const float4 *>(x + 8 * g);
+        const float4 b = *reinterpret_cast<const float4 *>(x + 8 * g + 4);
+        float *dst = xs + (g >> 2) * kXBlk + 8 * (g & 3);
+        *reinterpret_cast<float4 *>(dst) = make_float4(a.x, b.x, a.y, b.y);
+        *reinterpret_cast<float4 *>(dst + 4) = make_float4(a.z, b.z, a.w, b.w);
+        mx = max(mx, max(max(finite_mag_bits(a.x), finite_mag_bits(a.y)), max(finite_mag_bits(a.z), finite_mag_bits(a.w))));
+        mx = max(mx, max(max(finite_mag_bits(b.x), finite_mag_bits(b.y)), max(finite_mag_bits(b.z), finite_mag_bits(b.w))));
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) mx = max(mx, red[w]);
+    const int e = max(static_cast<int>(mx >> 23) - 127, -126);
+    const int c = e + 22;
+    for (int b = threadIdx.x; b < (K >> 5); b += blockDim.x) {
+        float *blk = xs + b * kXBlk;
+        float s = 0.f;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const float4 v = ld_xq4(blk, m);
+            s += v.x;
+            s += v.y;
+            s += v.z;
+            s += v.w;
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            // float4 m holds stored indices 4(m&1)..4(m&1)+3 of its 8-group: positions 2(m&1), 2(m&1)+1
+            const int i0 = 2 * (m & 1);
+            const int k0 = 127 - e - 4 * i0, k1 = k0 - 4;
+            const float4 v = ld_xq4(blk, m);
+            *reinterpret_cast<float4 *>(blk + 4 * m) =
+                make_float4(scale_pow2(v.x, k0), scale_pow2(v.y, k0), scale_pow2(v.z, k1), scale_pow2(v.w, k1));
+        }
+        blk[32] = scale_pow2(s, -c);
+    }
+    __syncthreads();
+    return c;
 }
 
 // Offset-binary bytes (u = q + 128) to exact f32 q: PRMT places byte k in

@@ -48,6 +48,36 @@ __device__ __forceinline__ void q4_block(const uint4 (&w)[NS], const float *xb, 
     for (int i = 0; i < NS; ++i) blk[i] = __fadd2_rn(a[i], c[i]);
 }
 
+// The same for offset-free codes against x staged by stage_x_q4k: the
+// partial sums come out scaled by 2^-c.
+template <int NS>
+__device__ __forceinline__ void q4_block_sub(const uint4 (&w)[NS], const float *xb, float2 (&blk)[NS])
+{
+    float2 a[NS], c[NS];
+    {
+        const float4 x0 = ld_xq4(xb, 0), x1 = ld_xq4(xb, 1);
+#pragma unroll
+        for (int i = 0; i < NS; ++i) a[i] = nib8_sub_fma<true>(w[i].x, x0, x1, mk2(0.f, 0.f));
+    }
+    {
+        const float4 x2 = ld_xq4(xb, 2), x3 = ld_xq4(xb, 3);
+#pragma unroll
+        for (int i = 0; i < NS; ++i) a[i] = nib8_sub_fma<false>(w[i].y, x2, x3, a[i]);
+    }
+    {
+        const float4 x4 = ld_xq4(xb, 4), x5 = ld_xq4(xb, 5);
+#pragma unroll
+        for (int i = 0; i < NS; ++i) c[i] = nib8_sub_fma<true>(w[i].z, x4, x5, mk2(0.f, 0.f));
+    }
+    {
+        const float4 x6 = ld_xq4(xb, 6), x7 = ld_xq4(xb, 7);
+#pragma unroll
+        for (int i = 0; i < NS; ++i) c[i] = nib8_sub_fma<false>(w[i].w, x6, x7, c[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < NS; ++i) blk[i] = __fadd2_rn(a[i], c[i]);
+}
+
 __device__ __forceinline__ float half_bits_to_float(uint32_t h)
 {
     return __half2float(__ushort_as_half(static_cast<uint16_t>(h)));
@@ -64,30 +94,35 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t h)
 // the bytes in flight (Little's law), not by a second register set.
 template <int LG, int NS, int U>
 struct Q40Stream {
-    const uint4 *wp[NS];
-    const uint16_t *sp[NS];
+    static constexpr int kStep = LG * U;
+    const uint4 *wp[NS];     // row i's payload plus this lane's first block
+    const uint16_t *sp[NS];  // row i's scales plus this lane's first block
     uint4 w[U][NS];
     uint32_t d[U][NS];
 
-    __device__ __forceinline__ void load(int b0, int nb)
+    // Batch [base, base + kStep) of the rows; kFull: wholly inside the row
+    // (no bounds test).
+    template <bool kFull>
+    __device__ __forceinline__ void load(int base, int nb, int lp)
     {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int b = b0 + u * LG;
-            const bool ok = b < nb;
+            if (kFull || base + lp + u * LG < nb) {
 #pragma unroll
-            for (int i = 0; i < NS; ++i) {
-                w[u][i] = ok ? ld_stream16(wp[i] + b) : make_uint4(0u, 0u, 0u, 0u);
-                d[u][i] = ok ? ld_stream_u16(sp[i] + b) : 0u;
+                for (int i = 0; i < NS; ++i) {
+                    w[u][i] = ld_stream16(wp[i] + base + u * LG);
+                    d[u][i] = ld_stream_u16(sp[i] + base + u * LG);
+                }
             }
         }
     }
-    __device__ __forceinline__ void compute(int b0, int nb, const float *xs, float2 (&acc)[NS]) const
+    template <bool kFull>
+    __device__ __forceinline__ void compute(int base, int nb, int lp, const float *xs, float2 (&acc)[NS]) const
     {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int b = b0 + u * LG;
-            if (b < nb) {
+            const int b = base + lp + u * LG;
+            if (kFull || b < nb) {
                 float2 blk[NS];
                 q4_block<8, NS>(w[u], xs + b * kXBlk, blk);
 #pragma unroll
@@ -98,18 +133,29 @@ struct Q40Stream {
             }
         }
     }
-    __device__ __forceinline__ void prime(int nb, int lp) { load(lp, nb); }
+    __device__ __forceinline__ void prime(int nb, int lp)
+    {
+        if (kStep <= nb)
+            load<true>(0, nb, lp);
+        else
+            load<false>(0, nb, lp);
+    }
     __device__ __forceinline__ void run(const float *xs, int nb, int lp, float (&out)[NS])
     {
-        constexpr int STEP = LG * U;
         float2 acc[NS];
 #pragma unroll
         for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
-        for (int b0 = lp;;) {
-            compute(b0, nb, xs, acc);
-            b0 += STEP;
-            if (b0 >= nb) break;
-            load(b0, nb);
+        for (int base = 0;;) {
+            if (base + kStep <= nb)
+                compute<true>(base, nb, lp, xs, acc);
+            else
+                compute<false>(base, nb, lp, xs, acc);
+            base += kStep;
+            if (base >= nb) break;
+            if (base + kStep <= nb)
+                load<true>(base, nb, lp);
+            else
+                load<false>(base, nb, lp);
         }
 #pragma unroll
         for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;
@@ -210,38 +256,44 @@ __device__ __forceinline__ void q4k_dm(uint4 rec, const Q4KSub &c, float &dsc, f
 }
 
 // One row task of NS Q4_K rows, in the same batched prime() / run() form as
-// Q40Stream.
+// Q40Stream, against x staged by stage_x_q4k (sums scaled by 2^-c).  The
+// row pointers already point at this lane's first sub-block and super-block
+// record; a batch covers sub-blocks [base, base + LG*U) of the rows, and
+// batches that lie wholly inside the row skip every bounds test.
 template <int LG, int NS, int U>
 struct Q4KStream {
     static_assert(LG % 8 == 0, "a lane's sub-block position must be fixed");
+    static constexpr int kStep = LG * U;
     const uint4 *wp[NS];
     const uint4 *rp[NS];
     uint4 w[U][NS], r[U][NS];
 
-    __device__ __forceinline__ void load(int b0, int nsb)
+    template <bool kFull>
+    __device__ __forceinline__ void load(int base, int nsb, int lp)
     {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int b = b0 + u * LG;
-            const bool ok = b < nsb;
+            if (kFull || base + lp + u * LG < nsb) {
 #pragma unroll
-            for (int i = 0; i < NS; ++i) {
-                w[u][i] = ok ? ld_stream16(wp[i] + b) : make_uint4(0u, 0u, 0u, 0u);
-                // the 16-byte record is shared by the 8 lanes of a super-block
-                r[u][i] = ok ? __ldg(rp[i] + (b >> 3)) : make_uint4(0u, 0u, 0u, 0u);
+                for (int i = 0; i < NS; ++i) {
+                    w[u][i] = ld_stream16(wp[i] + base + u * LG);
+                    // the 16-byte record is shared by the 8 lanes of a super-block
+                    r[u][i] = __ldg(rp[i] + ((base + u * LG) >> 3));
+                }
             }
         }
     }
-    __device__ __forceinline__ void compute(int b0, int nsb, const float *xs, const Q4KSub &sub,
+    template <bool kFull>
+    __device__ __forceinline__ void compute(int base, int nsb, int lp, const float *xs, const Q4KSub &sub,
                                             float2 (&acc)[NS]) const
     {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int b = b0 + u * LG;
-            if (b < nsb) {
+            const int b = base + lp + u * LG;
+            if (kFull || b < nsb) {
                 const float *xb = xs + b * kXBlk;
                 float2 blk[NS];
-                q4_block<0, NS>(w[u], xb, blk);
+                q4_block_sub<NS>(w[u], xb, blk);
                 const float xsb = xb[32];
 #pragma unroll
                 for (int i = 0; i < NS; ++i) {
@@ -253,19 +305,30 @@ struct Q4KStream {
             }
         }
     }
-    __device__ __forceinline__ void prime(int nsb, int lp) { load(lp, nsb); }
+    __device__ __forceinline__ void prime(int nsb, int lp)
+    {
+        if (kStep <= nsb)
+            load<true>(0, nsb, lp);
+        else
+            load<false>(0, nsb, lp);
+    }
     __device__ __forceinline__ void run(const float *xs, int nsb, int lp, float (&out)[NS])
     {
-        constexpr int STEP = LG * U;
         const Q4KSub sub = q4k_sub(lp & 7);
         float2 acc[NS];
 #pragma unroll
         for (int i = 0; i < NS; ++i) acc[i] = make_float2(0.f, 0.f);
-        for (int b0 = lp;;) {
-            compute(b0, nsb, xs, sub, acc);
-            b0 += STEP;
-            if (b0 >= nsb) break;
-            load(b0, nsb);
+        for (int base = 0;;) {
+            if (base + kStep <= nsb)
+                compute<true>(base, nsb, lp, xs, sub, acc);
+            else
+                compute<false>(base, nsb, lp, xs, sub, acc);
+            base += kStep;
+            if (base >= nsb) break;
+            if (base + kStep <= nsb)
+                load<true>(base, nsb, lp);
+            else
+                load<false>(base, nsb, lp);
         }
 #pragma unroll
         for (int i = 0; i < NS; ++i) out[i] = acc[i].x + acc[i].y;

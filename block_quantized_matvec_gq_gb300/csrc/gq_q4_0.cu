@@ -76,8 +76,8 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     #pragma unroll
             for (int i = 0; i < R; ++i) {
                 const int r = min(task * TR + g * R + i, rows - 1);
-                st.wp[i] = nib + static_cast<size_t>(r) * nb;
-                st.sp[i] = dsc + static_cast<size_t>(r) * nb;
+                st.wp[i] = nib + static_cast<size_t>(r) * nb + lp;
+                st.sp[i] = dsc + static_cast<size_t>(r) * nb + lp;
             }
             st.prime(nb, lp);
         };
@@ -121,8 +121,8 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     #pragma unroll
             for (int i = 0; i < R; ++i) {
                 const int r = min(r0 + g * R + i, rows - 1);
-                st.wp[i] = nib + static_cast<size_t>(r) * nb + blo;
-                st.sp[i] = dsc + static_cast<size_t>(r) * nb + blo;
+                st.wp[i] = nib + static_cast<size_t>(r) * nb + blo + lp;
+                st.sp[i] = dsc + static_cast<size_t>(r) * nb + blo + lp;
             }
             st.prime(bhi - blo, lp);
         };

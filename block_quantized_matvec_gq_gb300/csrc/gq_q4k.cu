@@ -6,6 +6,9 @@
 //   y_i = sum over super-blocks and sub-blocks s of
 //         d*sc_s * sum_j q_j x_j  -  dmin*m_s * sum_j x_j
 // The per-32 sums of x are computed once per CTA, inside the staged x blocks.
+// The codes enter the FMAs as subnormal floats against x staged with
+// per-position power-of-two scales (nib8_sub_fma, stage_x_q4k); every sum is
+// scaled by 2^-c until the row result, which is scaled back by 2^c.
 #include "gq_host.h"
 #include "gq_matvec.cuh"
 
@@ -21,6 +24,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     // schedule (chosen by the host): 0 round-robin; 1 balanced; 2 balanced, first loads early
     constexpr bool kBalanced = kMode >= 1, kEarly = kMode == 2;
     __shared__ float part[kWarpsPerCta][kWarpsPerCta * TR];  // tail partial sums [warp][row]
+    __shared__ uint32_t red[kWarpsPerCta];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane / LG, lp = lane % LG;
     const int ns = nsb >> 3;
@@ -35,8 +39,8 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     #pragma unroll
             for (int i = 0; i < R; ++i) {
                 const int r = min(task * TR + g * R + i, rows - 1);
-                st.wp[i] = nib + static_cast<size_t>(r) * nsb;
-                st.rp[i] = rec + static_cast<size_t>(r) * ns;
+                st.wp[i] = nib + static_cast<size_t>(r) * nsb + lp;
+                st.rp[i] = rec + static_cast<size_t>(r) * ns + (lp >> 3);
             }
             st.prime(nsb, lp);
         };
@@ -53,7 +57,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
             /* no early loads in this mode */
         }
         pdl_wait();
-        stage_x_q4<true>(xs, x, nsb * 32);
+        const int c = stage_x_q4k(xs, x, nsb * 32, red);
         pdl_launch_dependents();
 
         for (int task = first; task < ntasks; task += stride) {
@@ -68,7 +72,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     #pragma unroll
             for (int i = 0; i < R; ++i) {
                 const float s = group_sum<LG>(out[i]);
-                if (lp == 0 && r0 + i < rows) y[r0 + i] = s;
+                if (lp == 0 && r0 + i < rows) y[r0 + i] = scale_pow2(s, c);
             }
         }
     } else {
@@ -81,8 +85,8 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     #pragma unroll
             for (int i = 0; i < R; ++i) {
                 const int r = min(r0 + g * R + i, rows - 1);
-                st.wp[i] = nib + static_cast<size_t>(r) * nsb + blo;
-                st.rp[i] = rec + static_cast<size_t>(r) * ns + (blo >> 3);
+                st.wp[i] = nib + static_cast<size_t>(r) * nsb + blo + lp;
+                st.rp[i] = rec + static_cast<size_t>(r) * ns + ((blo + lp) >> 3);
             }
             st.prime(bhi - blo, lp);
         };
@@ -97,7 +101,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
             if (kEarly) setup(cr.start, 0, nsb);
         }
         pdl_wait();
-        stage_x_q4<true>(xs, x, nsb * 32);
+        const int c = stage_x_q4k(xs, x, nsb * 32, red);
         pdl_launch_dependents();
 
         for (int j = 0; j < cr.count; ++j) {
@@ -112,7 +116,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     #pragma unroll
             for (int i = 0; i < R; ++i) {
                 const float s = group_sum<LG>(out[i]);
-                if (lp == 0 && r0 + g * R + i < rows) y[r0 + g * R + i] = s;
+                if (lp == 0 && r0 + g * R + i < rows) y[r0 + g * R + i] = scale_pow2(s, c);
             }
         }
         if (kBalanced && cr.ntail > 0) {
@@ -133,7 +137,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
                 float s = 0.f;
     #pragma unroll
                 for (int w = 0; w < kWarpsPerCta; ++w) s += part[w][r];
-                y[cr.tail_begin + r] = s;
+                y[cr.tail_begin + r] = scale_pow2(s, c);
             }
         }
     }

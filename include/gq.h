@@ -124,6 +124,11 @@ int gq_unpack(int format, const void *W_packed, void *W_canon, int rows, int K,
  *   W  packed weights, rows x K   x  f32[K]   y  f32[rows] (overwritten)
  *   M  batch size; must be 1 (decode).  1 <= rows, 32 <= K <= GQ_MAX_K.
  * Accuracy: |y_i - exact_i| <= 1e-5 * sum_j |w_ij x_j| for finite inputs.
+ * gq_q4k_matvec works in a domain scaled by a power of two taken from the
+ * largest finite |x_j| = X: the bound holds for elements with
+ * |x_j| >= 2^-104 * X; a product involving a smaller element is rounded to
+ * an absolute grid of at most 2^-128 * X * |d * sc|.  Scaling x by 2^k scales
+ * y by exactly 2^k while nothing over- or underflows.
  * ------------------------------------------------------------------------ */
 int gq_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K, int M,
                    gq_stream_t stream);

@@ -129,6 +129,34 @@ def test_q4_k_zero_scales_and_mins():
     assert y[0] == 0.0 and y[6] == 0.0     # sc = 0 and m = 0
 
 
+@pytest.mark.parametrize("rows,K", [(515, 5376), (3000, 2048)])
+def test_q4_k_power_of_two_scaling_of_x_is_exact(rows, K):
+    """The Q4_K kernel stages x with power-of-two scales taken from max|x|,
+    so multiplying x by 2^k must multiply every y by exactly 2^k (no result
+    under- or overflows here)."""
+    W = synth.q4_k_weights(rows, K, synth.stream(8, 0))
+    x = synth.normal(K, synth.stream(8, 1))
+    y0 = run_matvec(oracle.FORMAT_Q4_K, W, x, rows, K)
+    for k in (-100, -37, 50, 90):
+        xk = (x.astype(np.float64) * 2.0 ** k).astype(np.float32)
+        yk = run_matvec(oracle.FORMAT_Q4_K, W, xk, rows, K)
+        assert np.array_equal(yk.astype(np.float64), y0.astype(np.float64) * 2.0 ** k), k
+
+
+def test_q4_k_x_with_wide_dynamic_range():
+    """Elements of x spread over 2^-60 .. 2^60 (and some zeros): every
+    product stays a normal number in the scaled domain, so the bound holds."""
+    rows, K = 600, 4096
+    W = synth.q4_k_weights(rows, K, synth.stream(9, 0))
+    rng = np.random.default_rng(9)
+    x = (synth.normal(K, synth.stream(9, 1)).astype(np.float64)
+         * np.exp2(rng.integers(-60, 61, K))).astype(np.float32)
+    x[rng.integers(0, K, 40)] = 0.0
+    y = run_matvec(oracle.FORMAT_Q4_K, W, x, rows, K)
+    y_ref, a_ref = oracle.matvec(oracle.FORMAT_Q4_K, W, x, rows, K)
+    assert_within(y, y_ref, a_ref, what="q4_k wide-range x")
+
+
 @pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K, oracle.FORMAT_Q6_K])
 def test_repeat_runs_are_bitwise_identical(fmt):
     rows, K = 3001, 5376 if fmt != oracle.FORMAT_Q4_0 else 4096
