@@ -82,6 +82,8 @@ MatvecGeo choose_logits_geo(int rows, int nb)
     return MatvecGeo{8, 2, 4, 8};
 }
 
+MatvecGeo choose_q6k_geo() { return tuned("GQ_Q6", MatvecGeo{16, 2, 4, 8}); }
+
 MatvecGeo choose_ffn_geo(int rows, int nb, bool pair_ok)
 {
     (void)rows;

@@ -116,6 +116,7 @@ struct MatvecGeo {
 MatvecGeo choose_matvec_geo(int format, int rows, int nb, bool pair_ok);
 MatvecGeo choose_logits_geo(int rows, int nb);
 MatvecGeo choose_ffn_geo(int rows, int nb, bool pair_ok);
+MatvecGeo choose_q6k_geo();
 
 int launch_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K, MatvecGeo g,
                        cudaStream_t s);

@@ -13,9 +13,10 @@
 //   Q4_K: [rows*ns x 128 B, sub-block s at 16 s, element order]
 //         [rows*ns x 16 B {d, dmin, 12 scale bytes}]
 //   Q6_K: [rows*ns x 128 B low 4 code bits, element order]
-//         [rows*ns x 64 B top 2 code bits: byte i holds elements 4i..4i+3 at
-//          bits 0, 2, 4, 6]
-//         [rows*ns x 18 B {16 int8 sub-scales, fp16 d}]
+//         [rows*ns x 64 B top 2 code bits: 32-bit word g holds the 16
+//          elements 16g..16g+15; element 16g + 4a + i (a, i = 0..3) at
+//          bits 4i + {0, 2, 16, 18}[a], +1]
+//         [rows*ns x 16 B int8 sub-scales] [rows*ns x fp16 d]
 // "Element order" means byte i of a 32-element group holds element 2i in
 // its low nibble and element 2i+1 in its high nibble.
 #include "gq_host.h"
@@ -155,6 +156,18 @@ __global__ void k_pack_q4_k(const uint8_t *__restrict__ src, uint8_t *__restrict
 // Q6_K canonical block (ql[128], qh[64], sc[16], d): in each 128-weight half
 // h, weight 32c + l has its low bits in ql[64h + l + 32(c % 2)] (low nibble
 // for c < 2, high nibble otherwise) and its top bits at bit 2c of qh[32h + l].
+// Packed top bits: bit position of element e's pair within its 32-bit word
+// (word e / 16): quarter a = (e / 4) % 4 of the 16 elements sits at offset
+// {0, 2, 16, 18}[a], element i = e % 4 of the quarter 4i above it.  Shifted
+// by {+4, +2, -12, -14}[a], every pair of a quarter lands at bits 4i + 4,
+// just above its element's nibble in the low-bit word (the matvec joins the
+// two with one bit-select per two elements).
+__device__ __forceinline__ int q6_top_bit(int e)
+{
+    const int a = (e >> 2) & 3;
+    return 4 * (e & 3) + ((a & 1) ? 2 : 0) + ((a & 2) ? 16 : 0);
+}
+
 __global__ void k_pack_q6_k(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, long long nsup,
                             bool unpack)
 {
@@ -163,30 +176,39 @@ __global__ void k_pack_q6_k(const uint8_t *__restrict__ src, uint8_t *__restrict
         if (!unpack) {
             const uint8_t *blk = src + b * 210;
             uint8_t *lo = dst + b * 128;
-            uint8_t *hi = dst + nsup * 128 + b * 64;
-            uint8_t *rec = dst + nsup * 192 + b * 18;
-            for (int j = 0; j < 18; ++j) rec[j] = blk[192 + j];
+            uint32_t hw[16];
+            uint8_t *sc = dst + nsup * 192 + b * 16;
+            uint8_t *dd = dst + nsup * 208 + b * 2;
+            for (int j = 0; j < 16; ++j) sc[j] = blk[192 + j];
+            dd[0] = blk[208];
+            dd[1] = blk[209];
             for (int i = 0; i < 128; ++i) lo[i] = 0;
-            for (int i = 0; i < 64; ++i) hi[i] = 0;
+            for (int i = 0; i < 16; ++i) hw[i] = 0u;
             for (int e = 0; e < 256; ++e) {
                 const int h = e >> 7, c = (e >> 5) & 3, l = e & 31;
                 const uint8_t qlb = blk[64 * h + l + 32 * (c & 1)];
                 const int q_lo = (c < 2) ? (qlb & 15) : (qlb >> 4);
-                const int q_hi = (blk[128 + 32 * h + l] >> (2 * c)) & 3;
+                const uint32_t q_hi = (blk[128 + 32 * h + l] >> (2 * c)) & 3;
                 lo[e >> 1] |= static_cast<uint8_t>(q_lo << (4 * (e & 1)));
-                hi[e >> 2] |= static_cast<uint8_t>(q_hi << (2 * (e & 3)));
+                hw[e >> 4] |= q_hi << q6_top_bit(e & 15);
             }
+            uint8_t *hi = dst + nsup * 128 + b * 64;
+            for (int i = 0; i < 64; ++i) hi[i] = static_cast<uint8_t>(hw[i >> 2] >> (8 * (i & 3)));
         } else {
             const uint8_t *lo = src + b * 128;
             const uint8_t *hi = src + nsup * 128 + b * 64;
-            const uint8_t *rec = src + nsup * 192 + b * 18;
+            const uint8_t *sc = src + nsup * 192 + b * 16;
+            const uint8_t *dd = src + nsup * 208 + b * 2;
             uint8_t *blk = dst + b * 210;
-            for (int j = 0; j < 18; ++j) blk[192 + j] = rec[j];
+            for (int j = 0; j < 16; ++j) blk[192 + j] = sc[j];
+            blk[208] = dd[0];
+            blk[209] = dd[1];
             for (int i = 0; i < 192; ++i) blk[i] = 0;
             for (int e = 0; e < 256; ++e) {
                 const int h = e >> 7, c = (e >> 5) & 3, l = e & 31;
                 const int q_lo = (lo[e >> 1] >> (4 * (e & 1))) & 15;
-                const int q_hi = (hi[e >> 2] >> (2 * (e & 3))) & 3;
+                const int g = e >> 4, p = q6_top_bit(e & 15);
+                const int q_hi = (hi[4 * g + (p >> 3)] >> (p & 7)) & 3;
                 blk[64 * h + l + 32 * (c & 1)] |= static_cast<uint8_t>(q_lo << ((c < 2) ? 0 : 4));
                 blk[128 + 32 * h + l] |= static_cast<uint8_t>(q_hi << (2 * c));
             }

@@ -106,9 +106,12 @@ const char *gq_status_string(int status);
  *         plane 1 = rows*ns 16-byte records {d, dmin, 12 scale bytes}
  *         copied unchanged.
  *   Q6_K: plane 0 = rows*ns 128-byte low-bit payloads in element order;
- *         plane 1 = rows*ns 64-byte top-bit payloads (byte i = elements
- *         4i..4i+3 at bits 0, 2, 4, 6); plane 2 = rows*ns 18-byte records
- *         {16 int8 sub-scales, fp16 d} copied unchanged.
+ *         plane 1 = rows*ns 64-byte top-bit payloads of 16 little-endian
+ *         32-bit words, word g holding elements 16g..16g+15: element
+ *         16g + 4a + i (a, i = 0..3) at bits p, p+1 with
+ *         p = 4i + {0, 2, 16, 18}[a]; plane 2 = rows*ns 16-byte int8
+ *         sub-scale records; plane 3 = rows*ns fp16 d (both copied
+ *         unchanged).
  * W_canon and W_packed must not overlap.  Both are device pointers.
  * ------------------------------------------------------------------------ */
 size_t gq_packed_bytes(int format, int rows, int K); /* 0 if invalid */

@@ -43,15 +43,18 @@ def _decode_packed_host(fmt, P, rows, K):
     if fmt == oracle.FORMAT_Q6_K:
         ns = K // 256
         lo = P[:rows * ns * 128].reshape(rows, ns, 128)
-        hi = P[rows * ns * 128:rows * ns * 192].reshape(rows, ns, 64)
-        rec = P[rows * ns * 192:].reshape(rows, ns, 18)
+        hw = P[rows * ns * 128:rows * ns * 192].copy().view("<u4").reshape(rows, ns, 16).astype(np.int64)
+        scp = P[rows * ns * 192:rows * ns * 208].reshape(rows, ns, 16)
+        dp = P[rows * ns * 208:].reshape(rows, ns, 2)
         q = np.empty((rows, ns, 256), np.int64)
         q[:, :, 0::2] = lo & 15
         q[:, :, 1::2] = lo >> 4
-        for k in range(4):
-            q[:, :, k::4] |= ((hi >> (2 * k)) & 3).astype(np.int64) << 4
-        sc = rec[:, :, :16].copy().view(np.int8).astype(np.float64)
-        d = rec[:, :, 16:18].copy().view(np.float16).reshape(rows, ns).astype(np.float64)
+        for j in range(16):               # element j of every 16-element word
+            a, i = j // 4, j % 4
+            p = 4 * i + (2 if a & 1 else 0) + (16 if a & 2 else 0)
+            q[:, :, j::16] |= ((hw >> p) & 3) << 4
+        sc = scp.copy().view(np.int8).astype(np.float64)
+        d = dp.copy().view(np.float16).reshape(rows, ns).astype(np.float64)
         return (d[:, :, None] * np.repeat(sc, 16, axis=2) * (q - 32)).reshape(rows, K)
     raise ValueError(fmt)
 
