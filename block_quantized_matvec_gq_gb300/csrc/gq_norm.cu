@@ -142,25 +142,6 @@ __device__ double exact_sum(const unsigned long long *bucket, const uint32_t (&o
     return __longlong_as_double((be << 52) | static_cast<long long>(m & 0xFFFFFFFFFFFFFull));
 }
 
-// x = m 2^(e - 150): biased exponent (subnormals and zero: 1) and the
-// significand with its hidden bit (0 for zero); non-finite values are
-// reported through `bad` (bit 0 infinity, bit 1 NaN) and contribute zero.
-__device__ __forceinline__ void split_f32(float f, uint32_t &e, uint32_t &m, int &bad)
-{
-    const uint32_t b = __float_as_uint(f) & 0x7FFFFFFFu;
-    e = b >> 23;
-    m = b & 0x7FFFFFu;
-    if (e == 255u) {
-        bad |= m ? 2 : 1;
-        m = 0u;
-        e = 1u;
-    } else if (e == 0u) {
-        e = 1u;
-    } else {
-        m |= 0x800000u;
-    }
-}
-
 // 64-bit shifts whose amount may reach 64: PTX clamps the amount to the
 // register width, so a shift by 64 or more gives 0 (no branch needed).
 __device__ __forceinline__ unsigned long long shl64(unsigned long long a, uint32_t n)
@@ -192,6 +173,52 @@ __device__ __forceinline__ void add_square_fixed(uint32_t e, uint32_t m, uint32_
     sticky |= s < 0 && shl64(sq, 64u - min(sn, 64u)) != 0ull;
     lo += tl;
     hi += th + (lo < tl ? 1ull : 0ull);
+}
+
+// Fixed-point partial of one thread: the 128-bit sum as four 32-bit limbs
+// (fast path) plus a (lo, hi, sticky) part for the rare small elements.
+struct FixedAcc {
+    uint32_t a0 = 0u, a1 = 0u, a2 = 0u, a3 = 0u;
+    unsigned long long lo = 0ull, hi = 0ull;
+    bool sticky = false;
+};
+
+// Adds x^2 for x with magnitude bits b (finite) in units of 2^(2E - 364).
+// Fast path, for normal x with e >= E - 24: with t = m << 8 (32 bits), the
+// term m^2 2^(2(e - E) + 64) is t^2 2^(2k), k = e - E + 24 in [0, 24]: one
+// 32 x 32 -> 64 multiply shifted by 2k < 64 into the limbs (funnel shifts
+// and a one-limb select), nothing dropped.  Smaller nonzero x take
+// add_square_fixed.
+__device__ __forceinline__ void add_square(uint32_t b, uint32_t E, FixedAcc &acc)
+{
+    const uint32_t e = b >> 23;
+    const int k = static_cast<int>(e) - static_cast<int>(E) + 24;
+    if (e >= 1u && k >= 0) {
+        const uint32_t t = ((b & 0x7FFFFFu) | 0x800000u) << 8;
+        const unsigned long long p = static_cast<unsigned long long>(t) * t;
+        const uint32_t p0 = static_cast<uint32_t>(p), p1 = static_cast<uint32_t>(p >> 32);
+        const uint32_t k2 = 2u * static_cast<uint32_t>(k), r = k2 & 31u;
+        const uint32_t l0 = p0 << r, l1 = __funnelshift_l(p0, p1, r), l2 = __funnelshift_l(p1, 0u, r);
+        const bool up = k2 >= 32u;  // one limb higher
+        const uint32_t c0 = up ? 0u : l0, c1 = up ? l0 : l1, c2 = up ? l1 : l2, c3 = up ? l2 : 0u;
+        asm("add.cc.u32 %0, %0, %4;\n\t"
+            "addc.cc.u32 %1, %1, %5;\n\t"
+            "addc.cc.u32 %2, %2, %6;\n\t"
+            "addc.u32 %3, %3, %7;"
+            : "+r"(acc.a0), "+r"(acc.a1), "+r"(acc.a2), "+r"(acc.a3)
+            : "r"(c0), "r"(c1), "r"(c2), "r"(c3));
+    } else if (b != 0u) {
+        add_square_fixed(e ? e : 1u, e ? ((b & 0x7FFFFFu) | 0x800000u) : b, E, acc.lo, acc.hi, acc.sticky);
+    }
+}
+
+// The thread's partial as (lo, hi): limbs plus the small-element part.
+__device__ __forceinline__ void fixed_total(const FixedAcc &acc, unsigned long long &lo, unsigned long long &hi)
+{
+    const unsigned long long flo = (static_cast<unsigned long long>(acc.a1) << 32) | acc.a0;
+    const unsigned long long fhi = (static_cast<unsigned long long>(acc.a3) << 32) | acc.a2;
+    lo = flo + acc.lo;
+    hi = fhi + acc.hi + (lo < flo ? 1ull : 0ull);
 }
 
 // The double nearest A 2^(2E - 364) given the dropped part's sticky flag,
@@ -255,24 +282,25 @@ struct SumSqSmem {
     int nonfinite;
     int slow;
     double ss;
+    float inv;
 };
 
-// Block-wide: the row's largest exponent from every thread's own maximum
-// (and non-finite flags), returned to every thread.
-__device__ __forceinline__ uint32_t block_emax(uint32_t emax, int bad, SumSqSmem &sm)
+// Block-wide: from every thread's largest magnitude bit pattern (|x| bits,
+// whose unsigned order is that of the magnitudes, infinities and NaNs above
+// every number), the row's largest exponent E (at least 1) returned to every
+// thread, and the non-finite flags (bit 0 an infinity, bit 1 a NaN: a NaN's
+// pattern is above the infinity's) set in sm.nonfinite.
+__device__ __forceinline__ uint32_t block_emax(uint32_t mbits, SumSqSmem &sm)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    emax = __reduce_max_sync(0xffffffffu, emax);
-    bad = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bad)));
-    if (lane == 0) {
-        sm.emax[warp] = emax;
-        if (bad) atomicOr(&sm.nonfinite, bad);
-    }
+    mbits = __reduce_max_sync(0xffffffffu, mbits);
+    if (lane == 0) sm.emax[warp] = mbits;
     __syncthreads();
-    uint32_t E = sm.emax[0];
+    uint32_t M = sm.emax[0];
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) E = max(E, sm.emax[w]);
-    return E;
+    for (int w = 1; w < kWarps; ++w) M = max(M, sm.emax[w]);
+    if (threadIdx.x == 0) sm.nonfinite = M > 0x7F800000u ? 2 : (M == 0x7F800000u ? 1 : 0);
+    return max(M >> 23, 1u);
 }
 
 // Block-wide: ss from every thread's fixed-point partial (lo, hi, sticky)
@@ -347,28 +375,22 @@ __device__ double block_sum_squares(unsigned long long lo, unsigned long long hi
     return sm.ss;
 }
 
-// The four squares of v into the fixed-point partial.
-__device__ __forceinline__ void add_chunk_fixed(const float4 &v, uint32_t E, unsigned long long &lo,
-                                                unsigned long long &hi, bool &sticky)
+// The four squares of v into the fixed-point partial (a non-finite value
+// adds nothing: the row's result is then decided by sm.nonfinite).
+__device__ __forceinline__ void add_chunk_fixed(const float4 &v, uint32_t E, FixedAcc &acc)
 {
     const float f[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        uint32_t e, m;
-        int ignored = 0;
-        split_f32(f[k], e, m, ignored);
-        add_square_fixed(e, m, E, lo, hi, sticky);
+        const uint32_t b = __float_as_uint(f[k]) & 0x7FFFFFFFu;
+        add_square(b < 0x7F800000u ? b : 0u, E, acc);
     }
 }
-__device__ __forceinline__ void max_chunk_exp(const float4 &v, uint32_t &emax, int &bad)
+// Largest magnitude bit pattern of the chunk, into mbits.
+__device__ __forceinline__ void max_chunk_bits(const float4 &v, uint32_t &mbits)
 {
-    const float f[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        uint32_t e, m;
-        split_f32(f[k], e, m, bad);
-        if (m != 0u && e > emax) emax = e;
-    }
+    mbits = max(mbits, max(max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu),
+                           max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu)));
 }
 
 // Rows of at most kRegChunks * kThreads float4 (K <= 8192) are read once:
@@ -382,15 +404,15 @@ constexpr int kRegChunks = 8;
 __device__ double row_sum_squares(const float4 *__restrict__ xr, int K, SumSqSmem &sm)
 {
     const int nq = K >> 2;
-    if (threadIdx.x == 0) sm.nonfinite = 0;
-    uint32_t emax = 1u;
-    int bad = 0;
-    for (int i = threadIdx.x; i < nq; i += kThreads) max_chunk_exp(__ldg(xr + i), emax, bad);
-    const uint32_t E = block_emax(emax, bad, sm);
-    unsigned long long lo = 0ull, hi = 0ull;
-    bool sticky = false;
-    for (int i = threadIdx.x; i < nq; i += kThreads) add_chunk_fixed(__ldg(xr + i), E, lo, hi, sticky);
-    return block_sum_squares(lo, hi, sticky, E, xr, K, sm);
+    uint32_t mbits = 0u;
+    for (int i = threadIdx.x; i < nq; i += kThreads) max_chunk_bits(__ldg(xr + i), mbits);
+    const uint32_t E = block_emax(mbits, sm);
+    FixedAcc acc;
+    if (E < 255u)  // else the row holds an infinity or a NaN: the sum is decided by sm.nonfinite
+        for (int i = threadIdx.x; i < nq; i += kThreads) add_chunk_fixed(__ldg(xr + i), E, acc);
+    unsigned long long lo, hi;
+    fixed_total(acc, lo, hi);
+    return block_sum_squares(lo, hi, acc.sticky, E, xr, K, sm);
 }
 
 // The same from the row's chunks already in registers (v[j] = chunk
@@ -399,19 +421,20 @@ __device__ double row_sum_squares_regs(const float4 (&v)[kRegChunks], const floa
                                        SumSqSmem &sm)
 {
     const int nq = K >> 2;
-    if (threadIdx.x == 0) sm.nonfinite = 0;
-    uint32_t emax = 1u;
-    int bad = 0;
+    uint32_t mbits = 0u;
 #pragma unroll
     for (int j = 0; j < kRegChunks; ++j)
-        if (static_cast<int>(threadIdx.x) + j * kThreads < nq) max_chunk_exp(v[j], emax, bad);
-    const uint32_t E = block_emax(emax, bad, sm);
-    unsigned long long lo = 0ull, hi = 0ull;
-    bool sticky = false;
+        if (static_cast<int>(threadIdx.x) + j * kThreads < nq) max_chunk_bits(v[j], mbits);
+    const uint32_t E = block_emax(mbits, sm);
+    FixedAcc acc;
+    if (E < 255u) {  // else the row holds an infinity or a NaN: the sum is decided by sm.nonfinite
 #pragma unroll
-    for (int j = 0; j < kRegChunks; ++j)
-        if (static_cast<int>(threadIdx.x) + j * kThreads < nq) add_chunk_fixed(v[j], E, lo, hi, sticky);
-    return block_sum_squares(lo, hi, sticky, E, xr, K, sm);
+        for (int j = 0; j < kRegChunks; ++j)
+            if (static_cast<int>(threadIdx.x) + j * kThreads < nq) add_chunk_fixed(v[j], E, acc);
+    }
+    unsigned long long lo, hi;
+    fixed_total(acc, lo, hi);
+    return block_sum_squares(lo, hi, acc.sticky, E, xr, K, sm);
 }
 
 // Q8_0 of the normalized chunk x4 (one of the eight chunks of its 32-block,
@@ -433,13 +456,39 @@ __device__ __forceinline__ uint32_t quant_chunk(float4 x4, float4 w4, float inv,
     d = __fdiv_rn(amax, 127.0f);
     uint32_t packed = 0;
     if (d != 0.0f) {
+        // round(e / d) with e / d correctly rounded, via y = e * RN(1/d):
+        // |y - e/d| <= 2^-16 and |RN(e/d) - e/d| <= 2^-17 for |e/d| <= 127
+        // (relative errors 2^-24 each), so y and RN(e/d) round to the same
+        // integer unless y is within 2^-15 of a half-integer (or 1/d
+        // overflowed); those take the division itself.
+        const float r = __frcp_rn(d);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float q = fminf(fmaxf(roundf(__fdiv_rn(e[i], d)), -127.0f), 127.0f);
+            const float y = __fmul_rn(e[i], r);
+            const float a = fabsf(y);
+            float q;
+            if (!(a <= 128.0f) || fabsf(a - floorf(a) - 0.5f) <= 0x1p-15f)
+                q = roundf(__fdiv_rn(e[i], d));
+            else
+                q = roundf(y);
+            q = fminf(fmaxf(q, -127.0f), 127.0f);
             packed |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xFFu) << (8 * i);
         }
     }
     return packed;
+}
+
+// inv = f32(1 / sqrt(ss / K + eps)) in double, each operation rounded to
+// nearest, computed by one thread (the double pipe is a small fraction of the
+// f32 one on this part) and returned to every thread.
+__device__ __forceinline__ float block_inv_rms(double ss, int K, float eps, SumSqSmem &sm)
+{
+    if (threadIdx.x == 0) {
+        const double r = __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(K)), static_cast<double>(eps)));
+        sm.inv = __double2float_rn(__ddiv_rn(1.0, r));
+    }
+    __syncthreads();
+    return sm.inv;
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -450,14 +499,17 @@ __global__ void __launch_bounds__(kThreads)
     const int t = blockIdx.x;
     const int nblk = K >> 5;
     const float4 *xr = X + static_cast<size_t>(t) * (K >> 2);
-    // dependents launch once every CTA has started; they still wait for this
-    // grid's completion before reading Xq and dx
-    pdl_launch_dependents();
-    pdl_wait();
     const int nq = K >> 2;
     uint32_t *qr = Xq + static_cast<size_t>(t) * (nblk * 8);
     float *dr = dx + static_cast<size_t>(t) * nblk;
     if (nq <= kRegChunks * kThreads) {
+        // the norm weights never depend on the previous kernel: ask L2 for
+        // them before waiting (K * 4 bytes, a multiple of 128)
+        if (threadIdx.x == 0) prefetch_l2_bulk(w, static_cast<uint32_t>(K) * 4u);
+        // dependents launch once every CTA has started; they still wait for
+        // this grid's completion before reading Xq and dx
+        pdl_launch_dependents();
+        pdl_wait();
         // the row is read once: chunk i = threadIdx.x + j kThreads is v[j];
         // the eight chunks of a 32-block sit in eight adjacent lanes
         float4 v[kRegChunks];
@@ -467,8 +519,7 @@ __global__ void __launch_bounds__(kThreads)
             v[j] = i < nq ? __ldg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         const double ss = row_sum_squares_regs(v, xr, K, sm);
-        const double r = __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(K)), static_cast<double>(eps)));
-        const float inv = __double2float_rn(__ddiv_rn(1.0, r));
+        const float inv = block_inv_rms(ss, K, eps, sm);
 #pragma unroll
         for (int j = 0; j < kRegChunks; ++j) {
             const int i = static_cast<int>(threadIdx.x) + j * kThreads;
@@ -484,9 +535,10 @@ __global__ void __launch_bounds__(kThreads)
         }
         return;
     }
+    pdl_launch_dependents();
+    pdl_wait();
     const double ss = row_sum_squares(xr, K, sm);
-    const double r = __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(K)), static_cast<double>(eps)));
-    const float inv = __double2float_rn(__ddiv_rn(1.0, r));
+    const float inv = block_inv_rms(ss, K, eps, sm);
 
     // Q8_0 of y: eight lanes per 32-block (four elements each), four blocks
     // per warp in a warp-uniform loop so the full-mask shuffles never diverge
