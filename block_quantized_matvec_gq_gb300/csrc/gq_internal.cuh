@@ -288,25 +288,41 @@ __device__ __forceinline__ uint32_t finite_mag_bits(float v)
 // Staging for the subnormal-code core (nib8_sub_fma): the layout of
 // stage_x_q4<true>, with every value multiplied by 2^(149-4i-c), i its
 // nibble position (stored index t of an 8-group has i = t/2), and the block
-// sums (taken from the unscaled values, in stage_x_q4's order) by 2^-c.
-// c = e + 22, e the binary exponent of the largest finite |x| (at least
-// -126): the largest scaled value stays below 2^128, and a product
-// q * x * 2^-c is a normal number whenever |x| >= 2^(e-104).  Infinities
-// and NaNs stay what they are.  Returns c (the same in every thread); all
-// threads of the CTA take part; `red` holds one word per warp; ends with a
-// CTA barrier.
+// sums (taken from the unscaled values: each lane sums its 8-group in stored
+// order, then the four lanes of the block add theirs with two butterfly
+// shuffles) by 2^-c.  c = e + 22, e the binary exponent of the largest finite
+// |x| (at least -126): the largest scaled value stays below 2^128, and a
+// product q * x * 2^-c is a normal number whenever |x| >= 2^(e-104).
+// Infinities and NaNs stay what they are.  K % 32 == 0.  Returns c (the same
+// in every thread); all threads of the CTA take part (blockDim.x a multiple
+// of 32); `red` holds one word per warp; ends with a CTA barrier.
 __device__ __forceinline__ int stage_x_q4k(float *xs, const float *__restrict__ x, int K, uint32_t *red)
 {
-    const int ngroups = K >> 3;
+    const int ngroups = K >> 3;  // a multiple of 4: the 4 groups of a block sit on 4 adjacent lanes
     uint32_t mx = 0u;
-    for (int g = threadIdx.x; g < ngroups; g += blockDim.x) {
-        const float4 a = *reinterpret_cast<const float4 *>(x + 8 * g);
-        const float4 b = *reinterpret_cast<const float4 *>(x + 8 * g + 4);
-        float *dst = xs + (g >> 2) * kXBlk + 8 * (g & 3);
-        *reinterpret_cast<float4 *>(dst) = make_float4(a.x, b.x, a.y, b.y);
-        *reinterpret_cast<float4 *>(dst + 4) = make_float4(a.z, b.z, a.w, b.w);
-        mx = max(mx, max(max(finite_mag_bits(a.x), finite_mag_bits(a.y)), max(finite_mag_bits(a.z), finite_mag_bits(a.w))));
-        mx = max(mx, max(max(finite_mag_bits(b.x), finite_mag_bits(b.y)), max(finite_mag_bits(b.z), finite_mag_bits(b.w))));
+    for (int g0 = threadIdx.x & ~31; g0 < ngroups; g0 += blockDim.x) {
+        const int g = g0 + (threadIdx.x & 31);
+        float s = 0.f;
+        if (g < ngroups) {
+            const float4 a = *reinterpret_cast<const float4 *>(x + 8 * g);
+            const float4 b = *reinterpret_cast<const float4 *>(x + 8 * g + 4);
+            float *dst = xs + (g >> 2) * kXBlk + 8 * (g & 3);
+            *reinterpret_cast<float4 *>(dst) = make_float4(a.x, b.x, a.y, b.y);
+            *reinterpret_cast<float4 *>(dst + 4) = make_float4(a.z, b.z, a.w, b.w);
+            mx = max(mx, max(max(finite_mag_bits(a.x), finite_mag_bits(a.y)), max(finite_mag_bits(a.z), finite_mag_bits(a.w))));
+            mx = max(mx, max(max(finite_mag_bits(b.x), finite_mag_bits(b.y)), max(finite_mag_bits(b.z), finite_mag_bits(b.w))));
+            s = a.x;
+            s += b.x;
+            s += a.y;
+            s += b.y;
+            s += a.z;
+            s += b.z;
+            s += a.w;
+            s += b.w;
+        }
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        if (g < ngroups && (g & 3) == 0) xs[(g >> 2) * kXBlk + 32] = s;
     }
     mx = __reduce_max_sync(0xffffffffu, mx);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
@@ -314,27 +330,25 @@ __device__ __forceinline__ int stage_x_q4k(float *xs, const float *__restrict__ 
     for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) mx = max(mx, red[w]);
     const int e = max(static_cast<int>(mx >> 23) - 127, -126);
     const int c = e + 22;
-    for (int b = threadIdx.x; b < (K >> 5); b += blockDim.x) {
-        float *blk = xs + b * kXBlk;
-        float s = 0.f;
+    // position i's factor 2^(127-e-4i) as two exact powers of two
+    float f1[4], f2[4];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const float4 v = ld_xq4(blk, m);
-            s += v.x;
-            s += v.y;
-            s += v.z;
-            s += v.w;
-        }
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            // float4 m holds stored indices 4(m&1)..4(m&1)+3 of its 8-group: positions 2(m&1), 2(m&1)+1
-            const int i0 = 2 * (m & 1);
-            const int k0 = 127 - e - 4 * i0, k1 = k0 - 4;
-            const float4 v = ld_xq4(blk, m);
-            *reinterpret_cast<float4 *>(blk + 4 * m) =
-                make_float4(scale_pow2(v.x, k0), scale_pow2(v.y, k0), scale_pow2(v.z, k1), scale_pow2(v.w, k1));
-        }
-        blk[32] = scale_pow2(s, -c);
+    for (int i = 0; i < 4; ++i) {
+        const int k = 127 - e - 4 * i, k1 = k >> 1;
+        f1[i] = pow2i(k1);
+        f2[i] = pow2i(k - k1);
+    }
+    const int ks = -c, ks1 = ks >> 1;
+    const float s1 = pow2i(ks1), s2 = pow2i(ks - ks1);
+    for (int g = threadIdx.x; g < ngroups; g += blockDim.x) {
+        float *p = xs + (g >> 2) * kXBlk + 8 * (g & 3);
+        const float4 a = *reinterpret_cast<const float4 *>(p);
+        const float4 b = *reinterpret_cast<const float4 *>(p + 4);
+        *reinterpret_cast<float4 *>(p) =
+            make_float4(a.x * f1[0] * f2[0], a.y * f1[0] * f2[0], a.z * f1[1] * f2[1], a.w * f1[1] * f2[1]);
+        *reinterpret_cast<float4 *>(p + 4) =
+            make_float4(b.x * f1[2] * f2[2], b.y * f1[2] * f2[2], b.z * f1[3] * f2[3], b.w * f1[3] * f2[3]);
+        if ((g & 3) == 0) p[32] = p[32] * s1 * s2;
     }
     __syncthreads();
     return c;

@@ -278,7 +278,8 @@ struct Q4KStream {
                 for (int i = 0; i < NS; ++i) {
                     w[u][i] = ld_stream16(wp[i] + base + u * LG);
                     // the 16-byte record is shared by the 8 lanes of a super-block
-                    r[u][i] = __ldg(rp[i] + ((base + u * LG) >> 3));
+                    // (base is a multiple of 8: whole super-blocks)
+                    r[u][i] = __ldg(rp[i] + (base >> 3) + u * (LG / 8));
                 }
             }
         }
