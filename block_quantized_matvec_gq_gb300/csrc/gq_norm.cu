@@ -175,6 +175,19 @@ __device__ __forceinline__ void add_square_fixed(uint32_t e, uint32_t m, uint32_
     hi += th + (lo < tl ? 1ull : 0ull);
 }
 
+// The term of a nonzero finite x below the fast path's range (e < E - 24,
+// subnormals counted as e = 1), out of line so the unrolled loops stay small:
+// m^2 2^(2(e - E) + 64) < 2^48 2^16, so the term is below 2^64 units; .y is
+// nonzero if bits below the unit were dropped.
+__device__ __noinline__ ulonglong2 small_square(uint32_t b, uint32_t E)
+{
+    const uint32_t e = b >> 23;
+    unsigned long long lo = 0ull, hi = 0ull;
+    bool sticky = false;
+    add_square_fixed(e ? e : 1u, e ? ((b & 0x7FFFFFu) | 0x800000u) : b, E, lo, hi, sticky);
+    return make_ulonglong2(lo, sticky ? 1ull : 0ull);
+}
+
 // Fixed-point partial of one thread: the 128-bit sum as four 32-bit limbs
 // (fast path) plus a (lo, hi, sticky) part for the rare small elements.
 struct FixedAcc {
@@ -184,17 +197,18 @@ struct FixedAcc {
 };
 
 // Adds x^2 for x with magnitude bits b (finite) in units of 2^(2E - 364).
-// Fast path, for normal x with e >= E - 24: with t = m << 8 (32 bits), the
+// Fast path, for x with e >= E - 24 (subnormals counted as e = 1 with no
+// hidden bit): with t = m << 8 (32 bits), the
 // term m^2 2^(2(e - E) + 64) is t^2 2^(2k), k = e - E + 24 in [0, 24]: one
 // 32 x 32 -> 64 multiply shifted by 2k < 64 into the limbs (funnel shifts
-// and a one-limb select), nothing dropped.  Smaller nonzero x take
-// add_square_fixed.
+// and a one-limb select), nothing dropped.  Smaller nonzero x take small_square
+// (add_square_fixed out of line).
 __device__ __forceinline__ void add_square(uint32_t b, uint32_t E, FixedAcc &acc)
 {
     const uint32_t e = b >> 23;
-    const int k = static_cast<int>(e) - static_cast<int>(E) + 24;
-    if (e >= 1u && k >= 0) {
-        const uint32_t t = ((b & 0x7FFFFFu) | 0x800000u) << 8;
+    const int k = static_cast<int>(e ? e : 1u) - static_cast<int>(E) + 24;  // subnormals: e = 1, no hidden bit
+    if (k >= 0) {
+        const uint32_t t = (e ? ((b & 0x7FFFFFu) | 0x800000u) : b) << 8;
         const unsigned long long p = static_cast<unsigned long long>(t) * t;
         const uint32_t p0 = static_cast<uint32_t>(p), p1 = static_cast<uint32_t>(p >> 32);
         const uint32_t k2 = 2u * static_cast<uint32_t>(k), r = k2 & 31u;
@@ -208,7 +222,10 @@ __device__ __forceinline__ void add_square(uint32_t b, uint32_t E, FixedAcc &acc
             : "+r"(acc.a0), "+r"(acc.a1), "+r"(acc.a2), "+r"(acc.a3)
             : "r"(c0), "r"(c1), "r"(c2), "r"(c3));
     } else if (b != 0u) {
-        add_square_fixed(e ? e : 1u, e ? ((b & 0x7FFFFFu) | 0x800000u) : b, E, acc.lo, acc.hi, acc.sticky);
+        const ulonglong2 t = small_square(b, E);
+        acc.lo += t.x;
+        acc.hi += acc.lo < t.x ? 1ull : 0ull;
+        acc.sticky |= t.y != 0ull;
     }
 }
 
@@ -440,6 +457,12 @@ __device__ double row_sum_squares_regs(const float4 (&v)[kRegChunks], const floa
 // Q8_0 of the normalized chunk x4 (one of the eight chunks of its 32-block,
 // the eight lanes of a block being adjacent): the packed codes and, from
 // every lane, the block's d.  All lanes of the warp take part (shuffles).
+// clamp(roundf(e / d), +-127) with the division itself (out of line: rare).
+__device__ __noinline__ int exact_code(float e, float d)
+{
+    return static_cast<int>(fminf(fmaxf(roundf(__fdiv_rn(e, d)), -127.0f), 127.0f));
+}
+
 __device__ __forceinline__ uint32_t quant_chunk(float4 x4, float4 w4, float inv, float offset, bool active,
                                                 float &d)
 {
@@ -461,18 +484,21 @@ __device__ __forceinline__ uint32_t quant_chunk(float4 x4, float4 w4, float inv,
         // (relative errors 2^-24 each), so y and RN(e/d) round to the same
         // integer unless y is within 2^-15 of a half-integer (or 1/d
         // overflowed); those take the division itself.
+        // Away from half-integers, y + copysign(0.5, y) is at least 2^-15
+        // from an integer and rounds by at most 2^-18, so truncating it is
+        // roundf(y).
         const float r = __frcp_rn(d);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float y = __fmul_rn(e[i], r);
             const float a = fabsf(y);
-            float q;
+            int q;
             if (!(a <= 128.0f) || fabsf(a - floorf(a) - 0.5f) <= 0x1p-15f)
-                q = roundf(__fdiv_rn(e[i], d));
+                q = exact_code(e[i], d);
             else
-                q = roundf(y);
-            q = fminf(fmaxf(q, -127.0f), 127.0f);
-            packed |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xFFu) << (8 * i);
+                q = __float2int_rz(__fadd_rn(y, copysignf(0.5f, y)));
+            q = min(max(q, -127), 127);
+            packed |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * i);
         }
     }
     return packed;
