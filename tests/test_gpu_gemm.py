@@ -141,12 +141,14 @@ def test_gemm_full_512x21504x5376_sampled():
     assert np.all(np.abs(Yg - Y_ref) <= 1e-5 * A)
 
 
-def test_gemm_scales_spread_over_many_octaves():
+@pytest.mark.parametrize("M", [40, 200])  # scale-folded f16 pieces (one CTA); exact block dots (CTA pairs)
+def test_gemm_scales_spread_over_many_octaves(M):
     """Block scales spread over many octaves inside each 8-block chunk (weight
     scales down to f16 subnormals, activation blocks 2^-12..2^12 apart, an
     all-zero block and an all-zero chunk): the power-of-two chunk factors of
-    the f16 operand pieces keep every output within the bound."""
-    rows, K, M = 200, 512, 40
+    the f16 operand pieces, and the per-block fold of the exact block dots,
+    keep every output within the bound."""
+    rows, K = 200, 512
     nb = K // 32
     rng = np.random.default_rng(77)
     W = synth.q4_0_weights(rows, K, synth.stream(77, 0))
@@ -167,10 +169,11 @@ def test_gemm_scales_spread_over_many_octaves():
     assert np.all(err <= 1e-5 * A_el), float(np.max(err / np.maximum(A_el, 1e-300)))
 
 
-@pytest.mark.parametrize("K", [128, 256])  # per-block fold; scale-folded f16 pieces
-def test_gemm_all_eight_weights_exact_zero(K):
+# per-block fold (one CTA); small batches; exact block dots on CTA pairs
+@pytest.mark.parametrize("K,M", [(128, 130), (256, 9), (256, 200)])
+def test_gemm_all_eight_weights_exact_zero(K, M):
     import blockenc as be
-    rows, M = 70, 9
+    rows = 70
     blk = be.enc_q4_0(np.full(32, 8), 0.5)
     W = be.rows_from_blocks([[blk] * (K // 32)] * rows)
     X = synth.normal((M, K), synth.stream(501, 1))
