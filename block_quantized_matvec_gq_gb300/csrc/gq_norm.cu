@@ -294,7 +294,7 @@ __device__ __forceinline__ double round_fixed(unsigned long long lo, unsigned lo
 struct SumSqSmem {
     unsigned long long wbk[kWarps][256];  // per-warp exponent buckets (slow path)
     unsigned long long bucket[256];
-    unsigned long long part_lo[kThreads], part_hi[kThreads];
+    unsigned long long part_lo[kWarps], part_hi[kWarps];
     uint32_t emax[kWarps];
     int nonfinite;
     int slow;
@@ -329,22 +329,25 @@ __device__ double block_sum_squares(unsigned long long lo, unsigned long long hi
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nq = K >> 2;
-    sm.part_lo[threadIdx.x] = lo;
-    sm.part_hi[threadIdx.x] = hi;
-    const int any_sticky = __syncthreads_or(sticky ? 1 : 0);
-    if (threadIdx.x < 32) {  // warp 0 adds the partial sums (exactly: the total stays below 2^128)
-        unsigned long long a = 0ull, b = 0ull;
-        for (int j = threadIdx.x; j < kThreads; j += 32) {
-            a += sm.part_lo[j];
-            b += sm.part_hi[j] + (a < sm.part_lo[j] ? 1ull : 0ull);
-        }
+    // every warp adds its lanes' partials, then warp 0 the warps' sums
+    // (exactly: the total stays below 2^128)
+    auto add128 = [](unsigned long long &a, unsigned long long &b, unsigned long long oa, unsigned long long ob) {
+        a += oa;
+        b += ob + (a < oa ? 1ull : 0ull);
+    };
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const unsigned long long oa = __shfl_xor_sync(0xffffffffu, a, o);
-            const unsigned long long ob = __shfl_xor_sync(0xffffffffu, b, o);
-            a += oa;
-            b += ob + (a < oa ? 1ull : 0ull);
-        }
+    for (int o = 16; o > 0; o >>= 1)
+        add128(lo, hi, __shfl_xor_sync(0xffffffffu, lo, o), __shfl_xor_sync(0xffffffffu, hi, o));
+    if (lane == 0) {
+        sm.part_lo[warp] = lo;
+        sm.part_hi[warp] = hi;
+    }
+    const int any_sticky = __syncthreads_or(sticky ? 1 : 0);
+    if (threadIdx.x < 32) {
+        unsigned long long a = lane < kWarps ? sm.part_lo[lane] : 0ull, b = lane < kWarps ? sm.part_hi[lane] : 0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            add128(a, b, __shfl_xor_sync(0xffffffffu, a, o), __shfl_xor_sync(0xffffffffu, b, o));
         if (threadIdx.x == 0) {
             double ss;
             if (sm.nonfinite & 2)
@@ -373,11 +376,11 @@ __device__ double block_sum_squares(unsigned long long lo, unsigned long long hi
             add_squares_warp(sm.wbk[warp], &sm.nonfinite, v.w, lane);
         }
         __syncthreads();
-        {  // the warps' buckets, added exactly (each total stays below K 2^48 < 2^64)
-            unsigned long long sb = 0ull;
+        for (int e = threadIdx.x; e < 256; e += kThreads) {  // the warps' buckets, added exactly (each total
+            unsigned long long sb = 0ull;                     // stays below K 2^48 < 2^64)
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) sb += sm.wbk[w][threadIdx.x];
-            sm.bucket[threadIdx.x] = sb;
+            for (int w = 0; w < kWarps; ++w) sb += sm.wbk[w][e];
+            sm.bucket[e] = sb;
         }
         __syncthreads();
         if (threadIdx.x < 32) {  // warp 0: which buckets are occupied, then lane 0 adds them
@@ -410,7 +413,7 @@ __device__ __forceinline__ void max_chunk_bits(const float4 &v, uint32_t &mbits)
                            max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu)));
 }
 
-// Rows of at most kRegChunks * kThreads float4 (K <= 8192) are read once:
+// Rows of at most kRegChunks * kThreads float4 (K <= 16384) are read once:
 // thread t keeps chunks t, t + kThreads, ... in registers.
 constexpr int kRegChunks = 8;
 
