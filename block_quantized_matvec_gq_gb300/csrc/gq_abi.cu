@@ -229,9 +229,11 @@ int gq_rmsnorm_sum_squares(const float *X, double *ss, int K, int M, gq_stream_t
 
 size_t gq_q4_0_gemm_workspace_bytes(int K, int M)
 {
-    // enough for either contraction path (the split path needs the most)
-    const size_t a = gemm_workspace_bytes(K, M), b = gemm_split_workspace_bytes(K, M);
-    return a > b ? a : b;
+    // enough for every contraction path
+    const size_t a = gemm_workspace_bytes(K, M), b = gemm_split_workspace_bytes(K, M),
+                 c = gemm_mma_workspace_bytes(K, M);
+    const size_t ab = a > b ? a : b;
+    return ab > c ? ab : c;
 }
 
 int gq_q4_0_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *Y, void *workspace,
@@ -243,7 +245,10 @@ int gq_q4_0_gemm_q8act(const void *W, const int8_t *Xq, const float *dx, float *
     if (rows < 1 || M < 1 || K < 32 || K % 32 != 0) return GQ_ERR_SHAPE;
     if (workspace_bytes < gq_q4_0_gemm_workspace_bytes(K, M)) return GQ_ERR_WORKSPACE;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // few tokens: decode each weight once on the CUDA cores and apply it to every token
+    // up to a few hundred tokens: exact block dots in registers (mma.sync)
+    if (gemm_mma_supported(K, M) && M <= gemm_mma_max_tokens())
+        return launch_gemm_mma(W, Xq, dx, Y, workspace, workspace_bytes, rows, K, M, st);
+    // few tokens, other K: decode each weight once on the CUDA cores and apply it to every token
     if (gemm_small_supported(K, M)) return launch_gemm_small(W, Xq, dx, Y, rows, K, M, st);
     if (gemm_split_supported(K) && !gemm_force_block_path())
         return launch_gemm_split(W, Xq, dx, Y, workspace, workspace_bytes, rows, K, M, st);

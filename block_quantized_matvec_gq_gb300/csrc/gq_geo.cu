@@ -82,6 +82,18 @@ MatvecGeo choose_logits_geo(int rows, int nb)
     return MatvecGeo{8, 2, 4, 8};
 }
 
+// Largest token batch that takes the register-operand contraction
+// (gq_gemm_mma.cu) rather than the tensor-memory tiles.  Measured on 21504 x
+// 5376 weights: 103 us at M = 96 against 127 us on the tiles (which take the
+// same time at any M <= 128); at M = 128 the tiles win (129 us).
+int gemm_mma_max_tokens()
+{
+#ifdef GQ_TUNING
+    if (const char *v = getenv("GQ_MMA_MAX")) return atoi(v);
+#endif
+    return 112;
+}
+
 MatvecGeo choose_q6k_geo() { return tuned("GQ_Q6", MatvecGeo{16, 2, 4, 8}); }
 
 MatvecGeo choose_ffn_geo(int rows, int nb, bool pair_ok)

@@ -141,6 +141,12 @@ size_t gemm_workspace_bytes(int K, int M);
 size_t gemm_split_workspace_bytes(int K, int M);
 bool gemm_split_supported(int K);
 bool gemm_small_supported(int K, int M);
+// register-operand tensor-core path with exact block dots (gq_gemm_mma.cu): K % 256 == 0
+bool gemm_mma_supported(int K, int M);
+size_t gemm_mma_workspace_bytes(int K, int M);
+int gemm_mma_max_tokens();
+int launch_gemm_mma(const void *W, const int8_t *Xq, const float *dx, float *Y, void *ws, size_t ws_bytes, int rows,
+                    int K, int M, cudaStream_t s);
 int launch_gemm_small(const void *W, const int8_t *Xq, const float *dx, float *Y, int rows, int K, int M,
                       cudaStream_t s);
 int launch_gemm_split(const void *W, const int8_t *Xq, const float *dx, float *Y, void *ws, size_t ws_bytes,

@@ -58,6 +58,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
             : "memory");
     return ok != 0;
 }
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ uint64_t globaltimer()
 {
     uint64_t t;
@@ -282,9 +294,10 @@ static inline EncodeTiledFn encode_tiled()
 }
 
 // 2-D tensor [outer][inner] of `dt` elements with row stride `stride` bytes;
-// box inner x outer elements.
+// box inner x outer elements; `sw` the shared-memory swizzle of the box.
 static inline bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
-                     uint64_t stride, uint32_t box_inner, uint32_t box_outer)
+                     uint64_t stride, uint32_t box_inner, uint32_t box_outer,
+                     CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE)
 {
     EncodeTiledFn fn = encode_tiled();
     if (!fn) return false;
@@ -293,7 +306,7 @@ static inline bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

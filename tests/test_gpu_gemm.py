@@ -103,10 +103,12 @@ def test_gemm_cta_pair_shapes(M, rows, K):
     assert np.all(err <= 1e-5 * A), float(np.max(err / np.maximum(A, 1e-300)))
 
 
-# Small batches (M <= 24 in passes of up to 8 tokens whose staged codes fit
-# in shared memory) run on the CUDA-core kernel: odd rows, one block, the
-# largest K an 8-token pass still stages, several passes with a short last
-# one; just past those limits the tensor-core paths take over.
+# Small batches: K % 256 == 0 runs on the register-operand kernel (exact
+# block dots, passes of up to 64 tokens); other K with M <= 24 in passes of
+# up to 8 tokens whose staged codes fit in shared memory on the CUDA-core
+# kernel: odd rows, one block, the largest K an 8-token pass still stages,
+# several passes with a short last one; just past those limits the
+# tensor-memory tiles take over.
 @pytest.mark.parametrize("M,rows,K", [(2, 1, 32), (3, 77, 96), (4, 100, 21504), (8, 300, 5376), (13, 1001, 256),
                                       (16, 3001, 5376), (17, 77, 96), (24, 300, 5376), (6, 50, 15744),
                                       # staging too large or too many tokens: tensor cores
@@ -141,7 +143,7 @@ def test_gemm_full_512x21504x5376_sampled():
     assert np.all(np.abs(Yg - Y_ref) <= 1e-5 * A)
 
 
-@pytest.mark.parametrize("M", [40, 200])  # scale-folded f16 pieces (one CTA); exact block dots (CTA pairs)
+@pytest.mark.parametrize("M", [40, 200])  # exact block dots in registers; scale-folded f16 pieces (CTA pairs)
 def test_gemm_scales_spread_over_many_octaves(M):
     """Block scales spread over many octaves inside each 8-block chunk (weight
     scales down to f16 subnormals, activation blocks 2^-12..2^12 apart, an
@@ -163,10 +165,12 @@ def test_gemm_scales_spread_over_many_octaves(M):
     X = X.astype(np.float32)
     Xq, dx = oracle.quantize_q8_0(X, M, K)
     Y = run_gemm(W, Xq, dx, rows, K, M)
-    Y_ref, _ = oracle.gemm_q8act(W, Xq, dx, rows, K, M)
+    Y_ref, A_blk = oracle.gemm_q8act(W, Xq, dx, rows, K, M)
     err = np.abs(Y.astype(np.float64) - Y_ref)
     A_el = element_bound(W, Xq, dx, K)
     assert np.all(err <= 1e-5 * A_el), float(np.max(err / np.maximum(A_el, 1e-300)))
+    if M <= 128:  # exact integer block dots: the block-level bound holds under any cancellation
+        assert np.all(err <= 1e-5 * A_blk), float(np.max(err / np.maximum(A_blk, 1e-300)))
 
 
 # per-block fold (one CTA); small batches; exact block dots on CTA pairs
@@ -237,3 +241,48 @@ def test_gemm_repeat_runs_bitwise_identical(M, rows, K):
         outs.append(Y.cpu().numpy().view(np.uint32))
     assert gq.gq_device_status() == gq.GQ_OK
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+# The register-operand kernel (K % 256 == 0, M <= 112): one row and fewer
+# than 16 rows, ragged 16-row tiles, every pass width (1, 2 and 4 token
+# tiles, a last pass of 3 tiles padded to 4), passes of 32 tokens with a
+# short last one, a single 16-block stage half past the end of the row
+# (K = 256) and many stages, more row groups than CTAs (each CTA then takes
+# two groups).
+@pytest.mark.parametrize("M,rows,K", [(1, 1, 256), (3, 17, 512), (9, 5, 256), (20, 1000, 768), (33, 130, 2048),
+                                      (64, 300, 5376), (65, 300, 512), (75, 257, 256), (112, 2000, 5376),
+                                      (32, 40000, 256), (100, 25000, 256), (7, 61, 21504)])
+def test_gemm_register_path_shapes(M, rows, K):
+    W = synth.q4_0_weights(rows, K, synth.stream(1100 + M, rows))
+    X = synth.normal((M, K), synth.stream(1100 + M, K))
+    Xq, dx = oracle.quantize_q8_0(X, M, K)
+    Y = run_gemm(W, Xq, dx, rows, K, M)
+    assert gq.gq_device_status() == gq.GQ_OK
+    Y_ref, A = oracle.gemm_q8act(W, Xq, dx, rows, K, M)
+    err = np.abs(Y.astype(np.float64) - Y_ref)
+    assert np.all(err <= 1e-5 * A), float(np.max(err / np.maximum(A, 1e-300)))
+
+
+@pytest.mark.parametrize("M,rows,K", [(1, 40, 5376), (8, 33, 5376), (13, 100, 2048), (64, 50, 5376),
+                                      (100, 70, 5376)])
+def test_gemm_register_path_block_dots_exact(M, rows, K):
+    """With every block scale 1 (d_w and dx), Y is the plain sum of the
+    integer block dots, an integer below 2^24: the register-operand kernel
+    must return it exactly, for codes over the whole int8 range (-128
+    included) and nibble blocks of all 0 and all 15 (the largest products)."""
+    nb = K // 32
+    W = synth.q4_0_weights(rows, K, synth.stream(1200 + M, rows))
+    Wb = W.reshape(rows, nb, 18)
+    Wb[:, :, 0:2] = np.full((rows, nb), 1.0, np.float16).view(np.uint8).reshape(rows, nb, 2)
+    Wb[0, :, 2:] = 0x00          # q = 0 everywhere: w = -8
+    Wb[1 % rows, ::2, 2:] = 0xFF  # q = 15 in every other block: w = 7
+    rng = np.random.default_rng(1200 + M)
+    Xq = rng.integers(-128, 128, size=(M, K)).astype(np.int8)
+    Xq[0, :] = -128
+    Xq[-1, ::2] = 127
+    dx = np.ones((M, nb), np.float32)
+    Y = run_gemm(W, Xq, dx, rows, K, M)
+    D = oracle.block_dots(W, Xq, rows, K, M, 0, M, 0, rows).astype(np.int64)
+    ref = D.sum(axis=2)
+    assert np.abs(ref).max() < 2 ** 24
+    assert np.array_equal(Y.astype(np.float64), ref.astype(np.float64))
