@@ -601,22 +601,36 @@ class Gemm(Workload):
                              "fp64 block-scaled contraction)")
 
 
-class GemmSmallBatch8(Gemm):
-    """The same contraction at a small batch (a verifier's eight tokens): every
-    weight is decoded once on the CUDA cores and applied to all eight tokens."""
+class GemmSmallBatch8(Gemm, Rotating):
+    """The same contraction at a small batch (a verifier's eight tokens): the
+    register-operand tensor-core kernel (exact integer block dots, every
+    weight streamed once per step).  The 65 MB weight matrix fits in L2, so
+    the step rotates over independent copies (working set > 4x L2)."""
     name = "q4_0_gemm_q8act_8x21504x5376"
-    kernel = "k_gemm_small"
+    kernel = "k_gemm_mma"
     bound = "hbm"  # reported as bytes per step (weights, X, Y) over the step time
     M = 8
+    launches_per_step = 3  # quantizer, activation image, contraction
     cpu_unit, cpu_scale = "GB/s", 1e9
     cpu_tokens = 32
 
+    def setup(self, torch, gq):
+        super().setup(torch, gq)
+        R = self._rotate(torch, self.weight_bytes)
+        self.copies = [self.Wp] + [self.Wp.clone() for _ in range(R - 1)]
+        self.working_set = self.weight_bytes * R
+        self.l2_policy = f"{R} rotating weight copies ({self.weight_bytes * R / 2**20:.0f} MiB > 4x L2)"
+
+    def step(self, i):
+        self.gq.gq_quantize_q8_0(self.X, self.Xq, self.dx, self.K, self.M)
+        self.gq.gq_q4_0_gemm_q8act(self.copies[i % len(self.copies)], self.Xq, self.dx, self.Y, self.ws,
+                                   self.ws_bytes, self.rows, self.K, self.M)
+
 
 class GemmSmallBatch32(GemmSmallBatch8):
-    """32 tokens (a short prompt): past the CUDA-core kernel's 24, one
-    128-token tile per CTA on the tensor cores."""
+    """32 tokens (a short prompt): the same kernel with four 8-token tiles."""
     name = "q4_0_gemm_q8act_32x21504x5376"
-    kernel = "k_gemm_split"
+    kernel = "k_gemm_mma"
     M = 32
 
 

@@ -169,7 +169,7 @@ def test_gemm_scales_spread_over_many_octaves(M):
     err = np.abs(Y.astype(np.float64) - Y_ref)
     A_el = element_bound(W, Xq, dx, K)
     assert np.all(err <= 1e-5 * A_el), float(np.max(err / np.maximum(A_el, 1e-300)))
-    if M <= 128:  # exact integer block dots: the block-level bound holds under any cancellation
+    if M <= 112:  # exact integer block dots: the block-level bound holds under any cancellation
         assert np.all(err <= 1e-5 * A_blk), float(np.max(err / np.maximum(A_blk, 1e-300)))
 
 
