@@ -132,6 +132,11 @@ int gq_unpack(int format, const void *W_packed, void *W_canon, int rows, int K,
  * |x_j| >= 2^-104 * X; a product involving a smaller element is rounded to
  * an absolute grid of at most 2^-128 * X * |d * sc|.  Scaling x by 2^k scales
  * y by exactly 2^k while nothing over- or underflows.
+ * Non-finite x: y_i is non-finite exactly where the definition's sum is.
+ * Q4_0, Q8_0 and Q6_K also give the definition's NaN or infinity; Q4_K forms
+ * each sub-block as d*sc*sum(q x) - dmin*m*sum(x), so an infinity that meets
+ * a zero code or the min term can give NaN where the per-weight sum is
+ * infinite.
  * ------------------------------------------------------------------------ */
 int gq_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K, int M,
                    gq_stream_t stream);
@@ -219,14 +224,23 @@ int gq_quantize_q8_0(const float *X, int8_t *Xq, float *dx, int K, int M, gq_str
  *   Y[t][r]    = sum_b d_w[r][b] * dx[t][b] * D[t][r][b]          (f32)
  * Y is f32[M][rows] row-major (one row of Y per token).
  *
- * Y is computed on the tensor cores in one of two ways, both equal to the
+ * Y is computed on the tensor cores in one of three ways, all equal to the
  * sum above up to f32 rounding (|Y - Y_ref| <= 1e-5 * sum_k |w x| over the
- * dequantized operands w = d_w*(q_w-8), x = dx*Xq): for K % 256 == 0 both
- * block scales are folded, per 8-block chunk and with power-of-two chunk
- * factors, into f16 operand pieces (dx*Xq as two, d_w*(q_w-8) as two exact
- * pieces) and Y accumulates a chunk at a time in tensor memory (with more
- * than 128 tokens on pairs of SMs); otherwise each block's exact integer D
- * is read out and folded in f32.
+ * dequantized operands w = d_w*(q_w-8), x = dx*Xq):
+ *   K % 256 == 0, M <= 112: each block's exact integer D is formed by
+ *     mma.sync on f16 operands holding the small integers and folded at once
+ *     as Y += (d_w*dx)*D in f32, block by block (this also meets the tighter
+ *     |Y - Y_ref| <= 1e-5 * sum_b |d_w dx D|);
+ *   K % 256 == 0, M > 112: both block scales are folded, per 8-block chunk
+ *     and with power-of-two chunk factors, into f16 operand pieces (dx*Xq as
+ *     two, d_w*(q_w-8) as two exact pieces) and Y accumulates a chunk at a
+ *     time in tensor memory (with more than 128 tokens on pairs of SMs);
+ *   other K: each block's exact integer D is read out of tensor memory and
+ *     folded in f32 (up to 24 tokens: the same D by dp4a on the CUDA cores).
+ * Non-finite scales (dx from a non-finite X, or an fp16 d_w that is infinite
+ * or NaN): Y[t][r] is non-finite exactly where the definition's sum is; the
+ * exact-D paths give the definition's NaN or infinity, the scale-folded path
+ * gives NaN for every such output (its pieces' difference of infinities).
  *
  * The workspace (device memory, 16-byte aligned, at least
  * gq_q4_0_gemm_workspace_bytes(K, M) bytes, owned by the caller) receives

@@ -53,3 +53,21 @@ def assert_within(y_gpu: np.ndarray, y_ref: np.ndarray, a_ref: np.ndarray, rel: 
             f"{what}: {bad.size} rows outside the bound; first row {i}: gpu={y_gpu[i]!r} "
             f"ref={y_ref[i]!r} err={err[i]:.3e} bound={bound[i]:.3e} (A={a_ref[i]:.3e})")
     return float(np.max(err / np.where(bound > 0, bound, 1.0))) if err.size else 0.0
+
+
+def assert_same_specials(y_gpu, y_ref, a_ref, rel: float = 1e-5, what="", exact: bool = True):
+    """Non-finite results exactly where the oracle's are (with exact: NaN
+    where it is NaN and the same infinity where it is infinite; else any
+    non-finite value), and the acceptance bound everywhere else."""
+    y = np.asarray(y_gpu, dtype=np.float64)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    nan_ref, inf_ref = np.isnan(y_ref), np.isinf(y_ref)
+    if exact:
+        assert np.array_equal(np.isnan(y), nan_ref), f"{what}: NaN pattern differs"
+        assert np.array_equal(y[inf_ref], y_ref[inf_ref]), f"{what}: infinities differ"
+    else:
+        assert np.array_equal(~np.isfinite(y), nan_ref | inf_ref), f"{what}: non-finite set differs"
+    fin = ~(nan_ref | inf_ref)
+    if fin.any():
+        assert_within(y[fin], y_ref[fin], np.asarray(a_ref)[fin], rel=rel, what=what)
+    return int(nan_ref.sum()), int(inf_ref.sum())

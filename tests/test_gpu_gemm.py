@@ -19,7 +19,7 @@ import pytest
 import block_quantized_matvec_gq_gb300 as gq
 import oracle
 import synth
-from gpu_util import dev, guarded, packed, torch
+from gpu_util import assert_same_specials, dev, guarded, packed, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -286,3 +286,38 @@ def test_gemm_register_path_block_dots_exact(M, rows, K):
     ref = D.sum(axis=2)
     assert np.abs(ref).max() < 2 ** 24
     assert np.array_equal(Y.astype(np.float64), ref.astype(np.float64))
+
+
+# register-operand path (two shapes); CUDA-core dp4a (K % 256 != 0, M <= 24);
+# per-block tcgen05 read-out (K % 256 != 0, M > 24); scale-folded pieces (M > 112)
+@pytest.mark.parametrize("M,rows,K", [(16, 300, 2048), (40, 97, 5376), (8, 77, 544), (30, 50, 544),
+                                      (200, 97, 5376)])
+def test_gemm_non_finite_scales(M, rows, K):
+    """Non-finite block scales: an activation scale of NaN makes its token's
+    row of Y NaN; an infinite activation scale or weight scale gives
+    +-inf, or NaN where it meets a zero block dot or another infinity of
+    the other sign, exactly as in the fp64 definition on the register-operand
+    path (exact block dots, then (d_w dx) D in f32).  The scale-folded path
+    (M > 112) splits d_w (q - 8) into two f16 pieces, whose difference of
+    infinities is NaN: there every non-finite result is NaN, on the same
+    set of outputs."""
+    nb = K // 32
+    W = synth.q4_0_weights(rows, K, synth.stream(1300 + M, rows))
+    Wb = W.reshape(rows, nb, 18)
+    d16 = Wb[:, :, 0:2].copy().view(np.float16).reshape(rows, nb)
+    d16[11 % rows, 3] = np.float16(np.inf)
+    d16[5 % rows, nb - 1] = np.float16(-np.inf)
+    Wb[:, :, 0:2] = d16.view(np.uint8).reshape(rows, nb, 2)
+    X = synth.normal((M, K), synth.stream(1300 + M, K))
+    Xq, dx = oracle.quantize_q8_0(X, M, K)
+    dx = dx.copy()
+    dx[2, 5] = np.nan
+    dx[7, 10] = np.inf
+    dx[M - 1, 0] = -np.inf
+    Y = run_gemm(W, Xq, dx, rows, K, M)
+    Y_ref, A = oracle.gemm_q8act(W, Xq, dx, rows, K, M)
+    folded = K % 256 == 0 and M > 112
+    n_nan, n_inf = assert_same_specials(Y.reshape(-1), Y_ref.reshape(-1), A.reshape(-1), what=f"{M}x{rows}x{K}",
+                                        exact=not folded)
+    assert n_nan > 0 and n_inf > 0
+    assert np.all(np.isnan(Y[2]))

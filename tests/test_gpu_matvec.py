@@ -13,7 +13,7 @@ import pytest
 import block_quantized_matvec_gq_gb300 as gq
 import oracle
 import synth
-from gpu_util import assert_within, dev, guarded, packed, torch
+from gpu_util import assert_same_specials, assert_within, dev, guarded, packed, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -212,3 +212,29 @@ def test_argument_errors_launch_nothing():
     assert e.value.status == gq.GQ_ERR_ALIGN
     t.cuda.synchronize()
     assert t.equal(y, t.full((4,), 3.0, dtype=t.float32, device="cuda"))
+
+
+@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K, oracle.FORMAT_Q6_K])
+@pytest.mark.parametrize("rows,K", [(300, 2048), (256, 21504)])  # register streams; short-wide split-K rings
+def test_non_finite_x_propagates_as_in_the_definition(fmt, rows, K):
+    """x holding +inf and -inf (rows get +-inf, or NaN where the two meet or
+    a weight is zero) and, separately, a NaN (every row NaN): the same
+    pattern of non-finite results as the fp64 definition, the bound on the
+    rest.  Q4_K forms each sub-block as d sc sum(q x) - dmin m sum(x), so an
+    infinity that meets a zero code or the min term can give NaN where the
+    per-weight definition gives an infinity: there the set of non-finite
+    rows is the definition's."""
+    W = synth.weights(fmt, rows, K, synth.stream(31, fmt))
+    x = synth.normal(K, synth.stream(31, 1))
+    xi = x.copy()
+    xi[3] = np.inf
+    xi[K - 40] = -np.inf
+    y = run_matvec(fmt, W, xi, rows, K)
+    y_ref, a_ref = oracle.matvec(fmt, W, xi, rows, K)
+    n_nan, n_inf = assert_same_specials(y, y_ref, a_ref, what=f"fmt{fmt} {rows}x{K} inf",
+                                        exact=fmt != oracle.FORMAT_Q4_K)
+    assert n_nan > 0 and n_inf > 0  # both kinds occur on these inputs
+    xn = x.copy()
+    xn[K // 2 + 1] = np.nan
+    y = run_matvec(fmt, W, xn, rows, K)
+    assert np.all(np.isnan(y))
