@@ -79,7 +79,7 @@ MatvecGeo choose_logits_geo(int rows, int nb)
 {
     (void)rows;
     (void)nb;
-    return MatvecGeo{8, 2, 4, 8};
+    return tuned("GQ_LOG", MatvecGeo{8, 2, 4, 8});
 }
 
 // Largest token batch that takes the register-operand contraction

@@ -51,9 +51,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
                        float *__restrict__ val, int rows, int nb)
 {
     extern __shared__ __align__(16) float xs[];
-    __shared__ unsigned long long cta_keys[kWarpsPerCta * GQ_MAX_TOPK];
+    __shared__ __align__(16) unsigned long long cta_keys[kWarpsPerCta * GQ_MAX_TOPK];
     __shared__ unsigned long long wmax[kWarpsPerCta];
     __shared__ int s_last;
+    __shared__ unsigned long long s_t2;
     // Candidates for a merge: every key >= the merge's threshold, gathered in
     // shared memory and sorted by one warp (the usual case: at most k keys
     // per list can reach the threshold, and only a few lists do).
@@ -162,12 +163,20 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
     if (!s_last) return;
     __threadfence();  // and the other CTAs' keys are visible here
 
-    // ---- the last CTA: merge all CTA lists (keys read through L2)
+    // ---- the last CTA: merge all CTA lists (keys read through L2; every list
+    // is sorted, largest first).  Two lower bounds on the final k-th key:
+    //   T1, the largest k-th key of any list (that list alone holds k keys
+    //       at or above it);
+    //   T2, the k-th largest list head (those k heads are k distinct keys at
+    //       or above it), usually far higher: with hundreds of similar lists
+    //       T1 lets a large fraction of all keys through.
+    // Only lists whose head reaches T = max(T1, T2) are read further.
     const int nlists = gridDim.x;
     unsigned long long t = 0ull;
     for (int c = threadIdx.x; c < nlists; c += kThreadsPerCta) {
         const unsigned long long v = __ldcg(keys + static_cast<size_t>(c) * k + (k - 1));
         t = v > t ? v : t;
+        if (nlists <= kWarpsPerCta * GQ_MAX_TOPK) cta_keys[c] = __ldcg(keys + static_cast<size_t>(c) * k);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -175,24 +184,63 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
         t = v > t ? v : t;
     }
     if (lane == 0) wmax[warp] = t;
-    if (threadIdx.x == 0) s_cnt = 0;
+    if (threadIdx.x == 0) {
+        s_cnt = 0;
+        s_t2 = 0ull;
+    }
     __syncthreads();
-    unsigned long long T = 0ull;
+    if (nlists <= kWarpsPerCta * GQ_MAX_TOPK && nlists >= k) {
+        // rank of each head among all heads, from pairs of heads in four
+        // independent counts (a zero pads an odd count: it is above no key);
+        // keys are unique apart from 0 (an empty entry), whose rank-(k-1)
+        // writers all write 0
+        if (threadIdx.x == 0 && (nlists & 1)) cta_keys[nlists] = 0ull;
+        __syncthreads();
+        const ulonglong2 *hp = reinterpret_cast<const ulonglong2 *>(cta_keys);
+        const int npairs = (nlists + 1) >> 1;
+        for (int c = threadIdx.x; c < nlists; c += kThreadsPerCta) {
+            const unsigned long long h = cta_keys[c];
+            int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+            int j = 0;
+            for (; j + 1 < npairs; j += 2) {
+                const ulonglong2 a = hp[j], b = hp[j + 1];
+                r0 += a.x > h ? 1 : 0;
+                r1 += a.y > h ? 1 : 0;
+                r2 += b.x > h ? 1 : 0;
+                r3 += b.y > h ? 1 : 0;
+            }
+            if (j < npairs) {
+                const ulonglong2 a = hp[j];
+                r0 += a.x > h ? 1 : 0;
+                r1 += a.y > h ? 1 : 0;
+            }
+            if (r0 + r1 + r2 + r3 == k - 1) s_t2 = h;
+        }
+        __syncthreads();
+    }
+    unsigned long long T = s_t2;
 #pragma unroll
     for (int w = 0; w < kWarpsPerCta; ++w) T = wmax[w] > T ? wmax[w] : T;
     const unsigned long long floor_thr = T > 0ull ? T - 1ull : 0ull;  // admit keys >= T
     const int nkeys = nlists * k;
-    // gather the candidates (keys >= T), four loads per lane in flight
+    // gather the candidates (keys >= T) from the lists whose head reaches T,
+    // eight keys of a list per batch of loads
     constexpr int kBatch = 4;
-    for (int base = threadIdx.x; base < nkeys; base += kBatch * kThreadsPerCta) {
-        unsigned long long kk[kBatch];
+    for (int c = threadIdx.x; c < nlists; c += kThreadsPerCta) {
+        const unsigned long long *lst = keys + static_cast<size_t>(c) * k;
+        if (__ldcg(lst) < T) continue;
+        for (int j0 = 0; j0 < k; j0 += 8) {
+            unsigned long long kk[8];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int j = base + u * kThreadsPerCta;
-            kk[u] = (j < nkeys) ? __ldcg(keys + j) : 0ull;
+            for (int u = 0; u < 8; ++u) kk[u] = (j0 + u < k) ? __ldcg(lst + j0 + u) : 0ull;
+            bool more = true;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                gather_candidate(kk[u], T);
+                more = more && kk[u] >= T;
+            }
+            if (!more) break;
         }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) gather_candidate(kk[u], T);
     }
     __syncthreads();
     unsigned long long e[4];
