@@ -12,10 +12,11 @@
 // (a counter at the start of the workspace, incremented with wrap-around so
 // it is back at zero after every call) merges all CTA lists: every key that
 // can still be in the final top k is at least the largest k-th key of any
-// CTA list (that list alone holds k keys above it), so keys below that
-// threshold are skipped before the remaining candidates are merged.  (A
-// separate one-CTA merge kernel cost 14.7 us per call at 262144 x 5376,
-// against 234 us for the whole stream.)
+// CTA list (that list alone holds k keys above it) and at least the k-th
+// largest list head (the k best heads are k keys above it), so only the
+// lists whose head reaches the larger of the two bounds are read, and only
+// their keys above it are merged.  (A separate one-CTA merge kernel cost
+// 14.7 us per call at 262144 x 5376, against 234 us for the whole stream.)
 #include "gq_host.h"
 #include "gq_matvec.cuh"
 
