@@ -321,3 +321,19 @@ def test_gemm_non_finite_scales(M, rows, K):
                                         exact=not folded)
     assert n_nan > 0 and n_inf > 0
     assert np.all(np.isnan(Y[2]))
+
+
+# The single-CTA tensor-memory tiles (K % 256 == 0, 112 < M <= 128): ragged
+# rows, one 8-block chunk, the full row width; and both sides of the 112-token
+# boundary with the register-operand kernel.
+@pytest.mark.parametrize("M,rows,K", [(113, 1000, 512), (120, 300, 5376), (128, 97, 256), (112, 33, 768),
+                                      (113, 33, 768)])
+def test_gemm_single_cta_tiles_and_the_register_boundary(M, rows, K):
+    W = synth.q4_0_weights(rows, K, synth.stream(1400 + M, rows))
+    X = synth.normal((M, K), synth.stream(1400 + M, K))
+    Xq, dx = oracle.quantize_q8_0(X, M, K)
+    Y = run_gemm(W, Xq, dx, rows, K, M)
+    assert gq.gq_device_status() == gq.GQ_OK
+    Y_ref, A = oracle.gemm_q8act(W, Xq, dx, rows, K, M)
+    err = np.abs(Y.astype(np.float64) - Y_ref)
+    assert np.all(err <= 1e-5 * A), float(np.max(err / np.maximum(A, 1e-300)))
