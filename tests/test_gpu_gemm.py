@@ -224,9 +224,11 @@ def test_gemm_extreme_block_dots_exact():
     assert np.all(got[1, :, 0] == -32 * 7 * 127) and np.all(got[1, :, 1] == 32 * 8 * 127)
 
 
-@pytest.mark.parametrize("M,rows,K", [(8, 2000, 5376), (100, 2000, 5376), (512, 3000, 5376)])  # small; one CTA; pairs
+# register operands (one pass; four passes); single-CTA tensor-memory tiles; CTA pairs
+@pytest.mark.parametrize("M,rows,K", [(8, 2000, 5376), (100, 2000, 5376), (120, 2000, 5376), (512, 3000, 5376)])
 def test_gemm_repeat_runs_bitwise_identical(M, rows, K):
-    """The chunk read-out adds in a fixed order: the same inputs give the same bits."""
+    """Partial sums are added in a fixed order on every path (K quarters,
+    chunk read-outs): the same inputs give the same bits."""
     t = torch()
     W = synth.q4_0_weights(rows, K, synth.stream(900 + M, 0))
     X = synth.normal((M, K), synth.stream(900 + M, 1))
