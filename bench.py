@@ -245,8 +245,12 @@ class LogitsTopK(Workload):
         self.x = _to_dev(torch, x)
         self.wsb = gq.gq_logits_topk_workspace_bytes(self.rows, self.K, self.k)
         self.ws = torch.zeros(self.wsb, dtype=torch.uint8, device="cuda")  # zero-filled once before first use
-        self.idx = torch.empty(self.k, dtype=torch.int32, device="cuda")
-        self.val = torch.empty(self.k, dtype=torch.float32, device="cuda")
+        # idx and val in one device buffer (16-byte aligned halves), so the
+        # end-to-end step reads the result back with one copy
+        self.kpad = -(-self.k // 4) * 4
+        self.out = torch.empty(2 * self.kpad * 4, dtype=torch.uint8, device="cuda")
+        self.idx = self.out[:self.k * 4].view(torch.int32)
+        self.val = self.out[self.kpad * 4:self.kpad * 4 + self.k * 4].view(torch.float32)
         self.gq = gq
         self.bytes_per_step = gq.gq_packed_bytes(1, self.rows, self.K) + 4 * self.K + 8 * self.k
         self.weight_bytes = gq.gq_packed_bytes(1, self.rows, self.K)
@@ -259,15 +263,13 @@ class LogitsTopK(Workload):
 
     def e2e_setup(self, torch):
         self.xh = torch.from_numpy(self.x_host.copy()).pin_memory()
-        self.idx_h = torch.empty(self.k, dtype=torch.int32).pin_memory()
-        self.val_h = torch.empty(self.k, dtype=torch.float32).pin_memory()
-        self.h2d, self.d2h = self.xh.numel() * 4, self.k * 8
+        self.out_h = torch.empty(self.out.numel(), dtype=torch.uint8).pin_memory()
+        self.h2d, self.d2h = self.xh.numel() * 4, self.out.numel()
 
     def e2e_step(self, torch):
         self.x.copy_(self.xh, non_blocking=True)
         self.step(0)
-        self.idx_h.copy_(self.idx, non_blocking=True)
-        self.val_h.copy_(self.val, non_blocking=True)
+        self.out_h.copy_(self.out, non_blocking=True)  # idx and val
         torch.cuda.current_stream().synchronize()
 
     def cpu_reference(self, oracle, rows_sample):
