@@ -109,7 +109,7 @@ int gq_q4_0_matvec(const void *W, const float *x, float *y, int rows, int K, int
     int st = check_matvec(GQ_FORMAT_Q4_0, W, x, y, rows, K, M);
     if (st != GQ_OK) return st;
     // rows of whole 8-block groups stream through the shared-memory ring; other K take the register path
-    if (ring_preferred(rows) && ring_q4_0_supported(K / 32)) {
+    if (ring_preferred(rows, K / 32) && ring_q4_0_supported(K / 32)) {
         st = launch_ring_q4_0(W, x, nullptr, nullptr, y, rows, K, reinterpret_cast<cudaStream_t>(stream));
         if (st != GQ_ERR_SHAPE) return st;
     }
@@ -130,7 +130,7 @@ int gq_q4k_matvec(const void *W, const float *x, float *y, int rows, int K, int 
 {
     int st = check_matvec(GQ_FORMAT_Q4_K, W, x, y, rows, K, M);
     if (st != GQ_OK) return st;
-    if (ring_preferred(rows)) {
+    if (ring_preferred(rows, K / 32)) {
         st = launch_ring_q4k(W, x, y, rows, K, reinterpret_cast<cudaStream_t>(stream));
         if (st != GQ_ERR_SHAPE) return st;
     }
@@ -152,7 +152,7 @@ int gq_ffn_gate_up_gelu(const void *W_gate, const void *W_up, const float *x, fl
     if (!aligned16(W_up)) return GQ_ERR_ALIGN;
     int st = check_matvec(GQ_FORMAT_Q4_0, W_gate, x, h, rows, K, M);
     if (st != GQ_OK) return st;
-    if (ring_preferred(rows) && ring_q4_0_supported(K / 32)) {
+    if (ring_preferred(rows, K / 32) && ring_q4_0_supported(K / 32)) {
         st = launch_ring_ffn(W_gate, W_up, x, h, rows, K, reinterpret_cast<cudaStream_t>(stream));
         if (st != GQ_ERR_SHAPE) return st;
     }
@@ -167,7 +167,7 @@ int gq_q4_0_geglu_down(const void *W_down, const float *g, const float *u, float
     int st = check_matvec(GQ_FORMAT_Q4_0, W_down, g, y, rows, K, M);
     if (st != GQ_OK) return st;
     if (!aligned16(u)) return GQ_ERR_ALIGN;
-    if (ring_preferred(rows) && ring_q4_0_supported(K / 32)) {
+    if (ring_preferred(rows, K / 32) && ring_q4_0_supported(K / 32)) {
         st = launch_ring_q4_0(W_down, nullptr, g, u, y, rows, K, reinterpret_cast<cudaStream_t>(stream));
         if (st != GQ_ERR_SHAPE) return st;
     }

@@ -44,27 +44,37 @@ static int ring_override() { return -1; }
 bool gemm_force_block_path() { return false; }
 #endif
 
-// Short, wide matrices (fewer than four rows per SM) take the shared-memory
-// ring with a cluster split-K: the register streams would leave most SMs
-// idle (measured on Q4_0: 256 x 21504 in 5.1 instead of 13.6 us, 8 x 49152 in
-// 3.8 instead of 17.9 us).  Larger matrices keep the register streams, which
-// were as fast or faster at every shape measured.
-// Register-stream schedule from tasks per resident warp: < 1.75 balanced
-// (mode 1), <= 1.25 balanced with the first loads issued early (mode 2),
-// else round-robin (mode 0).
-int schedule_mode(long long ntasks, long long warps)
+// Short, wide matrices (fewer than four rows per SM) of rows longer than 128
+// blocks take the shared-memory ring with a cluster split-K: the register
+// streams would leave most SMs idle (measured on Q4_0: 256 x 21504 in 5.1
+// instead of 13.6 us, 8 x 49152 in 3.8 instead of 17.9 us; 64 to 512 rows of
+// 5376 in 4.0-4.3 instead of 4.9-5.0 us).  At 4096 (128 blocks) the streams
+// are faster (64 to 512 rows: 2.3 against 4.0-4.1 us), and larger matrices
+// keep them too.
+// Register-stream schedule from tasks per resident warp: <= 1.25 balanced
+// with the first loads issued early (mode 2); < 1.75 balanced (mode 1) on
+// rows of at least 512 blocks, whose leftover rows split along K into eight
+// slices that still fill the lanes; else round-robin (mode 0).  Measured on
+// Q4_0 between 1.25 and 1.75 tasks per warp: at K = 21504 balanced 25.5 /
+// 27.6 / 31.1 us against 27.8 / 30.6 / 30.6 round-robin (6400 / 7296 / 8192
+// rows); at K = 5376 round-robin 14.9 / 15.3 / 15.7 against 14.8 / 16.5 /
+// 19.4 (12800 / 14592 / 16384 rows); at K = 4096 round-robin 6.5 / 6.8 / 6.9
+// against 7.9 / 9.5 / 11.8 (6144 / 7168 / 8192 rows).
+int schedule_mode(long long ntasks, long long warps, int nb)
 {
 #ifdef GQ_TUNING
     if (const char *v = getenv("GQ_MODE")) return atoi(v);
 #endif
-    return ntasks * 4 <= warps * 5 ? 2 : (ntasks * 4 < warps * 7 ? 1 : 0);
+    if (ntasks * 4 <= warps * 5) return 2;
+    if (ntasks * 4 < warps * 7) return nb >= 512 ? 1 : 0;
+    return 0;
 }
 
-bool ring_preferred(int rows)
+bool ring_preferred(int rows, int nb)
 {
     const int o = ring_override();
     if (o >= 0) return o != 0;
-    return rows < 4 * sm_count();
+    return rows < 4 * sm_count() && nb > 128;
 }
 
 MatvecGeo choose_matvec_geo(int format, int rows, int nb, bool pair_ok)

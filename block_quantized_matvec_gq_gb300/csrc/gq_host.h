@@ -156,8 +156,8 @@ int launch_gemm_q8act_tc(const void *W, const int8_t *Xq, const float *dx, float
 int launch_block_dots_tc(const void *W, const int8_t *Xq, int32_t *D, void *ws, size_t ws_bytes, int rows, int K,
                          int M, cudaStream_t s);
 // ring-streamed 4-bit matvecs (gq_stream.cu)
-bool ring_preferred(int rows);
-int schedule_mode(long long ntasks, long long warps);
+bool ring_preferred(int rows, int nb);
+int schedule_mode(long long ntasks, long long warps, int nb);
 bool gemm_force_block_path();
 bool ring_q4_0_supported(int nb);
 int launch_ring_q4_0(const void *W, const float *x, const float *g_or_null, const float *u, float *y, int rows,

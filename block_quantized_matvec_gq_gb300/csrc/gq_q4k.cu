@@ -158,7 +158,7 @@ int launch_q4k_matvec(const void *W, const float *x, float *y, int rows, int K, 
         if (grid <= 0) return GQ_ERR_SHAPE;                                                             \
         /* tasks per warp: < 1.75 balanced schedule, <= 1.25 also first loads early */                 \
         const long long w5 = static_cast<long long>(grid) * kWarpsPerCta;                               \
-        const int mode = schedule_mode(ntasks, w5);                                                     \
+        const int mode = schedule_mode(ntasks, w5, nsb);                                                     \
         auto kern = mode == 2 ? k_q4k_matvec<LG, R, U, 2> : (mode == 1 ? k_q4k_matvec<LG, R, U, 1> : rr);                 \
         if (mode != 0) { /* size through the launched instantiation too (raises its shared-memory limit) */ \
             const int g2 = persistent_grid(reinterpret_cast<const void *>(kern), kThreadsPerCta, smem, ntasks); \

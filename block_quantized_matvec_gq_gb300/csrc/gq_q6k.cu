@@ -321,7 +321,7 @@ int launch_q6k_matvec(const void *W, const float *x, float *y, int rows, int K, 
         int grid = persistent_grid(reinterpret_cast<const void *>(rr), kThreadsPerCta, smem, ntasks);        \
         if (grid <= 0) return GQ_ERR_SHAPE;                                                                   \
         const long long w5 = static_cast<long long>(grid) * kWarpsPerCta;                                     \
-        const int mode = schedule_mode(ntasks, w5);                                                           \
+        const int mode = schedule_mode(ntasks, w5, nsb);                                                           \
         auto kern = mode == 2 ? q6::k_q6k_matvec<LG, R, U, 2> : (mode == 1 ? q6::k_q6k_matvec<LG, R, U, 1> : rr); \
         if (mode != 0) { /* size through the launched instantiation too (raises its shared-memory limit) */  \
             const int g2 = persistent_grid(reinterpret_cast<const void *>(kern), kThreadsPerCta, smem, ntasks); \

@@ -238,3 +238,27 @@ def test_non_finite_x_propagates_as_in_the_definition(fmt, rows, K):
     xn[K // 2 + 1] = np.nan
     y = run_matvec(fmt, W, xn, rows, K)
     assert np.all(np.isnan(y))
+
+
+@pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q4_K, oracle.FORMAT_Q6_K])
+@pytest.mark.parametrize("rows,K", [(7296, 16384), (7168, 4096)])
+def test_matvec_between_one_and_two_tasks_per_warp(fmt, rows, K):
+    """Shapes with 1.25 to 1.75 row tasks per resident warp (on 152 SMs): long
+    rows take the balanced schedule (leftover rows split along K across a
+    CTA's warps, partial sums added in warp order), short rows round-robin.
+    Sampled rows against the oracle, and repeat runs bitwise identical."""
+    W = synth.weights(fmt, rows, K, synth.stream(60, fmt))
+    x = synth.normal(K, synth.stream(60, 1))
+    t = torch()
+    Wp = packed(fmt, W, rows, K)
+    xd = dev(x)
+    ys = []
+    for _ in range(2):
+        y = t.empty(rows, dtype=t.float32, device="cuda")
+        FMT_FN[fmt](Wp, xd, y, rows, K)
+        ys.append(y)
+    t.cuda.synchronize()
+    assert t.equal(ys[0], ys[1])
+    sel = np.concatenate([[0, 1, rows - 2, rows - 1], np.random.default_rng(fmt).choice(rows, 600, replace=False)])
+    y_ref, a_ref = oracle.matvec(fmt, W, x, rows, K, row_idx=sel)
+    assert_within(ys[0].cpu().numpy()[sel], y_ref, a_ref, what=f"fmt{fmt} {rows}x{K}")
