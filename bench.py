@@ -25,6 +25,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -708,6 +709,23 @@ def run_gpu(wl_cls, args, rank, world, torch, dist):
 
     ms = max_over_ranks(ms, dist, "cuda")
 
+    # Per-call spread: five more replays of the same K steps, each timed alone,
+    # with the timed run's own figure (rank 0; no collective in between).
+    per_call = None
+    if graph is not None and rank == 0:
+        vals = [ms * 1000.0 / args.steps]
+        for _ in range(5):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            vals.append(a.elapsed_time(b) * 1000.0 / args.steps)
+        per_call = {"samples": len(vals), "steps_per_sample": args.steps,
+                    "median_us": round(statistics.median(vals), 3), "min_us": round(min(vals), 3)}
+
     # End to end through the public API with host buffers (every workload).
     # Each step copies its inputs from pinned host memory, makes the API call
     # on the weight copy the device timing would use, copies the outputs back
@@ -758,7 +776,7 @@ def run_gpu(wl_cls, args, rank, world, torch, dist):
         e2e = {"value": round(ev, 3), "unit": eu,
                "h2d_bytes_per_step": wl.h2d, "d2h_bytes_per_step": wl.d2h,
                "ms_per_step": round(e2e_ms, 4), "launch": "graph" if graphs is not None else "eager"}
-    return wl, ms, clocks, e2e
+    return wl, ms, clocks, e2e, per_call
 
 
 def max_over_ranks(ms, dist, device):
@@ -784,11 +802,41 @@ def cpu_baseline(wl_cls, sample_rows):
     if not hasattr(wl, "cpu_reference"):
         return None
     run, amount, desc = wl.cpu_reference(oracle, sample_rows)
+    cores = oracle.threads()
     t = time.perf_counter()
     run()
     dt = time.perf_counter() - t
-    return {"value": round(amount / dt / wl.cpu_scale, 4), "unit": wl.cpu_unit, "cores": oracle.threads(),
-            "kind": "oracle", "sample": desc, "seconds": round(dt, 3)}
+    out = {"value": round(amount / dt / wl.cpu_scale, 4), "unit": wl.cpu_unit, "cores": cores,
+           "kind": "oracle", "sample": desc, "seconds": round(dt, 3), "cpu_model": cpu_model()}
+    if cores > 1:
+        # the same sample on one core (the row loops are the only parallel part)
+        oracle.set_threads(1)
+        try:
+            t = time.perf_counter()
+            run()
+            d1 = time.perf_counter() - t
+        finally:
+            oracle.set_threads(cores)
+        out["single_core"] = {"value": round(amount / d1 / wl.cpu_scale, 4), "seconds": round(d1, 3)}
+    return out
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform)."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine() or "unknown"
 
 
 def main():
@@ -827,7 +875,7 @@ def main():
         LogitsTopK.rows = args.rows
         LogitsTopK.name = f"q8_0_logits_topk_{args.rows}x5376"
     for name in names:
-        wl, ms, clocks, e2e = run_gpu(WORKLOADS[name], args, rank, world, torch, dist)
+        wl, ms, clocks, e2e, per_call = run_gpu(WORKLOADS[name], args, rank, world, torch, dist)
         if rank != 0:
             continue
         ms_step = ms / args.steps
@@ -857,7 +905,7 @@ def main():
             "config": {"workload": wl.name, "bytes_per_step": wl.bytes_per_step,
                        "weight_bytes": wl.weight_bytes, "working_set_bytes": wl.working_set,
                        "l2": wl.l2_policy, "parallelism": f"replicas x{world}"},
-            "roofline": roof, "clocks": clocks, "e2e": e2e,
+            "roofline": roof, "clocks": clocks, "per_call_us": per_call, "e2e": e2e,
             "gpu_launches": wl.launches_per_step * args.steps,
         }
         if not args.no_cpu_baseline and world == 1 and hasattr(wl, "cpu_reference"):

@@ -89,6 +89,8 @@ def lib():
         L.gqo_block_dots.restype = ctypes.c_int
         L.gqo_gemm_q8act.argtypes = [P, P, P, I64, I64, I64, P, I64, P, I64, P, P]
         L.gqo_gemm_q8act.restype = ctypes.c_int
+        L.gqo_set_threads.argtypes = [ctypes.c_int]
+        L.gqo_set_threads.restype = None
         _lib = L
     return _lib
 
@@ -255,6 +257,11 @@ def gemm_q8act(W, Xq, dx, rows: int, K: int, M: int, tok_idx=None, row_idx=None)
     if rc != 0:
         raise ValueError("oracle gemm rejected the shape")
     return Y, A
+
+
+def set_threads(n: int) -> None:
+    """Threads for the oracle's row-parallel loops from now on (n >= 1)."""
+    lib().gqo_set_threads(int(n))
 
 
 def threads() -> int:

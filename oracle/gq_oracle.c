@@ -466,3 +466,19 @@ int gqo_gemm_q8act(const uint8_t *W, const int8_t *Xq, const float *dx, int64_t 
     }
     return 0;
 }
+
+/* Threads of the row-parallel loops above (OpenMP builds; a no-op otherwise):
+ * lets a caller time the oracle on one core and on all of them in one process.
+ * Test and measurement infrastructure only; no arithmetic depends on it. */
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+void gqo_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
