@@ -68,3 +68,19 @@ def test_reference_arm_runs_for_every_workload(capsys):
         assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     bench.run_reference(argparse.Namespace(config=bench.DEFAULT_WORKLOAD, steps=1, warmup=1), rank=1)
     assert capsys.readouterr().out == ""   # ranks other than 0 print nothing
+
+
+def test_cpu_baseline_reports_one_core_and_the_model():
+    """The oracle baseline of a bench line: the sample on all host cores, the
+    same sample on one core (whenever the oracle has more than one thread),
+    and the CPU model; the thread count is restored afterwards."""
+    import oracle
+    cores = oracle.threads()
+    b = bench.cpu_baseline(bench.WORKLOADS["q4_0_matvec_4096x4096"], 512)
+    assert b["kind"] == "oracle" and b["cores"] == cores and b["value"] > 0
+    assert isinstance(b["cpu_model"], str) and b["cpu_model"]
+    if cores > 1:
+        assert b["single_core"]["value"] > 0 and b["single_core"]["seconds"] > 0
+    else:
+        assert "single_core" not in b
+    assert oracle.threads() == cores
