@@ -113,15 +113,20 @@ __global__ void __launch_bounds__(kThreadsPerCta, 2)
         }
         float out[R];
         q8_0_stream<LG, R, U>(wp, sp, xs, nb, lp, out);
+        // lane lp < R of a group keeps row r0 + lp: one soft-cap per lane and
+        // one offer per task cover all of the task's rows
+        static_assert(R <= LG, "a group needs a lane per row");
+        float l = 0.f;
 #pragma unroll
         for (int i = 0; i < R; ++i) {
-            float l = group_sum<LG>(out[i]);
-            const int r = r0 + i;
-            if (cap) l = softcap * tanhf(__fdiv_rn(l, softcap));
-            if (lp == 0 && r < rows && logits != nullptr) logits[r] = l;
-            const unsigned long long key = (lp == 0 && r < rows) ? topk_key(l, static_cast<uint32_t>(r)) : 0ull;
-            offer(top, thr, 0ull, key, k);
+            const float v = group_sum<LG>(out[i]);
+            if (lp == i) l = v;
         }
+        const int r = r0 + lp;
+        const bool mine = lp < R && r < rows;
+        if (cap) l = softcap * tanhf(__fdiv_rn(l, softcap));
+        if (mine && logits != nullptr) logits[r] = l;
+        offer(top, thr, 0ull, mine ? topk_key(l, static_cast<uint32_t>(r)) : 0ull, k);
     }
 
     // merge the warps' lists (lane j holds entry j in e0 and entry j+32 in e1)
