@@ -77,12 +77,28 @@ bool ring_preferred(int rows, int nb)
     return rows < 4 * sm_count() && nb > 128;
 }
 
+// 4-bit streams: 32 lanes per row group (2-row tasks) when the row length is
+// a multiple of 32 blocks, else 16 (4-row tasks).  Q4_0 rows shorter than 512
+// blocks that would leave 32-lane tasks at 1.25 to 1.75 per resident warp
+// take 16 lanes instead: half as many tasks fit one balanced round, where
+// the 32-lane tasks would run round-robin with a sparse second round.
+// Measured on Q4_0 (us per step, 32 lanes against 16): K = 4096, 6144 rows
+// 6.55 / 5.85, 8192 rows 6.89 / 6.08; K = 8192, 8192 rows 11.6 / 11.2;
+// K = 14336, 8192 rows 20.4 / 19.8.  Outside that band 32 lanes win (4096 x
+// 4096 3.77 / 4.36, 12288 x 4096 9.34 / 10.9, 4096 x 8192 6.31 / 7.94,
+// 7296 x 21504 27.5 / 30.1).
 MatvecGeo choose_matvec_geo(int format, int rows, int nb, bool pair_ok)
 {
-    (void)rows;
     (void)pair_ok;
     if (format == GQ_FORMAT_Q8_0) return tuned("GQ_Q8", MatvecGeo{16, 2, 4, 8});
-    return tuned("GQ_Q4", MatvecGeo{(nb % 32 == 0) ? 32 : 16, 2, 4, 8});
+    int lg = (nb % 32 == 0) ? 32 : 16;
+    if (lg == 32 && format == GQ_FORMAT_Q4_0 && nb < 512) {
+        const long long tasks = (static_cast<long long>(rows) + 1) / 2;
+        // resident warps: two CTAs of 256 threads per SM
+        const long long warps = static_cast<long long>(sm_count()) * 16;
+        if (tasks * 4 > warps * 5 && tasks * 4 <= warps * 7) lg = 16;
+    }
+    return tuned("GQ_Q4", MatvecGeo{lg, 2, 4, 8});
 }
 
 MatvecGeo choose_logits_geo(int rows, int nb)
