@@ -54,7 +54,9 @@ bool gemm_force_block_path() { return false; }
 // against 10.5 / 10.5 / 10.6 us, of 8192 in 3.9 / 4.0 / 4.1 against 4.0 / 4.0
 // / 4.2 us.  At 1536 rows the streams are level or ahead (5376: 5.2 against
 // 5.5 us).  At 4096 (128 blocks) the streams are faster at every row count
-// (64 to 512 rows: 2.3 against 4.0-4.1 us; 1024: 2.4 against 3.5).
+// (64 to 512 rows: 2.3 against 4.0-4.1 us; 1024: 2.4 against 3.5).  Q4_K
+// at 608 / 1024 / 1215 rows: 3.9 / 4.1 / 4.3 against 6.2 / 6.3 / 12.0 us
+// (K = 5376), 6.4 / 8.8 / 9.0 against 13.6 / 14.0 / 18.0 us (K = 21504).
 // Register-stream schedule from tasks per resident warp: <= 1.25 balanced
 // with the first loads issued early (mode 2); < 1.75 balanced (mode 1) on
 // rows of at least 512 blocks, whose leftover rows split along K into eight
