@@ -211,6 +211,11 @@ class Workload:
     def e2e_outputs(self):
         return []
 
+    def e2e_targets(self, i):
+        """The device tensors step i reads its host inputs into (the
+        e2e_inputs, unless the step rotates its input copies)."""
+        return self.e2e_inputs()
+
     def e2e_setup(self, torch):
         self._e2e_in = [(d, d.cpu().pin_memory()) for d in self.e2e_inputs()]
         self._e2e_out = [(d, torch.empty(d.shape, dtype=d.dtype).pin_memory()) for d in self.e2e_outputs()]
@@ -220,7 +225,7 @@ class Workload:
     def e2e_body(self, torch, i):
         """Step i end to end, without the final wait: the inputs' copy from
         pinned host memory, the API call, the outputs' copy back."""
-        for d, h in self._e2e_in:
+        for d, (_, h) in zip(self.e2e_targets(i), self._e2e_in):
             d.copy_(h, non_blocking=True)
         self.step(i)
         for d, h in self._e2e_out:
@@ -489,7 +494,10 @@ class RMSNormQ8(Rotating):
                                          self.K, self.M)
 
     def e2e_inputs(self):
-        return [self.copies[0]]   # step(0) reads copy 0
+        return [self.copies[0]]
+
+    def e2e_targets(self, i):
+        return [self.copies[i % len(self.copies)]]   # the copy step(i) reads
 
     def e2e_outputs(self):
         return [self.Xq, self.dx]
@@ -504,6 +512,51 @@ class RMSNormQ8(Rotating):
             oracle.rmsnorm_quantize_q8_0(Xs, w, 1.0, 1e-6, n, self.K)
         amount = n * (4 * self.K + self.K + 4 * (self.K // 32)) + 4 * self.K
         return run, amount, f"{n} of {self.M} tokens (exact sum of squares by math.fsum, f32 scaling, Q8_0)"
+
+
+class Q8Quantize(Rotating):
+    """The prefill activations (512 tokens x 5376, ~N(0,1)) quantized to
+    Q8_0, the contraction's prologue: X is read, Xq and dx are written."""
+    name = "q8_0_quantize_512x5376"
+    kernel = "k_quantize_q8_0"
+    M, K = 512, 5376
+    rows = M   # the rows of X
+
+    def setup(self, torch, gq):
+        X = synth.normal((self.M, self.K), synth.stream(9, 0))
+        xbytes = 4 * self.M * self.K
+        R = self._rotate(torch, xbytes)
+        X0 = _to_dev(torch, X)
+        self.copies = [X0] + [X0.clone() for _ in range(R - 1)]
+        self.Xq = torch.empty((self.M, self.K), dtype=torch.int8, device="cuda")
+        self.dx = torch.empty((self.M, self.K // 32), dtype=torch.float32, device="cuda")
+        self.gq = gq
+        self.bytes_per_step = xbytes + self.M * self.K + 4 * self.M * (self.K // 32)
+        self.weight_bytes = xbytes
+        self.working_set = xbytes * R
+        self.l2_policy = f"{R} rotating activation copies ({xbytes * R / 2**20:.0f} MiB > 4x L2)"
+
+    def step(self, i):
+        self.gq.gq_quantize_q8_0(self.copies[i % len(self.copies)], self.Xq, self.dx, self.K, self.M)
+
+    def e2e_inputs(self):
+        return [self.copies[0]]
+
+    def e2e_targets(self, i):
+        return [self.copies[i % len(self.copies)]]   # the copy step(i) reads
+
+    def e2e_outputs(self):
+        return [self.Xq, self.dx]
+
+    def cpu_reference(self, oracle, rows_sample):
+        X = synth.normal((self.M, self.K), synth.stream(9, 0))
+        n = min(rows_sample, self.M)
+        Xs = np.ascontiguousarray(X[:n])
+
+        def run():
+            oracle.quantize_q8_0(Xs, n, self.K)
+        amount = n * (4 * self.K + self.K + 4 * (self.K // 32))
+        return run, amount, f"{n} of {self.M} tokens (f32 division and rounding, Q8_0)"
 
 
 class FFN(Rotating):
@@ -638,7 +691,7 @@ class GemmSmallBatch32(GemmSmallBatch8):
 
 
 WORKLOADS = {w.name: w for w in (LogitsTopK, Q40Matvec, Q40MatvecShortWide, Q4KMatvec, Q6KMatvec, FFN, GegluDown,
-                                  RMSNormQ8, Gemm, GemmSmallBatch8, GemmSmallBatch32)}
+                                  RMSNormQ8, Q8Quantize, Gemm, GemmSmallBatch8, GemmSmallBatch32)}
 
 
 # ---------------------------------------------------------------- timing
