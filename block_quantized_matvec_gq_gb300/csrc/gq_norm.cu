@@ -40,6 +40,7 @@
 // ss = N 2^-298.
 #include "gq_host.h"
 #include "gq_internal.cuh"
+#include "gq_q8code.cuh"
 
 namespace gq {
 namespace norm {
@@ -460,12 +461,6 @@ __device__ double row_sum_squares_regs(const float4 (&v)[kRegChunks], const floa
 // Q8_0 of the normalized chunk x4 (one of the eight chunks of its 32-block,
 // the eight lanes of a block being adjacent): the packed codes and, from
 // every lane, the block's d.  All lanes of the warp take part (shuffles).
-// clamp(roundf(e / d), +-127) with the division itself (out of line: rare).
-__device__ __noinline__ int exact_code(float e, float d)
-{
-    return static_cast<int>(fminf(fmaxf(roundf(__fdiv_rn(e, d)), -127.0f), 127.0f));
-}
-
 __device__ __forceinline__ uint32_t quant_chunk(float4 x4, float4 w4, float inv, float offset, bool active,
                                                 float &d)
 {
@@ -480,31 +475,7 @@ __device__ __forceinline__ uint32_t quant_chunk(float4 x4, float4 w4, float inv,
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     d = __fdiv_rn(amax, 127.0f);
-    uint32_t packed = 0;
-    if (d != 0.0f) {
-        // round(e / d) with e / d correctly rounded, via y = e * RN(1/d):
-        // |y - e/d| <= 2^-16 and |RN(e/d) - e/d| <= 2^-17 for |e/d| <= 127
-        // (relative errors 2^-24 each), so y and RN(e/d) round to the same
-        // integer unless y is within 2^-15 of a half-integer (or 1/d
-        // overflowed); those take the division itself.
-        // Away from half-integers, y + copysign(0.5, y) is at least 2^-15
-        // from an integer and rounds by at most 2^-18, so truncating it is
-        // roundf(y).
-        const float r = __frcp_rn(d);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float y = __fmul_rn(e[i], r);
-            const float a = fabsf(y);
-            int q;
-            if (!(a <= 128.0f) || fabsf(a - floorf(a) - 0.5f) <= 0x1p-15f)
-                q = exact_code(e[i], d);
-            else
-                q = __float2int_rz(__fadd_rn(y, copysignf(0.5f, y)));
-            q = min(max(q, -127), 127);
-            packed |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * i);
-        }
-    }
-    return packed;
+    return q8_pack4(e, d);
 }
 
 // inv = f32(1 / sqrt(ss / K + eps)) in double, each operation rounded to

@@ -9,11 +9,13 @@
 // with IEEE-rounded f32 division; d = 0 gives q = 0.
 #include "gq_host.h"
 #include "gq_internal.cuh"
+#include "gq_q8code.cuh"
 
 namespace gq {
 
 // Eight lanes per 32-block, four consecutive elements per lane (16-byte
-// loads, 4-byte code stores); the per-element arithmetic is the definition's.
+// loads, 4-byte code stores); the codes follow q8_pack4 (one reciprocal per
+// block, full-rate arithmetic, the division itself next to a half-integer).
 __global__ void __launch_bounds__(256)
     k_quantize_q8_0(const float4 *__restrict__ X, uint32_t *__restrict__ Xq, float *__restrict__ dx,
                     long long nblocks)
@@ -34,15 +36,8 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         const float d = __fdiv_rn(amax, 127.0f);
-        uint32_t packed = 0;
-        if (d != 0.0f) {
-            const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float r = fminf(fmaxf(roundf(__fdiv_rn(e[i], d)), -127.0f), 127.0f);
-                packed |= (static_cast<uint32_t>(static_cast<int>(r)) & 0xFFu) << (8 * i);
-            }
-        }
+        const float e[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t packed = q8_pack4(e, d);
         if (active) {
             Xq[blk * 8 + sub] = packed;
             if (sub == 0) dx[blk] = d;
