@@ -45,6 +45,38 @@ def test_quantize_bit_exact(M, K):
     assert np.array_equal(Xq.cpu().numpy(), q_ref)
 
 
+def test_quantize_half_integer_window_and_extreme_scales():
+    """Blocks built so that x/d lands on half-integers (d = 1 exactly, and an
+    inexact d = RN(100/127)), within 2^-16 of them on both sides, at the
+    clamp, and at extreme scales (a largest value near FLT_MAX, and one so
+    small that 1/d overflows): every code takes the reciprocal form or the
+    division the rule keeps for such quotients, and all must equal the
+    oracle's division and roundf bit for bit."""
+    K, M = 256, 2
+    X = np.zeros((M, K), dtype=np.float32)
+    k = np.arange(-15, 16, dtype=np.float32)            # 31 half-integers k + 0.5 (|q| <= 15.5)
+    X[0, 0] = 127.0                                     # d = 1
+    X[0, 1:32] = k + 0.5
+    X[0, 32] = 127.0
+    X[0, 33:64] = k + np.float32(0.5) + np.float32(2.0 ** -16)
+    X[0, 64] = 127.0
+    X[0, 65:96] = k + np.float32(0.5) - np.float32(2.0 ** -16)
+    d = np.float32(np.float32(100.0) / np.float32(127.0))
+    X[0, 96] = 100.0                                    # d = RN(100/127), 1/d inexact
+    X[0, 97:128] = ((k + np.float32(0.5)) * d).astype(np.float32)
+    X[0, 128] = -127.0                                  # codes at the clamp, both signs
+    X[0, 129:160] = np.linspace(-127.0, 127.0, 31, dtype=np.float32)
+    X[0, 160] = np.float32(3.0e38)                      # near FLT_MAX
+    X[0, 161:192] = np.float32(3.0e38) * np.linspace(-1.0, 1.0, 31, dtype=np.float32)
+    X[0, 192] = np.float32(1.0e-41)                     # subnormal: 1/d overflows
+    X[0, 193:224] = np.float32(1.0e-41) * np.linspace(-1.0, 1.0, 31, dtype=np.float32)
+    X[1] = synth.normal(K, synth.stream(444, 0)) * np.float32(1e-30)
+    Xq, dx = gpu_quantize(X, M, K)
+    q_ref, d_ref = oracle.quantize_q8_0(X, M, K)
+    assert np.array_equal(dx.cpu().numpy().view(np.uint32), d_ref.view(np.uint32))
+    assert np.array_equal(Xq.cpu().numpy(), q_ref)
+
+
 def workspace(K, M):
     t = torch()
     n = gq.gq_q4_0_gemm_workspace_bytes(K, M)
