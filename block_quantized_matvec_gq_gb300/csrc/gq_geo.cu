@@ -44,19 +44,6 @@ static int ring_override() { return -1; }
 bool gemm_force_block_path() { return false; }
 #endif
 
-// Short, wide matrices (fewer than eight rows per SM) of rows longer than 128
-// blocks take the shared-memory ring (with a cluster split-K below four rows
-// per SM): the register streams would leave most SMs idle, since their grid
-// holds one CTA per eight row tasks.  Measured on Q4_0: 256 x 21504 in 5.1
-// instead of 13.6 us, 8 x 49152 in 3.8 instead of 17.9 us; 64 to 512 rows of
-// 5376 in 4.0-4.3 instead of 4.9-5.0 us; 608 / 768 / 1024 rows of 5376 in
-// 3.6 / 3.8 / 3.9 against 5.0 / 5.1 / 5.1 us, of 21504 in 6.0 / 8.0 / 8.2
-// against 10.5 / 10.5 / 10.6 us, of 8192 in 3.9 / 4.0 / 4.1 against 4.0 / 4.0
-// / 4.2 us.  At 1536 rows the streams are level or ahead (5376: 5.2 against
-// 5.5 us).  At 4096 (128 blocks) the streams are faster at every row count
-// (64 to 512 rows: 2.3 against 4.0-4.1 us; 1024: 2.4 against 3.5).  Q4_K
-// at 608 / 1024 / 1215 rows: 3.9 / 4.1 / 4.3 against 6.2 / 6.3 / 12.0 us
-// (K = 5376), 6.4 / 8.8 / 9.0 against 13.6 / 14.0 / 18.0 us (K = 21504).
 // Register-stream schedule from tasks per resident warp: <= 1.25 balanced
 // with the first loads issued early (mode 2); < 1.75 balanced (mode 1) on
 // rows of at least 512 blocks, whose leftover rows split along K into eight
@@ -76,6 +63,19 @@ int schedule_mode(long long ntasks, long long warps, int nb)
     return 0;
 }
 
+// Short, wide matrices (fewer than eight rows per SM) of rows longer than 128
+// blocks take the shared-memory ring (with a cluster split-K below four rows
+// per SM): the register streams would leave most SMs idle, since their grid
+// holds one CTA per eight row tasks.  Measured on Q4_0: 256 x 21504 in 5.1
+// instead of 13.6 us, 8 x 49152 in 3.8 instead of 17.9 us; 64 to 512 rows of
+// 5376 in 4.0-4.3 instead of 4.9-5.0 us; 608 / 768 / 1024 rows of 5376 in
+// 3.6 / 3.8 / 3.9 against 5.0 / 5.1 / 5.1 us, of 21504 in 6.0 / 8.0 / 8.2
+// against 10.5 / 10.5 / 10.6 us, of 8192 in 3.9 / 4.0 / 4.1 against 4.0 / 4.0
+// / 4.2 us.  At 1536 rows the streams are level or ahead (5376: 5.2 against
+// 5.5 us).  At 4096 (128 blocks) the streams are faster at every row count
+// (64 to 512 rows: 2.3 against 4.0-4.1 us; 1024: 2.4 against 3.5).  Q4_K
+// at 608 / 1024 / 1215 rows: 3.9 / 4.1 / 4.3 against 6.2 / 6.3 / 12.0 us
+// (K = 5376), 6.4 / 8.8 / 9.0 against 13.6 / 14.0 / 18.0 us (K = 21504).
 bool ring_preferred(int rows, int nb)
 {
     const int o = ring_override();
