@@ -37,7 +37,8 @@ def run_matvec(fmt, W_canon, x, rows, K):
 
 SHAPES = [(1, 32), (3, 64), (37, 96), (257, 256), (1000, 512), (129, 4096), (515, 5376), (77, 21504),
           (33, 2304), (250, 800), (8, 49152), (256, 21504), (5, 2048), (600, 1024), (2048, 49152),
-          (1000, 5376), (1213, 8192)]  # the last two: the ring at four to eight rows per SM
+          (1000, 5376), (1213, 8192),  # the ring at four to eight rows per SM
+          (1216, 5376)]  # the register streams just past the ring's limit (eight rows per SM)
 
 
 @pytest.mark.parametrize("fmt", [oracle.FORMAT_Q4_0, oracle.FORMAT_Q8_0, oracle.FORMAT_Q4_K, oracle.FORMAT_Q6_K])
